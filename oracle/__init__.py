@@ -1,0 +1,31 @@
+"""CPU oracle for the draft-tree verification step -- TEST INFRASTRUCTURE ONLY.
+
+A plain, slow, fp64 restatement of what the verification step computes, written from the pages'
+definitions.  It shares no code with the CUDA library (no kernels, headers, helpers, tables or
+constants) and never imports it.  Only tests/, __graft_entry__.smoke() and bench.py's CPU
+baseline / reference arm may import, call or execute anything in this package; the product path
+(the C-ABI library and its Python binding) never does, and fails loudly when its CUDA extension
+is missing.
+
+Modules (each function cites the passage it follows):
+  tree       -- flattening + ancestor mask + depth / position ids + internal-node flags
+  attention  -- dense softmax attention of every tree token over prefix + its ancestors
+  verify     -- temperature softmax, min(1, p/q) ratio test in tree order, residual resampling,
+                bonus token, greedy (tau = 0) argmax matching
+  compact    -- KV commit/rollback of the accepted path
+
+Pins (tests/test_oracle_*.py, run with -m "not gpu") tie each function to something other than
+itself: the page's 6-node mask table, the 123 / 45 node counts, E[L] = (1 - a^(g+1)) / (1 - a),
+exact losslessness by black-box bisection over the uniforms, chi-square against p, library
+scaled-dot-product attention for the T = 1 and chain special cases, and the sequential-decoding
+invariant for compaction.  No oracle function is "parity unpinned".
+"""
+from . import tree, attention, verify, compact  # noqa: F401
+
+# request status bits (the oracle's own numbering of the data errors it detects)
+BAD_PARENT = 1
+BAD_SIZE = 2
+BAD_TOKEN = 4
+BAD_DRAFT_ROW = 8
+BAD_DEPTH = 16
+BAD_BLOCK = 32

@@ -1,0 +1,316 @@
+"""Pins for oracle.verify.
+
+* E[L] = (1 - a^(g+1)) / (1 - a) for a chain of g drafts whose per-position acceptance rate is
+  a = sum_x min(p, q) = 1 - TV(p, q) ("【模型后训练与深度推理】9 推理加速：推测解码与级联推理" 7.2), by Monte
+  Carlo over 10^5 rounds, +-1%.
+* Losslessness (the emitted tokens follow p; "推测解码 2026" and section 7.1 of the CSDN page),
+  checked EXACTLY: the law of the oracle's output is integrated over every draft assignment and,
+  by bisection on the oracle's own accept / reject and sampling decisions (black box: only its
+  outputs are observed), over the uniforms; the first emitted token must follow p_root and the
+  next one p(. | first) to 1e-9.
+* The same losslessness by chi-square on vocab 16 with several iid siblings.
+* Greedy: with greedy drafts, tau -> 0+ sampling reproduces the tau = 0 argmax walk.
+"""
+from collections import defaultdict
+from itertools import product
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as OV
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers building explicit small cases
+# ----------------------------------------------------------------------------------------------
+def _dist(rng, V, conc=1.0):
+    return rng.dirichlet(np.full(V, conc))
+
+
+def _run(case, u_acc, u_samp, rule):
+    T = len(case["parent"])
+    uni = np.stack([u_acc, u_samp], axis=1)
+    res = OV.verify(case["target"], case["draft"], case["kind"], case["draft_row"],
+                    case["tokens"], case["parent"], [0, T], uni, case["tau"], case["V"],
+                    max_path=T, sibling_rule=rule, T_max=T)
+    assert res["status"][0] == 0
+    return tuple(res["out_tokens"][0]), res["path"][0], res["events"][0]
+
+
+_ONE_MINUS = np.nextafter(1.0, 0.0)
+
+
+def _bracket(pred, iters=44):
+    """pred(u) is True on [0, t) and False on [t, 1); return (lo, hi) with pred(lo) True,
+    pred(hi) False and hi - lo <= 2^-iters (hi = 1.0 when pred never fails)."""
+    if not pred(0.0):
+        return 0.0, 0.0
+    if pred(_ONE_MINUS):
+        return 1.0, 1.0
+    lo, hi = 0.0, 1.0
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        if pred(mid):
+            lo = mid
+        else:
+            hi = mid
+    return lo, hi
+
+
+def _threshold(pred, iters=44):
+    lo, hi = _bracket(pred, iters)
+    return 0.5 * (lo + hi)
+
+
+def _exact_law(case, rule):
+    """Law of the emitted sequence over the uniforms (draft tokens fixed in `case`)."""
+    T = len(case["parent"])
+    law = defaultdict(float)
+
+    def rec(fixed, weight):
+        u_acc = np.array([fixed.get(i, 0.5) for i in range(T)])
+        _, path, events = _run(case, u_acc, np.full(T, 0.5), rule)
+        pending = [e[2] for e in events if e[0] == "test" and e[2] not in fixed]
+        if pending:
+            c = pending[0]
+
+            def accepted(u):
+                ua = u_acc.copy()
+                ua[c] = u
+                return c in _run(case, ua, np.full(T, 0.5), rule)[1]
+
+            t = _threshold(accepted)
+            if t > 0:
+                rec({**fixed, c: 0.5 * t}, weight * t)
+            if t < 1:
+                rec({**fixed, c: 0.5 * (1 + t)}, weight * (1 - t))
+            return
+        stop = path[-1]
+
+        def final(u):
+            us = np.full(T, 0.5)
+            us[stop] = u
+            return _run(case, u_acc, us, rule)[0]
+
+        start, seq = 0.0, final(0.0)
+        while True:     # the final token is monotone in u_samp: walk its steps left to right
+            if final(_ONE_MINUS) == seq:
+                law[seq] += weight * (1.0 - start)
+                break
+            lo, hi = _bracket(lambda u: u < start or final(u) == seq)
+            mid = 0.5 * (lo + hi)
+            law[seq] += weight * (mid - start)
+            start, seq = mid, final(hi)
+
+    rec({}, 1.0)
+    return law
+
+
+def _tree_case(V, tau, kind, shape, rng):
+    """Contexts: every node's target / draft row is a function of its path's tokens, as for a
+    real model.  shape: parent array.  Returns a factory mapping draft tokens -> case."""
+    T = len(shape)
+    tables_t, tables_q = {}, {}
+
+    def rows(ctx):
+        if ctx not in tables_t:
+            tables_t[ctx] = rng.normal(size=V) * 1.5
+            tables_q[ctx] = rng.normal(size=V) * 1.5
+        return tables_t[ctx], tables_q[ctx]
+
+    def make(draft_tokens):
+        tokens = [0] + list(draft_tokens)
+        ctx = [()] * T
+        for i in range(1, T):
+            ctx[i] = ctx[shape[i]] + (tokens[i],)
+        tgt = np.stack([rows(ctx[i])[0] for i in range(T)])
+        drl = np.stack([rows(ctx[i])[1] for i in range(T)])
+        if kind == OV.DRAFT_PROBS:
+            drl = np.stack([OV.softmax_at(x, 1.0) for x in drl])
+        return dict(target=tgt, draft=drl, kind=kind, draft_row=np.arange(T), tokens=tokens,
+                    parent=shape, tau=tau, V=V, ctx=ctx)
+
+    return make, rows
+
+
+def _q_of(case, node):
+    row = case["draft"][node]
+    return OV.softmax_at(row, case["tau"]) if case["kind"] == OV.DRAFT_LOGITS else row
+
+
+def _p_of(rows, ctx, tau):
+    return torch.softmax(torch.tensor(rows(ctx)[0]) / tau, dim=0).numpy()
+
+
+@pytest.mark.parametrize("shape,V,tau,kind", [
+    ([-1, 0, 0, 0], 3, 1.0, OV.DRAFT_LOGITS),      # three iid siblings at the root
+    ([-1, 0, 0, 1], 3, 0.7, OV.DRAFT_PROBS),       # two siblings, the first one has a child
+    ([-1, 0, 1], 4, 1.3, OV.DRAFT_LOGITS),         # chain of two drafts
+])
+def test_exact_losslessness(shape, V, tau, kind):
+    rng = np.random.default_rng(11)
+    make, rows = _tree_case(V, tau, kind, shape, rng)
+    T = len(shape)
+    total = defaultdict(float)
+    probe = make([0] * (T - 1))
+    for draft in product(range(V), repeat=T - 1):
+        case = make(draft)
+        w = 1.0
+        for c in range(1, T):   # node c was drawn from q of its parent
+            w *= _q_of(case, shape[c])[draft[c - 1]]
+        for seq, pr in _exact_law(case, OV.SIBLING_RESIDUAL).items():
+            total[seq] += w * pr
+    assert abs(sum(total.values()) - 1.0) < 1e-9
+    p0 = _p_of(rows, (), tau)
+    first = np.zeros(V)
+    for seq, pr in total.items():
+        first[seq[0]] += pr
+    np.testing.assert_allclose(first, p0, atol=1e-9)
+    # second token, given the first one was an accepted draft x, follows p(. | x)
+    for x in range(V):
+        cond = np.zeros(V)
+        for seq, pr in total.items():
+            if seq[0] == x and len(seq) >= 2:
+                cond[seq[1]] += pr
+        if cond.sum() > 1e-6:
+            np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, (x,), tau), atol=1e-8)
+    del probe
+
+
+def test_independent_sibling_rule_is_biased():
+    """The literal per-sibling p/q test (every sibling against the original p) is not lossless
+    for several iid siblings: the exact law of the first token moves away from p."""
+    rng = np.random.default_rng(5)
+    shape, V, tau = [-1, 0, 0, 0], 3, 1.0
+    make, rows = _tree_case(V, tau, OV.DRAFT_LOGITS, shape, rng)
+    first = np.zeros(V)
+    for draft in product(range(V), repeat=3):
+        case = make(draft)
+        w = np.prod([_q_of(case, 0)[t] for t in draft])
+        for seq, pr in _exact_law(case, OV.SIBLING_INDEPENDENT).items():
+            first[seq[0]] += w * pr
+    assert np.abs(first - _p_of(rows, (), tau)).max() > 1e-3
+
+
+# ----------------------------------------------------------------------------------------------
+# Monte Carlo pins
+# ----------------------------------------------------------------------------------------------
+def _pq_with_alpha(rng, V, alpha):
+    p = _dist(rng, V)
+    r = _dist(rng, V, 0.3)
+
+    def acc(t):
+        return np.minimum(p, (1 - t) * p + t * r).sum()
+
+    lo, hi = 0.0, 1.0
+    assert acc(1.0) < alpha
+    for _ in range(100):
+        mid = 0.5 * (lo + hi)
+        if acc(mid) > alpha:
+            lo = mid
+        else:
+            hi = mid
+    q = (1 - lo) * p + lo * r
+    return p, q / q.sum(), np.minimum(p, q / q.sum()).sum()
+
+
+@pytest.mark.parametrize("gamma,alpha", [(1, 0.2), (4, 0.5), (8, 0.8), (5, 0.95)])
+def test_expected_emitted_length(gamma, alpha):
+    rng = np.random.default_rng(100 + gamma)
+    V, rounds = 16, 100_000
+    p, q, a = _pq_with_alpha(rng, V, alpha)
+    T = gamma + 1
+    B = rounds
+    parent = np.tile(np.array([-1] + list(range(gamma))), B)
+    no = np.arange(B + 1) * T
+    tgt = np.tile(np.log(p), (B * T, 1))
+    drf = q[None, :]
+    drow = np.zeros(B * T, dtype=np.int64)
+    cdf = np.cumsum(q)
+    tokens = np.minimum(np.searchsorted(cdf, rng.random(B * T) * cdf[-1], side="right"), V - 1)
+    uni = rng.random((B * T, 2))
+    res = OV.verify(tgt, drf, OV.DRAFT_PROBS, drow, tokens, parent, no, uni, 1.0, V,
+                    max_path=T, T_max=T)
+    mean_L = res["out_len"].mean()
+    want = (1 - a ** (gamma + 1)) / (1 - a)
+    assert abs(mean_L - want) / want < 0.01, (mean_L, want, a)
+
+
+def test_chi_square_first_token_follows_p():
+    from scipy.stats import chisquare
+    rng = np.random.default_rng(7)
+    V, k, rounds = 16, 3, 30_000
+    p_log = rng.normal(size=V) * 1.2
+    q_log = p_log + rng.normal(size=V) * 1.0
+    p = OV.softmax_at(p_log, 1.0)
+    q = OV.softmax_at(q_log, 1.0)
+    T = k + 1
+    parent = np.tile(np.array([-1] + [0] * k), rounds)
+    no = np.arange(rounds + 1) * T
+    tgt = np.tile(p_log, (rounds * T, 1))
+    drf = q_log[None, :]
+    drow = np.zeros(rounds * T, dtype=np.int64)
+    tokens = rng.choice(V, size=rounds * T, p=q)
+    uni = rng.random((rounds * T, 2))
+    res = OV.verify(tgt, drf, OV.DRAFT_LOGITS, drow, tokens, parent, no, uni, 1.0, V,
+                    max_path=T, T_max=T)
+    first = np.array([t[0] for t in res["out_tokens"]])
+    counts = np.bincount(first, minlength=V)
+    stat = chisquare(counts, p * rounds)
+    assert stat.pvalue > 0.01, stat
+
+
+def test_greedy_is_the_low_temperature_limit():
+    rng = np.random.default_rng(3)
+    V, gamma, B = 50, 5, 200
+    T = gamma + 1
+    tgt = rng.normal(size=(B * T, V)) * 3
+    drf = tgt + rng.normal(size=(B * T, V)) * 0.7
+    # keep cases where top-2 gaps are clear so tau = 1e-4 is numerically greedy
+    tokens = np.zeros(B * T, dtype=np.int64)
+    for r in range(B):
+        for i in range(gamma):
+            tokens[r * T + i + 1] = int(np.argmax(drf[r * T + i]))   # greedy drafts
+    parent = np.tile(np.array([-1] + list(range(gamma))), B)
+    no = np.arange(B + 1) * T
+    uni = rng.random((B * T, 2))
+    drow = np.arange(B * T)
+    g = OV.verify(tgt, drf, OV.DRAFT_LOGITS, drow, tokens, parent, no, uni, 0.0, V, T, T_max=T)
+    s = OV.verify(tgt, drf, OV.DRAFT_LOGITS, drow, tokens, parent, no, uni, 1e-4, V, T, T_max=T)
+    srt = np.sort(np.concatenate([tgt, drf]), axis=1)
+    clear = (srt[:, -1] - srt[:, -2]).reshape(2, B, T).min(axis=(0, 2)) > 0.02
+    assert clear.sum() > B // 2
+    for r in np.nonzero(clear)[0]:
+        assert g["out_tokens"][r] == s["out_tokens"][r]
+        assert g["path"][r] == s["path"][r]
+    # every accepted greedy token is the target argmax along the path; the last is argmax too
+    for r in range(B):
+        path = g["path"][r]
+        for d in range(len(path)):
+            assert g["out_tokens"][r][d] == int(np.argmax(tgt[r * T + path[d]]))
+
+
+def test_greedy_ties_go_to_lowest_token():
+    V = 8
+    tgt = np.zeros((2, V))
+    tgt[0, [2, 5]] = 4.0
+    tgt[1, [1, 6]] = 9.0
+    res = OV.verify(tgt, np.zeros((1, V)), OV.DRAFT_LOGITS, [0, -1], [0, 2], [-1, 0], [0, 2],
+                    np.zeros((2, 2)), 0.0, V, 2, T_max=2)
+    assert res["out_tokens"][0] == [2, 1]
+
+
+def test_data_errors_flagged():
+    V = 10
+    tgt = np.zeros((3, V))
+    base = dict(target=tgt, draft=np.zeros((2, V)), draft_kind=OV.DRAFT_LOGITS,
+                parent=[-1, 0, 1], node_offset=[0, 3], uniforms=np.zeros((3, 2)), tau=1.0, V=V)
+    r = OV.verify(draft_row=[0, 1, -1], tokens=[0, 3, V], max_path=3, **base)
+    assert r["status"][0] == OV.BAD_TOKEN and r["out_len"][0] == 0 and r["n_acc"][0] == -1
+    r = OV.verify(draft_row=[0, 2, -1], tokens=[0, 3, 4], max_path=3, **base)
+    assert r["status"][0] == OV.BAD_DRAFT_ROW
+    r = OV.verify(draft_row=[0, 1, -1], tokens=[0, 3, 4], max_path=2, **base)
+    assert r["status"][0] == OV.BAD_DEPTH
+    r = OV.verify(draft_row=[0, 1, -1], tokens=[0, 3, 4], max_path=3, **base)
+    assert r["status"][0] == 0 and r["out_len"][0] >= 1
