@@ -1,0 +1,239 @@
+/*
+ * spec_verify.h -- C ABI of the draft-tree verification step (tree attention, ratio-test
+ * verification with residual resampling, KV compaction) for one GB300 (sm_103a) GPU.
+ *
+ * Sources (page title, section):
+ *   [TREE]  "投机推理算法的常见优化手段" (cnblogs zrq96), 草稿树的验证——树形掩码: flattened tree, the
+ *           ancestor mask (a token sees itself and its ancestors), the forward call
+ *           logits = llm.forward(draft_tree, tree_mask, position_ids, kvcache) and tree
+ *           verification level by level.
+ *   [RATIO] "推测解码 2026" (guijiagi.com), 数学基础：拒绝采样: accept with min(1, p/q), resample from
+ *           relu(p - q) normalised, discard later candidates; 工程实践中的考量 / KV Cache管理:
+ *           roll back the K/V of rejected candidates.
+ *   [CSDN]  "【模型后训练与深度推理】9 推理加速：推测解码与级联推理", section 7.1 (alpha = min(1, p/q),
+ *           residual norm(max(0, p - q)), output distributed as p), section 5 (interface: prompt,
+ *           draft length, probability tensors, a boolean accept mask, accepted tokens).
+ *   [SURV]  "万字综述 10+ 种 LLM 投机采样推理加速方案" (m.haoling.cc), 5.2 (tree-based parallel
+ *           decoding through an attention mask), 4.3 (argmax sampling, temp = 0), 12.4.3
+ *           (PagedAttention / FlashDecoding as the framework features to fit).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise; the caller allocates
+ *     and owns all buffers, including workspaces.  The library never allocates, frees or
+ *     synchronises; each call enqueues kernels on `stream` and returns.
+ *   - The return code covers argument validation and launch errors only.  Errors in DEVICE DATA
+ *     (a bad parent index, a token id >= V, a block id out of range, ...) are OR-ed as SPEC_REQ_*
+ *     bits into the caller's per-request int32 `req_status[B]`; such a request produces
+ *     out_len = 0 / n_acc = -1 and is rolled back by spec_kv_compact.  No kernel traps.
+ *   - Nodes of all requests are packed: request r owns global nodes
+ *     node_offset[r] .. node_offset[r+1]-1 (CSR, node_offset has B+1 entries); node 0 of a request
+ *     is its root (the last committed token, whose K/V is not cached yet); `parent` holds LOCAL
+ *     indices with parent[root] = -1 and 0 <= parent[i] < i (BFS / topological order).
+ *   - T_r = node_offset[r+1] - node_offset[r] includes the root; T_max (host) bounds every T_r and
+ *     may not exceed SPEC_MAX_TREE (256).
+ *   - Row-major buffers whose rows are read with 16-byte vector loads (logits, probabilities,
+ *     Q, K/V, O) must start on 16-byte boundaries and have 16-byte-multiple row strides.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (pass 0 for the legacy default stream). */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or stride, tau < 0, ... */
+  SPEC_ERR_UNSUPPORTED = 2,    /* a valid but unimplemented shape (e.g. bf16 head_dim != 128) */
+  SPEC_ERR_CUDA = 3,           /* a CUDA launch / driver error (see spec_last_cuda_error) */
+  SPEC_ERR_TIMEOUT = 4,        /* reserved for host-side waits; device waits report via bits */
+  SPEC_ERR_BAD_INPUT_DATA = 5  /* reserved: data errors are reported per request, see below */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+typedef enum { SPEC_DRAFT_LOGITS = 0, SPEC_DRAFT_PROBS = 1 } spec_draft_kind_t;
+typedef enum {
+  SPEC_SIBLING_RESIDUAL = 0,   /* default: child k is tested against the k-fold residual */
+  SPEC_SIBLING_INDEPENDENT = 1 /* every sibling tested against p; resample from max(0, p - q) */
+} spec_sibling_rule_t;
+
+/* Per-request data-error bits OR-ed into req_status[r]. */
+#define SPEC_REQ_BAD_PARENT    1   /* parent[0] != -1 or parent[i] not in [0, i) */
+#define SPEC_REQ_BAD_SIZE      2   /* T_r < 1, T_r > T_max, or node_offset not monotone / > N */
+#define SPEC_REQ_BAD_TOKEN     4   /* a draft token id outside [0, V) */
+#define SPEC_REQ_BAD_DRAFT_ROW 8   /* tau > 0 and a node with children has draft_row outside [0, R) */
+#define SPEC_REQ_BAD_DEPTH     16  /* a root-to-node path longer than max_path */
+#define SPEC_REQ_BAD_BLOCK     32  /* a needed block_table entry outside [0, num_blocks) */
+#define SPEC_REQ_TIMEOUT       64  /* a bounded device-side wait gave up (the result is invalid) */
+
+#define SPEC_MAX_TREE 256
+
+/* ------------------------------------------------------------------------------------------
+ * spec_tree_build  [TREE]
+ * For each request: depth[i] = number of proper ancestors of node i (root 0);
+ * pos_id[i] = prefix_len[r] + depth[i] (position ids adapted to the tree);
+ * anc_mask row i (ceil(T_max/32) uint32 words, bit j of word j/32 = LOCAL node j) has bit j set
+ * iff j == i or j is an ancestor of i -- one row of the page's mask table;
+ * is_internal[i] = 1 iff node i has at least one child.
+ *   parent [N] int32, node_offset [B+1] int32, prefix_len [B] int32: inputs (device).
+ *   depth, pos_id [N] int32; anc_mask [N][ceil(T_max/32)] uint32; is_internal [N] uint8: outputs.
+ *   req_status [B] int32: output; this call (re)initialises it (0 or a SPEC_REQ_* bit) and the
+ *   later calls of the round OR their bits into it.
+ * Requests with a data error get their outputs set to -1 / 0 and a SPEC_REQ_BAD_* bit.
+ * Errors: SPEC_ERR_INVALID_ARG for null or inconsistent arguments (B < 1, N < 0, T_max outside
+ * [1, 256]); SPEC_ERR_CUDA on a launch failure.
+ * ------------------------------------------------------------------------------------------ */
+spec_status_t spec_tree_build(const int32_t* parent, const int32_t* node_offset,
+                              const int32_t* prefix_len, int32_t B, int32_t N, int32_t T_max,
+                              int32_t* depth, int32_t* pos_id, uint32_t* anc_mask,
+                              uint8_t* is_internal, int32_t* req_status, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_tree_attention  [TREE], [SURV 5.2, 12.4.3]
+ * O[n][h] = sum_j softmax_j(scale * q[n][h] . k_j) v_j over the logical KV slots
+ *   j in {0 .. P_r-1} U {P_r + a : a == i or a is an ancestor of i}
+ * for node n = node_offset[r] + i.  The caller has written node a's K/V into logical slot
+ * P_r + a before the call.  Logical slot s of request r is row s % block_size of physical block
+ * block_table[r][s / block_size].  Query head h reads KV head h / (H_q / H_kv).
+ * Layouts (element type `dtype`, contiguous, 16-byte aligned):
+ *   q [N][H_q][head_dim]; k_cache, v_cache [num_blocks][H_kv][block_size][head_dim] (one layer);
+ *   o [N][H_q][head_dim]; lse [N][H_q] fp32 (natural log of the softmax denominator of the
+ *   scaled scores) or NULL; block_table [B][max_blocks_per_req] int32; prefix_len [B];
+ *   node_offset [B+1]; anc_mask from spec_tree_build; req_status [B] in/out.
+ * Paths: dtype BF16 runs on the tcgen05 tensor cores (TMA-staged paged tiles, scores and output
+ * accumulated in TMEM) and requires head_dim == 128, block_size == 16 and
+ * H_q / H_kv in {1, 2, 4, 8, 16}; dtype F32 runs a CUDA-core kernel (head_dim <= 128,
+ * multiple of 4).  Long KV ranges are split across CTAs and merged by log-sum-exp in
+ * `workspace` (spec_attention_workspace_size bytes, 256-byte aligned, caller-owned, contents
+ * need not be initialised).  scale <= 0 selects 1/sqrt(head_dim).
+ * Errors: SPEC_ERR_INVALID_ARG (null / misaligned pointers, inconsistent sizes, too-small
+ * workspace), SPEC_ERR_UNSUPPORTED (a shape outside the paths above), SPEC_ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  spec_dtype_t dtype;
+  int32_t B, N, T_max;
+  int32_t H_q, H_kv, head_dim;
+  int32_t block_size;          /* tokens per KV block */
+  int32_t num_blocks;          /* physical blocks in the pool (bounds check) */
+  int32_t max_blocks_per_req;  /* row stride of block_table */
+  float scale;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* node_offset;
+  const uint32_t* anc_mask;
+  void* o;
+  float* lse;
+  int32_t* req_status;
+} spec_attn_params;
+
+size_t spec_attention_workspace_size(const spec_attn_params* p);
+spec_status_t spec_tree_attention(const spec_attn_params* p, void* workspace, size_t ws_bytes,
+                                  spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_verify  [RATIO], [CSDN 7.1, 7.2, 5], [TREE], [SURV 4.3]
+ * p_i = softmax(target[i] / tau), q_i = softmax(draft[draft_row[i]] / tau) (draft logits) or the
+ * given row (draft probabilities).  Walk from the root; at node i test its children c in
+ * increasing index with u_acc = uniforms[c][0]:
+ *   SIBLING_RESIDUAL: after k rejected siblings the target is R_k = max(0, p_i - C_k q_i),
+ *     C_0 = 0, N_k = sum R_k, C_{k+1} = C_k + N_k; accept iff u_acc < R_k(tok)/(N_k q_i(tok))
+ *     (k = 0: p/q, the pages' rule);
+ *   SIBLING_INDEPENDENT: accept iff u_acc < p_i(tok)/q_i(tok) for every sibling;
+ *   tau == 0: accept iff tok == argmax p_i (lowest id on ties).
+ * On acceptance descend to c.  The walk stops at a leaf (the final token is a bonus draw from
+ * p_leaf with u_samp = uniforms[leaf][1]) or when every child is rejected (the final token is
+ * drawn from the normalised residual with u_samp of that node; from p if the residual mass is
+ * 0); tau == 0 takes argmax p instead.  Draws use the inverse CDF over ascending token id: the
+ * smallest x with sum_{y<=x} w(y) > u * sum_y w(y).  Randomness is never generated inside.
+ * Outputs per request r (row stride max_path): path[r][0..n_acc] = accepted local node ids
+ * (root first), out_tokens[r][0..n_acc] = accepted draft tokens then the final token,
+ * out_len[r] = n_acc + 1, rejections[r] = rejected children on the walk; unused entries -1.
+ * Layouts: target [N][target_ld] (logits_dtype), draft [R][draft_ld] (logits_dtype for
+ * logits, fp32 for probabilities), rows 16-byte aligned; draft_row, tokens, parent, depth [N]
+ * int32 (depth from spec_tree_build); is_internal [N] uint8; uniforms [N][2] fp32.
+ * workspace: spec_verify_workspace_size bytes (256-byte aligned, caller-owned).
+ * Errors: SPEC_ERR_INVALID_ARG (null / misaligned pointers, V < 1, ld < V, tau < 0 or not
+ * finite, max_path < 1, small workspace), SPEC_ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  spec_dtype_t logits_dtype;
+  spec_draft_kind_t draft_kind;
+  spec_sibling_rule_t sibling_rule;
+  int32_t B, N, R, V;
+  int64_t target_ld, draft_ld;   /* row strides in elements */
+  int32_t T_max, max_path;
+  float tau;
+  const void* target;
+  const void* draft;
+  const int32_t* draft_row;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* node_offset;
+  const int32_t* depth;
+  const uint8_t* is_internal;
+  const float* uniforms;
+  int32_t* req_status;
+  int32_t* out_tokens;
+  int32_t* out_len;
+  int32_t* path;
+  int32_t* n_acc;
+  int32_t* rejections;           /* may be NULL */
+} spec_verify_params;
+
+size_t spec_verify_workspace_size(const spec_verify_params* p);
+spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
+                          spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_kv_compact  [RATIO: KV Cache管理], [CSDN 4]
+ * Commits the accepted path and rolls back the rest, in place, for every layer and KV head,
+ * K and V: new[P_r + d] = old[P_r + path[r][d]] for d = 0 .. n_acc[r] (gather semantics: every
+ * source is read as it was before the call), i.e. the cache sequential decoding of the accepted
+ * path would hold.  new_kv_len[r] = P_r + n_acc[r] + 1 (the final token has no K/V yet);
+ * blocks_in_use[r] = ceil(new_kv_len / block_size); slot_map[r][d] = (src, dst) logical slots,
+ * (-1, -1) past n_acc.  A request with req_status != 0 or n_acc < 0 is rolled back entirely
+ * (new_kv_len = P_r, nothing copied).  Slots past new_kv_len are released, not cleared.
+ * Layouts: k_cache, v_cache point at layer 0 of [num_layers] x [num_blocks][H_kv][block_size]
+ * [head_dim] with `layer_stride` elements between layers; head_dim * element size must be a
+ * multiple of 16 bytes.  path [B][max_path], n_acc [B] as written by spec_verify;
+ * slot_map [B][max_path][2], new_kv_len [B], blocks_in_use [B] int32 outputs.
+ * Errors: SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  spec_dtype_t dtype;
+  int32_t B, H_kv, head_dim, block_size, num_blocks, max_blocks_per_req, num_layers, max_path;
+  int64_t layer_stride;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* path;
+  const int32_t* n_acc;
+  int32_t* req_status;
+  int32_t* new_kv_len;
+  int32_t* slot_map;
+  int32_t* blocks_in_use;
+} spec_compact_params;
+
+spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* spec_status_string(spec_status_t status);
+
+/* The cudaError_t (as int) behind the most recent SPEC_ERR_CUDA on this thread, 0 if none. */
+int spec_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,126 @@
+"""One verification round on the GPU through the C-ABI: tree build -> tree attention (one layer)
+-> verify -> KV compaction.
+
+`VerifyStep` owns every output and workspace buffer for a fixed workload shape (allocated once
+with torch, never inside the timed calls) and runs the four library calls on the current stream.
+`run_from_host` is the end-to-end form: the step's inputs arrive in pinned host memory, are
+copied to the device, the round runs, and the accepted tokens come back to the host.
+"""
+from dataclasses import dataclass
+from typing import Dict, Optional
+
+import torch
+
+from . import binding as B
+from .workloads import Workload
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    # torch allocations are 256-byte aligned (caching allocator) -- the library checks it
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+class VerifyStep:
+    def __init__(self, w: Workload, sibling_rule: int = B.SPEC_SIBLING_RESIDUAL,
+                 with_lse: bool = True):
+        self.w = w
+        dev = w.target.device
+        if dev.type != "cuda":
+            raise ValueError("VerifyStep needs the workload on a CUDA device")
+        i32 = dict(dtype=torch.int32, device=dev)
+        Bn, N, W = w.B, w.N, (w.T_max + 31) // 32
+        self.req_status = torch.zeros(Bn, **i32)
+        self.depth = torch.empty(N, **i32)
+        self.pos_id = torch.empty(N, **i32)
+        self.anc_mask = torch.empty((N, W), **i32)
+        self.is_internal = torch.empty(N, dtype=torch.uint8, device=dev)
+        self.o = torch.empty_like(w.q)
+        self.lse = torch.empty((N, w.H_q), dtype=torch.float32, device=dev) if with_lse else None
+        self.out_tokens = torch.empty((Bn, w.max_path), **i32)
+        self.path = torch.empty((Bn, w.max_path), **i32)
+        self.out_len = torch.empty(Bn, **i32)
+        self.n_acc = torch.empty(Bn, **i32)
+        self.rejections = torch.empty(Bn, **i32)
+        self.new_kv_len = torch.empty(Bn, **i32)
+        self.blocks_in_use = torch.empty(Bn, **i32)
+        self.slot_map = torch.empty((Bn, w.max_path, 2), **i32)
+        self.k_layer0 = w.k_cache[0]
+        self.v_layer0 = w.v_cache[0]
+        self.attn = B.attention_params(w.q, self.k_layer0, self.v_layer0, w.block_table,
+                                       w.prefix_len, w.node_offset, self.anc_mask, w.T_max,
+                                       self.o, self.lse, self.req_status)
+        self.attn_ws = _ws(B.spec_attention_workspace_size(self.attn), dev)
+        self.ver = B.verify_params(w.target, w.draft, w.draft_kind, w.draft_row, w.tokens,
+                                   w.parent, w.node_offset, self.depth, self.is_internal,
+                                   w.uniforms, w.tau, w.V, w.T_max, w.max_path, self.req_status,
+                                   self.out_tokens, self.out_len, self.path, self.n_acc,
+                                   self.rejections, sibling_rule)
+        self.ver_ws = _ws(B.spec_verify_workspace_size(self.ver), dev)
+        self.comp = B.compact_params(w.k_cache, w.v_cache, w.block_table, w.prefix_len,
+                                     self.path, self.n_acc, self.req_status, self.new_kv_len,
+                                     self.slot_map, self.blocks_in_use, w.max_path)
+
+    # individual stages ---------------------------------------------------------------------
+    def tree_build(self, stream=None):
+        w = self.w
+        B.spec_tree_build(w.parent, w.node_offset, w.prefix_len, w.T_max, self.depth, self.pos_id,
+                          self.anc_mask, self.is_internal, self.req_status, stream)
+
+    def attention(self, stream=None):
+        B.spec_tree_attention(self.attn, self.attn_ws, stream)
+
+    def verify(self, stream=None):
+        B.spec_verify(self.ver, self.ver_ws, stream)
+
+    def compact(self, stream=None):
+        B.spec_kv_compact(self.comp, stream)
+
+    def run(self, stream=None):
+        """One full round (4 library calls, 1 + 2 + 3 + 1 kernel launches on the stream)."""
+        self.tree_build(stream)
+        self.attention(stream)
+        self.verify(stream)
+        self.compact(stream)
+
+    def results(self) -> Dict[str, torch.Tensor]:
+        return dict(req_status=self.req_status, depth=self.depth, pos_id=self.pos_id,
+                    anc_mask=self.anc_mask, is_internal=self.is_internal, o=self.o, lse=self.lse,
+                    out_tokens=self.out_tokens, out_len=self.out_len, path=self.path,
+                    n_acc=self.n_acc, rejections=self.rejections, new_kv_len=self.new_kv_len,
+                    slot_map=self.slot_map, blocks_in_use=self.blocks_in_use)
+
+    # end-to-end form ----------------------------------------------------------------------
+    def step_input_tensors(self) -> Dict[str, torch.Tensor]:
+        """Device tensors that a new round brings from the host: the draft tree, its logits,
+        uniforms, Q and the tree tokens' K/V rows (slots P..P+T-1 are written by the caller;
+        here the whole layer-0 tree region is represented by the block-table-addressed cache
+        rows, which stay resident) -- see run_from_host."""
+        w = self.w
+        return dict(parent=w.parent, node_offset=w.node_offset, prefix_len=w.prefix_len,
+                    tokens=w.tokens, draft_row=w.draft_row, uniforms=w.uniforms, target=w.target,
+                    draft=w.draft, q=w.q, block_table=w.block_table)
+
+    def pinned_host_inputs(self) -> Dict[str, torch.Tensor]:
+        return {k: v.detach().to("cpu").pin_memory() for k, v in self.step_input_tensors().items()}
+
+    def run_from_host(self, host_inputs: Dict[str, torch.Tensor], host_out: Dict[str, torch.Tensor],
+                      stream=None):
+        """Copy the round's inputs from pinned host memory, run the round, copy the accepted
+        tokens and lengths back.  Asynchronous on the stream; synchronise before reading
+        host_out."""
+        dev_in = self.step_input_tensors()
+        for k, h in host_inputs.items():
+            dev_in[k].copy_(h, non_blocking=True)
+        self.run(stream)
+        host_out["out_tokens"].copy_(self.out_tokens, non_blocking=True)
+        host_out["out_len"].copy_(self.out_len, non_blocking=True)
+        host_out["new_kv_len"].copy_(self.new_kv_len, non_blocking=True)
+
+    def host_output_buffers(self) -> Dict[str, torch.Tensor]:
+        return dict(out_tokens=torch.empty_like(self.out_tokens, device="cpu").pin_memory(),
+                    out_len=torch.empty_like(self.out_len, device="cpu").pin_memory(),
+                    new_kv_len=torch.empty_like(self.new_kv_len, device="cpu").pin_memory())
+
+    @staticmethod
+    def bytes_of(tensors: Dict[str, torch.Tensor]) -> int:
+        return sum(t.numel() * t.element_size() for t in tensors.values())

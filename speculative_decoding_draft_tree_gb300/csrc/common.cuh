@@ -1,0 +1,119 @@
+// Shared device and host helpers of the verification library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "spec_verify.h"
+
+#define SPEC_HOST_DEVICE __host__ __device__ __forceinline__
+
+namespace spec {
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+void set_last_cuda_error(cudaError_t e);
+int sm_count_current_device();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline spec_status_t launch_status() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ------------------------------------------------------------------------------------------
+// device side
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <typename T> struct elem;
+template <> struct elem<float> {
+  static constexpr int per16 = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* out) {
+    out[0] = __uint_as_float(v.x); out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z); out[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static float load1(const float* p) { return __ldg(p); }
+};
+template <> struct elem<__nv_bfloat16> {
+  static constexpr int per16 = 8;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* out) {
+    out[0] = bf16_lo(v.x); out[1] = bf16_hi(v.x); out[2] = bf16_lo(v.y); out[3] = bf16_hi(v.y);
+    out[4] = bf16_lo(v.z); out[5] = bf16_hi(v.z); out[6] = bf16_lo(v.w); out[7] = bf16_hi(v.w);
+  }
+  __device__ __forceinline__ static float load1(const __nv_bfloat16* p) {
+    uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(p));
+    return __uint_as_float(uint32_t(b) << 16);
+  }
+};
+
+// streaming 16-byte load (read once: do not keep in L1)
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Double-float (unevaluated sum hi + lo) accumulation: Knuth's TwoSum followed by a
+// renormalisation (Dekker 1971 / Hida-Li-Bailey double-double addition, fp32 edition).
+struct dfloat {
+  float hi, lo;
+};
+__device__ __forceinline__ dfloat df_make(float a) { return {a, 0.f}; }
+__device__ __forceinline__ dfloat df_add(dfloat a, dfloat b) {
+  float s = a.hi + b.hi;
+  float v = s - a.hi;
+  float e = (a.hi - (s - v)) + (b.hi - v);
+  e += a.lo + b.lo;
+  float hi = s + e;
+  float lo = e - (hi - s);
+  return {hi, lo};
+}
+__device__ __forceinline__ dfloat df_add_f(dfloat a, float b) { return df_add(a, df_make(b)); }
+__device__ __forceinline__ double df_to_d(dfloat a) { return double(a.hi) + double(a.lo); }
+__device__ __forceinline__ dfloat df_shfl_xor(dfloat a, int o) {
+  return {__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ dfloat df_shfl_up(dfloat a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ dfloat warp_sum_df(dfloat v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
+  return v;
+}
+// inclusive prefix sum across the warp
+__device__ __forceinline__ dfloat warp_scan_df(dfloat v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    dfloat t = df_shfl_up(v, o);
+    if (lane >= o) v = df_add(v, t);
+  }
+  return v;
+}
+
+}  // namespace spec

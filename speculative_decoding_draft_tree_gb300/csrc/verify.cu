@@ -1,0 +1,718 @@
+// spec_verify: ratio-test verification of packed draft trees with residual resampling.
+//
+// Sources (page title, section):
+//   "推测解码 2026" (guijiagi.com), 数学基础：拒绝采样 -- accept with min(1, p/q); on rejection resample
+//     from relu(p - q) normalised and drop the remaining candidates;
+//   "【模型后训练与深度推理】9 推理加速：推测解码与级联推理", 7.1 -- alpha = min(1, p/q), residual
+//     norm(max(0, p - q)); 7.2 -- the emitted count includes the final corrected / bonus token;
+//   "投机推理算法的常见优化手段" (cnblogs zrq96), 草稿树的验证——树形掩码 -- node i's logits give
+//     P(. | ancestors(i)); verification walks every level of the tree;
+//   "万字综述 10+ 种 LLM 投机采样推理加速方案" (m.haoling.cc) 4.3 -- argmax sampling at temp = 0.
+//
+// Three launches on the caller's stream:
+//   1. prep  (one CTA per request): validates tokens / draft rows / depths, marks the target
+//      rows of internal nodes and the draft rows they reference;
+//   2. rows  (one CTA per marked row, 256 threads): ONE streaming read of the row with 16-byte
+//      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over 32-element chunks
+//      (Kahan-compensated), then a block reduction (max, then a double-float sum) -> (m, Z);
+//      tau = 0 keeps (max, lowest argmax) instead;
+//   3. walk  (one CTA of 1024 threads per request): the tree walk.  Ratio tests are scalar work
+//      on thread 0 using (m, Z); every vocab-wide step (sibling residual mass, residual / bonus
+//      inverse CDF, leaf max / argmax) is a block-wide pass: 32 warps own contiguous vocab
+//      ranges, per-warp double-float sums are scanned in token order, the warp holding the
+//      crossing rescans its range with a warp scan and its crossing lane walks its 8 elements.
+// Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
+#include <math.h>
+
+#include "common.cuh"
+
+namespace spec {
+
+struct RowStat {
+  float m;      // row max of the raw logits
+  int32_t arg;  // lowest index of the max (tau = 0 rows)
+  double Z;     // sum over the row of 2^((x - m) * log2(e) / tau)
+};
+
+struct VerifyDev {
+  const void* target;
+  const void* draft;
+  int64_t tld, dld;
+  int32_t B, N, R, V, T_max, max_path;
+  float tau, k2, inv_tau;  // k2 = log2(e) / tau
+  int32_t probs, residual_rule;
+  const int32_t* draft_row;
+  const int32_t* tokens;
+  const int32_t* parent;
+  const int32_t* node_offset;
+  const int32_t* depth;
+  const uint8_t* is_internal;
+  const float* uniforms;
+  int32_t* req_status;
+  int32_t* out_tokens;
+  int32_t* out_len;
+  int32_t* path;
+  int32_t* n_acc;
+  int32_t* rejections;
+  RowStat* tstat;
+  RowStat* dstat;
+  uint8_t* t_need;
+  uint32_t* d_need;
+};
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
+template <typename T>
+__device__ __forceinline__ void load8(const T* __restrict__ row, int unit, int V, int full,
+                                      float fill, float (&x)[8]) {
+  if (unit < full) {
+    if constexpr (sizeof(T) == 2) {
+      uint4 v = ld_stream16(row + size_t(unit) * 8);
+      elem<T>::unpack(v, x);
+    } else {
+      uint4 a = ld_stream16(row + size_t(unit) * 8);
+      uint4 b = ld_stream16(row + size_t(unit) * 8 + 4);
+      x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y);
+      x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
+      x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y);
+      x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      int idx = unit * 8 + k;
+      x[k] = idx < V ? elem<T>::load1(row + idx) : fill;
+    }
+  }
+}
+
+__device__ __forceinline__ float sum8(const float (&w)[8]) {
+  return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+}
+
+// ---- 1. prep -------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) verify_prep_kernel(VerifyDev a) {
+  const int r = blockIdx.x;
+  const int o = a.node_offset[r];
+  const int e = a.node_offset[r + 1];
+  const int T = e - o;
+  const bool range_ok = o >= 0 && e <= a.N && T >= 1 && T <= a.T_max;
+  const int st = a.req_status[r];
+  if (!range_ok || st != 0) {
+    if (threadIdx.x == 0 && !range_ok) atomicOr(&a.req_status[r], SPEC_REQ_BAD_SIZE);
+    return;
+  }
+  int bad = 0;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    const int n = o + i;
+    if (i > 0) {
+      const int tok = a.tokens[n];
+      if (tok < 0 || tok >= a.V) bad |= SPEC_REQ_BAD_TOKEN;
+    }
+    if (a.depth[n] + 1 > a.max_path) bad |= SPEC_REQ_BAD_DEPTH;
+    if (a.tau > 0.f && a.is_internal[n]) {
+      const int dr = a.draft_row[n];
+      if (dr < 0 || dr >= a.R) bad |= SPEC_REQ_BAD_DRAFT_ROW;
+    }
+  }
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (bad) atomicOr(&s_bad, bad);
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) atomicOr(&a.req_status[r], s_bad);
+    return;
+  }
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    const int n = o + i;
+    if (a.is_internal[n]) {
+      a.t_need[n] = 1;
+      if (a.tau > 0.f && !a.probs) a.d_need[a.draft_row[n]] = 1u;  // benign: all store 1
+    }
+  }
+}
+
+// ---- 2. rows: (m, Z) or (max, argmax) in one streaming read --------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
+  const int b = blockIdx.x;
+  const T* row;
+  RowStat* out;
+  if (b < a.N) {
+    if (!a.t_need[b]) return;
+    row = reinterpret_cast<const T*>(a.target) + size_t(b) * a.tld;
+    out = a.tstat + b;
+  } else {
+    const int rr = b - a.N;
+    if (!a.d_need[rr]) return;
+    row = reinterpret_cast<const T*>(a.draft) + size_t(rr) * a.dld;
+    out = a.dstat + rr;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V, full = V / 8, nunits = (V + 7) / 8;
+  __shared__ float s_f[8];
+  __shared__ int s_i[8];
+  __shared__ float s_hi[8], s_lo[8];
+  if (a.tau == 0.f) {
+    float best = -INFINITY;
+    int arg = 0x7fffffff;
+    for (int u0 = tid; u0 < nunits; u0 += 4 * 256) {
+      float x[4][8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int unit = u0 + j * 256;
+        if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
+        else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) x[j][k] = -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (x[j][k] > best) { best = x[j][k]; arg = (u0 + j * 256) * 8 + k; }
+    }
+    // block (max value, lowest index)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      int oa = __shfl_xor_sync(0xffffffffu, arg, off);
+      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+    }
+    if (lane == 0) { s_f[warp] = best; s_i[warp] = arg; }
+    __syncthreads();
+    if (tid == 0) {
+      float bb = s_f[0];
+      int ba = s_i[0];
+      for (int w = 1; w < 8; ++w)
+        if (s_f[w] > bb || (s_f[w] == bb && s_i[w] < ba)) { bb = s_f[w]; ba = s_i[w]; }
+      out->m = bb;
+      out->arg = ba;
+      out->Z = 0.0;
+    }
+    return;
+  }
+  const float k2 = a.k2;
+  float m = -INFINITY, s = 0.f, c = 0.f;  // Kahan: true sum ~ s - c
+  for (int u0 = tid; u0 < nunits; u0 += 4 * 256) {
+    float x[4][8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int unit = u0 + j * 256;
+      if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
+      else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[j][k] = -INFINITY;
+      }
+    }
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) cm = fmaxf(cm, x[j][k]);
+    if (cm > m) {
+      const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
+      s *= f;
+      c *= f;
+      m = cm;
+    }
+    if (m != -INFINITY) {
+      float t4[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = ex2((x[j][k] - m) * k2);
+        t4[j] = sum8(w);
+      }
+      const float chunk = (t4[0] + t4[1]) + (t4[2] + t4[3]);
+      const float y = chunk - c;
+      const float t = s + y;
+      c = (t - s) - y;
+      s = t;
+    }
+  }
+  float M = warp_max(m);
+  if (lane == 0) s_f[warp] = M;
+  __syncthreads();
+  M = s_f[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_f[w]);
+  const float mine = (m == -INFINITY) ? 0.f : (s - c) * ex2((m - M) * k2);
+  dfloat acc = warp_sum_df(df_make(mine));
+  if (lane == 0) { s_hi[warp] = acc.hi; s_lo[warp] = acc.lo; }
+  __syncthreads();
+  if (tid == 0) {
+    dfloat tot = {s_hi[0], s_lo[0]};
+    for (int w = 1; w < 8; ++w) tot = df_add(tot, dfloat{s_hi[w], s_lo[w]});
+    out->m = M;
+    out->arg = -1;
+    out->Z = df_to_d(tot);
+  }
+}
+
+// ---- 3. walk -------------------------------------------------------------------------------
+constexpr int kWalkThreads = 1024;
+constexpr int kWalkWarps = kWalkThreads / 32;
+
+struct WalkSmem {
+  int16_t par[SPEC_MAX_TREE];
+  int16_t first_child[SPEC_MAX_TREE];
+  int16_t next_sib[SPEC_MAX_TREE];
+  int32_t path[SPEC_MAX_TREE];
+  dfloat wtot[kWalkWarps];
+  dfloat wpre[kWalkWarps];
+  int wlast[kWalkWarps];
+  float fred[kWalkWarps];
+  int ired[kWalkWarps];
+  double total, theta;
+  int wsel, found, fallback;
+  int decision;
+};
+
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <typename TT>
+__device__ float block_row_max(const TT* row, int V, WalkSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int full = V / 8, nunits = (V + 7) / 8;
+  float m = -INFINITY;
+  for (int unit = tid; unit < nunits; unit += kWalkThreads) {
+    float x[8];
+    load8(row, unit, V, full, -INFINITY, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m = fmaxf(m, x[k]);
+  }
+  m = warp_max(m);
+  if (lane == 0) sh.fred[warp] = m;
+  __syncthreads();
+  float M = sh.fred[0];
+  for (int w = 1; w < kWalkWarps; ++w) M = fmaxf(M, sh.fred[w]);
+  __syncthreads();
+  return M;
+}
+
+template <typename TT>
+__device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int full = V / 8, nunits = (V + 7) / 8;
+  float best = -INFINITY;
+  int arg = 0x7fffffff;
+  for (int unit = tid; unit < nunits; unit += kWalkThreads) {
+    float x[8];
+    load8(row, unit, V, full, -INFINITY, x);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (x[k] > best) { best = x[k]; arg = unit * 8 + k; }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float ob = __shfl_xor_sync(0xffffffffu, best, off);
+    int oa = __shfl_xor_sync(0xffffffffu, arg, off);
+    if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+  }
+  if (lane == 0) { sh.fred[warp] = best; sh.ired[warp] = arg; }
+  __syncthreads();
+  float bb = sh.fred[0];
+  int ba = sh.ired[0];
+  for (int w = 1; w < kWalkWarps; ++w)
+    if (sh.fred[w] > bb || (sh.fred[w] == bb && sh.ired[w] < ba)) { bb = sh.fred[w]; ba = sh.ired[w]; }
+  __syncthreads();
+  return ba;
+}
+
+// Element weights of the distribution being summed / sampled.
+struct WeightFn {
+  bool residual, probs;
+  float mt, md, k2, invZt, invZd, C;
+  template <typename TT, typename TD>
+  __device__ __forceinline__ void operator()(const TT* trow, const TD* drow, int unit, int V,
+                                             int full, float (&w)[8]) const {
+    float xt[8];
+    load8(trow, unit, V, full, -INFINITY, xt);
+    if (!residual) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = ex2((xt[k] - mt) * k2);
+      return;
+    }
+    float xd[8];
+    load8(drow, unit, V, full, probs ? 0.f : -INFINITY, xd);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float p = ex2((xt[k] - mt) * k2) * invZt;
+      const float q = probs ? xd[k] : ex2((xd[k] - md) * k2) * invZd;
+      w[k] = fmaxf(0.f, p - C * q);
+    }
+  }
+};
+
+// Block-wide pass over the vocabulary: total mass of the weights (returned in `total`) and,
+// when `search`, the smallest token x with sum_{y<=x} w(y) > u * total (-1 if the weights are
+// all zero).  Warp w owns units [w*upw, (w+1)*upw) so warp order is token order.
+template <typename TT, typename TD>
+__device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn, bool search,
+                          double u, WalkSmem& sh, double& total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int full = V / 8, nunits = (V + 7) / 8;
+  const int upw = ((nunits + kWalkWarps - 1) / kWalkWarps + 31) / 32 * 32;
+  const int ub = warp * upw;
+  const int ue = min(ub + upw, nunits);
+  dfloat acc = df_make(0.f);
+  int last = -1;
+  for (int base = ub; base < ue; base += 32) {
+    const int unit = base + lane;
+    float s = 0.f;
+    if (unit < ue) {
+      float w[8];
+      fn(trow, drow, unit, V, full, w);
+      s = sum8(w);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w[k] > 0.f) last = unit * 8 + k;
+    }
+    acc = df_add_f(acc, s);
+  }
+  const dfloat wt = warp_sum_df(acc);
+  last = warp_max_i(last);
+  if (lane == 0) { sh.wtot[warp] = wt; sh.wlast[warp] = last; }
+  __syncthreads();
+  if (tid == 0) {
+    dfloat run = df_make(0.f);
+    int fb = -1;
+    for (int w = 0; w < kWalkWarps; ++w) {
+      sh.wpre[w] = run;
+      run = df_add(run, sh.wtot[w]);
+      fb = max(fb, sh.wlast[w]);
+    }
+    const double tot = df_to_d(run);
+    sh.total = tot;
+    sh.fallback = fb;
+    sh.wsel = -1;
+    sh.found = fb;
+    if (search && tot > 0.0) {
+      const double theta = u * tot;
+      sh.theta = theta;
+      for (int w = 0; w < kWalkWarps; ++w) {
+        if (df_to_d(df_add(sh.wpre[w], sh.wtot[w])) > theta) { sh.wsel = w; break; }
+      }
+    }
+  }
+  __syncthreads();
+  total = sh.total;
+  if (!search) {
+    __syncthreads();
+    return -1;
+  }
+  const int ws = sh.wsel;
+  if (ws >= 0 && warp == ws) {
+    dfloat base_acc = sh.wpre[ws];
+    const double theta = sh.theta;
+    for (int base = ub; base < ue; base += 32) {
+      const int unit = base + lane;
+      float w[8];
+      float s = 0.f;
+      if (unit < ue) {
+        fn(trow, drow, unit, V, full, w);
+        s = sum8(w);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) w[k] = 0.f;
+      }
+      const dfloat incl = warp_scan_df(df_make(s), lane);
+      dfloat excl = df_shfl_up(incl, 1);
+      if (lane == 0) excl = df_make(0.f);
+      const bool cross = df_to_d(df_add(base_acc, incl)) > theta;
+      const unsigned mask = __ballot_sync(0xffffffffu, cross);
+      if (mask) {
+        if (lane == __ffs(mask) - 1) {
+          dfloat cum = df_add(base_acc, excl);
+          int tok = -1, lastpos = -1;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            cum = df_add_f(cum, w[k]);
+            if (w[k] > 0.f) lastpos = unit * 8 + k;
+            if (tok < 0 && df_to_d(cum) > theta) tok = unit * 8 + k;
+          }
+          sh.found = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : sh.fallback);
+        }
+        break;
+      }
+      const dfloat it_tot = {__shfl_sync(0xffffffffu, incl.hi, 31),
+                             __shfl_sync(0xffffffffu, incl.lo, 31)};
+      base_acc = df_add(base_acc, it_tot);
+    }
+  }
+  __syncthreads();
+  const int tok = sh.found;
+  __syncthreads();
+  return tok;
+}
+
+template <typename TT, typename TD>
+__global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
+  __shared__ WalkSmem sh;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int st = a.req_status[r];
+  int32_t* path_row = a.path + size_t(r) * a.max_path;
+  int32_t* tok_row = a.out_tokens + size_t(r) * a.max_path;
+  if (st != 0) {
+    for (int k = tid; k < a.max_path; k += kWalkThreads) { path_row[k] = -1; tok_row[k] = -1; }
+    if (tid == 0) {
+      a.out_len[r] = 0;
+      a.n_acc[r] = -1;
+      if (a.rejections) a.rejections[r] = 0;
+    }
+    return;
+  }
+  const int o = a.node_offset[r];
+  const int T = a.node_offset[r + 1] - o;
+  for (int i = tid; i < T; i += kWalkThreads) {
+    sh.par[i] = int16_t(a.parent[o + i]);
+    sh.first_child[i] = -1;
+    sh.next_sib[i] = -1;
+  }
+  __syncthreads();
+  for (int i = tid; i < T; i += kWalkThreads) {
+    if (i > 0) {
+      const int p = sh.par[i];
+      int nxt = -1;
+      for (int k = i + 1; k < T; ++k)
+        if (sh.par[k] == p) { nxt = k; break; }
+      sh.next_sib[i] = int16_t(nxt);
+      // first child of p: the sibling with no smaller sibling
+      bool first = true;
+      for (int k = p + 1; k < i; ++k)
+        if (sh.par[k] == p) { first = false; break; }
+      if (first) sh.first_child[p] = int16_t(i);
+    }
+  }
+  if (tid == 0) sh.path[0] = 0;
+  __syncthreads();
+
+  const TT* target = reinterpret_cast<const TT*>(a.target);
+  const TD* draft = reinterpret_cast<const TD*>(a.draft);
+  const bool greedy = a.tau == 0.f;
+  int node = 0, npath = 1, rejections = 0, final_tok = -1;
+  while (true) {
+    const TT* trow = target + size_t(o + node) * a.tld;
+    const int fc = sh.first_child[node];
+    if (greedy) {
+      const int best = fc < 0 ? block_row_argmax(trow, a.V, sh) : a.tstat[o + node].arg;
+      int acc = -1, rej = 0;
+      for (int c = fc; c >= 0; c = sh.next_sib[c]) {
+        if (a.tokens[o + c] == best) { acc = c; break; }
+        ++rej;
+      }
+      rejections += rej;
+      if (acc >= 0) {
+        if (tid == 0) sh.path[npath] = acc;
+        ++npath;
+        node = acc;
+        continue;
+      }
+      final_tok = best;
+      break;
+    }
+    const float u_samp = a.uniforms[2 * size_t(o + node) + 1];
+    if (fc < 0) {  // leaf: bonus token from p_leaf
+      WeightFn fn{};
+      fn.residual = false;
+      fn.mt = block_row_max(trow, a.V, sh);
+      fn.k2 = a.k2;
+      double tot;
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, double(u_samp), sh, tot);
+      break;
+    }
+    const RowStat ts = a.tstat[o + node];
+    const int drow_i = a.draft_row[o + node];
+    const TD* drow = draft + size_t(drow_i) * a.dld;
+    RowStat ds = {0.f, 0, 1.0};
+    if (!a.probs) ds = a.dstat[drow_i];
+    WeightFn res{};
+    res.residual = true;
+    res.probs = a.probs != 0;
+    res.mt = ts.m;
+    res.md = ds.m;
+    res.k2 = a.k2;
+    res.invZt = float(1.0 / ts.Z);
+    res.invZd = float(1.0 / ds.Z);
+    double C = 0.0, Nk = 1.0;
+    int accepted = -1;
+    bool from_p = false;
+    for (int c = fc; c >= 0; c = sh.next_sib[c]) {
+      if (tid == 0) {
+        const int tok = a.tokens[o + c];
+        const float xt = elem<TT>::load1(trow + tok);
+        const float xd = elem<TD>::load1(drow + tok);
+        double num, den;
+        const bool first_test = (C == 0.0) || !a.residual_rule;
+        if (!a.probs && first_test) {
+          // p/q = exp(((xt - mt) - (xd - md)) / tau) * Zd / Zt
+          num = double(expf(((xt - ts.m) - (xd - ds.m)) * a.inv_tau)) * ds.Z;
+          den = ts.Z;
+        } else {
+          const double p = double(expf((xt - ts.m) * a.inv_tau)) / ts.Z;
+          const double q = a.probs ? double(xd) : double(expf((xd - ds.m) * a.inv_tau)) / ds.Z;
+          num = first_test ? p : fmax(0.0, p - C * q);
+          den = first_test ? q : Nk * q;
+        }
+        const double ratio = den > 0.0 ? num / den : (num > 0.0 ? INFINITY : 0.0);
+        const float u_acc = a.uniforms[2 * size_t(o + c)];
+        sh.decision = double(u_acc) < ratio;
+      }
+      __syncthreads();
+      const bool acc = sh.decision != 0;
+      __syncthreads();
+      if (acc) { accepted = c; break; }
+      ++rejections;
+      if (a.residual_rule) {
+        C = C + Nk;
+        res.C = float(C);
+        double tot;
+        vocab_pass(trow, drow, a.V, res, false, 0.0, sh, tot);
+        Nk = tot;
+        if (!(Nk > 0.0)) { from_p = true; break; }
+      }
+    }
+    if (accepted >= 0) {
+      if (tid == 0) sh.path[npath] = accepted;
+      ++npath;
+      node = accepted;
+      continue;
+    }
+    if (!from_p) {
+      res.C = float(a.residual_rule ? C : 1.0);
+      double tot;
+      final_tok = vocab_pass(trow, drow, a.V, res, true, double(u_samp), sh, tot);
+      if (!(tot > 0.0)) from_p = true;
+    }
+    if (from_p) {
+      WeightFn fn{};
+      fn.residual = false;
+      fn.mt = ts.m;
+      fn.k2 = a.k2;
+      double tot;
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, double(u_samp), sh, tot);
+    }
+    break;
+  }
+  __syncthreads();
+  for (int k = tid; k < a.max_path; k += kWalkThreads) {
+    if (k < npath) {
+      path_row[k] = sh.path[k];
+      tok_row[k] = (k + 1 < npath) ? a.tokens[o + sh.path[k + 1]] : final_tok;
+    } else {
+      path_row[k] = -1;
+      tok_row[k] = -1;
+    }
+  }
+  if (tid == 0) {
+    a.out_len[r] = npath;
+    a.n_acc[r] = npath - 1;
+    if (a.rejections) a.rejections[r] = rejections;
+  }
+}
+
+struct VerifyWs {
+  size_t tstat, dstat, t_need, d_need, total;
+};
+
+static VerifyWs verify_ws_layout(int N, int R) {
+  VerifyWs w;
+  size_t off = 0;
+  w.tstat = off; off = align_up(off + sizeof(RowStat) * size_t(N > 0 ? N : 1), 256);
+  w.dstat = off; off = align_up(off + sizeof(RowStat) * size_t(R > 0 ? R : 1), 256);
+  w.t_need = off; off = align_up(off + size_t(N > 0 ? N : 1), 256);
+  w.d_need = off; off = align_up(off + 4 * size_t(R > 0 ? R : 1), 256);
+  w.total = off;
+  return w;
+}
+
+template <typename TT, typename TD>
+static void launch_verify(const VerifyDev& d, bool run_rows, cudaStream_t s) {
+  if (run_rows) verify_rows_kernel<TT><<<d.N + (d.probs ? 0 : d.R), 256, 0, s>>>(d);
+  verify_walk_kernel<TT, TD><<<d.B, kWalkThreads, 0, s>>>(d);
+}
+
+}  // namespace spec
+
+extern "C" {
+
+size_t spec_verify_workspace_size(const spec_verify_params* p) {
+  if (!p) return 0;
+  return spec::verify_ws_layout(p->N, p->R).total;
+}
+
+spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
+                          spec_stream_t stream) {
+  using namespace spec;
+  if (!p) return SPEC_ERR_INVALID_ARG;
+  if (p->B < 1 || p->N < 0 || p->R < 0 || p->V < 1 || p->T_max < 1 ||
+      p->T_max > SPEC_MAX_TREE || p->max_path < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (!(p->tau >= 0.f) || !isfinite(p->tau)) return SPEC_ERR_INVALID_ARG;
+  if (p->logits_dtype != SPEC_F32 && p->logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (p->draft_kind != SPEC_DRAFT_LOGITS && p->draft_kind != SPEC_DRAFT_PROBS)
+    return SPEC_ERR_INVALID_ARG;
+  if (p->sibling_rule != SPEC_SIBLING_RESIDUAL && p->sibling_rule != SPEC_SIBLING_INDEPENDENT)
+    return SPEC_ERR_INVALID_ARG;
+  if (!p->node_offset || !p->req_status || !p->out_tokens || !p->out_len || !p->path ||
+      !p->n_acc)
+    return SPEC_ERR_INVALID_ARG;
+  if (p->N > 0 && (!p->target || !p->tokens || !p->parent || !p->depth || !p->is_internal ||
+                   !p->uniforms || !p->draft_row))
+    return SPEC_ERR_INVALID_ARG;
+  const size_t tes = p->logits_dtype == SPEC_BF16 ? 2 : 4;
+  const size_t des = p->draft_kind == SPEC_DRAFT_PROBS ? 4 : tes;
+  if (p->target_ld < p->V || (size_t(p->target_ld) * tes) % 16 != 0) return SPEC_ERR_INVALID_ARG;
+  if (p->target && !aligned16(p->target)) return SPEC_ERR_INVALID_ARG;
+  if (p->R > 0) {
+    if (!p->draft || !aligned16(p->draft)) return SPEC_ERR_INVALID_ARG;
+    if (p->draft_ld < p->V || (size_t(p->draft_ld) * des) % 16 != 0) return SPEC_ERR_INVALID_ARG;
+  }
+  const VerifyWs lay = verify_ws_layout(p->N, p->R);
+  if (!workspace || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return SPEC_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  VerifyDev d;
+  d.target = p->target;
+  d.draft = p->draft;
+  d.tld = p->target_ld;
+  d.dld = p->draft_ld;
+  d.B = p->B; d.N = p->N; d.R = p->R; d.V = p->V; d.T_max = p->T_max; d.max_path = p->max_path;
+  d.tau = p->tau;
+  d.k2 = p->tau > 0.f ? float(1.4426950408889634 / double(p->tau)) : 0.f;
+  d.inv_tau = p->tau > 0.f ? 1.0f / p->tau : 0.f;
+  d.probs = p->draft_kind == SPEC_DRAFT_PROBS;
+  d.residual_rule = p->sibling_rule == SPEC_SIBLING_RESIDUAL;
+  d.draft_row = p->draft_row; d.tokens = p->tokens; d.parent = p->parent;
+  d.node_offset = p->node_offset; d.depth = p->depth; d.is_internal = p->is_internal;
+  d.uniforms = p->uniforms; d.req_status = p->req_status; d.out_tokens = p->out_tokens;
+  d.out_len = p->out_len; d.path = p->path; d.n_acc = p->n_acc; d.rejections = p->rejections;
+  d.tstat = reinterpret_cast<RowStat*>(ws + lay.tstat);
+  d.dstat = reinterpret_cast<RowStat*>(ws + lay.dstat);
+  d.t_need = reinterpret_cast<uint8_t*>(ws + lay.t_need);
+  d.d_need = reinterpret_cast<uint32_t*>(ws + lay.d_need);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws + lay.t_need, 0, lay.total - lay.t_need, s) != cudaSuccess)
+    return launch_status();
+  verify_prep_kernel<<<p->B, 256, 0, s>>>(d);
+  const bool run_rows = p->N > 0;
+  if (p->logits_dtype == SPEC_BF16) {
+    if (d.probs) launch_verify<__nv_bfloat16, float>(d, run_rows, s);
+    else launch_verify<__nv_bfloat16, __nv_bfloat16>(d, run_rows, s);
+  } else {
+    launch_verify<float, float>(d, run_rows, s);
+  }
+  return launch_status();
+}
+
+}  // extern "C"

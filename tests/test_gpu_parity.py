@@ -1,0 +1,193 @@
+"""GPU <-> oracle parity through the C-ABI (spec_tree_build, spec_tree_attention, spec_verify,
+spec_kv_compact) on the five workloads at oracle-friendly sizes, the edge cases, injected data
+errors and guard bands."""
+import numpy as np
+import pytest
+import torch
+
+import parity_util as PU
+from speculative_decoding_draft_tree_gb300 import binding as B
+from speculative_decoding_draft_tree_gb300 import workloads as W
+from speculative_decoding_draft_tree_gb300.api import VerifyStep
+
+pytestmark = pytest.mark.gpu
+
+
+def _sync():
+    torch.cuda.synchronize()
+
+
+def run_and_check(w, rule=B.SPEC_SIBLING_RESIDUAL, attention=True, rows=None):
+    snap = PU.snapshot(w)
+    step = VerifyStep(w, sibling_rule=rule)
+    step.tree_build()
+    _sync()
+    PU.check_tree(w, step, snap)
+    if attention:
+        step.attention()
+        _sync()
+        PU.check_attention(w, step, snap, rows)
+    step.verify()
+    _sync()
+    orc = PU.oracle_verify(w, snap, rule)
+    draws, exempt = PU.check_verify(w, step, orc)
+    kb = PU.cache_region(w.k_cache, w, snap, range(w.B))
+    vb = PU.cache_region(w.v_cache, w, snap, range(w.B))
+    step.compact()
+    _sync()
+    PU.check_compact(w, step, snap, kb, vb)
+    return step, orc, draws, exempt
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.0])
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_verify_small_configs(cid, tau):
+    w = W.make_config(cid, scale="small", device="cuda", tau=tau, num_layers=2)
+    run_and_check(w, attention=False)
+
+
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_attention_small_configs(cid):
+    w = W.make_config(cid, scale="small", device="cuda")
+    run_and_check(w, attention=True)
+
+
+@pytest.mark.parametrize("sigma", [0.5, 2.0])
+def test_chain_noise_sweep(sigma):
+    w = W.make_config(2, scale="small", device="cuda", sigma=sigma)
+    run_and_check(w, attention=False)
+
+
+@pytest.mark.parametrize("cid", [3, 4, 5])
+def test_independent_sibling_rule(cid):
+    w = W.make_config(cid, scale="small", device="cuda")
+    run_and_check(w, rule=B.SPEC_SIBLING_INDEPENDENT, attention=False)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_draft_probabilities(dtype):
+    w = W.chain_workload(B=5, gamma=4, V=2003, dtype=dtype, H_q=4, H_kv=4,
+                         d=64 if dtype == "f32" else 128, prefix=40, tau=1.0, target_std=2.0,
+                         noise_std=1.0, device="cuda", draft_kind=W.DRAFT_PROBS)
+    run_and_check(w, attention=False)
+
+
+@pytest.mark.parametrize("tau", [0.7, 1.6])
+def test_other_temperatures(tau):
+    w = W.make_config(4, scale="small", device="cuda", tau=tau)
+    run_and_check(w, attention=False)
+
+
+@pytest.mark.parametrize("P", [0, 15, 16, 17, 31])
+def test_single_token_trees_and_block_boundaries(P):
+    # T = 1 (plain decode), prefix lengths at block boundaries, odd vocabulary
+    w = W.chain_workload(B=3, gamma=0, V=1001, dtype="bf16", H_q=8, H_kv=2, d=128, prefix=P,
+                         tau=1.0, target_std=3.0, noise_std=1.0, device="cuda", T_max=4)
+    run_and_check(w, attention=True)
+
+
+def test_chain_block_boundaries_f32():
+    w = W.chain_workload(B=4, gamma=5, V=999, dtype="f32", H_q=4, H_kv=2, d=64,
+                         prefix=[0, 15, 16, 33], tau=1.0, target_std=2.0, noise_std=1.0,
+                         device="cuda")
+    run_and_check(w, attention=True)
+
+
+def _corrupt_workload():
+    w = W.make_config(5, scale="small", device="cuda", num_layers=2)
+    no = w.node_offset.cpu().numpy()
+    par = w.parent.clone()
+    par[no[0] + 3] = 3                       # request 0: parent[i] == i
+    w.parent.copy_(par)
+    w.tokens[no[1] + 2] = w.V                # request 1: token id >= V
+    # request 2: an internal node whose draft row is out of range
+    internal_local = int(torch.nonzero(w.draft_row[no[2]:no[3]] >= 0)[1])
+    w.draft_row[no[2] + internal_local] = w.R + 7
+    # request 3: a block-table entry of the tree region out of range
+    P3 = int(w.prefix_len[3])
+    w.block_table[3, P3 // w.bs] = w.k_cache.shape[1] + 5
+    return w
+
+
+def test_injected_data_errors():
+    w = _corrupt_workload()
+    snap = PU.snapshot(w)
+    step = VerifyStep(w)
+    step.run()
+    _sync()
+    st = PU.np_(step.req_status)
+    assert st[0] & B.REQ_BITS["BAD_PARENT"]
+    assert st[1] & B.REQ_BITS["BAD_TOKEN"]
+    assert st[2] & B.REQ_BITS["BAD_DRAFT_ROW"]
+    assert st[3] & B.REQ_BITS["BAD_BLOCK"]
+    assert (PU.np_(step.out_len)[:3] == 0).all()
+    assert (PU.np_(step.n_acc)[:3] == -1).all()
+    # the rolled-back requests keep their prefix length
+    assert PU.np_(step.new_kv_len)[:3].tolist() == snap["prefix_len"][:3].tolist()
+    # the library is still usable afterwards
+    w2 = W.make_config(5, scale="small", device="cuda")
+    run_and_check(w2, attention=False)
+
+
+def test_oversize_tree_flagged():
+    w = W.make_config(5, scale="small", device="cuda")
+    sizes = w.tree_sizes()
+    w.T_max = 40
+    w.max_path = 40
+    step = VerifyStep(w)
+    step.tree_build()
+    step.verify()
+    _sync()
+    st = PU.np_(step.req_status)
+    for r, T in enumerate(sizes):
+        assert bool(st[r] & B.REQ_BITS["BAD_SIZE"]) == (T > 40)
+
+
+def test_host_validation_errors():
+    w = W.make_config(2, scale="small", device="cuda")
+    step = VerifyStep(w)
+    bad = B.verify_params(w.target, w.draft, w.draft_kind, w.draft_row, w.tokens, w.parent,
+                          w.node_offset, step.depth, step.is_internal, w.uniforms, -1.0, w.V,
+                          w.T_max, w.max_path, step.req_status, step.out_tokens, step.out_len,
+                          step.path, step.n_acc)
+    with pytest.raises(B.SpecError, match="INVALID_ARG"):
+        B.spec_verify(bad, step.ver_ws)
+    with pytest.raises(B.SpecError, match="INVALID_ARG"):
+        B.spec_verify(step.ver, step.ver_ws[:16])   # workspace too small
+    p = B.attention_params(w.q, step.k_layer0, step.v_layer0, w.block_table, w.prefix_len,
+                           w.node_offset, step.anc_mask, w.T_max, step.o, None, step.req_status)
+    p.q = p.q + 2                                       # misaligned
+    with pytest.raises(B.SpecError, match="INVALID_ARG"):
+        B.spec_tree_attention(p, step.attn_ws)
+    with pytest.raises(B.SpecError, match="INVALID_ARG"):
+        B.spec_tree_build(w.parent, w.node_offset, w.prefix_len, 300, step.depth, step.pos_id,
+                          step.anc_mask, step.is_internal, step.req_status)
+
+
+def test_guard_bands_untouched():
+    w = W.make_config(4, scale="small", device="cuda")
+    step = VerifyStep(w)
+    pad = 1024
+    sentinel = -777
+    big = {}
+    for name in ("out_tokens", "path", "out_len", "n_acc", "rejections", "new_kv_len",
+                 "blocks_in_use", "slot_map", "depth", "pos_id"):
+        t = getattr(step, name)
+        buf = torch.full((t.numel() + 2 * pad,), sentinel, dtype=t.dtype, device=t.device)
+        view = buf[pad:pad + t.numel()].view(t.shape)
+        big[name] = buf
+        setattr(step, name, view)
+    # rebuild parameter blocks over the guarded views
+    step.ver = B.verify_params(w.target, w.draft, w.draft_kind, w.draft_row, w.tokens, w.parent,
+                               w.node_offset, step.depth, step.is_internal, w.uniforms, w.tau,
+                               w.V, w.T_max, w.max_path, step.req_status, step.out_tokens,
+                               step.out_len, step.path, step.n_acc, step.rejections)
+    step.comp = B.compact_params(w.k_cache, w.v_cache, w.block_table, w.prefix_len, step.path,
+                                 step.n_acc, step.req_status, step.new_kv_len, step.slot_map,
+                                 step.blocks_in_use, w.max_path)
+    step.tree_build()
+    step.verify()
+    step.compact()
+    _sync()
+    for name, buf in big.items():
+        assert (buf[:pad] == sentinel).all() and (buf[-pad:] == sentinel).all(), name

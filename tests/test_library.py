@@ -1,0 +1,55 @@
+"""CPU-side checks of the C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+function include/spec_verify.h declares, and the Python structs match the C layouts."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_draft_tree_gb300 import binding as B
+from speculative_decoding_draft_tree_gb300 import build
+
+HEADER = os.path.join(build.INCLUDE, "spec_verify.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return B.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"spec_tree_build", "spec_tree_attention", "spec_verify", "spec_kv_compact"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B.EXPORTS) == set(names)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "SPEC_OK"), (1, "SPEC_ERR_INVALID_ARG"), (2, "SPEC_ERR_UNSUPPORTED"),
+                       (3, "SPEC_ERR_CUDA")]:
+        assert lib.spec_status_string(code).decode() == name
+
+
+def test_struct_layouts_match_header():
+    # sizes follow from the C declarations (natural alignment on LP64)
+    assert ctypes.sizeof(B.SpecAttnParams) == 44 + 4 + 10 * 8
+    assert ctypes.sizeof(B.SpecVerifyParams) == 28 + 4 + 16 + 12 + 4 + 15 * 8
+    assert ctypes.sizeof(B.SpecCompactParams) == 36 + 4 + 8 + 10 * 8
+
+
+def test_host_validation_without_gpu(lib):
+    # null parameter blocks are rejected before any CUDA call
+    assert lib.spec_verify(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_tree_attention(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_kv_compact(None, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_tree_build(None, None, None, 0, 0, 0, None, None, None, None, None,
+                               None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_workspace_size(None) == 0
