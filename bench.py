@@ -1,0 +1,350 @@
+"""Benchmark of one draft-tree verification round on GB300.
+
+A step = one pass of the whole hot path over one batch of synthetic requests:
+spec_tree_build + spec_tree_attention (one layer) + spec_verify + spec_kv_compact, all through
+the C-ABI library.  Default workload: the Leviathan chain (16 requests x (1 root + 5 drafts),
+vocab 32000, 32 x d128 MHA heads, 2048 cached tokens per request, bf16, tau = 1).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload CID] [--impl reference]
+
+Prints ONE JSON line (rank 0).  `value` is verified tree tokens per second over all ranks
+(device time of the K timed steps, max over ranks); `e2e` repeats the measurement through
+VerifyStep.run_from_host with the round's inputs in pinned host memory and the accepted tokens
+copied back inside the timed region.  `roofline` is for the tree-attention call (the dominant
+kernel), with algorithmic bytes = the KV of every request read once + Q + O + LSE.
+`--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = 2
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-requests", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_description(w, cid):
+    from speculative_decoding_draft_tree_gb300 import workloads as W
+    sizes = w.tree_sizes()
+    P = w.prefix_len.cpu().tolist()
+    return {
+        "workload": W.CONFIG_NAMES[cid],
+        "batch_requests": w.B,
+        "tree_tokens_per_step": int(sum(sizes)),
+        "drafts_per_step": int(sum(sizes) - w.B),
+        "vocab": w.V,
+        "heads": f"{w.H_q}q/{w.H_kv}kv x d{w.d}",
+        "prefix_len": P[0] if len(set(P)) == 1 else f"{min(P)}..{max(P)}",
+        "kv_block": w.bs,
+        "tau": w.tau,
+        "tree": w.meta.get("kind"),
+        "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MB write)",
+    }
+
+
+def attention_bytes(w):
+    """Algorithmic bytes of one tree-attention launch: each request's P + T keys of K and V for
+    every KV head read once, Q read once, O and LSE written once."""
+    es = 2 if w.dtype == "bf16" else 4
+    sizes = w.tree_sizes()
+    P = w.prefix_len.cpu().tolist()
+    kv = sum((P[r] + sizes[r]) for r in range(w.B)) * w.H_kv * w.d * es * 2
+    q_o = 2 * w.N * w.H_q * w.d * es
+    return kv + q_o + w.N * w.H_q * 4
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), power=float(parts[3]),
+                                 hw=parts[5], hwt=parts[6], swt=parts[7], swp=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        sms = sorted(r["sm"] for r in rows)
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": sms[len(sms) // 2], "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+def run_oracle_sample(w, n_req):
+    """The CPU oracle (as it stands) on the first n_req requests of the workload: tree build,
+    attention of every tree token and head, verification and compaction.  Returns seconds."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import attention as OA, compact as OC, tree as OT, verify as OV
+    no = w.node_offset.cpu().numpy()
+    P = w.prefix_len.cpu().numpy()
+    o_end = int(no[n_req])
+    parent = w.parent.cpu().numpy()[:o_end]
+    nodeoff = no[:n_req + 1]
+    q = w.q[:o_end].float().cpu().numpy()
+    nblk_need = [-(-(int(P[r]) + int(no[r + 1] - no[r])) // w.bs) for r in range(n_req)]
+    table_full = w.block_table.cpu().numpy()[:n_req]
+    used = sorted(set(int(b) for r in range(n_req) for b in table_full[r, :nblk_need[r]]))
+    remap = {b: i for i, b in enumerate(used)}
+    table = np.full_like(table_full, -1)
+    for r in range(n_req):
+        for j in range(nblk_need[r]):
+            table[r, j] = remap[int(table_full[r, j])]
+    import torch
+    idx = torch.as_tensor(used, dtype=torch.long, device=w.k_cache.device)
+    kc = w.k_cache[:, idx].float().cpu().numpy()
+    vc = w.v_cache[:, idx].float().cpu().numpy()
+    target = w.target[:o_end].float().cpu().numpy()
+    draft = w.draft.float().cpu().numpy()
+    draft_row = w.draft_row.cpu().numpy()[:o_end]
+    tokens = w.tokens.cpu().numpy()[:o_end]
+    uni = w.uniforms.cpu().numpy()[:o_end]
+    t0 = time.perf_counter()
+    tb = OT.tree_build(parent, nodeoff, P[:n_req], w.T_max)
+    OA.tree_attention(q, kc[0], vc[0], table, P[:n_req], nodeoff, parent, w.bs)
+    ver = OV.verify(target, draft, w.draft_kind, draft_row, tokens, parent, nodeoff, uni, w.tau,
+                    w.V, w.max_path, T_max=w.T_max)
+    OC.kv_compact(kc, vc, table, P[:n_req], ver["path"], ver["n_acc"], w.bs, w.max_path,
+                  status=ver["status"])
+    del tb
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, n_req=None, budget_s=15.0):
+    """Time the oracle on a bounded sample sized to about `budget_s` seconds."""
+    sizes = w.tree_sizes()
+    if n_req is None or n_req <= 0:
+        probe = run_oracle_sample(w, 1)
+        n_req = max(1, min(w.B, int(budget_s / max(probe, 1e-3))))
+    secs = run_oracle_sample(w, n_req)
+    tokens = sum(sizes[:n_req])
+    return {"value": tokens / secs, "unit": "verified tree tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n_req} of {w.B} requests ({tokens} tree tokens), full vocab and KV, "
+                      f"{secs:.1f} s single-threaded numpy fp64"}
+
+
+# ---------------------------------------------------------------------------------------------
+def main():
+    args = parse()
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    rank, world, local_rank = dist_env()
+    import torch
+    from speculative_decoding_draft_tree_gb300 import workloads as W
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w = W.make_config(args.workload, scale="full", device="cpu")
+        tokens_per_step = int(sum(w.tree_sizes()))
+        steps = []
+        n_req = args.cpu_sample_requests or None
+        for i in range(args.warmup + args.steps):
+            cb = cpu_baseline(w, n_req=n_req, budget_s=4.0)
+            n_req = int(cb["sample"].split(" of ")[0])
+            if i >= args.warmup:
+                steps.append(cb["value"])
+        value = sum(steps) / len(steps)
+        cb["value"] = value
+        line = {"impl": "reference", "metric": "verified tree tokens/s", "value": value,
+                "unit": "verified tree tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1e3 * tokens_per_step / value,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": workload_description(w, args.workload),
+                "cpu_baseline": cb,
+                "e2e": {"value": value, "unit": "verified tree tokens/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch.distributed as dist
+    from speculative_decoding_draft_tree_gb300 import binding
+    from speculative_decoding_draft_tree_gb300.api import VerifyStep
+
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    binding.load_library(build_if_missing=True)
+    dev = torch.device("cuda", local_rank)
+    # weak scaling: every rank verifies its own batch of the same shape
+    w = W.make_config(args.workload, scale="full", device=dev,
+                      seeds=dict(logits=1 + 1000 * rank, drafting=2 + 1000 * rank,
+                                 qkv=3 + 1000 * rank))
+    tokens_per_step = int(sum(w.tree_sizes()))
+    step = VerifyStep(w)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        step.run()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        s0, a0, a1, s1 = ev[i]
+        s0.record(stream)
+        step.tree_build()
+        a0.record(stream)
+        step.attention()
+        a1.record(stream)
+        step.verify()
+        step.compact()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    t_total = sum(step_ms) / 1e3
+    t_attn = sum(attn_ms) / len(attn_ms) / 1e3
+    if world > 1:
+        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_total = float(tt.item())
+    ms_per_step = 1e3 * t_total / args.steps
+    value = world * tokens_per_step * args.steps / t_total
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = step.pinned_host_inputs()
+        host_out = step.host_output_buffers()
+        for _ in range(2):
+            step.run_from_host(host_in, host_out)
+        torch.cuda.synchronize()
+        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            e_ev[i][0].record(stream)
+            step.run_from_host(host_in, host_out)
+            e_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_e2e = sum(a.elapsed_time(b) for a, b in e_ev) / 1e3
+        if world > 1:
+            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        e2e = {"value": world * tokens_per_step * args.steps / t_e2e,
+               "unit": "verified tree tokens/s",
+               "h2d_bytes_per_step": VerifyStep.bytes_of(host_in),
+               "d2h_bytes_per_step": VerifyStep.bytes_of(host_out),
+               "ms_per_step": 1e3 * t_e2e / args.steps}
+
+    if rank != 0:
+        dist.destroy_process_group() if world > 1 else None
+        return
+    peak, peak_kind = measured_peaks()
+    abytes = attention_bytes(w)
+    achieved = abytes / t_attn / 1e9
+    out_len = step.out_len.cpu()
+    roofline = {"bound": "hbm", "kernel": "spec_tree_attention (prep + tcgen05 main + merge)",
+                "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": peak_kind, "algorithmic_bytes": abytes,
+                "us_per_launch": round(t_attn * 1e6, 2)}
+    cb = None
+    if not args.no_cpu_baseline:
+        w_cpu = W.make_config(args.workload, scale="full", device="cpu")
+        cb = cpu_baseline(w_cpu, n_req=args.cpu_sample_requests or None)
+    line = {
+        "metric": "verified tree tokens/s", "value": round(value, 1),
+        "unit": "verified tree tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": workload_description(w, args.workload),
+        "requests_per_s": round(world * w.B * args.steps / t_total, 1),
+        "accepted_tokens_per_request": round(float(out_len.float().mean()), 3),
+        "roofline": roofline, "cpu_baseline": cb, "e2e": e2e,
+        "clocks": clocks, "gpu_launches": 8 * args.steps,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

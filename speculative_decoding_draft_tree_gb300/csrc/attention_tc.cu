@@ -41,15 +41,19 @@ constexpr int kD = 128;
 constexpr int kBS = 16;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;               // 4 control warps + 8 softmax warps
 constexpr int kAtom = 16384;                  // 128 rows x 128 B
 constexpr int kTile = 2 * kAtom;              // 128 x 128 bf16
+constexpr int kKStages = 3;                   // K tiles are released right after QK^T
+constexpr int kVStages = 2;                   // V tiles are released after PV
 constexpr int kSmemQ = 0;
-constexpr int kSmemK = kSmemQ + kTile;        // 2 stages
-constexpr int kSmemV = kSmemK + 2 * kTile;    // 2 stages
-constexpr int kSmemP = kSmemV + 2 * kTile;
+constexpr int kSmemK = kSmemQ + kTile;
+constexpr int kSmemV = kSmemK + kKStages * kTile;
+constexpr int kSmemP = kSmemV + kVStages * kTile;
 constexpr int kSmemBar = kSmemP + kTile;
-constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // barriers + alignment slack
+constexpr int kSmemRed = kSmemBar + 256;      // [2 buffers][2 halves][128 rows] fp32 exchange
+constexpr int kSmemEnd = kSmemRed + 2048;
+constexpr int kSmemBytes = 232448;            // the per-CTA maximum; the slack aligns the base
 constexpr long long kWaitLimit = 4000000000LL;     // clock cycles (~2 s)
 constexpr int kSplitMinTiles = 4;
 constexpr int kItemsPerSm = 4;
@@ -284,34 +288,43 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kSmemBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;     // [2]
-  uint64_t* v_full = bars + 4;     // [2]
-  uint64_t* kv_empty = bars + 6;   // [2]
-  uint64_t* s_full = bars + 8;     // [2]
-  uint64_t* s_free = bars + 10;    // [2]
-  uint64_t* p_full = bars + 12;
-  uint64_t* pv_done = bars + 13;
-  uint64_t* o_free = bars + 14;
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
-  int* s_abort = reinterpret_cast<int*>(bars + 17);
+  uint64_t* k_full = bars + 2;     // [kKStages]
+  uint64_t* k_empty = bars + 5;    // [kKStages]
+  uint64_t* v_full = bars + 8;     // [kVStages]
+  uint64_t* v_empty = bars + 10;   // [kVStages]
+  uint64_t* s_full = bars + 12;    // [2]
+  uint64_t* s_free = bars + 14;    // [2]
+  uint64_t* p_full = bars + 16;
+  uint64_t* pv_done = bars + 17;
+  uint64_t* o_free = bars + 18;
+  uint64_t* drain = bars + 19;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  int* s_abort = reinterpret_cast<int*>(bars + 21);
+  uint64_t* ex_bar = bars + 22;    // [4]: row-max / row-sum exchange of the two softmax halves
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       tc::mbar_init(k_full + s, 1);
-      tc::mbar_init(v_full + s, 1);
-      tc::mbar_init(kv_empty + s, 1);
-      tc::mbar_init(s_full + s, 1);
-      tc::mbar_init(s_free + s, 4);
+      tc::mbar_init(k_empty + s, 1);
     }
-    tc::mbar_init(p_full, 4);
+    for (int s = 0; s < kVStages; ++s) {
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_empty + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(s_full + s, 1);
+      tc::mbar_init(s_free + s, 8);
+    }
+    tc::mbar_init(p_full, 8);
     tc::mbar_init(pv_done, 1);
-    tc::mbar_init(o_free, 4);
+    tc::mbar_init(o_free, 8);
     tc::mbar_init(drain, 1);
-    *s_abort = 0;
+    for (int q = 0; q < 4; ++q) tc::mbar_init(ex_bar + q, 2);
+    // the 1024-byte aligned layout must fit in the dynamic allocation
+    *s_abort = (tc::smem_u32(base) + kSmemEnd > tc::smem_u32(smem_raw) + kSmemBytes) ? 1 : 0;
     tc::fence_mbar_init();
   }
   if (warp == 0) {
@@ -325,63 +338,96 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   const int n_items = a.header[0];
   volatile int* abort_flag = s_abort;
   const int G = a.G, log2G = a.log2G, tpt = kBM >> log2G;
+  const bool layout_ok = *abort_flag == 0;
 
-  if (warp == 0) {
+  if (layout_ok && warp == 0) {
     // ===================================================================== TMA producer
+    // The whole warp runs the loop: lanes 0..7 fetch the eight block-table entries of a tile
+    // (prefetched one tile ahead), lane 0 waits for free stages and issues the copies.  K runs
+    // one tile ahead of V so that QK^T of the next tile never waits behind a V stage.
     if (lane == 0) {
       tc::prefetch_tensormap(&mQ);
       tc::prefetch_tensormap(&mK);
       tc::prefetch_tensormap(&mV);
-      int kv_it = 0, li = 0;
-      bool ok = true;
-      for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
-        const Item it = a.items[idx];
-        const int o = a.node_offset[it.r];
-        const int T = a.node_offset[it.r + 1] - o;
-        const int P = a.prefix_len[it.r];
-        const int nblk = (P + T + kBS - 1) / kBS;
-        if (li > 0 && !tc::mbar_wait(q_empty, (li - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+    }
+    int kt = 0, vt = 0, li = 0;
+    bool ok = true;
+    int prev_row = a.kv_rows;
+    bool prev_valid = false;
+    auto tile_rows = [&](const int32_t* table, int nblk, int j, int r, int h) -> int {
+      int row = a.kv_rows;  // out of range: TMA fills zeros
+      const int lb = j * 8 + lane;
+      if (lane < 8 && lb < nblk) {
+        const int pb = table[lb];
+        if (pb >= 0 && pb < a.num_blocks) row = (pb * a.H_kv + h) * kBS;
+        else atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
+      }
+      return row;
+    };
+    auto issue_kv = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* full, int row_lane) {
+      // lane b (0..7) copies block b of the tile: both 64-column halves (one swizzle atom each)
+      if (lane == 0) tc::mbar_arrive_expect_tx(full, kTile);
+      __syncwarp();
+      if (lane < 8) {
+        tc::tma_load_2d(dst + lane * 2048, map, 0, row_lane, full);
+        tc::tma_load_2d(dst + kAtom + lane * 2048, map, 64, row_lane, full);
+      }
+      __syncwarp();
+    };
+    auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool r = true;
+      if (lane == 0) r = tc::mbar_wait(bar, parity, abort_flag, kWaitLimit);
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
+      const Item it = a.items[idx];
+      const int o = a.node_offset[it.r];
+      const int T = a.node_offset[it.r + 1] - o;
+      const int P = a.prefix_len[it.r];
+      const int nblk = (P + T + kBS - 1) / kBS;
+      const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
+      if (li > 0 && !wait_lane0(q_empty, (li - 1) & 1)) { ok = false; break; }
+      if (lane == 0) {
         tc::mbar_arrive_expect_tx(q_full, kTile);
         tc::tma_load_3d(sQ, &mQ, 0, it.h * G, o + it.mt * tpt, q_full);
         tc::tma_load_3d(sQ + kAtom, &mQ, 64, it.h * G, o + it.mt * tpt, q_full);
-        const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
-        for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
-          const int st = kv_it & 1, use = kv_it >> 1;
-          if (use > 0 && !tc::mbar_wait(kv_empty + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-          int rows[8];
-          for (int b = 0; b < 8; ++b) {
-            const int lb = j * 8 + b;
-            int row = a.kv_rows;  // out of range: TMA fills zeros
-            if (lb < nblk) {
-              const int pb = table[lb];
-              if (pb >= 0 && pb < a.num_blocks) row = (pb * a.H_kv + it.h) * kBS;
-              else atomicOr(&a.req_status[it.r], SPEC_REQ_BAD_BLOCK);
-            }
-            rows[b] = row;
-          }
-          uint8_t* kdst = sK + st * kTile;
-          uint8_t* vdst = sV + st * kTile;
-          tc::mbar_arrive_expect_tx(k_full + st, kTile);
-          for (int b = 0; b < 8; ++b) {
-            tc::tma_load_2d(kdst + b * 2048, &mK, 0, rows[b], k_full + st);
-            tc::tma_load_2d(kdst + kAtom + b * 2048, &mK, 64, rows[b], k_full + st);
-          }
-          tc::mbar_arrive_expect_tx(v_full + st, kTile);
-          for (int b = 0; b < 8; ++b) {
-            tc::tma_load_2d(vdst + b * 2048, &mV, 0, rows[b], v_full + st);
-            tc::tma_load_2d(vdst + kAtom + b * 2048, &mV, 64, rows[b], v_full + st);
-          }
+      }
+      int row_cur = tile_rows(table, nblk, it.j0, it.r, it.h);
+      for (int j = it.j0; j < it.j1; ++j) {
+        const int row_next = (j + 1 < it.j1) ? tile_rows(table, nblk, j + 1, it.r, it.h) : a.kv_rows;
+        const int kst = kt % kKStages, kuse = kt / kKStages;
+        if (kuse > 0 && !wait_lane0(k_empty + kst, (kuse - 1) & 1)) { ok = false; break; }
+        issue_kv(&mK, sK + kst * kTile, k_full + kst, row_cur);
+        ++kt;
+        if (prev_valid) {
+          const int vst = vt % kVStages, vuse = vt / kVStages;
+          if (vuse > 0 && !wait_lane0(v_empty + vst, (vuse - 1) & 1)) { ok = false; break; }
+          issue_kv(&mV, sV + vst * kTile, v_full + vst, prev_row);
+          ++vt;
         }
+        prev_row = row_cur;
+        prev_valid = true;
+        row_cur = row_next;
       }
+    }
+    if (ok && prev_valid) {
+      const int vst = vt % kVStages, vuse = vt / kVStages;
+      if (vuse > 0 && !wait_lane0(v_empty + vst, (vuse - 1) & 1)) ok = false;
+      else {
+        issue_kv(&mV, sV + vst * kTile, v_full + vst, prev_row);
+        ++vt;
+      }
+    }
+    if (lane == 0) {
       if (!ok) *abort_flag = 1;
-      // drain: wait for the copies this thread issued last (bounded), so none is in flight
-      for (int k = max(0, kv_it - 2); k < kv_it; ++k) {
-        tc::mbar_wait(k_full + (k & 1), (k >> 1) & 1, abort_flag, kWaitLimit / 8);
-        tc::mbar_wait(v_full + (k & 1), (k >> 1) & 1, abort_flag, kWaitLimit / 8);
-      }
+      // drain: wait for the copies issued last (bounded), so none is in flight at exit
+      for (int k = max(0, kt - kKStages); k < kt; ++k)
+        tc::mbar_wait(k_full + k % kKStages, (k / kKStages) & 1, abort_flag, kWaitLimit / 8);
+      for (int v = max(0, vt - kVStages); v < vt; ++v)
+        tc::mbar_wait(v_full + v % kVStages, (v / kVStages) & 1, abort_flag, kWaitLimit / 8);
       if (li > 0) tc::mbar_wait(q_full, (li - 1) & 1, abort_flag, kWaitLimit / 8);
     }
-  } else if (warp == 1) {
+  } else if (layout_ok && warp == 1) {
     // ===================================================================== MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
@@ -392,7 +438,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       int kv_it = 0, li = 0;
       bool ok = true;
       auto issue_pv = [&](int prev, bool first_pv) -> bool {
-        const int pst = prev & 1, puse = prev >> 1;
+        const int pst = prev % kVStages, puse = prev / kVStages;
         if (!tc::mbar_wait(p_full, prev & 1, abort_flag, kWaitLimit)) return false;
         if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) return false;
         if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit))
@@ -404,7 +450,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           const uint64_t db = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
           tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
         }
-        tc::mma_commit(kv_empty + pst);
+        tc::mma_commit(v_empty + pst);
         tc::mma_commit(pv_done);
         return true;
       };
@@ -414,17 +460,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         bool first_pv = true;
         for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
           const int st = kv_it & 1, use = kv_it >> 1;
-          if (!tc::mbar_wait(k_full + st, use & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+          const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
+          if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
           if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
           tc::tc_fence_after();
           const uint32_t tS = tmem + st * 128;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint64_t da = tc::smem_desc(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = tc::smem_desc(aK + st * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
             tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
           }
           tc::mma_commit(s_full + st);
+          tc::mma_commit(k_empty + kst);
           if (j == it.j1 - 1) tc::mma_commit(q_empty);
           if (j > it.j0) {
             if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
@@ -439,13 +487,29 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       tc::mma_commit(drain);
       tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
     }
-  } else if (warp >= 4) {
+  } else if (layout_ok && warp >= 4) {
     // ===================================================================== softmax + epilogue
-    const int sw = warp - 4;
-    const int m = sw * 32 + lane;
-    const uint32_t lane_addr = uint32_t(sw * 32) << 16;
+    // Warps 4..11: lane quarter q = warp % 4 owns TMEM lanes / rows 32q..32q+31; the two warps of
+    // a quarter split the 128 keys of a score tile (half hh = 0: keys 0..63, 1: keys 64..127) and
+    // the 128 output columns, exchanging row maxima and row sums through shared memory.
+    const int q4 = warp & 3, hh = (warp - 4) >> 2;
+    const int m = q4 * 32 + lane;
+    const uint32_t lane_addr = uint32_t(q4 * 32) << 16;
     const int t_loc = m >> log2G, g = m & (G - 1);
     const float sl2 = a.scale_log2;
+    float* red = reinterpret_cast<float*>(base + kSmemRed);   // [2][2][128]
+    int ex_cnt = 0;
+    bool ex_ok = true;
+    // partner's value for this row: one mbarrier phase per exchange, double-buffered, bounded
+    auto exchange = [&](float v) -> float {
+      float* buf = red + (ex_cnt & 1) * 256;
+      buf[hh * 128 + m] = v;
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(ex_bar + q4);
+      ex_ok = ex_ok && warp_wait(ex_bar + q4, ex_cnt & 1, abort_flag);
+      ++ex_cnt;
+      return buf[(1 - hh) * 128 + m];
+    };
     int kv_it = 0, li = 0;
     bool ok = true;
     for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++li) {
@@ -459,92 +523,88 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       uint32_t anc[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) anc[k] = (valid && k < a.W) ? a.anc[size_t(o + t) * a.W + k] : 0u;
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;   // l: this half's share of the row sum
       for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
         const int st = kv_it & 1, use = kv_it >> 1;
         if (!warp_wait(s_full + st, use & 1, abort_flag)) { ok = false; break; }
         tc::tc_fence_after();
-        // mask + scale (log2 units); two passes over the TMEM scores keep the register
-        // footprint to the packed P row: pass 1 the masked max, pass 2 the exponentials
-        const int key0 = j * kBN;
-        const bool all_prefix = key0 + kBN <= P;
-        const int npre = max(0, min(kBN, P - key0));
-        uint32_t win[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) win[k] = all_prefix ? 0xffffffffu : anc_window(anc, a.W, key0 - P + 32 * k);
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t r32[32];
-          tc::tmem_ld32(tmem + lane_addr + st * 128 + c0, r32);
+        // this warp's 64 scores, one TMEM round trip; the S buffer is released right away
+        uint32_t sr[64];
+        {
+          uint32_t* lo = sr;
+          tc::tmem_ld32(tmem + lane_addr + st * 128 + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(lo));
+          tc::tmem_ld32(tmem + lane_addr + st * 128 + 64 * hh + 32,
+                        *reinterpret_cast<uint32_t(*)[32]>(lo + 32));
           tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const bool vis = valid && ((c0 + c < npre) || ((win[c0 >> 5] >> c) & 1u));
-            tmax = fmaxf(tmax, vis ? __uint_as_float(r32[c]) * sl2 : -INFINITY);
-          }
-        }
-        const bool grow = tmax > m_ref + kLazyRescale;
-        const float new_ref = grow ? tmax : m_ref;
-        const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
-        float rowsum = 0.f;
-        uint32_t pk[64];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t r32[32];
-          tc::tmem_ld32(tmem + lane_addr + st * 128 + c0, r32);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            const bool v0 = valid && ((c0 + c < npre) || ((win[c0 >> 5] >> c) & 1u));
-            const bool v1 = valid && ((c0 + c + 1 < npre) || ((win[c0 >> 5] >> (c + 1)) & 1u));
-            const float p0 = (v0 && new_ref != -INFINITY) ? ex2(__uint_as_float(r32[c]) * sl2 - new_ref) : 0.f;
-            const float p1 = (v1 && new_ref != -INFINITY) ? ex2(__uint_as_float(r32[c + 1]) * sl2 - new_ref) : 0.f;
-            rowsum += p0 + p1;
-            pk[(c0 + c) >> 1] = pack_bf16(p0, p1);
-          }
         }
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(s_free + st);
+        // mask + scale (log2 units)
+        const int key0 = j * kBN + 64 * hh;
+        const bool all_prefix = key0 + 64 <= P;
+        const int npre = P - key0;    // columns below npre are prefix keys
+        const uint32_t w0 = all_prefix ? 0xffffffffu : anc_window(anc, a.W, key0 - P);
+        const uint32_t w1 = all_prefix ? 0xffffffffu : anc_window(anc, a.W, key0 - P + 32);
+        float pmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const uint32_t wd = c < 32 ? w0 : w1;
+          const bool vis = valid && ((c < npre) || ((wd >> (c & 31)) & 1u));
+          const float x = vis ? __uint_as_float(sr[c]) * sl2 : -INFINITY;
+          sr[c] = __float_as_uint(x);
+          pmax = fmaxf(pmax, x);
+        }
+        const float tmax = fmaxf(pmax, exchange(pmax));
+        if (!ex_ok) { ok = false; break; }
+        const bool grow = tmax > m_ref + kLazyRescale;
+        const float new_ref = grow ? tmax : m_ref;
+        const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
         // PV of the previous tile must be complete before P and O are touched
         if (j > it.j0 && !warp_wait(pv_done, (kv_it - 1) & 1, abort_flag)) { ok = false; break; }
-        // P row -> swizzled K-major tile (two 64-key atoms)
+        float rowsum = 0.f;
+        const bool live = new_ref != -INFINITY;
+        uint8_t* rowp = sP + hh * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const int atom = c >> 3, ch = c & 7;
-          uint8_t* dst = sP + atom * kAtom + (m >> 3) * 1024 + (m & 7) * 128 + ((ch ^ (m & 7)) << 4);
-          *reinterpret_cast<uint4*>(dst) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        for (int ch = 0; ch < 8; ++ch) {   // 8 keys = one 16-byte chunk of the swizzled row
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float x0 = __uint_as_float(sr[ch * 8 + e]);
+            const float x1 = __uint_as_float(sr[ch * 8 + e + 1]);
+            const float p0 = live ? ex2(x0 - new_ref) : 0.f;
+            const float p1 = live ? ex2(x1 - new_ref) : 0.f;
+            rowsum += p0 + p1;
+            pk[e >> 1] = pack_bf16(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(rowp + ((ch ^ (m & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        // lazy rescale of the O accumulator (warp-collective TMEM access)
+        // lazy rescale of this warp's half of the O accumulator (warp-collective TMEM access)
         const bool any_rescale = __any_sync(0xffffffffu, factor != 1.f) && j > it.j0;
         if (any_rescale) {
           tc::tc_fence_after();
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < 64; c0 += 32) {
             uint32_t r32[32];
-            tc::tmem_ld32(tmem + lane_addr + 256 + c0, r32);
+            tc::tmem_ld32(tmem + lane_addr + 256 + 64 * hh + c0, r32);
             tc::tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < 32; ++c) r32[c] = __float_as_uint(__uint_as_float(r32[c]) * factor);
-            tc::tmem_st32(tmem + lane_addr + 256 + c0, r32);
+            tc::tmem_st32(tmem + lane_addr + 256 + 64 * hh + c0, r32);
           }
           tc::tmem_st_wait();
         }
         l = l * factor + rowsum;
         m_ref = new_ref;
         // last tile: zero V rows past the request's KV length (stale cache rows times P = 0
-        // must not turn into NaN); TMA must have landed first
-        if (key0 + kBN > kv_len) {
+        // must not turn into NaN); TMA must have landed first.  Half hh clears d-atom hh.
+        if (j * kBN + kBN > kv_len) {
           if (!warp_wait(v_full + st, use & 1, abort_flag)) { ok = false; break; }
-          const int key = m;  // this thread clears key row m
-          if (key >= kv_len - key0) {
-            uint8_t* vrow = sV + st * kTile + (key >> 3) * 1024 + (key & 7) * 128;
+          const int key = m;
+          if (key >= kv_len - j * kBN) {
+            uint8_t* vrow = sV + st * kTile + hh * kAtom + (key >> 3) * 1024 + (key & 7) * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(vrow + kAtom + c * 16) = make_uint4(0, 0, 0, 0);
-            }
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         tc::fence_proxy_async_smem();
@@ -553,17 +613,19 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         if (lane == 0) tc::mbar_arrive(p_full);
       }
       if (!ok) break;
-      // epilogue
+      // epilogue: this warp writes output columns 64*hh .. 64*hh+63 of its rows
       if (!warp_wait(pv_done, (kv_it - 1) & 1, abort_flag)) { ok = false; break; }
       tc::tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse2 = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+      const float lt = l + exchange(l);
+      if (!ex_ok) { ok = false; break; }
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = lt > 0.f ? m_ref + __log2f(lt) : -INFINITY;
       if (it.slot < 0) {
-        __nv_bfloat16* orow = a.o + (size_t(o + t) * a.H_q + it.h * G + g) * kD;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        __nv_bfloat16* orow = a.o + (size_t(o + t) * a.H_q + it.h * G + g) * kD + 64 * hh;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r32[32];
-          tc::tmem_ld32(tmem + lane_addr + 256 + c0, r32);
+          tc::tmem_ld32(tmem + lane_addr + 256 + 64 * hh + c0, r32);
           tc::tmem_ld_wait();
           if (valid) {
 #pragma unroll
@@ -577,13 +639,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             }
           }
         }
-        if (valid && a.lse) a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
+        if (valid && hh == 0 && a.lse) a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
       } else {
-        float* prow = a.part_o + (size_t(it.slot) * kBM + m) * kD;
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        float* prow = a.part_o + (size_t(it.slot) * kBM + m) * kD + 64 * hh;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r32[32];
-          tc::tmem_ld32(tmem + lane_addr + 256 + c0, r32);
+          tc::tmem_ld32(tmem + lane_addr + 256 + 64 * hh + c0, r32);
           tc::tmem_ld_wait();
           if (valid) {
 #pragma unroll
@@ -593,7 +655,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                               __uint_as_float(r32[c + 2]) * inv, __uint_as_float(r32[c + 3]) * inv);
           }
         }
-        if (valid) a.part_lse[size_t(it.slot) * kBM + m] = lse2;
+        if (valid && hh == 0) a.part_lse[size_t(it.slot) * kBM + m] = lse2;
       }
       tc::tc_fence_before();
       __syncwarp();
