@@ -44,7 +44,6 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttnF32Dev a) {
   if (a.req_status[r] != 0) return;
   const int o = a.node_offset[r];
   const int T = a.node_offset[r + 1] - o;
-  const int i = n - o;
   const int P = a.prefix_len[r];
   const int kvh = h / (a.H_q / a.H_kv);
   const int kv_len = P + T;

@@ -60,8 +60,6 @@ struct VerifyDev {
   uint32_t* d_need;
 };
 
-constexpr float kLog2e = 1.4426950408889634f;
-
 // ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
 template <typename T>
 __device__ __forceinline__ void load8(const T* __restrict__ row, int unit, int V, int full,
