@@ -194,6 +194,23 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
                           spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * spec_verify_noalloc -- no counterpart on the pages; an addition for callers that may not
+ * allocate device memory (an engine that reserves its whole memory budget up front and forbids
+ * allocation while serving, or a plugin that is handed only tensors and a stream).
+ * Same inputs, outputs and results as spec_verify, but the workspace is a fixed array in device
+ * memory that belongs to this library (every GPU that loads the library keeps it until the
+ * process exits), so the caller passes none and nothing is allocated.
+ * Limits: N <= 32768 tree nodes and R <= 32768 draft rows per call; larger batches return
+ * SPEC_ERR_UNSUPPORTED (use spec_verify with a caller-owned workspace instead).
+ * The first call on each device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  All calls share the one array: calls whose
+ * kernels overlap on the GPU (other streams, other host threads on the same device) race.
+ * Errors: as spec_verify, plus SPEC_ERR_UNSUPPORTED for sizes beyond the limits above and
+ * SPEC_ERR_CUDA if the address lookup fails.
+ * ------------------------------------------------------------------------------------------ */
+spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * spec_kv_compact  [RATIO: KV Cache管理], [CSDN 4]
  * Commits the accepted path and rolls back the rest, in place, for every layer and KV head,
  * K and V: new[P_r + d] = old[P_r + path[r][d]] for d = 0 .. n_acc[r] (gather semantics: every

@@ -20,8 +20,8 @@ SPEC_SIBLING_RESIDUAL, SPEC_SIBLING_INDEPENDENT = 0, 1
 REQ_BITS = dict(BAD_PARENT=1, BAD_SIZE=2, BAD_TOKEN=4, BAD_DRAFT_ROW=8, BAD_DEPTH=16,
                 BAD_BLOCK=32, TIMEOUT=64)
 EXPORTS = ["spec_tree_build", "spec_tree_attention", "spec_attention_workspace_size",
-           "spec_verify", "spec_verify_workspace_size", "spec_kv_compact", "spec_status_string",
-           "spec_last_cuda_error"]
+           "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
+           "spec_status_string", "spec_last_cuda_error"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -85,6 +85,8 @@ def load_library(build_if_missing=False):
     lib.spec_attention_workspace_size.argtypes = [ctypes.POINTER(SpecAttnParams)]
     lib.spec_verify.restype = st
     lib.spec_verify.argtypes = [ctypes.POINTER(SpecVerifyParams), _vp, ctypes.c_size_t, _vp]
+    lib.spec_verify_noalloc.restype = st
+    lib.spec_verify_noalloc.argtypes = [ctypes.POINTER(SpecVerifyParams), _vp]
     lib.spec_verify_workspace_size.restype = ctypes.c_size_t
     lib.spec_verify_workspace_size.argtypes = [ctypes.POINTER(SpecVerifyParams)]
     lib.spec_kv_compact.restype = st
@@ -237,6 +239,14 @@ def spec_verify(params, workspace, stream=None):
     wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
     code = lib.spec_verify(ctypes.byref(params), _ptr(workspace), wsz, _stream(stream))
     _check(code, "spec_verify")
+
+
+def spec_verify_noalloc(params, stream=None):
+    """spec_verify without a caller workspace (see include/spec_verify.h): for callers that may
+    not allocate device memory.  Calls whose kernels overlap on the GPU share one scratch array
+    and race."""
+    code = load_library().spec_verify_noalloc(ctypes.byref(params), _stream(stream))
+    _check(code, "spec_verify_noalloc")
 
 
 def compact_params(k_cache, v_cache, block_table, prefix_len, path, n_acc, req_status,

@@ -28,7 +28,7 @@ inline spec_status_t launch_status() {
   return SPEC_OK;
 }
 
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------------------------------------
 // device side

@@ -24,6 +24,8 @@
 // Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 
 namespace spec {
@@ -714,3 +716,58 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------
+// spec_verify_noalloc: spec_verify for callers that may not allocate device memory at all --
+// for example an inference engine that reserves its whole memory budget at start-up and
+// forbids any allocation on the request path, or a plugin that is handed only tensors and a
+// stream by a host framework.  The verification workspace lives in one fixed array in device
+// memory that is part of this library; every GPU that loads the library holds it until the
+// process exits.  It covers up to kNoAllocMaxNodes tree nodes and kNoAllocMaxDraftRows draft
+// rows; larger batches are refused with SPEC_ERR_UNSUPPORTED.
+// The first call on each device looks the array's device address up (cudaGetSymbolAddress)
+// with that device current; make that first call before any stream capture.  All calls share
+// the array: calls whose kernels overlap on the GPU (different streams, or different host
+// threads on the same device) race on it.  spec_verify clears the part that must start at zero
+// on every call, so the contents left by an earlier call do not matter.
+// ------------------------------------------------------------------------------------------
+namespace spec {
+constexpr int kNoAllocMaxNodes = 32768;
+constexpr int kNoAllocMaxDraftRows = 32768;
+constexpr size_t kNoAllocScratchBytes =
+    align_up(sizeof(RowStat) * kNoAllocMaxNodes, 256) +
+    align_up(sizeof(RowStat) * kNoAllocMaxDraftRows, 256) + align_up(kNoAllocMaxNodes, 256) +
+    align_up(4 * size_t(kNoAllocMaxDraftRows), 256);
+static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
+}  // namespace spec
+
+extern "C" spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_stream_t stream) {
+  using namespace spec;
+  static std::mutex mu;
+  static void* scratch_of[64] = {nullptr};
+  if (!p) return SPEC_ERR_INVALID_ARG;
+  if (p->N > kNoAllocMaxNodes || p->R > kNoAllocMaxDraftRows) return SPEC_ERR_UNSUPPORTED;
+  const size_t need = spec_verify_workspace_size(p);
+  if (need > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    return SPEC_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return SPEC_ERR_UNSUPPORTED;
+  void* ptr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!scratch_of[dev]) {
+      e = cudaGetSymbolAddress(&scratch_of[dev], g_verify_scratch);
+      if (e != cudaSuccess) {
+        scratch_of[dev] = nullptr;
+        set_last_cuda_error(e);
+        return SPEC_ERR_CUDA;
+      }
+    }
+    ptr = scratch_of[dev];
+  }
+  return spec_verify(p, ptr, kNoAllocScratchBytes, stream);
+}
