@@ -163,27 +163,38 @@ __device__ int block_excl_scan(int v, int* s_warp, int& excl) {
   return total;
 }
 
+// Per-request geometry used by the range walk: shared memory for batches up to kPrepSmemReqs
+// requests (the usual case), global memory beyond.
+constexpr int kPrepSmemReqs = 2048;
+
+struct PrepGeo {
+  const int* tiles;   // [B + 1] exclusive prefix of tile work
+  const int* nts;     // [B] KV tiles per unit
+  const int* mts;     // [B] M-tiles per KV head
+};
+
 // Walks range [t0, t1) of the global tile stream; calls emit(r, h, mt, j0, j1, nts, mts) for
 // every piece of a unit that falls in the range, in stream order.
 template <typename F>
-__device__ void walk_range(const TcDev& a, long long t0, long long t1, F&& emit) {
+__device__ void walk_range(const TcDev& a, const PrepGeo& geo, long long t0, long long t1,
+                           F&& emit) {
   if (t0 >= t1) return;
   int lo = 0, hi = a.B - 1;  // last request whose work starts at or before t0
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (a.req_tiles[mid] <= t0) lo = mid; else hi = mid - 1;
+    if (geo.tiles[mid] <= t0) lo = mid; else hi = mid - 1;
   }
   long long t = t0;
   for (int r = lo; r < a.B && t < t1; ++r) {
-    const long long rbeg = a.req_tiles[r], rend = a.req_tiles[r + 1];
+    const long long rbeg = geo.tiles[r], rend = geo.tiles[r + 1];
     if (rend <= t) continue;
-    const ReqGeom g = req_geom(a, r);
+    const int nts = geo.nts[r], mts = geo.mts[r];
     while (t < t1 && t < rend) {
       const long long off = t - rbeg;
-      const int u = int(off / g.nts);
-      const int j0 = int(off - (long long)u * g.nts);
-      const int j1 = int(min((long long)g.nts, (long long)j0 + (t1 - t)));
-      emit(r, u / g.mts, u % g.mts, j0, j1, g.nts, g.mts);
+      const int u = int(off / nts);
+      const int j0 = int(off - (long long)u * nts);
+      const int j1 = int(min((long long)nts, (long long)j0 + (t1 - t)));
+      emit(r, u / mts, u % mts, j0, j1, nts, mts);
       t += j1 - j0;
     }
   }
@@ -191,8 +202,13 @@ __device__ void walk_range(const TcDev& a, long long t0, long long t1, F&& emit)
 
 __global__ void __launch_bounds__(1024) attn_prep_kernel(TcDev a) {
   __shared__ int s_warp[32];
+  __shared__ int s_tiles[kPrepSmemReqs + 1];
+  __shared__ int s_nts[kPrepSmemReqs];
+  __shared__ int s_mts[kPrepSmemReqs];
   const int tid = threadIdx.x;
-  // per-request tile work, exclusive prefix (in chunks of 1024 requests)
+  const bool in_smem = a.B <= kPrepSmemReqs;
+  // per-request geometry and tile work, exclusive prefix (in chunks of 1024 requests); the
+  // global copies (req_tiles, and nts / mts recomputed on the fly) back batches that do not fit
   int carry = 0;
   for (int r0 = 0; r0 < a.B; r0 += 1024) {
     const int r = r0 + tid;
@@ -200,24 +216,75 @@ __global__ void __launch_bounds__(1024) attn_prep_kernel(TcDev a) {
     if (r < a.B) {
       const ReqGeom g0 = req_geom(a, r);
       const int nblk = (g0.P + g0.T + attn::kBS - 1) / attn::kBS;
-      if (g0.units > 0 && nblk > a.max_blocks) atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
-      const ReqGeom g = req_geom(a, r);
+      ReqGeom g = g0;
+      if (g0.units > 0 && nblk > a.max_blocks) {
+        atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
+        g.mts = g.nts = g.units = 0;
+      }
       tiles = g.units * g.nts;
+      if (in_smem) {
+        s_nts[r] = g.nts;
+        s_mts[r] = g.mts;
+      }
     }
     int e;
     const int tot = block_excl_scan(tiles, s_warp, e);
-    if (r < a.B) a.req_tiles[r] = carry + e;
+    if (r < a.B) {
+      a.req_tiles[r] = carry + e;
+      if (in_smem) s_tiles[r] = carry + e;
+    }
     carry += tot;
   }
-  if (tid == 0) a.req_tiles[a.B] = carry;
+  if (tid == 0) {
+    a.req_tiles[a.B] = carry;
+    if (in_smem) s_tiles[a.B] = carry;
+  }
   __syncthreads();
+  PrepGeo geo;
+  if (in_smem) {
+    geo.tiles = s_tiles;
+    geo.nts = s_nts;
+    geo.mts = s_mts;
+  } else {
+    // large batches: global prefix; nts / mts are recomputed from the inputs per request
+    geo.tiles = a.req_tiles;
+    geo.nts = nullptr;
+    geo.mts = nullptr;
+  }
   const long long total = carry;
   const int C = int(max(1LL, min((long long)a.ctas, total / attn::kMinTilesPerRange)));
   const bool mine = tid < C;
   const long long t0 = mine ? total * tid / C : 0, t1 = mine ? total * (tid + 1) / C : 0;
+  auto walk = [&](auto&& emit) {
+    if (in_smem) {
+      walk_range(a, geo, t0, t1, emit);
+    } else {
+      // same walk with geometry from global memory
+      if (t0 >= t1) return;
+      int lo = 0, hi = a.B - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.req_tiles[mid] <= t0) lo = mid; else hi = mid - 1;
+      }
+      long long t = t0;
+      for (int r = lo; r < a.B && t < t1; ++r) {
+        const long long rbeg = a.req_tiles[r], rend = a.req_tiles[r + 1];
+        if (rend <= t) continue;
+        const ReqGeom g = req_geom(a, r);
+        while (t < t1 && t < rend) {
+          const long long off = t - rbeg;
+          const int u = int(off / g.nts);
+          const int j0 = int(off - (long long)u * g.nts);
+          const int j1 = int(min((long long)g.nts, (long long)j0 + (t1 - t)));
+          emit(r, u / g.mts, u % g.mts, j0, j1, g.nts, g.mts);
+          t += j1 - j0;
+        }
+      }
+    }
+  };
   // pass 1: pieces, partial pieces and merge records per range
   int n = 0, np = 0, nc = 0;
-  walk_range(a, t0, t1, [&](int, int, int, int j0, int j1, int nts, int) {
+  walk([&](int, int, int, int j0, int j1, int nts, int) {
     ++n;
     if (j0 > 0 || j1 < nts) ++np;
     if (j0 == 0 && j1 < nts) ++nc;   // the unit starts here and continues in the next range
@@ -235,13 +302,14 @@ __global__ void __launch_bounds__(1024) attn_prep_kernel(TcDev a) {
   // pass 2: items with partial slots (consecutive across ranges for a cut unit: its pieces are
   // the last partial piece of one range and the first of the following ones) + merge records
   int idx = e_items, slot = e_part, ci = e_comb;
-  walk_range(a, t0, t1, [&](int r, int h, int mt, int j0, int j1, int nts, int mts) {
+  const int* tiles_pref = in_smem ? s_tiles : a.req_tiles;
+  walk([&](int r, int h, int mt, int j0, int j1, int nts, int mts) {
     Item it;
     it.r = r; it.h = h; it.mt = mt; it.j0 = j0; it.j1 = j1; it.pad0 = it.pad1 = 0;
     const bool partial = j0 > 0 || j1 < nts;
     it.slot = partial ? slot : -1;
     if (j0 == 0 && j1 < nts) {
-      const long long ubeg = a.req_tiles[r] + (long long)(h * mts + mt) * nts;
+      const long long ubeg = tiles_pref[r] + (long long)(h * mts + mt) * nts;
       const long long uend = ubeg + nts;
       int pieces = 1;
       for (int c = tid + 1; c < C; ++c) {

@@ -135,8 +135,12 @@ __global__ void __launch_bounds__(256) verify_prep_kernel(VerifyDev a) {
 }
 
 // ---- 2. rows: (m, Z) or (max, argmax) in one streaming read --------------------------------
+constexpr int kRowThreads = 512;
+constexpr int kRowUnroll = 8;   // 8 x 16-byte loads in flight per thread
+constexpr int kRowWarps = kRowThreads / 32;
+
 template <typename T>
-__global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
+__global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
   const int b = blockIdx.x;
   const T* row;
   RowStat* out;
@@ -152,17 +156,18 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
   }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int V = a.V, full = V / 8, nunits = (V + 7) / 8;
-  __shared__ float s_f[8];
-  __shared__ int s_i[8];
-  __shared__ float s_hi[8], s_lo[8];
+  __shared__ float s_f[kRowWarps];
+  __shared__ int s_i[kRowWarps];
+  __shared__ float s_hi[kRowWarps], s_lo[kRowWarps];
+  constexpr int kStep = kRowUnroll * kRowThreads;
   if (a.tau == 0.f) {
     float best = -INFINITY;
     int arg = 0x7fffffff;
-    for (int u0 = tid; u0 < nunits; u0 += 4 * 256) {
-      float x[4][8];
+    for (int u0 = tid; u0 < nunits; u0 += kStep) {
+      float x[kRowUnroll][8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int unit = u0 + j * 256;
+      for (int j = 0; j < kRowUnroll; ++j) {
+        const int unit = u0 + j * kRowThreads;
         if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
         else {
 #pragma unroll
@@ -170,10 +175,10 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
         }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < kRowUnroll; ++j)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          if (x[j][k] > best) { best = x[j][k]; arg = (u0 + j * 256) * 8 + k; }
+          if (x[j][k] > best) { best = x[j][k]; arg = (u0 + j * kRowThreads) * 8 + k; }
     }
     // block (max value, lowest index)
 #pragma unroll
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
     if (tid == 0) {
       float bb = s_f[0];
       int ba = s_i[0];
-      for (int w = 1; w < 8; ++w)
+      for (int w = 1; w < kRowWarps; ++w)
         if (s_f[w] > bb || (s_f[w] == bb && s_i[w] < ba)) { bb = s_f[w]; ba = s_i[w]; }
       out->m = bb;
       out->arg = ba;
@@ -197,11 +202,11 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
   }
   const float k2 = a.k2;
   float m = -INFINITY, s = 0.f, c = 0.f;  // Kahan: true sum ~ s - c
-  for (int u0 = tid; u0 < nunits; u0 += 4 * 256) {
-    float x[4][8];
+  for (int u0 = tid; u0 < nunits; u0 += kStep) {
+    float x[kRowUnroll][8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int unit = u0 + j * 256;
+    for (int j = 0; j < kRowUnroll; ++j) {
+      const int unit = u0 + j * kRowThreads;
       if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
       else {
 #pragma unroll
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
     }
     float cm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
+    for (int j = 0; j < kRowUnroll; ++j)
 #pragma unroll
       for (int k = 0; k < 8; ++k) cm = fmaxf(cm, x[j][k]);
     if (cm > m) {
@@ -220,15 +225,15 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
       m = cm;
     }
     if (m != -INFINITY) {
-      float t4[4];
+      float tj[kRowUnroll];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < kRowUnroll; ++j) {
         float w[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) w[k] = ex2((x[j][k] - m) * k2);
-        t4[j] = sum8(w);
+        tj[j] = sum8(w);
       }
-      const float chunk = (t4[0] + t4[1]) + (t4[2] + t4[3]);
+      const float chunk = ((tj[0] + tj[1]) + (tj[2] + tj[3])) + ((tj[4] + tj[5]) + (tj[6] + tj[7]));
       const float y = chunk - c;
       const float t = s + y;
       c = (t - s) - y;
@@ -240,14 +245,14 @@ __global__ void __launch_bounds__(256) verify_rows_kernel(VerifyDev a) {
   __syncthreads();
   M = s_f[0];
 #pragma unroll
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, s_f[w]);
+  for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_f[w]);
   const float mine = (m == -INFINITY) ? 0.f : (s - c) * ex2((m - M) * k2);
   dfloat acc = warp_sum_df(df_make(mine));
   if (lane == 0) { s_hi[warp] = acc.hi; s_lo[warp] = acc.lo; }
   __syncthreads();
   if (tid == 0) {
     dfloat tot = {s_hi[0], s_lo[0]};
-    for (int w = 1; w < 8; ++w) tot = df_add(tot, dfloat{s_hi[w], s_lo[w]});
+    for (int w = 1; w < kRowWarps; ++w) tot = df_add(tot, dfloat{s_hi[w], s_lo[w]});
     out->m = M;
     out->arg = -1;
     out->Z = df_to_d(tot);
@@ -263,6 +268,15 @@ struct WalkSmem {
   int16_t first_child[SPEC_MAX_TREE];
   int16_t next_sib[SPEC_MAX_TREE];
   int32_t path[SPEC_MAX_TREE];
+  // per local node, gathered once in parallel before the walk
+  int32_t tok[SPEC_MAX_TREE];
+  int32_t drow[SPEC_MAX_TREE];     // draft row of the node's children (internal nodes)
+  float xt[SPEC_MAX_TREE];         // target logit of the node's token in its parent's row
+  float xd[SPEC_MAX_TREE];         // draft logit / probability of the node's token (parent's q)
+  float uacc[SPEC_MAX_TREE], usamp[SPEC_MAX_TREE];
+  float st_m[SPEC_MAX_TREE], sd_m[SPEC_MAX_TREE];
+  double st_Z[SPEC_MAX_TREE], sd_Z[SPEC_MAX_TREE];
+  int32_t st_arg[SPEC_MAX_TREE];
   dfloat wtot[kWalkWarps];
   dfloat wpre[kWalkWarps];
   int wlast[kWalkWarps];
@@ -293,8 +307,7 @@ __device__ float block_row_max(const TT* row, int V, WalkSmem& sh) {
   m = warp_max(m);
   if (lane == 0) sh.fred[warp] = m;
   __syncthreads();
-  float M = sh.fred[0];
-  for (int w = 1; w < kWalkWarps; ++w) M = fmaxf(M, sh.fred[w]);
+  const float M = warp_max(sh.fred[lane]);  // kWalkWarps == 32: every warp reduces the 32 maxima
   __syncthreads();
   return M;
 }
@@ -320,10 +333,14 @@ __device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
   }
   if (lane == 0) { sh.fred[warp] = best; sh.ired[warp] = arg; }
   __syncthreads();
-  float bb = sh.fred[0];
-  int ba = sh.ired[0];
-  for (int w = 1; w < kWalkWarps; ++w)
-    if (sh.fred[w] > bb || (sh.fred[w] == bb && sh.ired[w] < ba)) { bb = sh.fred[w]; ba = sh.ired[w]; }
+  float bb = sh.fred[lane];
+  int ba = sh.ired[lane];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    float ob = __shfl_xor_sync(0xffffffffu, bb, off);
+    int oa = __shfl_xor_sync(0xffffffffu, ba, off);
+    if (ob > bb || (ob == bb && oa < ba)) { bb = ob; ba = oa; }
+  }
   __syncthreads();
   return ba;
 }
@@ -366,42 +383,54 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
   const int ue = min(ub + upw, nunits);
   dfloat acc = df_make(0.f);
   int last = -1;
-  for (int base = ub; base < ue; base += 32) {
-    const int unit = base + lane;
-    float s = 0.f;
-    if (unit < ue) {
-      float w[8];
-      fn(trow, drow, unit, V, full, w);
-      s = sum8(w);
+  // two units per lane per step so that two row loads are in flight
+  for (int base = ub; base < ue; base += 64) {
+    const int u0 = base + lane, u1 = base + 32 + lane;
+    float w0[8], w1[8];
+    if (u0 < ue) fn(trow, drow, u0, V, full, w0);
+    if (u1 < ue) fn(trow, drow, u1, V, full, w1);
+    if (u0 < ue) {
+      acc = df_add_f(acc, sum8(w0));
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (w[k] > 0.f) last = unit * 8 + k;
+        if (w0[k] > 0.f) last = u0 * 8 + k;
     }
-    acc = df_add_f(acc, s);
+    if (u1 < ue) {
+      acc = df_add_f(acc, sum8(w1));
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w1[k] > 0.f) last = u1 * 8 + k;
+    }
   }
   const dfloat wt = warp_sum_df(acc);
   last = warp_max_i(last);
   if (lane == 0) { sh.wtot[warp] = wt; sh.wlast[warp] = last; }
   __syncthreads();
-  if (tid == 0) {
-    dfloat run = df_make(0.f);
-    int fb = -1;
-    for (int w = 0; w < kWalkWarps; ++w) {
-      sh.wpre[w] = run;
-      run = df_add(run, sh.wtot[w]);
-      fb = max(fb, sh.wlast[w]);
-    }
+  if (warp == 0) {
+    // lane w holds warp w's total: scan them in token order
+    const dfloat incl = warp_scan_df(sh.wtot[lane], lane);
+    dfloat excl = df_shfl_up(incl, 1);
+    if (lane == 0) excl = df_make(0.f);
+    sh.wpre[lane] = excl;
+    const dfloat run = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+    const int fb = warp_max_i(sh.wlast[lane]);
     const double tot = df_to_d(run);
-    sh.total = tot;
-    sh.fallback = fb;
-    sh.wsel = -1;
-    sh.found = fb;
+    int wsel = -1;
+    double theta = 0.0;
     if (search && tot > 0.0) {
-      const double theta = u * tot;
+      theta = u * tot;
+      // incl > theta, evaluated as a double-float difference (exact for nearby values)
+      const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
+      const bool cross = ((incl.hi - th_hi) + (incl.lo - th_lo)) > 0.f;
+      const unsigned mask = __ballot_sync(0xffffffffu, cross);
+      wsel = mask ? __ffs(mask) - 1 : -1;
+    }
+    if (lane == 0) {
+      sh.total = tot;
+      sh.fallback = fb;
+      sh.found = fb;
+      sh.wsel = wsel;
       sh.theta = theta;
-      for (int w = 0; w < kWalkWarps; ++w) {
-        if (df_to_d(df_add(sh.wpre[w], sh.wtot[w])) > theta) { sh.wsel = w; break; }
-      }
     }
   }
   __syncthreads();
@@ -414,6 +443,7 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
   if (ws >= 0 && warp == ws) {
     dfloat base_acc = sh.wpre[ws];
     const double theta = sh.theta;
+    const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
     for (int base = ub; base < ue; base += 32) {
       const int unit = base + lane;
       float w[8];
@@ -428,7 +458,8 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
       const dfloat incl = warp_scan_df(df_make(s), lane);
       dfloat excl = df_shfl_up(incl, 1);
       if (lane == 0) excl = df_make(0.f);
-      const bool cross = df_to_d(df_add(base_acc, incl)) > theta;
+      const dfloat cum_incl = df_add(base_acc, incl);
+      const bool cross = ((cum_incl.hi - th_hi) + (cum_incl.lo - th_lo)) > 0.f;
       const unsigned mask = __ballot_sync(0xffffffffu, cross);
       if (mask) {
         if (lane == __ffs(mask) - 1) {
@@ -438,7 +469,7 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
           for (int k = 0; k < 8; ++k) {
             cum = df_add_f(cum, w[k]);
             if (w[k] > 0.f) lastpos = unit * 8 + k;
-            if (tok < 0 && df_to_d(cum) > theta) tok = unit * 8 + k;
+            if (tok < 0 && ((cum.hi - th_hi) + (cum.lo - th_lo)) > 0.f) tok = unit * 8 + k;
           }
           sh.found = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : sh.fallback);
         }
@@ -474,10 +505,43 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   }
   const int o = a.node_offset[r];
   const int T = a.node_offset[r + 1] - o;
+  const TT* target = reinterpret_cast<const TT*>(a.target);
+  const TD* draft = reinterpret_cast<const TD*>(a.draft);
+  const bool greedy = a.tau == 0.f;
+  // gather, in parallel, everything the scalar part of the walk will read: tree links, tokens,
+  // uniforms, the row statistics of internal nodes and, for every non-root node, its token's
+  // target and draft values in its parent's rows (the operands of its ratio test)
   for (int i = tid; i < T; i += kWalkThreads) {
-    sh.par[i] = int16_t(a.parent[o + i]);
+    const int p = a.parent[o + i];
+    const int t = a.tokens[o + i];
+    sh.par[i] = int16_t(p);
+    sh.tok[i] = t;
     sh.first_child[i] = -1;
     sh.next_sib[i] = -1;
+    sh.uacc[i] = a.uniforms[2 * size_t(o + i)];
+    sh.usamp[i] = a.uniforms[2 * size_t(o + i) + 1];
+    if (a.is_internal[o + i]) {
+      const RowStat ts = a.tstat[o + i];
+      sh.st_m[i] = ts.m;
+      sh.st_Z[i] = ts.Z;
+      sh.st_arg[i] = ts.arg;
+      if (!greedy) {
+        const int dr = a.draft_row[o + i];
+        sh.drow[i] = dr;
+        if (!a.probs) {
+          const RowStat ds = a.dstat[dr];
+          sh.sd_m[i] = ds.m;
+          sh.sd_Z[i] = ds.Z;
+        } else {
+          sh.sd_m[i] = 0.f;
+          sh.sd_Z[i] = 1.0;
+        }
+      }
+    }
+    if (i > 0 && !greedy) {
+      sh.xt[i] = elem<TT>::load1(target + size_t(o + p) * a.tld + t);
+      sh.xd[i] = elem<TD>::load1(draft + size_t(a.draft_row[o + p]) * a.dld + t);
+    }
   }
   __syncthreads();
   for (int i = tid; i < T; i += kWalkThreads) {
@@ -497,18 +561,15 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   if (tid == 0) sh.path[0] = 0;
   __syncthreads();
 
-  const TT* target = reinterpret_cast<const TT*>(a.target);
-  const TD* draft = reinterpret_cast<const TD*>(a.draft);
-  const bool greedy = a.tau == 0.f;
   int node = 0, npath = 1, rejections = 0, final_tok = -1;
   while (true) {
     const TT* trow = target + size_t(o + node) * a.tld;
     const int fc = sh.first_child[node];
     if (greedy) {
-      const int best = fc < 0 ? block_row_argmax(trow, a.V, sh) : a.tstat[o + node].arg;
+      const int best = fc < 0 ? block_row_argmax(trow, a.V, sh) : sh.st_arg[node];
       int acc = -1, rej = 0;
       for (int c = fc; c >= 0; c = sh.next_sib[c]) {
-        if (a.tokens[o + c] == best) { acc = c; break; }
+        if (sh.tok[c] == best) { acc = c; break; }
         ++rej;
       }
       rejections += rej;
@@ -521,7 +582,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       final_tok = best;
       break;
     }
-    const float u_samp = a.uniforms[2 * size_t(o + node) + 1];
+    const float u_samp = sh.usamp[node];
     if (fc < 0) {  // leaf: bonus token from p_leaf
       WeightFn fn{};
       fn.residual = false;
@@ -531,11 +592,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       final_tok = vocab_pass(trow, draft, a.V, fn, true, double(u_samp), sh, tot);
       break;
     }
-    const RowStat ts = a.tstat[o + node];
-    const int drow_i = a.draft_row[o + node];
-    const TD* drow = draft + size_t(drow_i) * a.dld;
-    RowStat ds = {0.f, 0, 1.0};
-    if (!a.probs) ds = a.dstat[drow_i];
+    const RowStat ts = {sh.st_m[node], 0, sh.st_Z[node]};
+    const TD* drow = draft + size_t(sh.drow[node]) * a.dld;
+    const RowStat ds = {sh.sd_m[node], 0, sh.sd_Z[node]};
     WeightFn res{};
     res.residual = true;
     res.probs = a.probs != 0;
@@ -549,9 +608,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     bool from_p = false;
     for (int c = fc; c >= 0; c = sh.next_sib[c]) {
       if (tid == 0) {
-        const int tok = a.tokens[o + c];
-        const float xt = elem<TT>::load1(trow + tok);
-        const float xd = elem<TD>::load1(drow + tok);
+        const float xt = sh.xt[c];
+        const float xd = sh.xd[c];
         double num, den;
         const bool first_test = (C == 0.0) || !a.residual_rule;
         if (!a.probs && first_test) {
@@ -565,8 +623,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
           den = first_test ? q : Nk * q;
         }
         const double ratio = den > 0.0 ? num / den : (num > 0.0 ? INFINITY : 0.0);
-        const float u_acc = a.uniforms[2 * size_t(o + c)];
-        sh.decision = double(u_acc) < ratio;
+        sh.decision = double(sh.uacc[c]) < ratio;
       }
       __syncthreads();
       const bool acc = sh.decision != 0;
@@ -608,7 +665,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   for (int k = tid; k < a.max_path; k += kWalkThreads) {
     if (k < npath) {
       path_row[k] = sh.path[k];
-      tok_row[k] = (k + 1 < npath) ? a.tokens[o + sh.path[k + 1]] : final_tok;
+      tok_row[k] = (k + 1 < npath) ? sh.tok[sh.path[k + 1]] : final_tok;
     } else {
       path_row[k] = -1;
       tok_row[k] = -1;
@@ -638,7 +695,7 @@ static VerifyWs verify_ws_layout(int N, int R) {
 
 template <typename TT, typename TD>
 static void launch_verify(const VerifyDev& d, bool run_rows, cudaStream_t s) {
-  if (run_rows) verify_rows_kernel<TT><<<d.N + (d.probs ? 0 : d.R), 256, 0, s>>>(d);
+  if (run_rows) verify_rows_kernel<TT><<<d.N + (d.probs ? 0 : d.R), kRowThreads, 0, s>>>(d);
   verify_walk_kernel<TT, TD><<<d.B, kWalkThreads, 0, s>>>(d);
 }
 
