@@ -16,11 +16,13 @@
 //      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over 32-element chunks
 //      (Kahan-compensated), then a block reduction (max, then a double-float sum) -> (m, Z);
 //      tau = 0 keeps (max, lowest argmax) instead;
-//   3. walk  (one CTA of 1024 threads per request): the tree walk.  Ratio tests are scalar work
-//      on thread 0 using (m, Z); every vocab-wide step (sibling residual mass, residual / bonus
-//      inverse CDF, leaf max / argmax) is a block-wide pass: 32 warps own contiguous vocab
-//      ranges, per-warp double-float sums are scanned in token order, the warp holding the
-//      crossing rescans its range with a warp scan and its crossing lane walks its 8 elements.
+//   3. walk  (one CTA of 512 threads per request): the tree walk.  A parallel prologue gathers
+//      every node's test operands and decides every plain ratio test u < p / q at once (thread
+//      per node, from (m, Z)); only later siblings under the residual rule are tested on the way,
+//      on thread 0.  Every vocab-wide step (sibling residual mass, residual / bonus inverse CDF,
+//      leaf max / argmax) is a block-wide pass: 16 warps own contiguous vocab ranges, per-warp
+//      double-float sums are scanned in token order, and the warp holding the crossing rescans
+//      its unit sums (kept in shared memory) to find the unit, then the unit's 8 elements.
 // Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
 #include <math.h>
 
@@ -34,6 +36,8 @@ struct RowStat {
   float m;      // row max of the raw logits
   int32_t arg;  // lowest index of the max (tau = 0 rows)
   double Z;     // sum over the row of 2^((x - m) * log2(e) / tau)
+  float inv_Z;  // float(1 / Z), for the vocab-wide weights
+  int32_t pad;
 };
 
 struct VerifyDev {
@@ -197,6 +201,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
       out->m = bb;
       out->arg = ba;
       out->Z = 0.0;
+      out->inv_Z = 0.f;
     }
     return;
   }
@@ -255,13 +260,21 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
     for (int w = 1; w < kRowWarps; ++w) tot = df_add(tot, dfloat{s_hi[w], s_lo[w]});
     out->m = M;
     out->arg = -1;
-    out->Z = df_to_d(tot);
+    const double Z = df_to_d(tot);
+    out->Z = Z;
+    out->inv_Z = float(1.0 / Z);
   }
 }
 
 // ---- 3. walk -------------------------------------------------------------------------------
-constexpr int kWalkThreads = 1024;
+// fp64 runs on thread 0 (or one warp) only: GB300's fp64 rate is a small fraction of fp32, and a
+// double division executed by all 32 warps of the block costs microseconds.
+constexpr int kWalkThreads = 512;   // 128 registers per thread: four units' loads in flight
 constexpr int kWalkWarps = kWalkThreads / 32;
+static_assert(kWalkWarps <= 32, "one warp scans the per-warp totals");
+// per-unit sums of a vocab pass stay in dynamic shared memory for vocabularies up to this many
+// 8-element units (V <= 262144); the search step then rescans them instead of the rows
+constexpr int kWalkMaxSmemUnits = 32768;
 
 struct WalkSmem {
   int16_t par[SPEC_MAX_TREE];
@@ -274,16 +287,20 @@ struct WalkSmem {
   float xt[SPEC_MAX_TREE];         // target logit of the node's token in its parent's row
   float xd[SPEC_MAX_TREE];         // draft logit / probability of the node's token (parent's q)
   float uacc[SPEC_MAX_TREE], usamp[SPEC_MAX_TREE];
-  float st_m[SPEC_MAX_TREE], sd_m[SPEC_MAX_TREE];
+  float st_m[SPEC_MAX_TREE], sd_m[SPEC_MAX_TREE];     // row max of the node's target / draft row
+  float st_iz[SPEC_MAX_TREE], sd_iz[SPEC_MAX_TREE];   // float(1 / Z) of those rows
   double st_Z[SPEC_MAX_TREE], sd_Z[SPEC_MAX_TREE];
   int32_t st_arg[SPEC_MAX_TREE];
+  uint8_t dec0[SPEC_MAX_TREE];     // outcome of the node's plain ratio test u < p / q
   dfloat wtot[kWalkWarps];
   dfloat wpre[kWalkWarps];
   int wlast[kWalkWarps];
   float fred[kWalkWarps];
   int ired[kWalkWarps];
   double total, theta;
-  int wsel, found, fallback;
+  double C, Nk;                    // sibling residual state (thread 0 only)
+  float Cf;
+  int wsel, found, fallback, pos;
   int decision;
 };
 
@@ -307,7 +324,7 @@ __device__ float block_row_max(const TT* row, int V, WalkSmem& sh) {
   m = warp_max(m);
   if (lane == 0) sh.fred[warp] = m;
   __syncthreads();
-  const float M = warp_max(sh.fred[lane]);  // kWalkWarps == 32: every warp reduces the 32 maxima
+  const float M = warp_max(lane < kWalkWarps ? sh.fred[lane] : -INFINITY);  // every warp reduces
   __syncthreads();
   return M;
 }
@@ -333,8 +350,8 @@ __device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
   }
   if (lane == 0) { sh.fred[warp] = best; sh.ired[warp] = arg; }
   __syncthreads();
-  float bb = sh.fred[lane];
-  int ba = sh.ired[lane];
+  float bb = lane < kWalkWarps ? sh.fred[lane] : -INFINITY;
+  int ba = lane < kWalkWarps ? sh.ired[lane] : 0x7fffffff;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     float ob = __shfl_xor_sync(0xffffffffu, bb, off);
@@ -345,22 +362,46 @@ __device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
   return ba;
 }
 
-// Element weights of the distribution being summed / sampled.
+// One 8-element unit of a row as raw 16-byte vectors, so that several units' loads can be
+// issued before any of them is used.
+template <typename T>
+struct RawUnit {
+  static constexpr int kVec = int(sizeof(T)) / 2;   // 1 for bf16, 2 for fp32
+  uint4 v[kVec];
+  __device__ __forceinline__ void load(const T* row, int unit) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) v[k] = ld_stream16(row + size_t(unit) * 8 + k * (8 / kVec));
+  }
+  // the unit's 8 values; the ragged last unit (unit >= full) is read element by element
+  __device__ __forceinline__ void get(const T* row, int unit, int V, int full, float fill,
+                                      float (&x)[8]) const {
+    if (unit < full) {
+      if constexpr (kVec == 1) {
+        elem<T>::unpack(v[0], x);
+      } else {
+        elem<float>::unpack(v[0], x);
+        float y[4];
+        elem<float>::unpack(v[1], y);
+        x[4] = y[0]; x[5] = y[1]; x[6] = y[2]; x[7] = y[3];
+      }
+    } else {
+      load8(row, unit, V, full, fill, x);
+    }
+  }
+};
+
+// Element weights of the distribution being summed / sampled: p itself (bonus token, up to the
+// constant 1 / Z) or the sibling residual max(0, p - C q).
 struct WeightFn {
   bool residual, probs;
   float mt, md, k2, invZt, invZd, C;
-  template <typename TT, typename TD>
-  __device__ __forceinline__ void operator()(const TT* trow, const TD* drow, int unit, int V,
-                                             int full, float (&w)[8]) const {
-    float xt[8];
-    load8(trow, unit, V, full, -INFINITY, xt);
+  __device__ __forceinline__ void operator()(const float (&xt)[8], const float (&xd)[8],
+                                             float (&w)[8]) const {
     if (!residual) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) w[k] = ex2((xt[k] - mt) * k2);
       return;
     }
-    float xd[8];
-    load8(drow, unit, V, full, probs ? 0.f : -INFINITY, xd);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float p = ex2((xt[k] - mt) * k2) * invZt;
@@ -368,14 +409,35 @@ struct WeightFn {
       w[k] = fmaxf(0.f, p - C * q);
     }
   }
+  template <typename TT, typename TD>
+  __device__ __forceinline__ void unit(const TT* trow, const TD* drow, int u, int V, int full,
+                                       float (&w)[8]) const {
+    float xt[8], xd[8];
+    load8(trow, u, V, full, -INFINITY, xt);
+    if (residual) load8(drow, u, V, full, probs ? 0.f : -INFINITY, xd);
+    (*this)(xt, xd, w);
+  }
 };
 
-// Block-wide pass over the vocabulary: total mass of the weights (returned in `total`) and,
-// when `search`, the smallest token x with sum_{y<=x} w(y) > u * total (-1 if the weights are
-// all zero).  Warp w owns units [w*upw, (w+1)*upw) so warp order is token order.
+struct PassResult {
+  int tok;    // sampled token (search passes), -1 otherwise
+  bool pos;   // the total mass is > 0
+};
+
+// double-float value minus theta (th_hi + th_lo) is > 0
+__device__ __forceinline__ bool df_above(dfloat x, float th_hi, float th_lo) {
+  return ((x.hi - th_hi) + (x.lo - th_lo)) > 0.f;
+}
+
+// Block-wide pass over the vocabulary: total mass of the weights (sh.total, thread 0) and, when
+// `search`, the smallest token x with sum_{y<=x} w(y) > u * total.  Warp w owns units
+// [w*upw, (w+1)*upw), so warp order is token order; each lane issues the loads of kUnits units
+// before it uses any.  With `usum` the unit sums stay in shared memory and the search rescans
+// them; without it (very large vocabularies) the crossing warp recomputes its units.
 template <typename TT, typename TD>
-__device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn, bool search,
-                          double u, WalkSmem& sh, double& total) {
+__device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn,
+                                 bool search, float u, float* usum, WalkSmem& sh) {
+  constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
   const int upw = ((nunits + kWalkWarps - 1) / kWalkWarps + 31) / 32 * 32;
@@ -383,23 +445,32 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
   const int ue = min(ub + upw, nunits);
   dfloat acc = df_make(0.f);
   int last = -1;
-  // two units per lane per step so that two row loads are in flight
-  for (int base = ub; base < ue; base += 64) {
-    const int u0 = base + lane, u1 = base + 32 + lane;
-    float w0[8], w1[8];
-    if (u0 < ue) fn(trow, drow, u0, V, full, w0);
-    if (u1 < ue) fn(trow, drow, u1, V, full, w1);
-    if (u0 < ue) {
-      acc = df_add_f(acc, sum8(w0));
+  for (int base = ub; base < ue; base += 32 * kUnits) {
+    RawUnit<TT> rt[kUnits];
+    RawUnit<TD> rd[kUnits];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (w0[k] > 0.f) last = u0 * 8 + k;
+    for (int j = 0; j < kUnits; ++j) {
+      const int unit = base + 32 * j + lane;
+      if (unit < ue && unit < full) {
+        rt[j].load(trow, unit);
+        if (fn.residual) rd[j].load(drow, unit);
+      }
     }
-    if (u1 < ue) {
-      acc = df_add_f(acc, sum8(w1));
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (w1[k] > 0.f) last = u1 * 8 + k;
+    for (int j = 0; j < kUnits; ++j) {
+      const int unit = base + 32 * j + lane;
+      if (unit < ue) {
+        float xt[8], xd[8], w[8];
+        rt[j].get(trow, unit, V, full, -INFINITY, xt);
+        if (fn.residual) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
+        fn(xt, xd, w);
+        const float su = sum8(w);
+        acc = df_add_f(acc, su);
+        if (usum) usum[unit] = su;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (w[k] > 0.f) last = unit * 8 + k;
+      }
     }
   }
   const dfloat wt = warp_sum_df(acc);
@@ -408,25 +479,25 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
   __syncthreads();
   if (warp == 0) {
     // lane w holds warp w's total: scan them in token order
-    const dfloat incl = warp_scan_df(sh.wtot[lane], lane);
+    const dfloat incl = warp_scan_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f), lane);
     dfloat excl = df_shfl_up(incl, 1);
     if (lane == 0) excl = df_make(0.f);
-    sh.wpre[lane] = excl;
-    const dfloat run = {__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-    const int fb = warp_max_i(sh.wlast[lane]);
+    if (lane < kWalkWarps) sh.wpre[lane] = excl;
+    const dfloat run = {__shfl_sync(0xffffffffu, incl.hi, 31),
+                        __shfl_sync(0xffffffffu, incl.lo, 31)};
+    const int fb = warp_max_i(lane < kWalkWarps ? sh.wlast[lane] : -1);
     const double tot = df_to_d(run);
     int wsel = -1;
     double theta = 0.0;
     if (search && tot > 0.0) {
-      theta = u * tot;
-      // incl > theta, evaluated as a double-float difference (exact for nearby values)
+      theta = double(u) * tot;
       const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
-      const bool cross = ((incl.hi - th_hi) + (incl.lo - th_lo)) > 0.f;
-      const unsigned mask = __ballot_sync(0xffffffffu, cross);
+      const unsigned mask = __ballot_sync(0xffffffffu, df_above(incl, th_hi, th_lo));
       wsel = mask ? __ffs(mask) - 1 : -1;
     }
     if (lane == 0) {
       sh.total = tot;
+      sh.pos = tot > 0.0;
       sh.fallback = fb;
       sh.found = fb;
       sh.wsel = wsel;
@@ -434,61 +505,79 @@ __device__ int vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn&
     }
   }
   __syncthreads();
-  total = sh.total;
+  PassResult res{-1, sh.pos != 0};
   if (!search) {
     __syncthreads();
-    return -1;
+    return res;
   }
   const int ws = sh.wsel;
   if (ws >= 0 && warp == ws) {
-    dfloat base_acc = sh.wpre[ws];
+    // lane L rescans a contiguous run of the warp's units; a warp scan of the run totals finds
+    // the crossing lane, which walks its units and then the 8 elements of the crossing unit
     const double theta = sh.theta;
     const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
-    for (int base = ub; base < ue; base += 32) {
-      const int unit = base + lane;
+    const dfloat base_acc = sh.wpre[ws];
+    const int per = (ue - ub + 31) / 32;
+    const int l0 = min(ub + lane * per, ue), l1 = min(l0 + per, ue);
+    auto unit_sum = [&](int unit) {
+      if (usum) return usum[unit];
       float w[8];
-      float s = 0.f;
-      if (unit < ue) {
-        fn(trow, drow, unit, V, full, w);
-        s = sum8(w);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = 0.f;
+      fn.unit(trow, drow, unit, V, full, w);
+      return sum8(w);
+    };
+    dfloat run = df_make(0.f);
+    for (int unit = l0; unit < l1; ++unit) run = df_add_f(run, unit_sum(unit));
+    const dfloat incl = warp_scan_df(run, lane);
+    dfloat excl = df_shfl_up(incl, 1);
+    if (lane == 0) excl = df_make(0.f);
+    const unsigned mask = __ballot_sync(0xffffffffu, df_above(df_add(base_acc, incl), th_hi, th_lo));
+    if (mask && lane == __ffs(mask) - 1) {
+      dfloat cum = df_add(base_acc, excl);
+      int cross_unit = -1, last_pos_unit = -1;
+      for (int unit = l0; unit < l1; ++unit) {
+        const float su = unit_sum(unit);
+        const dfloat next = df_add_f(cum, su);
+        if (su > 0.f) last_pos_unit = unit;
+        if (df_above(next, th_hi, th_lo)) { cross_unit = unit; break; }
+        cum = next;
       }
-      const dfloat incl = warp_scan_df(df_make(s), lane);
-      dfloat excl = df_shfl_up(incl, 1);
-      if (lane == 0) excl = df_make(0.f);
-      const dfloat cum_incl = df_add(base_acc, incl);
-      const bool cross = ((cum_incl.hi - th_hi) + (cum_incl.lo - th_lo)) > 0.f;
-      const unsigned mask = __ballot_sync(0xffffffffu, cross);
-      if (mask) {
-        if (lane == __ffs(mask) - 1) {
-          dfloat cum = df_add(base_acc, excl);
-          int tok = -1, lastpos = -1;
+      // rounding can leave the crossing inside the run total only: take its last live unit
+      const int cu = cross_unit >= 0 ? cross_unit : last_pos_unit;
+      int tok = -1, lastpos = -1;
+      if (cu >= 0) {
+        float w[8];
+        fn.unit(trow, drow, cu, V, full, w);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            cum = df_add_f(cum, w[k]);
-            if (w[k] > 0.f) lastpos = unit * 8 + k;
-            if (tok < 0 && ((cum.hi - th_hi) + (cum.lo - th_lo)) > 0.f) tok = unit * 8 + k;
-          }
-          sh.found = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : sh.fallback);
+        for (int k = 0; k < 8; ++k) {
+          cum = df_add_f(cum, w[k]);
+          if (w[k] > 0.f) lastpos = cu * 8 + k;
+          if (tok < 0 && cross_unit >= 0 && df_above(cum, th_hi, th_lo)) tok = cu * 8 + k;
         }
-        break;
       }
-      const dfloat it_tot = {__shfl_sync(0xffffffffu, incl.hi, 31),
-                             __shfl_sync(0xffffffffu, incl.lo, 31)};
-      base_acc = df_add(base_acc, it_tot);
+      sh.found = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : sh.fallback);
     }
   }
   __syncthreads();
-  const int tok = sh.found;
+  res.tok = sh.found;
   __syncthreads();
-  return tok;
+  return res;
+}
+
+// Thread 0: the ratio test of a later sibling under the sibling residual rule,
+// u < max(0, p - C q) / (N q) written as u * N * q < max(0, p - C q) (q >= 0).
+template <typename TT, typename TD>
+__device__ bool residual_ratio_test(const VerifyDev& a, const WalkSmem& sh, int node, int c) {
+  const double p = double(expf((sh.xt[c] - sh.st_m[node]) * a.inv_tau)) / sh.st_Z[node];
+  const double q = a.probs ? double(sh.xd[c])
+                           : double(expf((sh.xd[c] - sh.sd_m[node]) * a.inv_tau)) / sh.sd_Z[node];
+  const double num = fmax(0.0, p - sh.C * q);
+  return double(sh.uacc[c]) * (sh.Nk * q) < num;
 }
 
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
   __shared__ WalkSmem sh;
+  extern __shared__ float usum_dyn[];
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
   const int st = a.req_status[r];
@@ -503,6 +592,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     }
     return;
   }
+  float* usum = (a.V + 7) / 8 <= kWalkMaxSmemUnits ? usum_dyn : nullptr;
   const int o = a.node_offset[r];
   const int T = a.node_offset[r + 1] - o;
   const TT* target = reinterpret_cast<const TT*>(a.target);
@@ -524,6 +614,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       const RowStat ts = a.tstat[o + i];
       sh.st_m[i] = ts.m;
       sh.st_Z[i] = ts.Z;
+      sh.st_iz[i] = ts.inv_Z;
       sh.st_arg[i] = ts.arg;
       if (!greedy) {
         const int dr = a.draft_row[o + i];
@@ -532,9 +623,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
           const RowStat ds = a.dstat[dr];
           sh.sd_m[i] = ds.m;
           sh.sd_Z[i] = ds.Z;
+          sh.sd_iz[i] = ds.inv_Z;
         } else {
           sh.sd_m[i] = 0.f;
           sh.sd_Z[i] = 1.0;
+          sh.sd_iz[i] = 1.f;
         }
       }
     }
@@ -556,6 +649,20 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       for (int k = p + 1; k < i; ++k)
         if (sh.par[k] == p) { first = false; break; }
       if (first) sh.first_child[p] = int16_t(i);
+      if (!greedy) {
+        // plain ratio test u < p / q, as u * Zt < exp(((xt - mt) - (xd - md)) / tau) * Zd for
+        // draft logits and u * q * Zt < exp((xt - mt) / tau) for draft probabilities
+        const double u = double(sh.uacc[i]);
+        bool acc;
+        if (!a.probs) {
+          const float e = expf(((sh.xt[i] - sh.st_m[p]) - (sh.xd[i] - sh.sd_m[p])) * a.inv_tau);
+          acc = u * sh.st_Z[p] < double(e) * sh.sd_Z[p];
+        } else {
+          const float e = expf((sh.xt[i] - sh.st_m[p]) * a.inv_tau);
+          acc = u * double(sh.xd[i]) * sh.st_Z[p] < double(e);
+        }
+        sh.dec0[i] = acc ? 1 : 0;
+      }
     }
   }
   if (tid == 0) sh.path[0] = 0;
@@ -588,55 +695,44 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       fn.residual = false;
       fn.mt = block_row_max(trow, a.V, sh);
       fn.k2 = a.k2;
-      double tot;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, double(u_samp), sh, tot);
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh).tok;
       break;
     }
-    const RowStat ts = {sh.st_m[node], 0, sh.st_Z[node]};
     const TD* drow = draft + size_t(sh.drow[node]) * a.dld;
-    const RowStat ds = {sh.sd_m[node], 0, sh.sd_Z[node]};
     WeightFn res{};
     res.residual = true;
     res.probs = a.probs != 0;
-    res.mt = ts.m;
-    res.md = ds.m;
+    res.mt = sh.st_m[node];
+    res.md = sh.sd_m[node];
     res.k2 = a.k2;
-    res.invZt = float(1.0 / ts.Z);
-    res.invZd = float(1.0 / ds.Z);
-    double C = 0.0, Nk = 1.0;
+    res.invZt = sh.st_iz[node];
+    res.invZd = sh.sd_iz[node];
+    res.C = 1.f;
+    if (tid == 0) { sh.C = 0.0; sh.Nk = 1.0; }
     int accepted = -1;
     bool from_p = false;
     for (int c = fc; c >= 0; c = sh.next_sib[c]) {
-      if (tid == 0) {
-        const float xt = sh.xt[c];
-        const float xd = sh.xd[c];
-        double num, den;
-        const bool first_test = (C == 0.0) || !a.residual_rule;
-        if (!a.probs && first_test) {
-          // p/q = exp(((xt - mt) - (xd - md)) / tau) * Zd / Zt
-          num = double(expf(((xt - ts.m) - (xd - ds.m)) * a.inv_tau)) * ds.Z;
-          den = ts.Z;
-        } else {
-          const double p = double(expf((xt - ts.m) * a.inv_tau)) / ts.Z;
-          const double q = a.probs ? double(xd) : double(expf((xd - ds.m) * a.inv_tau)) / ds.Z;
-          num = first_test ? p : fmax(0.0, p - C * q);
-          den = first_test ? q : Nk * q;
-        }
-        const double ratio = den > 0.0 ? num / den : (num > 0.0 ? INFINITY : 0.0);
-        sh.decision = double(sh.uacc[c]) < ratio;
+      bool acc;
+      if (c == fc || !a.residual_rule) {
+        acc = sh.dec0[c] != 0;
+      } else {
+        if (tid == 0) sh.decision = residual_ratio_test<TT, TD>(a, sh, node, c);
+        __syncthreads();
+        acc = sh.decision != 0;
+        __syncthreads();
       }
-      __syncthreads();
-      const bool acc = sh.decision != 0;
-      __syncthreads();
       if (acc) { accepted = c; break; }
       ++rejections;
       if (a.residual_rule) {
-        C = C + Nk;
-        res.C = float(C);
-        double tot;
-        vocab_pass(trow, drow, a.V, res, false, 0.0, sh, tot);
-        Nk = tot;
-        if (!(Nk > 0.0)) { from_p = true; break; }
+        // C_{k+1} = C_k + N_k, N_{k+1} = sum_x max(0, p(x) - C_{k+1} q(x))
+        if (tid == 0) { sh.C += sh.Nk; sh.Cf = float(sh.C); }
+        __syncthreads();
+        res.C = sh.Cf;
+        // after the last sibling the search pass below computes N_{k+1} itself
+        if (sh.next_sib[c] < 0) break;
+        const PassResult pr = vocab_pass(trow, drow, a.V, res, false, 0.f, usum, sh);
+        if (tid == 0) sh.Nk = sh.total;
+        if (!pr.pos) { from_p = true; break; }
       }
     }
     if (accepted >= 0) {
@@ -646,18 +742,16 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       continue;
     }
     if (!from_p) {
-      res.C = float(a.residual_rule ? C : 1.0);
-      double tot;
-      final_tok = vocab_pass(trow, drow, a.V, res, true, double(u_samp), sh, tot);
-      if (!(tot > 0.0)) from_p = true;
+      const PassResult pr = vocab_pass(trow, drow, a.V, res, true, u_samp, usum, sh);
+      final_tok = pr.tok;
+      if (!pr.pos) from_p = true;
     }
     if (from_p) {
       WeightFn fn{};
       fn.residual = false;
-      fn.mt = ts.m;
+      fn.mt = res.mt;
       fn.k2 = a.k2;
-      double tot;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, double(u_samp), sh, tot);
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh).tok;
     }
     break;
   }
@@ -694,9 +788,28 @@ static VerifyWs verify_ws_layout(int N, int R) {
 }
 
 template <typename TT, typename TD>
-static void launch_verify(const VerifyDev& d, bool run_rows, cudaStream_t s) {
+static spec_status_t launch_verify(const VerifyDev& d, bool run_rows, cudaStream_t s) {
   if (run_rows) verify_rows_kernel<TT><<<d.N + (d.probs ? 0 : d.R), kRowThreads, 0, s>>>(d);
-  verify_walk_kernel<TT, TD><<<d.B, kWalkThreads, 0, s>>>(d);
+  const int nunits = (d.V + 7) / 8;
+  const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
+  if (dyn > 0) {
+    // raise the opt-in limit once per device for this instantiation
+    static bool raised[64] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status();
+    if (!raised[dev]) {
+      const cudaError_t e = cudaFuncSetAttribute(verify_walk_kernel<TT, TD>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 int(sizeof(float) * kWalkMaxSmemUnits));
+      if (e != cudaSuccess) {
+        set_last_cuda_error(e);
+        return SPEC_ERR_CUDA;
+      }
+      raised[dev] = true;
+    }
+  }
+  verify_walk_kernel<TT, TD><<<d.B, kWalkThreads, dyn, s>>>(d);
+  return launch_status();
 }
 
 }  // namespace spec
@@ -762,14 +875,13 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   if (cudaMemsetAsync(ws + lay.t_need, 0, lay.total - lay.t_need, s) != cudaSuccess)
     return launch_status();
   verify_prep_kernel<<<p->B, 256, 0, s>>>(d);
+  if (cudaGetLastError() != cudaSuccess) return launch_status();
   const bool run_rows = p->N > 0;
   if (p->logits_dtype == SPEC_BF16) {
-    if (d.probs) launch_verify<__nv_bfloat16, float>(d, run_rows, s);
-    else launch_verify<__nv_bfloat16, __nv_bfloat16>(d, run_rows, s);
-  } else {
-    launch_verify<float, float>(d, run_rows, s);
+    if (d.probs) return launch_verify<__nv_bfloat16, float>(d, run_rows, s);
+    return launch_verify<__nv_bfloat16, __nv_bfloat16>(d, run_rows, s);
   }
-  return launch_status();
+  return launch_verify<float, float>(d, run_rows, s);
 }
 
 }  // extern "C"
