@@ -9,10 +9,12 @@
 // Work unit = (request r, KV head h, M-tile mt): the G query heads of h times up to 128/G tree
 // tokens, stacked token-major into 128 MMA rows (row m = t_local * G + g), against the
 // request's P_r + T_r logical KV slots in tiles of 128 keys (8 paged blocks of 16).  The units
-// are laid end to end (request, head, M-tile order) as one stream of KV tiles, and a one-CTA
-// prep kernel cuts the stream into equal contiguous ranges, one per persistent CTA (one CTA per
-// SM).  A unit cut by a range boundary is computed in pieces whose fp32 partial outputs and
-// log-sum-exps a merge kernel combines; every other unit writes its output directly.
+// are laid end to end (request, head, M-tile order) as one stream of KV tiles cut into equal
+// contiguous ranges, one per persistent CTA (one CTA per SM); each CTA finds its own range with
+// two block-wide passes over the requests at start-up, so there is no separate partition launch.
+// A unit cut by a range boundary is computed in pieces that write fp32 partial outputs and
+// log-sum-exps; the CTA holding a cut unit's first piece leaves a merge record, and a small merge
+// kernel combines the pieces by log-sum-exp.  Every other unit writes its output directly.
 //
 // CTA (384 threads):
 //   warp 0      Q and K producer, warp 2 V producer: 128-byte-swizzled TMA boxes (one per
@@ -60,15 +62,14 @@ constexpr int kSmemEnd = kSmemRed + 2048;
 constexpr int kSmemBytes = 232448;            // the per-CTA maximum; the slack aligns the base
 constexpr long long kWaitLimit = 4000000000LL;     // clock cycles (~2 s)
 constexpr float kLazyRescale = 8.0f;          // log2 units
-constexpr int kMaxCtas = 1024;                // prep handles up to this many persistent CTAs
+constexpr int kMaxCtas = 1024;                // persistent CTAs at most
 constexpr int kMinTilesPerRange = 4;          // small problems use fewer, longer ranges
 }  // namespace attn
 
-struct Item {
-  int r, h, mt, j0, j1, slot, pad0, pad1;
-};
-struct CombineUnit {
-  int r, h, mt, slot0, npieces, pad0, pad1, pad2;
+// A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1.
+struct MergeRec {
+  int np, h, mt, o, T, ca, C, pad;
+  long long ubeg, total;
 };
 
 struct TcDev {
@@ -79,254 +80,225 @@ struct TcDev {
   __nv_bfloat16* o;
   float* lse;
   int32_t* req_status;
-  int* header;        // [0] items, [1] merge records
-  int* cta_off;       // [ctas + 1] item range of each CTA
-  int* req_tiles;     // [B + 1] exclusive prefix of tile work per request
-  Item* items;
-  CombineUnit* combine;
-  float* part_o;
-  float* part_lse;
+  struct MergeRec* recs;   // [ctas]: the cut unit whose first piece CTA c holds (np = 0: none)
+  float* part_o;      // [2 ctas][128][128] partial outputs of the pieces of cut units
+  float* part_lse;    // [2 ctas][2][128] their log2-sum-exps, one copy per column half
   int B, N, H_q, H_kv, G, log2G, T_max, W, num_blocks, max_blocks, kv_rows, ctas;
-  int max_items, max_combine;
   float scale_log2;
 };
 
 // ------------------------------------------------------------------------------ workspace
 struct TcWs {
-  size_t header, cta_off, req_tiles, items, combine, part_o, part_lse, total;
-  int max_items, max_combine, max_slots;
+  size_t recs, part_o, part_lse, total;
 };
 
-static TcWs tc_ws_layout(const spec_attn_params* p, int ctas) {
+static TcWs tc_ws_layout(int ctas) {
   TcWs w;
-  const int G = p->H_q / p->H_kv;
-  const int tpt = attn::kBM / G;
-  const long units = long(p->B) * p->H_kv * ((p->T_max + tpt - 1) / tpt);
-  w.max_items = int(units + ctas);      // each range boundary adds at most one piece
-  w.max_combine = ctas;                 // a cut unit spans >= 2 ranges
-  w.max_slots = 2 * ctas;               // at most two partial pieces per range
+  const size_t slots = 2 * size_t(ctas);   // at most two partial pieces per range
   size_t off = 0;
-  w.header = off; off = align_up(off + 64, 256);
-  w.cta_off = off; off = align_up(off + sizeof(int) * size_t(ctas + 1), 256);
-  w.req_tiles = off; off = align_up(off + sizeof(int) * size_t(p->B + 1), 256);
-  w.items = off; off = align_up(off + sizeof(Item) * size_t(w.max_items), 256);
-  w.combine = off; off = align_up(off + sizeof(CombineUnit) * size_t(w.max_combine), 256);
-  w.part_o = off; off = align_up(off + sizeof(float) * size_t(w.max_slots) * attn::kBM * attn::kD, 256);
-  w.part_lse = off; off = align_up(off + sizeof(float) * size_t(w.max_slots) * attn::kBM, 256);
+  w.recs = off; off = align_up(off + sizeof(MergeRec) * size_t(ctas), 256);
+  w.part_o = off; off = align_up(off + sizeof(float) * slots * attn::kBM * attn::kD, 256);
+  w.part_lse = off; off = align_up(off + sizeof(float) * slots * 2 * attn::kBM, 256);
   w.total = off;
   return w;
 }
 
-// ------------------------------------------------------------------------------ prep
+// ------------------------------------------------------------------------------ partition
 struct ReqGeom {
   int o, T, P, mts, nts, units;
 };
 
+// Geometry of request r.  The status bits this kernel sets itself (BAD_BLOCK, TIMEOUT) are
+// ignored, so every role of every CTA derives the same work from the same inputs; a request whose
+// KV slots do not fit its block-table row gets no work.
 __device__ __forceinline__ ReqGeom req_geom(const TcDev& a, int r) {
   ReqGeom g;
   g.o = a.node_offset[r];
   g.T = a.node_offset[r + 1] - g.o;
   g.P = a.prefix_len[r];
   const int tpt = attn::kBM >> a.log2G;
-  const bool ok = a.req_status[r] == 0 && g.T >= 1 && g.P >= 0;
+  const int st = a.req_status[r] & ~(SPEC_REQ_BAD_BLOCK | SPEC_REQ_TIMEOUT);
+  const bool ok = st == 0 && g.T >= 1 && g.P >= 0 &&
+                  (g.P + g.T + attn::kBS - 1) / attn::kBS <= a.max_blocks;
   g.mts = ok ? (g.T + tpt - 1) / tpt : 0;
   g.nts = ok ? (g.P + g.T + attn::kBN - 1) / attn::kBN : 0;
   g.units = a.H_kv * g.mts;
   return g;
 }
 
-// Block-wide exclusive scan of one int per thread (1024 threads); returns the block total.
-__device__ int block_excl_scan(int v, int* s_warp, int& excl) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += t;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int y = s_warp[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, y, o);
-      if (lane >= o) y += t;
-    }
-    s_warp[lane] = y;
-  }
-  __syncthreads();
-  const int warp_base = warp ? s_warp[warp - 1] : 0;
-  excl = warp_base + x - v;
-  const int total = s_warp[31];
-  __syncthreads();
-  return total;
-}
-
-// Per-request geometry used by the range walk: shared memory for batches up to kPrepSmemReqs
-// requests (the usual case), global memory beyond.
-constexpr int kPrepSmemReqs = 2048;
-
-struct PrepGeo {
-  const int* tiles;   // [B + 1] exclusive prefix of tile work
-  const int* nts;     // [B] KV tiles per unit
-  const int* mts;     // [B] M-tiles per KV head
+// This CTA's share of the tile stream.
+struct Range {
+  long long total;   // tiles in the stream
+  long long t0, t1;  // this CTA's range [t0, t1)
+  int C;             // ranges (CTAs blockIdx.x >= C have none)
+  int r0, r1;        // requests holding tiles t0 and t1 - 1
+  long long rbeg0, rbeg1;   // stream indices of their first tiles
 };
 
-// Walks range [t0, t1) of the global tile stream; calls emit(r, h, mt, j0, j1, nts, mts) for
-// every piece of a unit that falls in the range, in stream order.
-template <typename F>
-__device__ void walk_range(const TcDev& a, const PrepGeo& geo, long long t0, long long t1,
-                           F&& emit) {
-  if (t0 >= t1) return;
-  int lo = 0, hi = a.B - 1;  // last request whose work starts at or before t0
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (geo.tiles[mid] <= t0) lo = mid; else hi = mid - 1;
-  }
-  long long t = t0;
-  for (int r = lo; r < a.B && t < t1; ++r) {
-    const long long rbeg = geo.tiles[r], rend = geo.tiles[r + 1];
-    if (rend <= t) continue;
-    const int nts = geo.nts[r], mts = geo.mts[r];
-    while (t < t1 && t < rend) {
-      const long long off = t - rbeg;
-      const int u = int(off / nts);
-      const int j0 = int(off - (long long)u * nts);
-      const int j1 = int(min((long long)nts, (long long)j0 + (t1 - t)));
-      emit(r, u / mts, u % mts, j0, j1, nts, mts);
-      t += j1 - j0;
-    }
-  }
+__device__ __forceinline__ long long range_start(long long total, int C, int c) {
+  return total * c / C;
+}
+// the range holding tile t (0 <= t < total): the largest c with range_start(c) <= t
+__device__ __forceinline__ int range_of(long long t, long long total, int C) {
+  const long long c = ((t + 1) * C + total - 1) / total - 1;
+  return int(c < 0 ? 0 : (c >= C ? C - 1 : c));
+}
+// slot of the piece of the unit starting at tile ubeg that lies in range c
+__device__ __forceinline__ int piece_slot(long long ubeg, long long total, int C, int c) {
+  const long long rs = range_start(total, C, c);
+  return (ubeg > rs) ? 2 * c + 1 : 2 * c;
 }
 
-__global__ void __launch_bounds__(1024) attn_prep_kernel(TcDev a) {
-  __shared__ int s_warp[32];
-  __shared__ int s_tiles[kPrepSmemReqs + 1];
-  __shared__ int s_nts[kPrepSmemReqs];
-  __shared__ int s_mts[kPrepSmemReqs];
-  const int tid = threadIdx.x;
-  const bool in_smem = a.B <= kPrepSmemReqs;
-  // per-request geometry and tile work, exclusive prefix (in chunks of 1024 requests); the
-  // global copies (req_tiles, and nts / mts recomputed on the fly) back batches that do not fit
-  int carry = 0;
-  for (int r0 = 0; r0 < a.B; r0 += 1024) {
-    const int r = r0 + tid;
-    int tiles = 0;
-    if (r < a.B) {
-      const ReqGeom g0 = req_geom(a, r);
-      const int nblk = (g0.P + g0.T + attn::kBS - 1) / attn::kBS;
-      ReqGeom g = g0;
-      if (g0.units > 0 && nblk > a.max_blocks) {
-        atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
-        g.mts = g.nts = g.units = 0;
-      }
-      tiles = g.units * g.nts;
-      if (in_smem) {
-        s_nts[r] = g.nts;
-        s_mts[r] = g.mts;
-      }
-    }
-    int e;
-    const int tot = block_excl_scan(tiles, s_warp, e);
-    if (r < a.B) {
-      a.req_tiles[r] = carry + e;
-      if (in_smem) s_tiles[r] = carry + e;
-    }
-    carry += tot;
+// Every thread of the CTA computes the same Range: pass 1 sums the tile work of all requests,
+// pass 2 scans it in chunks of kThreads requests until the chunk holding t1 - 1.  `s64` is
+// scratch of at least kThreads / 32 + 2 entries, `s32` of two.  Contains __syncthreads.
+__device__ Range cta_range(const TcDev& a, long long* s64, int* s32) {
+  using namespace attn;
+  constexpr int kW = kThreads / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  long long mine = 0;
+  for (int r = tid; r < a.B; r += kThreads) {
+    const ReqGeom g = req_geom(a, r);
+    mine += (long long)g.units * g.nts;
+    if (blockIdx.x == 0 && g.units == 0 && a.req_status[r] == 0 && g.T >= 1 && g.P >= 0)
+      atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);   // KV slots beyond the table row
   }
-  if (tid == 0) {
-    a.req_tiles[a.B] = carry;
-    if (in_smem) s_tiles[a.B] = carry;
-  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+  if (lane == 0) s64[warp] = mine;
   __syncthreads();
-  PrepGeo geo;
-  if (in_smem) {
-    geo.tiles = s_tiles;
-    geo.nts = s_nts;
-    geo.mts = s_mts;
-  } else {
-    // large batches: global prefix; nts / mts are recomputed from the inputs per request
-    geo.tiles = a.req_tiles;
-    geo.nts = nullptr;
-    geo.mts = nullptr;
-  }
-  const long long total = carry;
-  const int C = int(max(1LL, min((long long)a.ctas, total / attn::kMinTilesPerRange)));
-  const bool mine = tid < C;
-  const long long t0 = mine ? total * tid / C : 0, t1 = mine ? total * (tid + 1) / C : 0;
-  auto walk = [&](auto&& emit) {
-    if (in_smem) {
-      walk_range(a, geo, t0, t1, emit);
-    } else {
-      // same walk with geometry from global memory
-      if (t0 >= t1) return;
-      int lo = 0, hi = a.B - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.req_tiles[mid] <= t0) lo = mid; else hi = mid - 1;
-      }
-      long long t = t0;
-      for (int r = lo; r < a.B && t < t1; ++r) {
-        const long long rbeg = a.req_tiles[r], rend = a.req_tiles[r + 1];
-        if (rend <= t) continue;
-        const ReqGeom g = req_geom(a, r);
-        while (t < t1 && t < rend) {
-          const long long off = t - rbeg;
-          const int u = int(off / g.nts);
-          const int j0 = int(off - (long long)u * g.nts);
-          const int j1 = int(min((long long)g.nts, (long long)j0 + (t1 - t)));
-          emit(r, u / g.mts, u % g.mts, j0, j1, g.nts, g.mts);
-          t += j1 - j0;
-        }
-      }
+  long long total = 0;
+#pragma unroll
+  for (int w = 0; w < kW; ++w) total += s64[w];
+  Range R;
+  R.total = total;
+  R.C = int(max(1LL, min((long long)a.ctas, total / kMinTilesPerRange)));
+  R.t0 = R.t1 = 0;
+  R.r0 = R.r1 = 0;
+  R.rbeg0 = R.rbeg1 = 0;
+  const int c = blockIdx.x;
+  if (total == 0 || c >= R.C) return R;   // uniform: no work for this CTA
+  R.t0 = range_start(total, R.C, c);
+  R.t1 = range_start(total, R.C, c + 1);
+  long long base = 0;
+  for (int r00 = 0; r00 < a.B; r00 += kThreads) {
+    __syncthreads();   // s64 is rewritten below
+    const int r = r00 + tid;
+    long long tiles = 0;
+    if (r < a.B) {
+      const ReqGeom g = req_geom(a, r);
+      tiles = (long long)g.units * g.nts;
     }
-  };
-  // pass 1: pieces, partial pieces and merge records per range
-  int n = 0, np = 0, nc = 0;
-  walk([&](int, int, int, int j0, int j1, int nts, int) {
-    ++n;
-    if (j0 > 0 || j1 < nts) ++np;
-    if (j0 == 0 && j1 < nts) ++nc;   // the unit starts here and continues in the next range
-  });
-  int e_items, e_part, e_comb;
-  const int n_items = block_excl_scan(n, s_warp, e_items);
-  block_excl_scan(np, s_warp, e_part);
-  const int n_comb = block_excl_scan(nc, s_warp, e_comb);
-  if (mine) a.cta_off[tid] = min(e_items, a.max_items);
-  for (int c = C + tid; c <= a.ctas; c += 1024) a.cta_off[c] = min(n_items, a.max_items);
-  if (tid == 0) {
-    a.header[0] = min(n_items, a.max_items);
-    a.header[1] = min(n_comb, a.max_combine);
-  }
-  // pass 2: items with partial slots (consecutive across ranges for a cut unit: its pieces are
-  // the last partial piece of one range and the first of the following ones) + merge records
-  int idx = e_items, slot = e_part, ci = e_comb;
-  const int* tiles_pref = in_smem ? s_tiles : a.req_tiles;
-  walk([&](int r, int h, int mt, int j0, int j1, int nts, int mts) {
-    Item it;
-    it.r = r; it.h = h; it.mt = mt; it.j0 = j0; it.j1 = j1; it.pad0 = it.pad1 = 0;
-    const bool partial = j0 > 0 || j1 < nts;
-    it.slot = partial ? slot : -1;
-    if (j0 == 0 && j1 < nts) {
-      const long long ubeg = tiles_pref[r] + (long long)(h * mts + mt) * nts;
-      const long long uend = ubeg + nts;
-      int pieces = 1;
-      for (int c = tid + 1; c < C; ++c) {
-        const long long c0 = total * c / C;
-        if (c0 >= uend) break;
-        if (total * (c + 1) / C > c0) ++pieces;
-      }
-      CombineUnit cu;
-      cu.r = r; cu.h = h; cu.mt = mt; cu.slot0 = slot; cu.npieces = pieces;
-      cu.pad0 = cu.pad1 = cu.pad2 = 0;
-      if (ci < a.max_combine) a.combine[ci] = cu;
-      ++ci;
+    long long incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long x = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += x;
     }
-    if (partial) ++slot;
-    if (idx < a.max_items) a.items[idx] = it;
-    ++idx;
-  });
+    if (lane == 31) s64[warp] = incl;
+    __syncthreads();
+    long long before = 0, chunk = 0;
+#pragma unroll
+    for (int w = 0; w < kW; ++w) {
+      if (w < warp) before += s64[w];
+      chunk += s64[w];
+    }
+    const long long hi = base + before + incl, lo = hi - tiles;
+    const bool found = base + chunk > R.t1 - 1;   // uniform
+    __syncthreads();
+    if (tiles > 0 && lo <= R.t0 && R.t0 < hi) {
+      s32[0] = r;
+      s64[kW] = lo;
+    }
+    if (tiles > 0 && lo <= R.t1 - 1 && R.t1 - 1 < hi) {
+      s32[1] = r;
+      s64[kW + 1] = lo;
+    }
+    __syncthreads();
+    base += chunk;
+    if (found) break;
+  }
+  R.r0 = s32[0];
+  R.rbeg0 = s64[kW];
+  R.r1 = s32[1];
+  R.rbeg1 = s64[kW + 1];
+  return R;
+}
+
+// One piece of work: tiles [j0, j1) of unit (r, h, mt).
+struct Item {
+  int r, h, mt, j0, j1;
+  int slot;           // >= 0: a partial piece of a cut unit, written to part_o[slot]
+  int o, T, P, nts;
+  long long ubeg;     // stream index of the unit's first tile
+};
+
+// Walks this CTA's range in stream order; every role runs its own copy.
+struct ItemIter {
+  long long t, rbeg, rend;
+  int r;
+  ReqGeom g;
+  __device__ __forceinline__ void start(const TcDev& a, const Range& R) {
+    t = R.t0;
+    r = R.r0;
+    rbeg = rend = R.rbeg0;
+    if (t < R.t1) {
+      g = req_geom(a, r);
+      rend = rbeg + (long long)g.units * g.nts;
+    }
+  }
+  __device__ __forceinline__ bool next(const TcDev& a, const Range& R, Item& it) {
+    if (t >= R.t1) return false;
+    while (t >= rend) {
+      if (r + 1 >= a.B) return false;
+      ++r;
+      g = req_geom(a, r);
+      rbeg = rend;
+      rend = rbeg + (long long)g.units * g.nts;
+    }
+    const long long off = t - rbeg;
+    const int u = int(off / g.nts);
+    it.r = r;
+    it.h = u / g.mts;
+    it.mt = u - it.h * g.mts;
+    it.j0 = int(off - (long long)u * g.nts);
+    it.j1 = int(min((long long)g.nts, (long long)it.j0 + (R.t1 - t)));
+    it.o = g.o;
+    it.T = g.T;
+    it.P = g.P;
+    it.nts = g.nts;
+    it.ubeg = rbeg + (long long)u * g.nts;
+    const bool partial = it.j0 > 0 || it.j1 < g.nts;
+    it.slot = partial ? (t == R.t0 ? 2 * int(blockIdx.x) : 2 * int(blockIdx.x) + 1) : -1;
+    t += it.j1 - it.j0;
+    return true;
+  }
+};
+
+// Thread 0 of CTA c: the merge record of range c -- the unit holding the range's last tile, if it
+// starts in this range and continues past it.
+__device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& R) {
+  MergeRec rec;
+  rec.np = 0;
+  rec.h = rec.mt = rec.o = rec.T = rec.ca = rec.pad = 0;
+  rec.C = R.C;
+  rec.ubeg = 0;
+  rec.total = R.total;
+  if (R.t0 < R.t1) {
+    const ReqGeom g = req_geom(a, R.r1);
+    const long long u = (R.t1 - 1 - R.rbeg1) / g.nts;
+    const long long ubeg = R.rbeg1 + u * g.nts;
+    if (ubeg >= R.t0 && ubeg + g.nts > R.t1) {
+      rec.ca = int(blockIdx.x);
+      rec.np = range_of(ubeg + g.nts - 1, R.total, R.C) - rec.ca + 1;
+      rec.h = int(u) / g.mts;
+      rec.mt = int(u) - rec.h * g.mts;
+      rec.o = g.o;
+      rec.T = g.T;
+      rec.ubeg = ubeg;
+    }
+  }
+  a.recs[blockIdx.x] = rec;
 }
 
 // ------------------------------------------------------------------------------ main kernel
@@ -413,6 +385,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   uint64_t* ex_bar = bars + 22;    // [4]: row-sum exchange of the two softmax halves
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // this CTA's range of the tile stream (the P tile is free scratch until the first scores)
+  const Range R = cta_range(a, reinterpret_cast<long long*>(sP), reinterpret_cast<int*>(sP + 256));
+  if (tid == 0) write_merge_record(a, R);
+  if (R.t0 >= R.t1) return;   // uniform across the CTA: no work, nothing allocated yet
   if (tid == 0) {
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
@@ -445,7 +421,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int it_beg = a.cta_off[blockIdx.x], it_end = a.cta_off[blockIdx.x + 1];
   volatile int* abort_flag = s_abort;
   const int G = a.G, log2G = a.log2G, tpt = kBM >> log2G;
   const bool layout_ok = *abort_flag == 0;
@@ -475,11 +450,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       if (lane == 0) r = tc::mbar_wait(bar, parity, abort_flag, kWaitLimit);
       return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
-    for (int idx = it_beg; idx < it_end && ok; ++idx, ++li) {
-      const Item it = a.items[idx];
-      const int o = a.node_offset[it.r];
-      const int T = a.node_offset[it.r + 1] - o;
-      const int P = a.prefix_len[it.r];
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    for (; ok && iter.next(a, R, it); ++li) {
+      const int o = it.o, T = it.T, P = it.P;
       const int nblk = (P + T + kBS - 1) / kBS;
       const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
       // physical block of this lane's page of tile j: -1 past the request, -2 if invalid
@@ -561,8 +536,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         tc::mma_commit(pv_done);
         return true;
       };
-      for (int idx = it_beg; idx < it_end && ok; ++idx, ++li) {
-        const Item it = a.items[idx];
+      ItemIter iter;
+      iter.start(a, R);
+      Item it;
+      for (; ok && iter.next(a, R, it); ++li) {
         if (!tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
         bool first_pv = true;
         for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
@@ -616,11 +593,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     };
     int kv_it = 0, li = 0;
     bool ok = true;
-    for (int idx = it_beg; idx < it_end && ok; ++idx, ++li) {
-      const Item it = a.items[idx];
-      const int o = a.node_offset[it.r];
-      const int T = a.node_offset[it.r + 1] - o;
-      const int P = a.prefix_len[it.r];
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    for (; ok && iter.next(a, R, it); ++li) {
+      const int o = it.o, T = it.T, P = it.P;
       const int kv_len = P + T;
       const int t = it.mt * tpt + t_loc;
       const bool valid = t < T;
@@ -775,7 +752,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                               __uint_as_float(r32[c + 2]) * inv, __uint_as_float(r32[c + 3]) * inv);
           }
         }
-        if (valid && hh == 0) a.part_lse[size_t(it.slot) * kBM + m] = lse2;
+        if (valid) a.part_lse[(size_t(it.slot) * 2 + hh) * kBM + m] = lse2;
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -787,50 +764,95 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   __syncthreads();
   if (*abort_flag && tid == 0) {
     // every request of this CTA's range is unreliable after an expired wait
-    for (int idx = it_beg; idx < it_end; ++idx) atomicOr(&a.req_status[a.items[idx].r], SPEC_REQ_TIMEOUT);
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    while (iter.next(a, R, it)) atomicOr(&a.req_status[it.r], SPEC_REQ_TIMEOUT);
   }
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
 }
 
 // ------------------------------------------------------------------------------ merge
-// One warp per output row of a cut unit: lane L covers output columns 4L .. 4L+3.
-__global__ void __launch_bounds__(128) attn_combine_kernel(TcDev a) {
-  const int n_comb = a.header[1];
+// CTA c merges the cut unit of record c by log-sum-exp of its pieces, in range order, into O and
+// lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2; pieces are read
+// kMergeGroup at a time with all of a group's loads issued together.
+constexpr int kMergeGroup = 2;
+
+__global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
+  using namespace attn;
+  const MergeRec rec = a.recs[blockIdx.x];
+  if (rec.np < 2) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tpt = attn::kBM >> a.log2G;
-  for (int u = blockIdx.x; u < n_comb; u += gridDim.x) {
-    const CombineUnit cu = a.combine[u];
-    const int o = a.node_offset[cu.r];
-    const int T = a.node_offset[cu.r + 1] - o;
-    for (int m = warp; m < attn::kBM; m += 4) {
-      const int t = cu.mt * tpt + (m >> a.log2G);
-      const int g = m & (a.G - 1);
-      if (t >= T) break;   // rows are token-major: this warp's remaining rows are past T
-      float M = -INFINITY;
-      for (int s = 0; s < cu.npieces; ++s)
-        M = fmaxf(M, a.part_lse[size_t(cu.slot0 + s) * attn::kBM + m]);
-      float wsum = 0.f;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < cu.npieces; ++s) {
-        const float ls = a.part_lse[size_t(cu.slot0 + s) * attn::kBM + m];
-        if (ls == -INFINITY) continue;
-        const float w = ex2(ls - M);
-        wsum += w;
-        const float4 v = *reinterpret_cast<const float4*>(
-            a.part_o + (size_t(cu.slot0 + s) * attn::kBM + m) * attn::kD + 4 * lane);
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  const int m = (warp & 3) * 32 + lane, hh = warp >> 2;
+  const int tpt = kBM >> a.log2G;
+  const int t = rec.mt * tpt + (m >> a.log2G), g = m & (a.G - 1);
+  if (t >= rec.T) return;
+  const int np = rec.np;
+  const float* lse_col = a.part_lse + size_t(hh) * kBM + m;   // + slot * 2 * kBM
+  auto slot_of = [&](int p) { return piece_slot(rec.ubeg, rec.total, rec.C, rec.ca + p); };
+  float M = -INFINITY;
+  for (int p0 = 0; p0 < np; p0 += kMergeGroup) {
+    float ls[kMergeGroup];
+#pragma unroll
+    for (int k = 0; k < kMergeGroup; ++k)
+      ls[k] = p0 + k < np ? lse_col[size_t(slot_of(p0 + k)) * 2 * kBM] : -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kMergeGroup; ++k) M = fmaxf(M, ls[k]);
+  }
+  float wsum = 0.f;
+  for (int p = 0; p < np; ++p) {
+    const float ls = lse_col[size_t(slot_of(p)) * 2 * kBM];
+    if (ls != -INFINITY) wsum += ex2(ls - M);
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* orow = a.o + (size_t(rec.o + t) * a.H_q + rec.h * a.G + g) * kD + 64 * hh;
+#pragma unroll 1
+  for (int c0 = 0; c0 < 64; c0 += 32) {
+    float acc[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    for (int p0 = 0; p0 < np; p0 += kMergeGroup) {
+      float4 v[kMergeGroup][8];
+      float wt[kMergeGroup];
+#pragma unroll
+      for (int k = 0; k < kMergeGroup; ++k) {
+        wt[k] = 0.f;
+        if (p0 + k < np) {
+          const int sl = slot_of(p0 + k);
+          const float ls = lse_col[size_t(sl) * 2 * kBM];
+          wt[k] = ls != -INFINITY ? ex2(ls - M) : 0.f;
+          const float4* src =
+              reinterpret_cast<const float4*>(a.part_o + (size_t(sl) * kBM + m) * kD + 64 * hh + c0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) v[k][q] = src[q];
+        }
       }
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      __nv_bfloat16* orow = a.o + (size_t(o + t) * a.H_q + cu.h * a.G + g) * attn::kD + 4 * lane;
-      uint2 v;
-      v.x = pack_bf16(acc.x * inv, acc.y * inv);
-      v.y = pack_bf16(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(orow) = v;
-      if (lane == 0 && a.lse)
-        a.lse[size_t(o + t) * a.H_q + cu.h * a.G + g] = (M + __log2f(wsum)) * 0.6931471805599453f;
+#pragma unroll
+      for (int k = 0; k < kMergeGroup; ++k) {
+        if (p0 + k < np && wt[k] != 0.f) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            acc[4 * q] += wt[k] * v[k][q].x;
+            acc[4 * q + 1] += wt[k] * v[k][q].y;
+            acc[4 * q + 2] += wt[k] * v[k][q].z;
+            acc[4 * q + 3] += wt[k] * v[k][q].w;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 o4;
+      o4.x = pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv);
+      o4.y = pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
+      o4.z = pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
+      o4.w = pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
+      *reinterpret_cast<uint4*>(orow + c0 + 8 * q) = o4;
     }
   }
+  if (hh == 0 && a.lse)
+    a.lse[size_t(rec.o + t) * a.H_q + rec.h * a.G + g] = (M + __log2f(wsum)) * 0.6931471805599453f;
 }
 
 // ------------------------------------------------------------------------------ host
@@ -852,8 +874,8 @@ static int attention_ctas() {
   return sms < attn::kMaxCtas ? sms : attn::kMaxCtas;
 }
 
-size_t attention_tc_workspace_size(const spec_attn_params* p) {
-  return tc_ws_layout(p, attention_ctas()).total;
+size_t attention_tc_workspace_size(const spec_attn_params*) {
+  return tc_ws_layout(attention_ctas()).total;
 }
 
 spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws_bytes,
@@ -867,7 +889,7 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
     return SPEC_ERR_UNSUPPORTED;
   const int ctas = attention_ctas();
   if (ctas <= 0) return SPEC_ERR_CUDA;
-  const TcWs lay = tc_ws_layout(p, ctas);
+  const TcWs lay = tc_ws_layout(ctas);
   if (!ws || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SPEC_ERR_INVALID_ARG;
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return SPEC_ERR_CUDA;
@@ -915,11 +937,7 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   d.o = static_cast<__nv_bfloat16*>(p->o);
   d.lse = p->lse;
   d.req_status = p->req_status;
-  d.header = reinterpret_cast<int*>(w + lay.header);
-  d.cta_off = reinterpret_cast<int*>(w + lay.cta_off);
-  d.req_tiles = reinterpret_cast<int*>(w + lay.req_tiles);
-  d.items = reinterpret_cast<Item*>(w + lay.items);
-  d.combine = reinterpret_cast<CombineUnit*>(w + lay.combine);
+  d.recs = reinterpret_cast<MergeRec*>(w + lay.recs);
   d.part_o = reinterpret_cast<float*>(w + lay.part_o);
   d.part_lse = reinterpret_cast<float*>(w + lay.part_lse);
   d.B = p->B; d.N = p->N; d.H_q = p->H_q; d.H_kv = p->H_kv; d.G = G;
@@ -928,16 +946,14 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   d.num_blocks = p->num_blocks; d.max_blocks = p->max_blocks_per_req;
   d.kv_rows = int(kv_rows);
   d.ctas = ctas;
-  d.max_items = lay.max_items; d.max_combine = lay.max_combine;
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf(float(kD));
   d.scale_log2 = scale * 1.4426950408889634f;
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
-  attn_prep_kernel<<<1, 1024, 0, s>>>(d);
   attn_tc_kernel<<<ctas, kThreads, kSmemBytes, s>>>(mQ, mK, mV, mK8, mV8, d);
-  attn_combine_kernel<<<lay.max_combine, 128, 0, s>>>(d);
+  attn_merge_kernel<<<ctas, 256, 0, s>>>(d);
   return launch_status();
 }
 
