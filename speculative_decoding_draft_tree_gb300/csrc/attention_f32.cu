@@ -30,6 +30,8 @@ struct AttnF32Dev {
 };
 
 __global__ void __launch_bounds__(128) attention_f32_kernel(AttnF32Dev a) {
+  pdl_wait();
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long pair = long(blockIdx.x) * 4 + warp;
   if (pair >= long(a.N) * a.H_q) return;
@@ -128,8 +130,7 @@ spec_status_t launch_attention_f32(const spec_attn_params* p, cudaStream_t s) {
   const long pairs = long(p->N) * p->H_q;
   if (pairs == 0) return SPEC_OK;
   const unsigned grid = unsigned((pairs + 3) / 4);
-  attention_f32_kernel<<<grid, 128, 0, s>>>(d);
-  return launch_status();
+  return launch_result(launch_pdl(attention_f32_kernel, dim3(grid), dim3(128), 0, s, d));
 }
 
 }  // namespace spec

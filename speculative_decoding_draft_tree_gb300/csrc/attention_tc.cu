@@ -385,6 +385,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   uint64_t* ex_bar = bars + 22;    // [4]: row-sum exchange of the two softmax halves
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
   // this CTA's range of the tile stream (the P tile is free scratch until the first scores)
   const Range R = cta_range(a, reinterpret_cast<long long*>(sP), reinterpret_cast<int*>(sP + 256));
   if (tid == 0) write_merge_record(a, R);
@@ -781,6 +783,8 @@ constexpr int kMergeGroup = 2;
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   using namespace attn;
+  pdl_wait();
+  pdl_trigger();
   const MergeRec rec = a.recs[blockIdx.x];
   if (rec.np < 2) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -952,9 +956,10 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   std::call_once(attr_once, [] {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
-  attn_tc_kernel<<<ctas, kThreads, kSmemBytes, s>>>(mQ, mK, mV, mK8, mV8, d);
-  attn_merge_kernel<<<ctas, 256, 0, s>>>(d);
-  return launch_status();
+  cudaError_t le = launch_pdl(attn_tc_kernel, dim3(ctas), dim3(kThreads), size_t(kSmemBytes), s,
+                              mQ, mK, mV, mK8, mV8, d);
+  if (le == cudaSuccess) le = launch_pdl(attn_merge_kernel, dim3(ctas), dim3(256), 0, s, d);
+  return launch_result(le);
 }
 
 }  // namespace spec

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "spec_verify.h"
 
 #define SPEC_HOST_DEVICE __host__ __device__ __forceinline__
@@ -30,9 +32,47 @@ inline spec_status_t launch_status() {
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Launch with programmatic stream serialization allowed: the kernel may be scheduled while the
+// previous kernel on the stream is still running (once every CTA of that kernel has executed
+// pdl_trigger or exited), and waits in pdl_wait until that kernel has completed and its memory
+// is visible.  This hides the launch latency between the dependent kernels of one call and
+// across calls.  After any other stream operation it behaves like a plain launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+inline spec_status_t launch_result(cudaError_t e) {
+  if (e != cudaSuccess) {
+    set_last_cuda_error(e);
+    cudaGetLastError();   // the error is reported here; do not leave it for the next call
+    return SPEC_ERR_CUDA;
+  }
+  return launch_status();
+}
+
 // ------------------------------------------------------------------------------------------
 // device side
 // ------------------------------------------------------------------------------------------
+// Every kernel of the library calls pdl_wait() before its first global memory access (the
+// previous kernel on the stream may still be writing its inputs) and then pdl_trigger(), which
+// lets the next kernel be scheduled early.  Both are no-ops for a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -31,6 +31,8 @@ struct CompactDev {
 };
 
 __global__ void __launch_bounds__(256) kv_compact_kernel(CompactDev a) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int layer = blockIdx.y;
   const int tid = threadIdx.x;
@@ -150,6 +152,5 @@ extern "C" spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stre
   d.max_blocks = p->max_blocks_per_req;
   d.max_path = p->max_path;
   dim3 grid(p->B, p->num_layers);
-  kv_compact_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(d);
-  return launch_status();
+  return launch_result(launch_pdl(kv_compact_kernel, grid, dim3(256), 0, (cudaStream_t)stream, d));
 }

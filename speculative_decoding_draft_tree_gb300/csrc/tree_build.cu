@@ -43,6 +43,8 @@ tree_build_kernel(const int32_t* __restrict__ parent, const int32_t* __restrict_
                   int32_t* __restrict__ req_status) {
   __shared__ int16_t s_par[SPEC_MAX_TREE];
   __shared__ uint8_t s_has_child[SPEC_MAX_TREE];
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int i = threadIdx.x;
   const int o = node_offset[r];
@@ -120,10 +122,10 @@ spec_status_t spec_tree_build(const int32_t* parent, const int32_t* node_offset,
   if (N > 0 && (!parent || !depth || !pos_id || !anc_mask || !is_internal))
     return SPEC_ERR_INVALID_ARG;
   const int W = (T_max + 31) / 32;
-  spec::tree_build_kernel<<<B, spec::kTreeThreads, 0, (cudaStream_t)stream>>>(
+  return spec::launch_result(spec::launch_pdl(
+      spec::tree_build_kernel, dim3(B), dim3(spec::kTreeThreads), 0, (cudaStream_t)stream,
       parent, node_offset, prefix_len, N, T_max, W, depth, pos_id, anc_mask, is_internal,
-      req_status);
-  return spec::launch_status();
+      req_status));
 }
 
 }  // extern "C"

@@ -9,14 +9,14 @@
 //     P(. | ancestors(i)); verification walks every level of the tree;
 //   "万字综述 10+ 种 LLM 投机采样推理加速方案" (m.haoling.cc) 4.3 -- argmax sampling at temp = 0.
 //
-// Three launches on the caller's stream:
-//   1. prep  (one CTA per request): validates tokens / draft rows / depths, marks the target
-//      rows of internal nodes and the draft rows they reference;
-//   2. rows  (one CTA per marked row, 256 threads): ONE streaming read of the row with 16-byte
+// Two launches on the caller's stream:
+//   1. rows  (one CTA per internal node's target row and, for tau > 0 with draft logits, per
+//      draft row; 512 threads): ONE streaming read of the row with 16-byte
 //      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over 32-element chunks
 //      (Kahan-compensated), then a block reduction (max, then a double-float sum) -> (m, Z);
 //      tau = 0 keeps (max, lowest argmax) instead;
-//   3. walk  (one CTA of 512 threads per request): the tree walk.  A parallel prologue gathers
+//   2. walk  (one CTA of 512 threads per request): validates the request's tokens, draft rows
+//      and depths, then walks the tree.  A parallel prologue gathers
 //      every node's test operands and decides every plain ratio test u < p / q at once (thread
 //      per node, from (m, Z)); only later siblings under the residual rule are tested on the way,
 //      on thread 0.  Every vocab-wide step (sibling residual mass, residual / bonus inverse CDF,
@@ -62,8 +62,6 @@ struct VerifyDev {
   int32_t* rejections;
   RowStat* tstat;
   RowStat* dstat;
-  uint8_t* t_need;
-  uint32_t* d_need;
 };
 
 // ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
@@ -95,66 +93,26 @@ __device__ __forceinline__ float sum8(const float (&w)[8]) {
   return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
 }
 
-// ---- 1. prep -------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) verify_prep_kernel(VerifyDev a) {
-  const int r = blockIdx.x;
-  const int o = a.node_offset[r];
-  const int e = a.node_offset[r + 1];
-  const int T = e - o;
-  const bool range_ok = o >= 0 && e <= a.N && T >= 1 && T <= a.T_max;
-  const int st = a.req_status[r];
-  if (!range_ok || st != 0) {
-    if (threadIdx.x == 0 && !range_ok) atomicOr(&a.req_status[r], SPEC_REQ_BAD_SIZE);
-    return;
-  }
-  int bad = 0;
-  for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int n = o + i;
-    if (i > 0) {
-      const int tok = a.tokens[n];
-      if (tok < 0 || tok >= a.V) bad |= SPEC_REQ_BAD_TOKEN;
-    }
-    if (a.depth[n] + 1 > a.max_path) bad |= SPEC_REQ_BAD_DEPTH;
-    if (a.tau > 0.f && a.is_internal[n]) {
-      const int dr = a.draft_row[n];
-      if (dr < 0 || dr >= a.R) bad |= SPEC_REQ_BAD_DRAFT_ROW;
-    }
-  }
-  __shared__ int s_bad;
-  if (threadIdx.x == 0) s_bad = 0;
-  __syncthreads();
-  if (bad) atomicOr(&s_bad, bad);
-  __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) atomicOr(&a.req_status[r], s_bad);
-    return;
-  }
-  for (int i = threadIdx.x; i < T; i += blockDim.x) {
-    const int n = o + i;
-    if (a.is_internal[n]) {
-      a.t_need[n] = 1;
-      if (a.tau > 0.f && !a.probs) a.d_need[a.draft_row[n]] = 1u;  // benign: all store 1
-    }
-  }
-}
-
-// ---- 2. rows: (m, Z) or (max, argmax) in one streaming read --------------------------------
+// ---- 1. rows: (m, Z) or (max, argmax) in one streaming read --------------------------------
 constexpr int kRowThreads = 512;
 constexpr int kRowUnroll = 8;   // 8 x 16-byte loads in flight per thread
 constexpr int kRowWarps = kRowThreads / 32;
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   const T* row;
   RowStat* out;
   if (b < a.N) {
-    if (!a.t_need[b]) return;
+    // statistics of every internal node's target row (also in requests the walk will reject:
+    // reading a row of [0, N) is always safe, and skipping them would need the validation first)
+    if (!a.is_internal[b]) return;
     row = reinterpret_cast<const T*>(a.target) + size_t(b) * a.tld;
     out = a.tstat + b;
   } else {
     const int rr = b - a.N;
-    if (!a.d_need[rr]) return;
     row = reinterpret_cast<const T*>(a.draft) + size_t(rr) * a.dld;
     out = a.dstat + rr;
   }
@@ -266,7 +224,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
   }
 }
 
-// ---- 3. walk -------------------------------------------------------------------------------
+// ---- 2. walk -------------------------------------------------------------------------------
 // fp64 runs on thread 0 (or one warp) only: GB300's fp64 rate is a small fraction of fp32, and a
 // double division executed by all 32 warps of the block costs microseconds.
 constexpr int kWalkThreads = 512;   // 128 registers per thread: four units' loads in flight
@@ -302,6 +260,7 @@ struct WalkSmem {
   float Cf;
   int wsel, found, fallback, pos;
   int decision;
+  int bad;                         // SPEC_REQ_* bits found by the validation
 };
 
 __device__ __forceinline__ int warp_max_i(int v) {
@@ -578,12 +537,39 @@ template <typename TT, typename TD>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
   __shared__ WalkSmem sh;
   extern __shared__ float usum_dyn[];
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
-  const int st = a.req_status[r];
   int32_t* path_row = a.path + size_t(r) * a.max_path;
   int32_t* tok_row = a.out_tokens + size_t(r) * a.max_path;
+  // validation: the node range, then every node's token, depth and (tau > 0) draft row
+  const int st0 = a.req_status[r];
+  const int o = a.node_offset[r];
+  const int T = a.node_offset[r + 1] - o;
+  const bool range_ok = o >= 0 && T >= 1 && T <= a.T_max && o + T <= a.N;
+  if (tid == 0) sh.bad = range_ok ? 0 : SPEC_REQ_BAD_SIZE;
+  __syncthreads();
+  if (st0 == 0 && range_ok) {
+    int bad = 0;
+    for (int i = tid; i < T; i += kWalkThreads) {
+      const int n = o + i;
+      if (i > 0) {
+        const int tok = a.tokens[n];
+        if (tok < 0 || tok >= a.V) bad |= SPEC_REQ_BAD_TOKEN;
+      }
+      if (a.depth[n] + 1 > a.max_path) bad |= SPEC_REQ_BAD_DEPTH;
+      if (a.tau > 0.f && a.is_internal[n]) {
+        const int dr = a.draft_row[n];
+        if (dr < 0 || dr >= a.R) bad |= SPEC_REQ_BAD_DRAFT_ROW;
+      }
+    }
+    if (bad) atomicOr(&sh.bad, bad);
+  }
+  __syncthreads();
+  const int st = st0 | sh.bad;
   if (st != 0) {
+    if (tid == 0 && sh.bad) atomicOr(&a.req_status[r], sh.bad);
     for (int k = tid; k < a.max_path; k += kWalkThreads) { path_row[k] = -1; tok_row[k] = -1; }
     if (tid == 0) {
       a.out_len[r] = 0;
@@ -593,8 +579,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     return;
   }
   float* usum = (a.V + 7) / 8 <= kWalkMaxSmemUnits ? usum_dyn : nullptr;
-  const int o = a.node_offset[r];
-  const int T = a.node_offset[r + 1] - o;
   const TT* target = reinterpret_cast<const TT*>(a.target);
   const TD* draft = reinterpret_cast<const TD*>(a.draft);
   const bool greedy = a.tau == 0.f;
@@ -773,7 +757,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
 }
 
 struct VerifyWs {
-  size_t tstat, dstat, t_need, d_need, total;
+  size_t tstat, dstat, total;
 };
 
 static VerifyWs verify_ws_layout(int N, int R) {
@@ -781,15 +765,18 @@ static VerifyWs verify_ws_layout(int N, int R) {
   size_t off = 0;
   w.tstat = off; off = align_up(off + sizeof(RowStat) * size_t(N > 0 ? N : 1), 256);
   w.dstat = off; off = align_up(off + sizeof(RowStat) * size_t(R > 0 ? R : 1), 256);
-  w.t_need = off; off = align_up(off + size_t(N > 0 ? N : 1), 256);
-  w.d_need = off; off = align_up(off + 4 * size_t(R > 0 ? R : 1), 256);
   w.total = off;
   return w;
 }
 
 template <typename TT, typename TD>
-static spec_status_t launch_verify(const VerifyDev& d, bool run_rows, cudaStream_t s) {
-  if (run_rows) verify_rows_kernel<TT><<<d.N + (d.probs ? 0 : d.R), kRowThreads, 0, s>>>(d);
+static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
+  // draft-row statistics are needed only for tau > 0 with draft logits
+  const int rows = d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
+  if (rows > 0) {
+    const cudaError_t e = launch_pdl(verify_rows_kernel<TT>, dim3(rows), dim3(kRowThreads), 0, s, d);
+    if (e != cudaSuccess) return launch_result(e);
+  }
   const int nunits = (d.V + 7) / 8;
   const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
   if (dyn > 0) {
@@ -808,8 +795,7 @@ static spec_status_t launch_verify(const VerifyDev& d, bool run_rows, cudaStream
       raised[dev] = true;
     }
   }
-  verify_walk_kernel<TT, TD><<<d.B, kWalkThreads, dyn, s>>>(d);
-  return launch_status();
+  return launch_result(launch_pdl(verify_walk_kernel<TT, TD>, dim3(d.B), dim3(kWalkThreads), dyn, s, d));
 }
 
 }  // namespace spec
@@ -869,19 +855,12 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   d.out_len = p->out_len; d.path = p->path; d.n_acc = p->n_acc; d.rejections = p->rejections;
   d.tstat = reinterpret_cast<RowStat*>(ws + lay.tstat);
   d.dstat = reinterpret_cast<RowStat*>(ws + lay.dstat);
-  d.t_need = reinterpret_cast<uint8_t*>(ws + lay.t_need);
-  d.d_need = reinterpret_cast<uint32_t*>(ws + lay.d_need);
   cudaStream_t s = (cudaStream_t)stream;
-  if (cudaMemsetAsync(ws + lay.t_need, 0, lay.total - lay.t_need, s) != cudaSuccess)
-    return launch_status();
-  verify_prep_kernel<<<p->B, 256, 0, s>>>(d);
-  if (cudaGetLastError() != cudaSuccess) return launch_status();
-  const bool run_rows = p->N > 0;
   if (p->logits_dtype == SPEC_BF16) {
-    if (d.probs) return launch_verify<__nv_bfloat16, float>(d, run_rows, s);
-    return launch_verify<__nv_bfloat16, __nv_bfloat16>(d, run_rows, s);
+    if (d.probs) return launch_verify<__nv_bfloat16, float>(d, s);
+    return launch_verify<__nv_bfloat16, __nv_bfloat16>(d, s);
   }
-  return launch_verify<float, float>(d, run_rows, s);
+  return launch_verify<float, float>(d, s);
 }
 
 }  // extern "C"
@@ -897,16 +876,15 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
 // The first call on each device looks the array's device address up (cudaGetSymbolAddress)
 // with that device current; make that first call before any stream capture.  All calls share
 // the array: calls whose kernels overlap on the GPU (different streams, or different host
-// threads on the same device) race on it.  spec_verify clears the part that must start at zero
-// on every call, so the contents left by an earlier call do not matter.
+// threads on the same device) race on it.  Every call writes the statistics it reads before
+// reading them, so the contents left by an earlier call do not matter.
 // ------------------------------------------------------------------------------------------
 namespace spec {
 constexpr int kNoAllocMaxNodes = 32768;
 constexpr int kNoAllocMaxDraftRows = 32768;
 constexpr size_t kNoAllocScratchBytes =
     align_up(sizeof(RowStat) * kNoAllocMaxNodes, 256) +
-    align_up(sizeof(RowStat) * kNoAllocMaxDraftRows, 256) + align_up(kNoAllocMaxNodes, 256) +
-    align_up(4 * size_t(kNoAllocMaxDraftRows), 256);
+    align_up(sizeof(RowStat) * kNoAllocMaxDraftRows, 256);
 static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
 }  // namespace spec
 
