@@ -66,10 +66,11 @@ constexpr int kMaxCtas = 1024;                // persistent CTAs at most
 constexpr int kMinTilesPerRange = 4;          // small problems use fewer, longer ranges
 }  // namespace attn
 
-// A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1.
+// A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1; the first piece's
+// partial slot is slot0 (2 ca, or 2 ca + 1 when the unit starts inside range ca), piece p > 0
+// starts range ca + p and uses slot 2 (ca + p).
 struct MergeRec {
-  int np, h, mt, o, T, ca, C, pad;
-  long long ubeg, total;
+  int np, h, mt, o, T, ca, slot0, pad;
 };
 
 struct TcDev {
@@ -280,10 +281,7 @@ struct ItemIter {
 __device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& R) {
   MergeRec rec;
   rec.np = 0;
-  rec.h = rec.mt = rec.o = rec.T = rec.ca = rec.pad = 0;
-  rec.C = R.C;
-  rec.ubeg = 0;
-  rec.total = R.total;
+  rec.h = rec.mt = rec.o = rec.T = rec.ca = rec.slot0 = rec.pad = 0;
   if (R.t0 < R.t1) {
     const ReqGeom g = req_geom(a, R.r1);
     const long long u = (R.t1 - 1 - R.rbeg1) / g.nts;
@@ -295,7 +293,7 @@ __device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& 
       rec.mt = int(u) - rec.h * g.mts;
       rec.o = g.o;
       rec.T = g.T;
-      rec.ubeg = ubeg;
+      rec.slot0 = piece_slot(ubeg, R.total, R.C, rec.ca);
     }
   }
   a.recs[blockIdx.x] = rec;
@@ -777,9 +775,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 
 // ------------------------------------------------------------------------------ merge
 // CTA c merges the cut unit of record c by log-sum-exp of its pieces, in range order, into O and
-// lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2; pieces are read
-// kMergeGroup at a time with all of a group's loads issued together.
-constexpr int kMergeGroup = 2;
+// lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2.  A unit has at most
+// kMergeFast pieces in the common case: their log-sum-exps and all 64 partial columns are loaded
+// in one batch; longer units take the general loop.
+constexpr int kMergeFast = 2;
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   using namespace attn;
@@ -793,70 +792,85 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   const int t = rec.mt * tpt + (m >> a.log2G), g = m & (a.G - 1);
   if (t >= rec.T) return;
   const int np = rec.np;
-  const float* lse_col = a.part_lse + size_t(hh) * kBM + m;   // + slot * 2 * kBM
-  auto slot_of = [&](int p) { return piece_slot(rec.ubeg, rec.total, rec.C, rec.ca + p); };
-  float M = -INFINITY;
-  for (int p0 = 0; p0 < np; p0 += kMergeGroup) {
-    float ls[kMergeGroup];
-#pragma unroll
-    for (int k = 0; k < kMergeGroup; ++k)
-      ls[k] = p0 + k < np ? lse_col[size_t(slot_of(p0 + k)) * 2 * kBM] : -INFINITY;
-#pragma unroll
-    for (int k = 0; k < kMergeGroup; ++k) M = fmaxf(M, ls[k]);
-  }
-  float wsum = 0.f;
-  for (int p = 0; p < np; ++p) {
-    const float ls = lse_col[size_t(slot_of(p)) * 2 * kBM];
-    if (ls != -INFINITY) wsum += ex2(ls - M);
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  auto slot_of = [&](int p) { return p == 0 ? rec.slot0 : 2 * (rec.ca + p); };
+  auto lse_of = [&](int p) { return a.part_lse[(size_t(slot_of(p)) * 2 + hh) * kBM + m]; };
+  auto part_of = [&](int p) {
+    return reinterpret_cast<const float4*>(a.part_o + (size_t(slot_of(p)) * kBM + m) * kD + 64 * hh);
+  };
   __nv_bfloat16* orow = a.o + (size_t(rec.o + t) * a.H_q + rec.h * a.G + g) * kD + 64 * hh;
-#pragma unroll 1
-  for (int c0 = 0; c0 < 64; c0 += 32) {
-    float acc[32];
+  float M = -INFINITY, wsum = 0.f, out_lse;
+  if (np <= kMergeFast) {
+    float ls[kMergeFast];
+    float4 v[kMergeFast][16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-    for (int p0 = 0; p0 < np; p0 += kMergeGroup) {
-      float4 v[kMergeGroup][8];
-      float wt[kMergeGroup];
+    for (int p = 0; p < kMergeFast; ++p) {
+      ls[p] = p < np ? lse_of(p) : -INFINITY;
+      if (p < np) {
+        const float4* src = part_of(p);
 #pragma unroll
-      for (int k = 0; k < kMergeGroup; ++k) {
-        wt[k] = 0.f;
-        if (p0 + k < np) {
-          const int sl = slot_of(p0 + k);
-          const float ls = lse_col[size_t(sl) * 2 * kBM];
-          wt[k] = ls != -INFINITY ? ex2(ls - M) : 0.f;
-          const float4* src =
-              reinterpret_cast<const float4*>(a.part_o + (size_t(sl) * kBM + m) * kD + 64 * hh + c0);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) v[k][q] = src[q];
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < kMergeGroup; ++k) {
-        if (p0 + k < np && wt[k] != 0.f) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            acc[4 * q] += wt[k] * v[k][q].x;
-            acc[4 * q + 1] += wt[k] * v[k][q].y;
-            acc[4 * q + 2] += wt[k] * v[k][q].z;
-            acc[4 * q + 3] += wt[k] * v[k][q].w;
-          }
-        }
+        for (int q = 0; q < 16; ++q) v[p][q] = src[q];
       }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int p = 0; p < kMergeFast; ++p) M = fmaxf(M, ls[p]);
+    float wt[kMergeFast];
+#pragma unroll
+    for (int p = 0; p < kMergeFast; ++p) {
+      wt[p] = ls[p] != -INFINITY ? ex2(ls[p] - M) : 0.f;
+      wsum += wt[p];
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; q += 2) {
+      float acc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+      for (int p = 0; p < kMergeFast; ++p) {
+        if (wt[p] != 0.f) {
+          acc[0] += wt[p] * v[p][q].x; acc[1] += wt[p] * v[p][q].y;
+          acc[2] += wt[p] * v[p][q].z; acc[3] += wt[p] * v[p][q].w;
+          acc[4] += wt[p] * v[p][q + 1].x; acc[5] += wt[p] * v[p][q + 1].y;
+          acc[6] += wt[p] * v[p][q + 1].z; acc[7] += wt[p] * v[p][q + 1].w;
+        }
+      }
       uint4 o4;
-      o4.x = pack_bf16(acc[8 * q] * inv, acc[8 * q + 1] * inv);
-      o4.y = pack_bf16(acc[8 * q + 2] * inv, acc[8 * q + 3] * inv);
-      o4.z = pack_bf16(acc[8 * q + 4] * inv, acc[8 * q + 5] * inv);
-      o4.w = pack_bf16(acc[8 * q + 6] * inv, acc[8 * q + 7] * inv);
-      *reinterpret_cast<uint4*>(orow + c0 + 8 * q) = o4;
+      o4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      o4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      o4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+      o4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(orow + 4 * q) = o4;
+    }
+  } else {
+    for (int p = 0; p < np; ++p) M = fmaxf(M, lse_of(p));
+    for (int p = 0; p < np; ++p) {
+      const float ls = lse_of(p);
+      if (ls != -INFINITY) wsum += ex2(ls - M);
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll 1
+    for (int q = 0; q < 16; q += 2) {
+      float acc[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+      for (int p = 0; p < np; ++p) {
+        const float ls = lse_of(p);
+        if (ls == -INFINITY) continue;
+        const float wt = ex2(ls - M);
+        const float4 v0 = part_of(p)[q], v1 = part_of(p)[q + 1];
+        acc[0] += wt * v0.x; acc[1] += wt * v0.y; acc[2] += wt * v0.z; acc[3] += wt * v0.w;
+        acc[4] += wt * v1.x; acc[5] += wt * v1.y; acc[6] += wt * v1.z; acc[7] += wt * v1.w;
+      }
+      uint4 o4;
+      o4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+      o4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+      o4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+      o4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(orow + 4 * q) = o4;
     }
   }
-  if (hh == 0 && a.lse)
-    a.lse[size_t(rec.o + t) * a.H_q + rec.h * a.G + g] = (M + __log2f(wsum)) * 0.6931471805599453f;
+  out_lse = (M + __log2f(wsum)) * 0.6931471805599453f;
+  if (hh == 0 && a.lse) a.lse[size_t(rec.o + t) * a.H_q + rec.h * a.G + g] = out_lse;
 }
 
 // ------------------------------------------------------------------------------ host

@@ -40,6 +40,7 @@ struct RowStat {
   int32_t pad;
 };
 
+
 struct VerifyDev {
   const void* target;
   const void* draft;
@@ -93,13 +94,183 @@ __device__ __forceinline__ float sum8(const float (&w)[8]) {
   return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
 }
 
+// One 8-element unit of a row as raw 16-byte vectors, so that several units' loads can be
+// issued before any of them is used.
+template <typename T>
+struct RawUnit {
+  static constexpr int kVec = int(sizeof(T)) / 2;   // 1 for bf16, 2 for fp32
+  uint4 v[kVec];
+  __device__ __forceinline__ void load(const T* row, int unit) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) v[k] = ld_stream16(row + size_t(unit) * 8 + k * (8 / kVec));
+  }
+  // the unit's 8 values; the ragged last unit (unit >= full) is read element by element
+  __device__ __forceinline__ void get(const T* row, int unit, int V, int full, float fill,
+                                      float (&x)[8]) const {
+    if (unit < full) {
+      if constexpr (kVec == 1) {
+        elem<T>::unpack(v[0], x);
+      } else {
+        elem<float>::unpack(v[0], x);
+        float y[4];
+        elem<float>::unpack(v[1], y);
+        x[4] = y[0]; x[5] = y[1]; x[6] = y[2]; x[7] = y[3];
+      }
+    } else {
+      load8(row, unit, V, full, fill, x);
+    }
+  }
+};
+
 // ---- 1. rows: (m, Z) or (max, argmax) in one streaming read --------------------------------
-constexpr int kRowThreads = 512;
-constexpr int kRowUnroll = 8;   // 8 x 16-byte loads in flight per thread
+// One row's statistics take one CTA of kRowThreads threads (several CTAs fit on an SM, which
+// keeps more loads in flight per SM than one large CTA per row).
+constexpr int kRowThreads = 256;
 constexpr int kRowWarps = kRowThreads / 32;
+
+struct RowScratch {
+  float f[kRowWarps];
+  int i[kRowWarps];
+  float hi[kRowWarps], lo[kRowWarps];
+  RowStat out;
+};
+
+// barrier over the kRowThreads threads of one row (named barrier `bar`)
+__device__ __forceinline__ void row_sync(int bar) {
+  asm volatile("bar.sync %0, %1;" ::"r"(bar), "n"(kRowThreads) : "memory");
+}
+
+// pairwise sum of n values (n a power of two), a fixed tree
+template <int n>
+__device__ __forceinline__ float tree_sum(const float* t) {
+  if constexpr (n == 1) {
+    return t[0];
+  } else {
+    return tree_sum<n / 2>(t) + tree_sum<n / 2>(t + n / 2);
+  }
+}
+
+// (m, Z) -- or (max, lowest argmax) for tau = 0 -- of one row, computed by kRowThreads threads
+// and returned to each of them.  Each thread keeps kUnroll 16-byte loads in flight, then folds
+// them into an online max / Kahan-compensated sum of 2^((x - m) log2(e) / tau); the block
+// combines maxima, then double-float sums.
+template <typename T>
+__device__ RowStat row_stats(const T* row, const VerifyDev& a, RowScratch& sc, int bar) {
+  constexpr int kUnroll = 8;
+  constexpr int kStep = kUnroll * kRowThreads;
+  const int tid = threadIdx.x % kRowThreads, lane = tid & 31, warp = tid >> 5;
+  const int V = a.V, full = V / 8, nunits = (V + 7) / 8;
+  if (a.tau == 0.f) {
+    float best = -INFINITY;
+    int arg = 0x7fffffff;
+    for (int u0 = tid; u0 < nunits; u0 += kStep) {
+      RawUnit<T> raw[kUnroll];
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int unit = u0 + j * kRowThreads;
+        if (unit < full) raw[j].load(row, unit);
+      }
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int unit = u0 + j * kRowThreads;
+        if (unit < nunits) {
+          float x[8];
+          raw[j].get(row, unit, V, full, -INFINITY, x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (x[k] > best) { best = x[k]; arg = unit * 8 + k; }
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float ob = __shfl_xor_sync(0xffffffffu, best, off);
+      int oa = __shfl_xor_sync(0xffffffffu, arg, off);
+      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
+    }
+    if (lane == 0) { sc.f[warp] = best; sc.i[warp] = arg; }
+    row_sync(bar);
+    if (tid == 0) {
+      float bb = sc.f[0];
+      int ba = sc.i[0];
+      for (int w = 1; w < kRowWarps; ++w)
+        if (sc.f[w] > bb || (sc.f[w] == bb && sc.i[w] < ba)) { bb = sc.f[w]; ba = sc.i[w]; }
+      sc.out = RowStat{bb, ba, 0.0, 0.f, 0};
+    }
+  } else {
+    const float k2 = a.k2;
+    float m = -INFINITY, s = 0.f, c = 0.f;  // Kahan: true sum ~ s - c
+    for (int u0 = tid; u0 < nunits; u0 += kStep) {
+      RawUnit<T> raw[kUnroll];
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int unit = u0 + j * kRowThreads;
+        if (unit < full) raw[j].load(row, unit);
+      }
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kUnroll; ++j) {
+        const int unit = u0 + j * kRowThreads;
+        if (unit < nunits) {
+          float x[8];
+          raw[j].get(row, unit, V, full, -INFINITY, x);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) cm = fmaxf(cm, x[k]);
+        }
+      }
+      if (cm > m) {
+        const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
+        s *= f;
+        c *= f;
+        m = cm;
+      }
+      if (m != -INFINITY) {
+        float tj[kUnroll];
+#pragma unroll
+        for (int j = 0; j < kUnroll; ++j) {
+          const int unit = u0 + j * kRowThreads;
+          tj[j] = 0.f;
+          if (unit < nunits) {
+            float x[8], w[8];
+            raw[j].get(row, unit, V, full, -INFINITY, x);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = ex2((x[k] - m) * k2);
+            tj[j] = sum8(w);
+          }
+        }
+        const float chunk = tree_sum<kUnroll>(tj);
+        const float y = chunk - c;
+        const float t = s + y;
+        c = (t - s) - y;
+        s = t;
+      }
+    }
+    float M = warp_max(m);
+    if (lane == 0) sc.f[warp] = M;
+    row_sync(bar);
+    M = sc.f[0];
+#pragma unroll
+    for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, sc.f[w]);
+    const float mine = (m == -INFINITY) ? 0.f : (s - c) * ex2((m - M) * k2);
+    dfloat acc = warp_sum_df(df_make(mine));
+    if (lane == 0) { sc.hi[warp] = acc.hi; sc.lo[warp] = acc.lo; }
+    row_sync(bar);
+    if (tid == 0) {
+      dfloat tot = {sc.hi[0], sc.lo[0]};
+      for (int w = 1; w < kRowWarps; ++w) tot = df_add(tot, dfloat{sc.hi[w], sc.lo[w]});
+      const double Z = df_to_d(tot);
+      sc.out = RowStat{M, -1, Z, float(1.0 / Z), 0};
+    }
+  }
+  row_sync(bar);
+  const RowStat out = sc.out;
+  row_sync(bar);
+  return out;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
+  __shared__ RowScratch sc;
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -116,112 +287,8 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
     row = reinterpret_cast<const T*>(a.draft) + size_t(rr) * a.dld;
     out = a.dstat + rr;
   }
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int V = a.V, full = V / 8, nunits = (V + 7) / 8;
-  __shared__ float s_f[kRowWarps];
-  __shared__ int s_i[kRowWarps];
-  __shared__ float s_hi[kRowWarps], s_lo[kRowWarps];
-  constexpr int kStep = kRowUnroll * kRowThreads;
-  if (a.tau == 0.f) {
-    float best = -INFINITY;
-    int arg = 0x7fffffff;
-    for (int u0 = tid; u0 < nunits; u0 += kStep) {
-      float x[kRowUnroll][8];
-#pragma unroll
-      for (int j = 0; j < kRowUnroll; ++j) {
-        const int unit = u0 + j * kRowThreads;
-        if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
-        else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) x[j][k] = -INFINITY;
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < kRowUnroll; ++j)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (x[j][k] > best) { best = x[j][k]; arg = (u0 + j * kRowThreads) * 8 + k; }
-    }
-    // block (max value, lowest index)
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float ob = __shfl_xor_sync(0xffffffffu, best, off);
-      int oa = __shfl_xor_sync(0xffffffffu, arg, off);
-      if (ob > best || (ob == best && oa < arg)) { best = ob; arg = oa; }
-    }
-    if (lane == 0) { s_f[warp] = best; s_i[warp] = arg; }
-    __syncthreads();
-    if (tid == 0) {
-      float bb = s_f[0];
-      int ba = s_i[0];
-      for (int w = 1; w < kRowWarps; ++w)
-        if (s_f[w] > bb || (s_f[w] == bb && s_i[w] < ba)) { bb = s_f[w]; ba = s_i[w]; }
-      out->m = bb;
-      out->arg = ba;
-      out->Z = 0.0;
-      out->inv_Z = 0.f;
-    }
-    return;
-  }
-  const float k2 = a.k2;
-  float m = -INFINITY, s = 0.f, c = 0.f;  // Kahan: true sum ~ s - c
-  for (int u0 = tid; u0 < nunits; u0 += kStep) {
-    float x[kRowUnroll][8];
-#pragma unroll
-    for (int j = 0; j < kRowUnroll; ++j) {
-      const int unit = u0 + j * kRowThreads;
-      if (unit < nunits) load8(row, unit, V, full, -INFINITY, x[j]);
-      else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[j][k] = -INFINITY;
-      }
-    }
-    float cm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kRowUnroll; ++j)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) cm = fmaxf(cm, x[j][k]);
-    if (cm > m) {
-      const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
-      s *= f;
-      c *= f;
-      m = cm;
-    }
-    if (m != -INFINITY) {
-      float tj[kRowUnroll];
-#pragma unroll
-      for (int j = 0; j < kRowUnroll; ++j) {
-        float w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = ex2((x[j][k] - m) * k2);
-        tj[j] = sum8(w);
-      }
-      const float chunk = ((tj[0] + tj[1]) + (tj[2] + tj[3])) + ((tj[4] + tj[5]) + (tj[6] + tj[7]));
-      const float y = chunk - c;
-      const float t = s + y;
-      c = (t - s) - y;
-      s = t;
-    }
-  }
-  float M = warp_max(m);
-  if (lane == 0) s_f[warp] = M;
-  __syncthreads();
-  M = s_f[0];
-#pragma unroll
-  for (int w = 1; w < kRowWarps; ++w) M = fmaxf(M, s_f[w]);
-  const float mine = (m == -INFINITY) ? 0.f : (s - c) * ex2((m - M) * k2);
-  dfloat acc = warp_sum_df(df_make(mine));
-  if (lane == 0) { s_hi[warp] = acc.hi; s_lo[warp] = acc.lo; }
-  __syncthreads();
-  if (tid == 0) {
-    dfloat tot = {s_hi[0], s_lo[0]};
-    for (int w = 1; w < kRowWarps; ++w) tot = df_add(tot, dfloat{s_hi[w], s_lo[w]});
-    out->m = M;
-    out->arg = -1;
-    const double Z = df_to_d(tot);
-    out->Z = Z;
-    out->inv_Z = float(1.0 / Z);
-  }
+  const RowStat st = row_stats<T>(row, a, sc, 1);
+  if (threadIdx.x == 0) *out = st;
 }
 
 // ---- 2. walk -------------------------------------------------------------------------------
@@ -233,6 +300,17 @@ static_assert(kWalkWarps <= 32, "one warp scans the per-warp totals");
 // per-unit sums of a vocab pass stay in dynamic shared memory for vocabularies up to this many
 // 8-element units (V <= 262144); the search step then rescans them instead of the rows
 constexpr int kWalkMaxSmemUnits = 32768;
+
+// scratch of the block-wide vocabulary passes
+struct PassSmem {
+  dfloat wtot[kWalkWarps];
+  dfloat wpre[kWalkWarps];
+  int wlast[kWalkWarps];
+  float fred[kWalkWarps];
+  int ired[kWalkWarps];
+  double total, theta;
+  int wsel, found, fallback, pos;
+};
 
 struct WalkSmem {
   int16_t par[SPEC_MAX_TREE];
@@ -250,15 +328,9 @@ struct WalkSmem {
   double st_Z[SPEC_MAX_TREE], sd_Z[SPEC_MAX_TREE];
   int32_t st_arg[SPEC_MAX_TREE];
   uint8_t dec0[SPEC_MAX_TREE];     // outcome of the node's plain ratio test u < p / q
-  dfloat wtot[kWalkWarps];
-  dfloat wpre[kWalkWarps];
-  int wlast[kWalkWarps];
-  float fred[kWalkWarps];
-  int ired[kWalkWarps];
-  double total, theta;
+  PassSmem ps;
   double C, Nk;                    // sibling residual state (thread 0 only)
   float Cf;
-  int wsel, found, fallback, pos;
   int decision;
   int bad;                         // SPEC_REQ_* bits found by the validation
 };
@@ -270,7 +342,7 @@ __device__ __forceinline__ int warp_max_i(int v) {
 }
 
 template <typename TT>
-__device__ float block_row_max(const TT* row, int V, WalkSmem& sh) {
+__device__ float block_row_max(const TT* row, int V, PassSmem& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
   float m = -INFINITY;
@@ -289,7 +361,7 @@ __device__ float block_row_max(const TT* row, int V, WalkSmem& sh) {
 }
 
 template <typename TT>
-__device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
+__device__ int block_row_argmax(const TT* row, int V, PassSmem& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
   float best = -INFINITY;
@@ -320,34 +392,6 @@ __device__ int block_row_argmax(const TT* row, int V, WalkSmem& sh) {
   __syncthreads();
   return ba;
 }
-
-// One 8-element unit of a row as raw 16-byte vectors, so that several units' loads can be
-// issued before any of them is used.
-template <typename T>
-struct RawUnit {
-  static constexpr int kVec = int(sizeof(T)) / 2;   // 1 for bf16, 2 for fp32
-  uint4 v[kVec];
-  __device__ __forceinline__ void load(const T* row, int unit) {
-#pragma unroll
-    for (int k = 0; k < kVec; ++k) v[k] = ld_stream16(row + size_t(unit) * 8 + k * (8 / kVec));
-  }
-  // the unit's 8 values; the ragged last unit (unit >= full) is read element by element
-  __device__ __forceinline__ void get(const T* row, int unit, int V, int full, float fill,
-                                      float (&x)[8]) const {
-    if (unit < full) {
-      if constexpr (kVec == 1) {
-        elem<T>::unpack(v[0], x);
-      } else {
-        elem<float>::unpack(v[0], x);
-        float y[4];
-        elem<float>::unpack(v[1], y);
-        x[4] = y[0]; x[5] = y[1]; x[6] = y[2]; x[7] = y[3];
-      }
-    } else {
-      load8(row, unit, V, full, fill, x);
-    }
-  }
-};
 
 // Element weights of the distribution being summed / sampled: p itself (bonus token, up to the
 // constant 1 / Z) or the sibling residual max(0, p - C q).
@@ -395,7 +439,7 @@ __device__ __forceinline__ bool df_above(dfloat x, float th_hi, float th_lo) {
 // them; without it (very large vocabularies) the crossing warp recomputes its units.
 template <typename TT, typename TD>
 __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn,
-                                 bool search, float u, float* usum, WalkSmem& sh) {
+                                 bool search, float u, float* usum, PassSmem& sh) {
   constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
@@ -657,7 +701,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     const TT* trow = target + size_t(o + node) * a.tld;
     const int fc = sh.first_child[node];
     if (greedy) {
-      const int best = fc < 0 ? block_row_argmax(trow, a.V, sh) : sh.st_arg[node];
+      const int best = fc >= 0 ? sh.st_arg[node] : block_row_argmax(trow, a.V, sh.ps);
       int acc = -1, rej = 0;
       for (int c = fc; c >= 0; c = sh.next_sib[c]) {
         if (sh.tok[c] == best) { acc = c; break; }
@@ -677,9 +721,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     if (fc < 0) {  // leaf: bonus token from p_leaf
       WeightFn fn{};
       fn.residual = false;
-      fn.mt = block_row_max(trow, a.V, sh);
+      fn.mt = block_row_max(trow, a.V, sh.ps);
       fn.k2 = a.k2;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh).tok;
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
       break;
     }
     const TD* drow = draft + size_t(sh.drow[node]) * a.dld;
@@ -712,10 +756,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
         if (tid == 0) { sh.C += sh.Nk; sh.Cf = float(sh.C); }
         __syncthreads();
         res.C = sh.Cf;
-        // after the last sibling the search pass below computes N_{k+1} itself
+        // after the last sibling the final draw below yields N_{k+1} itself
         if (sh.next_sib[c] < 0) break;
-        const PassResult pr = vocab_pass(trow, drow, a.V, res, false, 0.f, usum, sh);
-        if (tid == 0) sh.Nk = sh.total;
+        const PassResult pr = vocab_pass(trow, drow, a.V, res, false, 0.f, usum, sh.ps);
+        if (tid == 0) sh.Nk = sh.ps.total;
         if (!pr.pos) { from_p = true; break; }
       }
     }
@@ -726,7 +770,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       continue;
     }
     if (!from_p) {
-      const PassResult pr = vocab_pass(trow, drow, a.V, res, true, u_samp, usum, sh);
+      const PassResult pr = vocab_pass(trow, drow, a.V, res, true, u_samp, usum, sh.ps);
       final_tok = pr.tok;
       if (!pr.pos) from_p = true;
     }
@@ -735,7 +779,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       fn.residual = false;
       fn.mt = res.mt;
       fn.k2 = a.k2;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh).tok;
+      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
     }
     break;
   }
@@ -769,31 +813,43 @@ static VerifyWs verify_ws_layout(int N, int R) {
   return w;
 }
 
+// raise a kernel's dynamic shared memory limit to the unit-sum array's maximum, once per device
+template <typename K>
+static spec_status_t allow_unit_sums(K kernel, bool* raised) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) set_last_cuda_error(e);
+    return SPEC_ERR_CUDA;
+  }
+  if (!raised[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(sizeof(float) * kWalkMaxSmemUnits));
+    if (e != cudaSuccess) {
+      set_last_cuda_error(e);
+      return SPEC_ERR_CUDA;
+    }
+    raised[dev] = true;
+  }
+  return SPEC_OK;
+}
+
 template <typename TT, typename TD>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
-  // draft-row statistics are needed only for tau > 0 with draft logits
-  const int rows = d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
-  if (rows > 0) {
-    const cudaError_t e = launch_pdl(verify_rows_kernel<TT>, dim3(rows), dim3(kRowThreads), 0, s, d);
-    if (e != cudaSuccess) return launch_result(e);
-  }
   const int nunits = (d.V + 7) / 8;
   const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
-  if (dyn > 0) {
-    // raise the opt-in limit once per device for this instantiation
-    static bool raised[64] = {false};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return launch_status();
-    if (!raised[dev]) {
-      const cudaError_t e = cudaFuncSetAttribute(verify_walk_kernel<TT, TD>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 int(sizeof(float) * kWalkMaxSmemUnits));
-      if (e != cudaSuccess) {
-        set_last_cuda_error(e);
-        return SPEC_ERR_CUDA;
-      }
-      raised[dev] = true;
+  {
+    // draft-row statistics are needed only for tau > 0 with draft logits
+    const int rows = d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
+    if (rows > 0) {
+      const cudaError_t e = launch_pdl(verify_rows_kernel<TT>, dim3(rows), dim3(kRowThreads), 0, s, d);
+      if (e != cudaSuccess) return launch_result(e);
     }
+  }
+  static bool raised_walk[64] = {false};
+  if (dyn > 0) {
+    const spec_status_t st = allow_unit_sums(verify_walk_kernel<TT, TD>, raised_walk);
+    if (st != SPEC_OK) return st;
   }
   return launch_result(launch_pdl(verify_walk_kernel<TT, TD>, dim3(d.B), dim3(kWalkThreads), dyn, s, d));
 }
