@@ -50,13 +50,12 @@ constexpr int kBN = 128;
 constexpr int kThreads = 384;                 // 4 control warps + 8 softmax warps
 constexpr int kAtom = 16384;                  // 128 rows x 128 B
 constexpr int kTile = 2 * kAtom;              // 128 x 128 bf16
-constexpr int kKStages = 3;
+constexpr int kKStages = 4;
 constexpr int kVStages = 2;
 constexpr int kSmemQ = 0;
 constexpr int kSmemK = kSmemQ + kTile;
 constexpr int kSmemV = kSmemK + kKStages * kTile;
-constexpr int kSmemP = kSmemV + kVStages * kTile;
-constexpr int kSmemBar = kSmemP + kTile;
+constexpr int kSmemBar = kSmemV + kVStages * kTile;
 constexpr int kSmemRed = kSmemBar + 256;      // [2 buffers][2 halves][128 rows] fp32 exchange
 constexpr int kSmemEnd = kSmemRed + 2048;
 constexpr int kSmemBytes = 232448;            // the per-CTA maximum; the slack aligns the base
@@ -64,6 +63,8 @@ constexpr long long kWaitLimit = 4000000000LL;     // clock cycles (~2 s)
 constexpr float kLazyRescale = 8.0f;          // log2 units
 constexpr int kMaxCtas = 1024;                // persistent CTAs at most
 constexpr int kMinTilesPerRange = 4;          // small problems use fewer, longer ranges
+// TMEM columns: S buffers 0-127 and 128-255, O accumulator 256-383, P buffers 384-447, 448-511
+constexpr uint32_t kTmemP = 384;
 }  // namespace attn
 
 // A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1; the first piece's
@@ -364,29 +365,32 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   uint8_t* sQ = base + kSmemQ;
   uint8_t* sK = base + kSmemK;
   uint8_t* sV = base + kSmemV;
-  uint8_t* sP = base + kSmemP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kSmemBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;     // [kKStages]
-  uint64_t* k_empty = bars + 5;    // [kKStages]
-  uint64_t* v_full = bars + 8;     // [kVStages]
-  uint64_t* v_empty = bars + 10;   // [kVStages]
-  uint64_t* s_full = bars + 12;    // [2]
-  uint64_t* s_free = bars + 14;    // [2]
-  uint64_t* p_full = bars + 16;
-  uint64_t* pv_done = bars + 17;
-  uint64_t* o_free = bars + 18;
-  uint64_t* drain = bars + 19;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
-  int* s_abort = reinterpret_cast<int*>(bars + 21);
-  uint64_t* ex_bar = bars + 22;    // [4]: row-sum exchange of the two softmax halves
+  uint64_t* k_full = bars + 2;                    // [kKStages]
+  uint64_t* k_empty = k_full + kKStages;          // [kKStages]
+  uint64_t* v_full = k_empty + kKStages;          // [kVStages]
+  uint64_t* v_empty = v_full + kVStages;          // [kVStages]
+  uint64_t* s_full = v_empty + kVStages;          // [2]
+  uint64_t* s_free = s_full + 2;                  // [2]
+  uint64_t* p_full = s_free + 2;                  // [2]: P buffer b written (8 softmax warps)
+  uint64_t* pv_done = p_full + 2;                 // [2]: the PV that read P buffer b completed
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* drain = o_free + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  int* s_abort = reinterpret_cast<int*>(drain + 2);
+  uint64_t* ex_bar = drain + 3;                   // [4]: row-sum exchange of the softmax halves
+  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 1 + 4 <= 32,
+                "barriers fit their 256-byte region");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
   pdl_trigger();
-  // this CTA's range of the tile stream (the P tile is free scratch until the first scores)
-  const Range R = cta_range(a, reinterpret_cast<long long*>(sP), reinterpret_cast<int*>(sP + 256));
+  // this CTA's range of the tile stream (the row-sum exchange area is free until the first
+  // epilogue)
+  const Range R = cta_range(a, reinterpret_cast<long long*>(base + kSmemRed),
+                            reinterpret_cast<int*>(base + kSmemRed + 256));
   if (tid == 0) write_merge_record(a, R);
   if (R.t0 >= R.t1) return;   // uniform across the CTA: no work, nothing allocated yet
   if (tid == 0) {
@@ -404,8 +408,10 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       tc::mbar_init(s_full + s, 1);
       tc::mbar_init(s_free + s, 8);
     }
-    tc::mbar_init(p_full, 8);
-    tc::mbar_init(pv_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(p_full + b, 8);
+      tc::mbar_init(pv_done + b, 1);
+    }
     tc::mbar_init(o_free, 8);
     tc::mbar_init(drain, 1);
     for (int q = 0; q < 4; ++q) tc::mbar_init(ex_bar + q, 2);
@@ -514,26 +520,26 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     if (lane == 0) {
       const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, 128, false, true);
-      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV),
-                     aP = tc::smem_u32(sP);
+      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
       const uint32_t tO = tmem + 256;
       int kv_it = 0, li = 0;
       bool ok = true;
       auto issue_pv = [&](int prev, bool first_pv) -> bool {
         const int pst = prev % kVStages, puse = prev / kVStages;
-        if (!tc::mbar_wait(p_full, prev & 1, abort_flag, kWaitLimit)) return false;
+        if (!tc::mbar_wait(p_full + (prev & 1), (prev >> 1) & 1, abort_flag, kWaitLimit)) return false;
         if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) return false;
         if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit))
           return false;
         tc::tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t da = tc::smem_desc(aP + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+          // P buffer prev & 1 in TMEM columns 384 + 64 b: 16 keys = 8 columns per MMA
+          const uint32_t ta = tmem + kTmemP + 64 * (prev & 1) + 8 * kk;
           const uint64_t db = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
-          tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+          tc::mma_bf16_ts(tO, ta, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
         }
         tc::mma_commit(v_empty + pst);
-        tc::mma_commit(pv_done);
+        tc::mma_commit(pv_done + (prev & 1));
         return true;
       };
       ItemIter iter;
@@ -615,11 +621,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         tc::tc_fence_after();
         const uint32_t srow = tmem + lane_addr + st * 128;
         const int kbase = j * kBN;
+        // P buffer st was last read by the PV of tile kv_it - 2: it must be complete before the
+        // buffer is rewritten and before this tile's P is declared ready (all warps, live or
+        // not, so that no warp gets two tiles ahead on p_full)
+        auto wait_p_buffer = [&]() -> bool {
+          return kv_it < 2 || warp_wait(pv_done + st, (use - 1) & 1, abort_flag);
+        };
         if (!live) {
           tc::tc_fence_before();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(s_free + st);
-          if (j > it.j0 && !warp_wait(pv_done, (kv_it - 1) & 1, abort_flag)) { ok = false; break; }
+          if (!wait_p_buffer()) { ok = false; break; }
         } else {
         // the partner half's 64 scores: only their max is needed
         float tmax;
@@ -662,16 +674,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           rowsum += p0 + p1;
           pk[16 + (c >> 1)] = pack_bf16(p0, p1);
         }
-        // PV of the previous tile must be complete before P and O are touched
-        if (j > it.j0 && !warp_wait(pv_done, (kv_it - 1) & 1, abort_flag)) { ok = false; break; }
-        uint8_t* rowp = sP + hh * kAtom + (m >> 3) * 1024 + (m & 7) * 128;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(rowp + ((ch ^ (m & 7)) << 4)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        // lazy rescale of this warp's half of the O accumulator (warp-collective TMEM access)
+        // P of this tile into TMEM buffer st: this warp's rows, keys 64 hh .. 64 hh + 63
+        if (!wait_p_buffer()) { ok = false; break; }
+        tc::tc_fence_after();
+        tc::tmem_st32(tmem + lane_addr + kTmemP + 64 * st + 32 * hh, pk);
+        // lazy rescale of this warp's half of the O accumulator (warp-collective TMEM access):
+        // the previous tile's PV must have landed in O first
         const bool any_rescale = __any_sync(0xffffffffu, factor != 1.f) && j > it.j0;
         if (any_rescale) {
+          const int pv = kv_it - 1;
+          if (!warp_wait(pv_done + (pv & 1), (pv >> 1) & 1, abort_flag)) { ok = false; break; }
           tc::tc_fence_after();
 #pragma unroll 1
           for (int c0 = 0; c0 < 64; c0 += 32) {
@@ -682,8 +694,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             for (int c = 0; c < 32; ++c) r32[c] = __float_as_uint(__uint_as_float(r32[c]) * factor);
             tc::tmem_st32(tmem + lane_addr + 256 + 64 * hh + c0, r32);
           }
-          tc::tmem_st_wait();
         }
+        tc::tmem_st_wait();
         l = l * factor + rowsum;
         m_ref = new_ref;
         }  // live
@@ -697,15 +709,15 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 #pragma unroll
             for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
           }
+          tc::fence_proxy_async_smem();
         }
-        tc::fence_proxy_async_smem();
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(p_full);
+        if (lane == 0) tc::mbar_arrive(p_full + st);
       }
       if (!ok) break;
       // epilogue: this warp writes output columns 64*hh .. 64*hh+63 of its rows
-      if (!warp_wait(pv_done, (kv_it - 1) & 1, abort_flag)) { ok = false; break; }
+      if (!warp_wait(pv_done + ((kv_it - 1) & 1), ((kv_it - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
       tc::tc_fence_after();
       if (!live) {
         tc::tc_fence_before();
