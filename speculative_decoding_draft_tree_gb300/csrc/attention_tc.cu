@@ -151,11 +151,13 @@ __device__ __forceinline__ int piece_slot(long long ubeg, long long total, int C
   return (ubeg > rs) ? 2 * c + 1 : 2 * c;
 }
 
-// Every thread of the CTA computes the same Range: pass 1 sums the tile work of all requests,
-// pass 2 scans it in chunks of kThreads requests until the chunk holding t1 - 1.  `s64` is
-// scratch of at least kThreads / 32 + 2 entries, `s32` of two.  Contains __syncthreads.
+// Every thread of the CTA (kThreads of them) computes the same Range: pass 1 sums the tile work
+// of all requests, pass 2 scans it in chunks of kThreads requests until the chunk holding
+// t1 - 1.  `s64` is scratch of at least kThreads / 32 + 2 entries, `s32` of two.  Contains
+// __syncthreads.
+template <int kThreads>
 __device__ Range cta_range(const TcDev& a, long long* s64, int* s32) {
-  using namespace attn;
+  using attn::kMinTilesPerRange;
   constexpr int kW = kThreads / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   long long mine = 0;
@@ -224,6 +226,9 @@ __device__ Range cta_range(const TcDev& a, long long* s64, int* s32) {
   R.rbeg0 = s64[kW];
   R.r1 = s32[1];
   R.rbeg1 = s64[kW + 1];
+  // the scan always finds both requests; anything else would index out of bounds: no work
+  if (R.r0 < 0 || R.r0 >= a.B || R.r1 < R.r0 || R.r1 >= a.B || R.rbeg0 > R.t0 || R.rbeg1 > R.t1 - 1)
+    R.t0 = R.t1 = 0;
   return R;
 }
 
@@ -354,6 +359,95 @@ __device__ __forceinline__ float mask_max32(uint32_t (&x)[32], bool valid, int k
   return mx;
 }
 
+// One lane waits (bounded), the warp gets the outcome.
+__device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  bool r = true;
+  if ((threadIdx.x & 31) == 0) r = tc::mbar_wait(bar, parity, abort, attn::kWaitLimit);
+  return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+}
+
+// TMA producer warp (K and Q: is_k; V otherwise) walking the CTA's items.  Lanes 0..7 fetch
+// the eight block-table entries of a tile (a tile ahead).  When the tile's pages are
+// consecutive physical blocks one 4-D box per 64-column half brings all eight (16 KB);
+// otherwise each lane issues the two boxes of its own page (2 KB each) -- small boxes cap the
+// copy rate well below HBM speed.  Pages past the request or with a bad block id are read from
+// an out-of-range row (TMA fills zeros).  The K warp also loads each item's Q: q_bytes from two
+// boxes of `qmap` at (0 | 64, head * G, first tree token + mt * q_tokens) into sQ, sQ + q_half.
+// Inlined into the kernel so that every tensor map address is the kernel parameter's own; a map
+// address in local or shared memory (which TMA cannot read) aborts without issuing a copy.
+// Returns false if a wait expired; every copy issued is waited for (bounded) before return.
+__device__ __forceinline__ bool tma_producer(
+    const TcDev& a, const Range& R, bool is_k, const CUtensorMap* map, const CUtensorMap* map8,
+    int nstage, uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* qmap,
+    uint8_t* sQ, int q_half, int q_bytes, int q_tokens, uint64_t* q_full, uint64_t* q_empty,
+    volatile int* abort_flag) {
+  using namespace attn;
+  const int lane = threadIdx.x & 31;
+  int kt = 0, li = 0;
+  bool ok = !(__isLocal(map) || __isShared(map) || __isLocal(map8) || __isShared(map8) ||
+              __isLocal(qmap) || __isShared(qmap));
+  ItemIter iter;
+  iter.start(a, R);
+  Item it;
+  for (; ok && iter.next(a, R, it); ++li) {
+    const int nblk = (it.P + it.T + kBS - 1) / kBS;
+    const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
+    // physical block of this lane's page of tile j: -1 past the request, -2 if invalid
+    auto tile_pb = [&](int j) -> int {
+      int pb = -1;
+      const int lb = j * 8 + lane;
+      if (lane < 8 && lb < nblk) {
+        pb = table[lb];
+        if (pb < 0 || pb >= a.num_blocks) {
+          atomicOr(&a.req_status[it.r], SPEC_REQ_BAD_BLOCK);
+          pb = -2;
+        }
+      }
+      return pb;
+    };
+    if (is_k) {
+      if (li > 0 && !lane0_wait(q_empty, (li - 1) & 1, abort_flag)) { ok = false; break; }
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(q_full, q_bytes);
+        const int row = it.o + it.mt * q_tokens;
+        tc::tma_load_3d(sQ, qmap, 0, it.h * a.G, row, q_full);
+        tc::tma_load_3d(sQ + q_half, qmap, 64, it.h * a.G, row, q_full);
+      }
+    }
+    int pb_cur = tile_pb(it.j0);
+    for (int j = it.j0; j < it.j1; ++j, ++kt) {
+      const int pb_next = (j + 1 < it.j1) ? tile_pb(j + 1) : -1;
+      const int st = kt % nstage, use = kt / nstage;
+      if (use > 0 && !lane0_wait(empty + st, (use - 1) & 1, abort_flag)) { ok = false; break; }
+      const int pb0 = __shfl_sync(0xffffffffu, pb_cur, 0);
+      const bool contig = __all_sync(0xffffffffu, lane >= 8 || pb_cur == -1 || pb_cur == pb0 + lane) && pb0 >= 0;
+      if (lane == 0) tc::mbar_arrive_expect_tx(full + st, kTile);
+      __syncwarp();
+      uint8_t* dst = ring + st * kTile;
+      if (contig) {
+        if (lane == 0) {
+          tc::tma_load_4d(dst, map8, 0, 0, it.h, pb0, full + st);
+          tc::tma_load_4d(dst + kAtom, map8, 64, 0, it.h, pb0, full + st);
+        }
+      } else if (lane < 8) {
+        const int row = pb_cur >= 0 ? (pb_cur * a.H_kv + it.h) * kBS : a.kv_rows;  // zeros
+        tc::tma_load_2d(dst + lane * 2048, map, 0, row, full + st);
+        tc::tma_load_2d(dst + kAtom + lane * 2048, map, 64, row, full + st);
+      }
+      __syncwarp();
+      pb_cur = pb_next;
+    }
+  }
+  if (lane == 0) {
+    if (!ok) *abort_flag = 1;
+    // drain: wait for the copies issued last (bounded), so none is in flight at exit
+    for (int k = max(0, kt - nstage); k < kt; ++k)
+      tc::mbar_wait(full + k % nstage, (k / nstage) & 1, abort_flag, kWaitLimit / 8);
+    if (is_k && li > 0) tc::mbar_wait(q_full, (li - 1) & 1, abort_flag, kWaitLimit / 8);
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 __global__ void __launch_bounds__(attn::kThreads, 1)
 attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mK8,
@@ -389,8 +483,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   pdl_trigger();
   // this CTA's range of the tile stream (the row-sum exchange area is free until the first
   // epilogue)
-  const Range R = cta_range(a, reinterpret_cast<long long*>(base + kSmemRed),
-                            reinterpret_cast<int*>(base + kSmemRed + 256));
+  const Range R = cta_range<kThreads>(a, reinterpret_cast<long long*>(base + kSmemRed),
+                                      reinterpret_cast<int*>(base + kSmemRed + 256));
   if (tid == 0) write_merge_record(a, R);
   if (R.t0 >= R.t1) return;   // uniform across the CTA: no work, nothing allocated yet
   if (tid == 0) {
@@ -433,88 +527,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
 
   if (layout_ok && (warp == 0 || warp == 2)) {
     // ===================================================================== TMA producers
-    // warp 0 loads Q and K, warp 2 loads V.  Lanes 0..7 fetch the eight block-table entries
-    // of a tile (a tile ahead).  When the tile's pages are consecutive physical blocks one
-    // 4-D box per 64-column half brings all eight (16 KB); otherwise each lane issues the two
-    // boxes of its own page (2 KB each) -- small boxes cap the copy rate well below HBM speed.
+    // warp 0 loads Q and K, warp 2 loads V
     const bool is_k = warp == 0;
     if (lane == 0) {
       tc::prefetch_tensormap(is_k ? &mK : &mV);
       tc::prefetch_tensormap(is_k ? &mK8 : &mV8);
       if (is_k) tc::prefetch_tensormap(&mQ);
     }
+    // on an expired wait the producer raises the abort flag itself
+    // Q: the unit's 128 rows (G heads x 128 / G tree tokens)
     const CUtensorMap* map = is_k ? &mK : &mV;
     const CUtensorMap* map8 = is_k ? &mK8 : &mV8;
-    const int nstage = is_k ? kKStages : kVStages;
-    uint8_t* ring = is_k ? sK : sV;
-    uint64_t* full = is_k ? k_full : v_full;
-    uint64_t* empty = is_k ? k_empty : v_empty;
-    int kt = 0, li = 0;
-    bool ok = true;
-    auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-      bool r = true;
-      if (lane == 0) r = tc::mbar_wait(bar, parity, abort_flag, kWaitLimit);
-      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-    };
-    ItemIter iter;
-    iter.start(a, R);
-    Item it;
-    for (; ok && iter.next(a, R, it); ++li) {
-      const int o = it.o, T = it.T, P = it.P;
-      const int nblk = (P + T + kBS - 1) / kBS;
-      const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
-      // physical block of this lane's page of tile j: -1 past the request, -2 if invalid
-      auto tile_pb = [&](int j) -> int {
-        int pb = -1;
-        const int lb = j * 8 + lane;
-        if (lane < 8 && lb < nblk) {
-          pb = table[lb];
-          if (pb < 0 || pb >= a.num_blocks) {
-            atomicOr(&a.req_status[it.r], SPEC_REQ_BAD_BLOCK);
-            pb = -2;
-          }
-        }
-        return pb;
-      };
-      if (is_k) {
-        if (li > 0 && !wait_lane0(q_empty, (li - 1) & 1)) { ok = false; break; }
-        if (lane == 0) {
-          tc::mbar_arrive_expect_tx(q_full, kTile);
-          tc::tma_load_3d(sQ, &mQ, 0, it.h * G, o + it.mt * tpt, q_full);
-          tc::tma_load_3d(sQ + kAtom, &mQ, 64, it.h * G, o + it.mt * tpt, q_full);
-        }
-      }
-      int pb_cur = tile_pb(it.j0);
-      for (int j = it.j0; j < it.j1; ++j, ++kt) {
-        const int pb_next = (j + 1 < it.j1) ? tile_pb(j + 1) : -1;
-        const int st = kt % nstage, use = kt / nstage;
-        if (use > 0 && !wait_lane0(empty + st, (use - 1) & 1)) { ok = false; break; }
-        const int pb0 = __shfl_sync(0xffffffffu, pb_cur, 0);
-        const bool contig = __all_sync(0xffffffffu, lane >= 8 || pb_cur == -1 || pb_cur == pb0 + lane) && pb0 >= 0;
-        if (lane == 0) tc::mbar_arrive_expect_tx(full + st, kTile);
-        __syncwarp();
-        uint8_t* dst = ring + st * kTile;
-        if (contig) {
-          if (lane == 0) {
-            tc::tma_load_4d(dst, map8, 0, 0, it.h, pb0, full + st);
-            tc::tma_load_4d(dst + kAtom, map8, 64, 0, it.h, pb0, full + st);
-          }
-        } else if (lane < 8) {
-          const int row = pb_cur >= 0 ? (pb_cur * a.H_kv + it.h) * kBS : a.kv_rows;  // zeros
-          tc::tma_load_2d(dst + lane * 2048, map, 0, row, full + st);
-          tc::tma_load_2d(dst + kAtom + lane * 2048, map, 64, row, full + st);
-        }
-        __syncwarp();
-        pb_cur = pb_next;
-      }
-    }
-    if (lane == 0) {
-      if (!ok) *abort_flag = 1;
-      // drain: wait for the copies issued last (bounded), so none is in flight at exit
-      for (int k = max(0, kt - nstage); k < kt; ++k)
-        tc::mbar_wait(full + k % nstage, (k / nstage) & 1, abort_flag, kWaitLimit / 8);
-      if (is_k && li > 0) tc::mbar_wait(q_full, (li - 1) & 1, abort_flag, kWaitLimit / 8);
-    }
+    tma_producer(a, R, is_k, map, map8, is_k ? kKStages : kVStages, is_k ? sK : sV,
+                 is_k ? k_full : v_full, is_k ? k_empty : v_empty, &mQ, sQ, kAtom, kTile, tpt,
+                 q_full, q_empty, abort_flag);
   } else if (layout_ok && warp == 1) {
     // ===================================================================== MMA issuer
     if (lane == 0) {
@@ -702,10 +728,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         // last tile: zero V rows past the request's KV length (stale cache rows times P = 0
         // must not turn into NaN); TMA must have landed first.  Half hh clears d-atom hh.
         if (kbase + kBN > kv_len) {
-          if (!warp_wait(v_full + st, use & 1, abort_flag)) { ok = false; break; }
+          const int vst = kv_it % kVStages, vuse = kv_it / kVStages;
+          if (!warp_wait(v_full + vst, vuse & 1, abort_flag)) { ok = false; break; }
           const int key = m;
           if (key >= kv_len - kbase) {
-            uint8_t* vrow = sV + st * kTile + hh * kAtom + (key >> 3) * 1024 + (key & 7) * 128;
+            uint8_t* vrow = sV + vst * kTile + hh * kAtom + (key >> 3) * 1024 + (key & 7) * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -783,6 +810,400 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   }
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------------ small units
+// For units of at most 16 query rows (T x G <= 16: plain decode and short chains) the scores are
+// computed transposed, S^T = K Q^T (M = 128 keys on the TMEM lanes, N = 16 query rows), so the
+// softmax spends its lanes on keys instead of on padding rows: 16 exponentials per lane and tile,
+// spread over the four TMEM lane quarters (one softmax warp each), where the row-major kernel
+// runs 64 per lane on the one sub-partition that owns the live rows.  O^T += V^T P^T (V as an
+// M-major A operand, P^T a 4 KB K-major B tile in shared memory) accumulates in TMEM.  The lazy
+// rescale reference of each row is shared by the four warps through a bounded exchange per tile;
+// row sums stay per lane until the epilogue.  Q is a 16-row (4 KB) box.
+namespace attn_s {
+constexpr int kRows = 16;                        // N of both MMAs
+constexpr int kThreads = 256;                    // 4 control warps + 4 softmax warps
+constexpr int kQAtom = kRows * 128;              // 16 rows x 128 B
+constexpr int kQBytes = 2 * kQAtom;              // Q: 16 rows x 128 d (bf16)
+constexpr int kPTile = 2 * kQAtom;               // P^T: 16 rows x 128 keys (bf16)
+constexpr int kKStages = 3;
+constexpr int kVStages = 3;
+constexpr int kSmemQ = 0;
+constexpr int kSmemP = kSmemQ + kQBytes;                       // 2 P^T buffers
+constexpr int kSmemK = kSmemP + 2 * kPTile;                    // 1024-aligned
+constexpr int kSmemV = kSmemK + kKStages * attn::kTile;
+constexpr int kSmemBar = kSmemV + kVStages * attn::kTile;
+constexpr int kSmemX = kSmemBar + 512;                         // exchanges between softmax warps
+constexpr int kSmemEnd = kSmemX + 1280;
+constexpr int kSmemBytes = kSmemEnd + 1024;                    // slack for 1024-byte alignment
+constexpr uint32_t kTmemCols = 64;                             // S^T 0-15, 16-31; O^T 32-47
+constexpr uint32_t kTmemO = 32;
+static_assert(kSmemK % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+static_assert(kSmemBytes <= 232448, "fits one CTA's shared memory");
+
+struct Xchg {
+  int flag[2][4];          // per tile (parity): some key of warp q passed its row's reference
+  float mx[2][4][kRows];   // per update (parity): warp q's row maxima
+  float sum[2][4][kRows];  // per item (parity): warp q's row sums
+};
+static_assert(sizeof(Xchg) <= 1280, "exchange area");
+}  // namespace attn_s
+
+__global__ void __launch_bounds__(attn_s::kThreads, 1)
+attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_constant__ CUtensorMap mK,
+                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mK8,
+                     const __grid_constant__ CUtensorMap mV8, TcDev a) {
+  using namespace attn_s;
+  using attn::kAtom;
+  using attn::kBM;
+  using attn::kBN;
+  using attn::kD;
+  using attn::kLazyRescale;
+  using attn::kTile;
+  using attn::kWaitLimit;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = base + kSmemQ;
+  uint8_t* sPT = base + kSmemP;
+  uint8_t* sK = base + kSmemK;
+  uint8_t* sV = base + kSmemV;
+  Xchg* xs = reinterpret_cast<Xchg*>(base + kSmemX);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kSmemBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;                    // [kKStages]
+  uint64_t* k_empty = k_full + kKStages;          // [kKStages]
+  uint64_t* v_full = k_empty + kKStages;          // [kVStages]
+  uint64_t* v_empty = v_full + kVStages;          // [kVStages]
+  uint64_t* s_full = v_empty + kVStages;          // [2]
+  uint64_t* s_free = s_full + 2;                  // [2]
+  uint64_t* p_full = s_free + 2;                  // [2]
+  uint64_t* pv_done = p_full + 2;                 // [2]
+  uint64_t* o_free = pv_done + 2;
+  uint64_t* drain = o_free + 1;
+  uint64_t* xa_bar = drain + 1;                   // [2] flag exchange
+  uint64_t* xb_bar = xa_bar + 2;                  // [2] maxima exchange
+  uint64_t* xc_bar = xb_bar + 2;                  // [2] row-sum exchange
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xc_bar + 2);
+  int* s_abort = reinterpret_cast<int*>(xc_bar + 3);
+  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 6 + 2 <= 64,
+                "barriers fit their 512-byte region");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
+  const Range R = cta_range<kThreads>(a, reinterpret_cast<long long*>(base + kSmemX),
+                                      reinterpret_cast<int*>(base + kSmemX + 256));
+  if (tid == 0) write_merge_record(a, R);
+  if (R.t0 >= R.t1) return;   // uniform across the CTA: no work, nothing allocated yet
+  __syncthreads();            // the exchange area was scratch for the range computation
+  if (tid == 0) {
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(s_full + b, 1);
+      tc::mbar_init(s_free + b, 4);
+      tc::mbar_init(p_full + b, 4);
+      tc::mbar_init(pv_done + b, 1);
+      tc::mbar_init(xa_bar + b, 4);
+      tc::mbar_init(xb_bar + b, 4);
+      tc::mbar_init(xc_bar + b, 4);
+    }
+    tc::mbar_init(o_free, 4);
+    tc::mbar_init(drain, 1);
+    *s_abort = (tc::smem_u32(base) + kSmemEnd > tc::smem_u32(smem_raw) + kSmemBytes) ? 1 : 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort_flag = s_abort;
+  const int G = a.G, log2G = a.log2G;
+  const bool layout_ok = *abort_flag == 0;
+
+  if (layout_ok && (warp == 0 || warp == 2)) {
+    // ===================================================================== TMA producers
+    const bool is_k = warp == 0;
+    if (lane == 0) {
+      tc::prefetch_tensormap(is_k ? &mK : &mV);
+      tc::prefetch_tensormap(is_k ? &mK8 : &mV8);
+      if (is_k) tc::prefetch_tensormap(&mQs);
+    }
+    // Q: the unit's rows (G heads x 16 / G tree tokens; one M-tile per unit)
+    const CUtensorMap* map = is_k ? &mK : &mV;
+    const CUtensorMap* map8 = is_k ? &mK8 : &mV8;
+    tma_producer(a, R, is_k, map, map8, is_k ? kKStages : kVStages, is_k ? sK : sV,
+                 is_k ? k_full : v_full, is_k ? k_empty : v_empty, &mQs, sQ, kQAtom, kQBytes,
+                 kRows / G, q_full, q_empty, abort_flag);
+  } else if (layout_ok && warp == 1) {
+    // ===================================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_bf16_f32(128, kRows, false, false);
+      const uint32_t id_pv = tc::idesc_bf16_f32(128, kRows, true, false);
+      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV),
+                     aP = tc::smem_u32(sPT);
+      const uint32_t tO = tmem + kTmemO;
+      int kv_it = 0, li = 0;
+      bool ok = true;
+      auto issue_pv = [&](int prev, bool first_pv) -> bool {
+        const int pst = prev % kVStages, puse = prev / kVStages;
+        if (!tc::mbar_wait(p_full + (prev & 1), (prev >> 1) & 1, abort_flag, kWaitLimit)) return false;
+        if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) return false;
+        if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit))
+          return false;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // A = V^T (M = d, M-major), B = P^T (16 rows x 16 keys per step, K-major)
+          const uint64_t da = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
+          const uint64_t db = tc::smem_desc(aP + (prev & 1) * kPTile + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
+          tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+        }
+        tc::mma_commit(v_empty + pst);
+        tc::mma_commit(pv_done + (prev & 1));
+        return true;
+      };
+      ItemIter iter;
+      iter.start(a, R);
+      Item it;
+      for (; ok && iter.next(a, R, it); ++li) {
+        if (!tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+        bool first_pv = true;
+        for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
+          const int st = kv_it & 1, use = kv_it >> 1;
+          const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
+          if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+          if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t tS = tmem + st * kRows;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // A = K (128 keys x 16 d per step, K-major), B = Q (16 rows x 16 d, K-major)
+            const uint64_t da = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            const uint64_t db = tc::smem_desc(aQ + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(s_full + st);
+          tc::mma_commit(k_empty + kst);
+          if (j == it.j1 - 1) tc::mma_commit(q_empty);
+          if (j > it.j0) {
+            if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
+            first_pv = false;
+          }
+        }
+        if (!ok) break;
+        if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
+      }
+      if (!ok) *abort_flag = 1;
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
+    }
+  } else if (layout_ok && warp >= 4) {
+    // ===================================================================== softmax + epilogue
+    const int q = warp & 3;                       // TMEM lane quarter: keys (S^T) / d (O^T)
+    const uint32_t lane_addr = uint32_t(q * 32) << 16;
+    const int kl = q * 32 + lane;                 // this lane's key within a tile; its d in O^T
+    const float sl2 = a.scale_log2;
+    int kv_it = 0, li = 0, xa = 0, xb = 0, xc = 0;
+    bool ok = true;
+    // bounded exchange among the four softmax warps: one phase of bar[n & 1] per use
+    auto xwait = [&](uint64_t* bar, int n) -> bool {
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(bar + (n & 1));
+      return warp_wait(bar + (n & 1), (n >> 1) & 1, abort_flag);
+    };
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    for (; ok && iter.next(a, R, it); ++li) {
+      const int o = it.o, T = it.T, P = it.P;
+      const int kv_len = P + T;
+      const int nrows = min(T << log2G, kRows);   // valid rows: n < nrows
+      float ref[kRows], lsum[kRows];
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) { ref[n] = -INFINITY; lsum[n] = 0.f; }
+      for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
+        const int st = kv_it & 1, use = kv_it >> 1;
+        if (!warp_wait(s_full + st, use & 1, abort_flag)) { ok = false; break; }
+        tc::tc_fence_after();
+        uint32_t sv[kRows];
+        tc::tmem_ld16(tmem + lane_addr + st * kRows, sv);
+        tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(s_free + st);
+        // visibility of this lane's key for each row: the prefix is visible to every valid row;
+        // a tree slot a = key - P only to the rows whose token has a as ancestor-or-self
+        const int key = j * kBN + kl;
+        uint32_t vis = 0;
+        if (key < P) {
+          vis = (nrows >= 32) ? 0xFFFFFFFFu : ((1u << nrows) - 1u);
+        } else if (key < kv_len) {
+          const int slot = key - P;
+#pragma unroll
+          for (int n = 0; n < kRows; ++n) {
+            if (n < nrows) {
+              const uint32_t w0 = a.anc[size_t(o + (n >> log2G)) * a.W + (slot >> 5)];
+              vis |= ((w0 >> (slot & 31)) & 1u) << n;
+            }
+          }
+        }
+        float x[kRows];
+        bool above = false;
+#pragma unroll
+        for (int n = 0; n < kRows; ++n) {
+          x[n] = ((vis >> n) & 1u) ? __uint_as_float(sv[n]) * sl2 : -INFINITY;
+          above = above || (x[n] > ref[n] + kLazyRescale);
+        }
+        // some key of some warp passed its row's reference: all four warps move the references
+        const int flag = __any_sync(0xffffffffu, above) ? 1 : 0;
+        if (lane == 0) xs->flag[xa & 1][q] = flag;
+        if (!xwait(xa_bar, xa)) { ok = false; break; }
+        const bool update = (xs->flag[xa & 1][0] | xs->flag[xa & 1][1] | xs->flag[xa & 1][2] |
+                             xs->flag[xa & 1][3]) != 0;
+        ++xa;
+        if (update) {
+          float mx[kRows];
+#pragma unroll
+          for (int n = 0; n < kRows; ++n) mx[n] = warp_max(x[n]);
+          if (lane == 0) {
+#pragma unroll
+            for (int n = 0; n < kRows; ++n) xs->mx[xb & 1][q][n] = mx[n];
+          }
+          if (!xwait(xb_bar, xb)) { ok = false; break; }
+          float factor[kRows];
+          bool any_factor = false;
+#pragma unroll
+          for (int n = 0; n < kRows; ++n) {
+            float nr = ref[n];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) nr = fmaxf(nr, xs->mx[xb & 1][w][n]);
+            factor[n] = (ref[n] == -INFINITY || nr == ref[n]) ? 1.f : ex2(ref[n] - nr);
+            any_factor = any_factor || factor[n] != 1.f;
+            ref[n] = nr;
+          }
+          ++xb;
+          // rescale the accumulated O^T rows (this warp's d quarter) once the previous PV landed
+          if (any_factor && j > it.j0) {
+            const int pv = kv_it - 1;
+            if (!warp_wait(pv_done + (pv & 1), (pv >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t ov[kRows];
+            tc::tmem_ld16(tmem + lane_addr + kTmemO, ov);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int n = 0; n < kRows; ++n) ov[n] = __float_as_uint(__uint_as_float(ov[n]) * factor[n]);
+            tc::tmem_st16(tmem + lane_addr + kTmemO, ov);
+            tc::tmem_st_wait();
+          }
+#pragma unroll
+          for (int n = 0; n < kRows; ++n) lsum[n] *= factor[n];
+        }
+        // P^T of this key into buffer st, once the PV that last read it (tile kv_it - 2) is done
+        if (kv_it >= 2 && !warp_wait(pv_done + st, (use - 1) & 1, abort_flag)) { ok = false; break; }
+        uint8_t* pcol = sPT + st * kPTile + (kl >> 6) * kQAtom;
+        const int chunk = (kl & 63) >> 3, within = (kl & 7) * 2;
+#pragma unroll
+        for (int n = 0; n < kRows; ++n) {
+          const float p = (x[n] == -INFINITY) ? 0.f : ex2(x[n] - ref[n]);
+          lsum[n] += p;
+          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+          *reinterpret_cast<__nv_bfloat16*>(pcol + (n >> 3) * 1024 + (n & 7) * 128 +
+                                            ((chunk ^ (n & 7)) << 4) + within) = pb;
+        }
+        // last tile: zero the V rows of keys past the KV length (stale rows times P = 0 must not
+        // turn into NaN); the V copy must have landed first
+        if (j * kBN + kBN > kv_len) {
+          const int vst = kv_it % kVStages, vuse = kv_it / kVStages;
+          if (!warp_wait(v_full + vst, vuse & 1, abort_flag)) { ok = false; break; }
+          if (key >= kv_len) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint8_t* vrow = sV + vst * kTile + hh * kAtom + (kl >> 3) * 1024 + (kl & 7) * 128;
+#pragma unroll
+              for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(p_full + st);
+      }
+      if (!ok) break;
+      // epilogue: row sums over lanes and warps, then this warp's d quarter of every valid row
+      if (!warp_wait(pv_done + ((kv_it - 1) & 1), ((kv_it - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+      tc::tc_fence_after();
+      float tot[kRows];
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) {
+        float v = lsum[n];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        tot[n] = v;
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int n = 0; n < kRows; ++n) xs->sum[xc & 1][q][n] = tot[n];
+      }
+      if (!xwait(xc_bar, xc)) { ok = false; break; }
+#pragma unroll
+      for (int n = 0; n < kRows; ++n)
+        tot[n] = ((xs->sum[xc & 1][0][n] + xs->sum[xc & 1][1][n]) + xs->sum[xc & 1][2][n]) + xs->sum[xc & 1][3][n];
+      ++xc;
+      uint32_t ov[kRows];
+      tc::tmem_ld16(tmem + lane_addr + kTmemO, ov);
+      tc::tmem_ld_wait();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(o_free);
+#pragma unroll
+      for (int n = 0; n < kRows; ++n) {
+        if (n < nrows) {
+          const float lt = tot[n];
+          const float inv = lt > 0.f ? 1.f / lt : 0.f;
+          const float lse2 = lt > 0.f ? ref[n] + __log2f(lt) : -INFINITY;
+          const int t = n >> log2G, g = n & (G - 1);
+          const float val = __uint_as_float(ov[n]) * inv;
+          if (it.slot < 0) {
+            a.o[(size_t(o + t) * a.H_q + it.h * G + g) * kD + kl] = __float2bfloat16_rn(val);
+            if (q == 0 && lane == 0 && a.lse)
+              a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
+          } else {
+            a.part_o[(size_t(it.slot) * kBM + n) * kD + kl] = val;
+            if (q == 0 && lane < 2) a.part_lse[(size_t(it.slot) * 2 + lane) * kBM + n] = lse2;
+          }
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // every request of this CTA's range is unreliable after an expired wait
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    while (iter.next(a, R, it)) atomicOr(&a.req_status[it.r], SPEC_REQ_TIMEOUT);
+  }
+  tc::tc_fence_after();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------------------ merge
@@ -981,9 +1402,27 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaFuncSetAttribute(attn_tc_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         attn_s::kSmemBytes);
   });
-  cudaError_t le = launch_pdl(attn_tc_kernel, dim3(ctas), dim3(kThreads), size_t(kSmemBytes), s,
-                              mQ, mK, mV, mK8, mV8, d);
+  cudaError_t le;
+  if ((long long)p->T_max * G <= attn_s::kRows) {
+    // every unit has at most 16 query rows: the transposed kernel with a 16-row Q box
+    CUtensorMap mQs;
+    cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(p->H_q), cuuint64_t(p->N)};
+    cuuint64_t strides[2] = {cuuint64_t(kD) * 2, cuuint64_t(p->H_q) * kD * 2};
+    cuuint32_t box[3] = {64, cuuint32_t(G), cuuint32_t(attn_s::kRows / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&mQs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->q), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SPEC_ERR_INVALID_ARG;
+    le = launch_pdl(attn_tc_small_kernel, dim3(ctas), dim3(attn_s::kThreads),
+                    size_t(attn_s::kSmemBytes), s, mQs, mK, mV, mK8, mV8, d);
+  } else {
+    le = launch_pdl(attn_tc_kernel, dim3(ctas), dim3(kThreads), size_t(kSmemBytes), s,
+                    mQ, mK, mV, mK8, mV8, d);
+  }
   if (le == cudaSuccess) le = launch_pdl(attn_merge_kernel, dim3(ctas), dim3(256), 0, s, d);
   return launch_result(le);
 }
