@@ -420,7 +420,10 @@ __device__ __forceinline__ bool tma_producer(
       const int st = kt % nstage, use = kt / nstage;
       if (use > 0 && !lane0_wait(empty + st, (use - 1) & 1, abort_flag)) { ok = false; break; }
       const int pb0 = __shfl_sync(0xffffffffu, pb_cur, 0);
-      const bool contig = __all_sync(0xffffffffu, lane >= 8 || pb_cur == -1 || pb_cur == pb0 + lane) && pb0 >= 0;
+      // one wide box only when all eight pages exist and are consecutive: on a request's last
+      // tile the pages past its end are zero-filled per page (out of bounds, no DRAM traffic)
+      // instead of being read from whatever blocks follow
+      const bool contig = __all_sync(0xffffffffu, lane >= 8 || pb_cur == pb0 + lane) && pb0 >= 0;
       if (lane == 0) tc::mbar_arrive_expect_tx(full + st, kTile);
       __syncwarp();
       uint8_t* dst = ring + st * kTile;

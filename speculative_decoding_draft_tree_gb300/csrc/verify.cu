@@ -63,6 +63,7 @@ struct VerifyDev {
   int32_t* rejections;
   RowStat* tstat;
   RowStat* dstat;
+  int32_t after_rows;   // the walk follows a rows kernel of the same call
 };
 
 // ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
@@ -271,6 +272,9 @@ __device__ RowStat row_stats(const T* row, const VerifyDev& a, RowScratch& sc, i
 template <typename T>
 __global__ void __launch_bounds__(kRowThreads) verify_rows_kernel(VerifyDev a) {
   __shared__ RowScratch sc;
+  // the first kernel of the call: the previous kernel on the stream may have produced the logits
+  // or the tree flags, so wait for it before reading anything (the walk's early prologue relies
+  // on this kernel having waited before it triggers)
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -581,7 +585,11 @@ template <typename TT, typename TD>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
   __shared__ WalkSmem sh;
   extern __shared__ float usum_dyn[];
-  pdl_wait();
+  // After the rows kernel (which waited for everything before this call before it let this
+  // kernel launch), everything up to the row statistics is already complete, so validation and
+  // the gather of the tree run while the rows kernel may still be running; pdl_wait() comes
+  // before the statistics and before any store.  Without a rows kernel, wait first.
+  if (!a.after_rows) pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
@@ -613,6 +621,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   __syncthreads();
   const int st = st0 | sh.bad;
   if (st != 0) {
+    pdl_wait();
     if (tid == 0 && sh.bad) atomicOr(&a.req_status[r], sh.bad);
     for (int k = tid; k < a.max_path; k += kWalkThreads) { path_row[k] = -1; tok_row[k] = -1; }
     if (tid == 0) {
@@ -627,8 +636,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   const TD* draft = reinterpret_cast<const TD*>(a.draft);
   const bool greedy = a.tau == 0.f;
   // gather, in parallel, everything the scalar part of the walk will read: tree links, tokens,
-  // uniforms, the row statistics of internal nodes and, for every non-root node, its token's
-  // target and draft values in its parent's rows (the operands of its ratio test)
+  // uniforms and, for every non-root node, its token's target and draft values in its parent's
+  // rows (the operands of its ratio test); then, once the rows kernel is done, the row
+  // statistics of internal nodes and every node's plain ratio test
   for (int i = tid; i < T; i += kWalkThreads) {
     const int p = a.parent[o + i];
     const int t = a.tokens[o + i];
@@ -638,27 +648,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     sh.next_sib[i] = -1;
     sh.uacc[i] = a.uniforms[2 * size_t(o + i)];
     sh.usamp[i] = a.uniforms[2 * size_t(o + i) + 1];
-    if (a.is_internal[o + i]) {
-      const RowStat ts = a.tstat[o + i];
-      sh.st_m[i] = ts.m;
-      sh.st_Z[i] = ts.Z;
-      sh.st_iz[i] = ts.inv_Z;
-      sh.st_arg[i] = ts.arg;
-      if (!greedy) {
-        const int dr = a.draft_row[o + i];
-        sh.drow[i] = dr;
-        if (!a.probs) {
-          const RowStat ds = a.dstat[dr];
-          sh.sd_m[i] = ds.m;
-          sh.sd_Z[i] = ds.Z;
-          sh.sd_iz[i] = ds.inv_Z;
-        } else {
-          sh.sd_m[i] = 0.f;
-          sh.sd_Z[i] = 1.0;
-          sh.sd_iz[i] = 1.f;
-        }
-      }
-    }
+    if (!greedy && a.is_internal[o + i]) sh.drow[i] = a.draft_row[o + i];
     if (i > 0 && !greedy) {
       sh.xt[i] = elem<TT>::load1(target + size_t(o + p) * a.tld + t);
       sh.xd[i] = elem<TD>::load1(draft + size_t(a.draft_row[o + p]) * a.dld + t);
@@ -677,7 +667,35 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       for (int k = p + 1; k < i; ++k)
         if (sh.par[k] == p) { first = false; break; }
       if (first) sh.first_child[p] = int16_t(i);
+    }
+  }
+  pdl_wait();   // the rows kernel's statistics are complete
+  for (int i = tid; i < T; i += kWalkThreads) {
+    if (a.is_internal[o + i]) {
+      const RowStat ts = a.tstat[o + i];
+      sh.st_m[i] = ts.m;
+      sh.st_Z[i] = ts.Z;
+      sh.st_iz[i] = ts.inv_Z;
+      sh.st_arg[i] = ts.arg;
       if (!greedy) {
+        if (!a.probs) {
+          const RowStat ds = a.dstat[sh.drow[i]];
+          sh.sd_m[i] = ds.m;
+          sh.sd_Z[i] = ds.Z;
+          sh.sd_iz[i] = ds.inv_Z;
+        } else {
+          sh.sd_m[i] = 0.f;
+          sh.sd_Z[i] = 1.0;
+          sh.sd_iz[i] = 1.f;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!greedy) {
+    for (int i = tid; i < T; i += kWalkThreads) {
+      if (i > 0) {
+        const int p = sh.par[i];
         // plain ratio test u < p / q, as u * Zt < exp(((xt - mt) - (xd - md)) / tau) * Zd for
         // draft logits and u * q * Zt < exp((xt - mt) / tau) for draft probabilities
         const double u = double(sh.uacc[i]);
@@ -838,9 +856,11 @@ template <typename TT, typename TD>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   const int nunits = (d.V + 7) / 8;
   const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
+  VerifyDev dw = d;
   {
     // draft-row statistics are needed only for tau > 0 with draft logits
     const int rows = d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
+    dw.after_rows = rows > 0 ? 1 : 0;
     if (rows > 0) {
       const cudaError_t e = launch_pdl(verify_rows_kernel<TT>, dim3(rows), dim3(kRowThreads), 0, s, d);
       if (e != cudaSuccess) return launch_result(e);
@@ -851,7 +871,7 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
     const spec_status_t st = allow_unit_sums(verify_walk_kernel<TT, TD>, raised_walk);
     if (st != SPEC_OK) return st;
   }
-  return launch_result(launch_pdl(verify_walk_kernel<TT, TD>, dim3(d.B), dim3(kWalkThreads), dyn, s, d));
+  return launch_result(launch_pdl(verify_walk_kernel<TT, TD>, dim3(d.B), dim3(kWalkThreads), dyn, s, dw));
 }
 
 }  // namespace spec
@@ -895,6 +915,7 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
     return SPEC_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
   VerifyDev d;
+  d.after_rows = 0;
   d.target = p->target;
   d.draft = p->draft;
   d.tld = p->target_ld;
