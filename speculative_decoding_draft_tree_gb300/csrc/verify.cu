@@ -307,13 +307,13 @@ constexpr int kWalkMaxSmemUnits = 32768;
 
 // scratch of the block-wide vocabulary passes
 struct PassSmem {
-  dfloat wtot[kWalkWarps];
-  dfloat wpre[kWalkWarps];
-  int wlast[kWalkWarps];
+  dfloat wtot[kWalkWarps];   // per-warp inclusive sums of the threads' unit runs
+  int wlast[kWalkWarps];     // per-warp last unit with mass
+  int wfirst[kWalkWarps];    // per-warp first thread whose inclusive prefix passes theta
   float fred[kWalkWarps];
   int ired[kWalkWarps];
-  double total, theta;
-  int wsel, found, fallback, pos;
+  double total;              // the pass's total mass (read by thread 0)
+  int found;
 };
 
 struct WalkSmem {
@@ -437,137 +437,136 @@ __device__ __forceinline__ bool df_above(dfloat x, float th_hi, float th_lo) {
 }
 
 // Block-wide pass over the vocabulary: total mass of the weights (sh.total, thread 0) and, when
-// `search`, the smallest token x with sum_{y<=x} w(y) > u * total.  Warp w owns units
-// [w*upw, (w+1)*upw), so warp order is token order; each lane issues the loads of kUnits units
-// before it uses any.  With `usum` the unit sums stay in shared memory and the search rescans
-// them; without it (very large vocabularies) the crossing warp recomputes its units.
+// `search`, the smallest token x with sum_{y<=x} w(y) > u * total.  Phase 1 stores every 8-element
+// unit's weight sum in shared memory (each thread issues the loads of kUnits units before it uses
+// any).  Phase 2 gives thread t the contiguous units [t * per, (t + 1) * per): a block scan of the
+// threads' double-float run sums gives every thread its prefix, the first thread whose inclusive
+// prefix passes theta walks its units, then the crossing unit's 8 elements.  No fp64: theta is a
+// double-float product.  Without `usum` (very large vocabularies) phase 2 recomputes unit sums.
 template <typename TT, typename TD>
 __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn,
                                  bool search, float u, float* usum, PassSmem& sh) {
   constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
-  const int upw = ((nunits + kWalkWarps - 1) / kWalkWarps + 31) / 32 * 32;
-  const int ub = warp * upw;
-  const int ue = min(ub + upw, nunits);
-  dfloat acc = df_make(0.f);
-  int last = -1;
-  for (int base = ub; base < ue; base += 32 * kUnits) {
-    RawUnit<TT> rt[kUnits];
-    RawUnit<TD> rd[kUnits];
+  if (usum) {
+    for (int base = 0; base < nunits; base += kWalkThreads * kUnits) {
+      RawUnit<TT> rt[kUnits];
+      RawUnit<TD> rd[kUnits];
 #pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-      const int unit = base + 32 * j + lane;
-      if (unit < ue && unit < full) {
-        rt[j].load(trow, unit);
-        if (fn.residual) rd[j].load(drow, unit);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kUnits; ++j) {
-      const int unit = base + 32 * j + lane;
-      if (unit < ue) {
-        float xt[8], xd[8], w[8];
-        rt[j].get(trow, unit, V, full, -INFINITY, xt);
-        if (fn.residual) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
-        fn(xt, xd, w);
-        const float su = sum8(w);
-        acc = df_add_f(acc, su);
-        if (usum) usum[unit] = su;
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (w[k] > 0.f) last = unit * 8 + k;
-      }
-    }
-  }
-  const dfloat wt = warp_sum_df(acc);
-  last = warp_max_i(last);
-  if (lane == 0) { sh.wtot[warp] = wt; sh.wlast[warp] = last; }
-  __syncthreads();
-  if (warp == 0) {
-    // lane w holds warp w's total: scan them in token order
-    const dfloat incl = warp_scan_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f), lane);
-    dfloat excl = df_shfl_up(incl, 1);
-    if (lane == 0) excl = df_make(0.f);
-    if (lane < kWalkWarps) sh.wpre[lane] = excl;
-    const dfloat run = {__shfl_sync(0xffffffffu, incl.hi, 31),
-                        __shfl_sync(0xffffffffu, incl.lo, 31)};
-    const int fb = warp_max_i(lane < kWalkWarps ? sh.wlast[lane] : -1);
-    const double tot = df_to_d(run);
-    int wsel = -1;
-    double theta = 0.0;
-    if (search && tot > 0.0) {
-      theta = double(u) * tot;
-      const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
-      const unsigned mask = __ballot_sync(0xffffffffu, df_above(incl, th_hi, th_lo));
-      wsel = mask ? __ffs(mask) - 1 : -1;
-    }
-    if (lane == 0) {
-      sh.total = tot;
-      sh.pos = tot > 0.0;
-      sh.fallback = fb;
-      sh.found = fb;
-      sh.wsel = wsel;
-      sh.theta = theta;
-    }
-  }
-  __syncthreads();
-  PassResult res{-1, sh.pos != 0};
-  if (!search) {
-    __syncthreads();
-    return res;
-  }
-  const int ws = sh.wsel;
-  if (ws >= 0 && warp == ws) {
-    // lane L rescans a contiguous run of the warp's units; a warp scan of the run totals finds
-    // the crossing lane, which walks its units and then the 8 elements of the crossing unit
-    const double theta = sh.theta;
-    const float th_hi = float(theta), th_lo = float(theta - double(th_hi));
-    const dfloat base_acc = sh.wpre[ws];
-    const int per = (ue - ub + 31) / 32;
-    const int l0 = min(ub + lane * per, ue), l1 = min(l0 + per, ue);
-    auto unit_sum = [&](int unit) {
-      if (usum) return usum[unit];
-      float w[8];
-      fn.unit(trow, drow, unit, V, full, w);
-      return sum8(w);
-    };
-    dfloat run = df_make(0.f);
-    for (int unit = l0; unit < l1; ++unit) run = df_add_f(run, unit_sum(unit));
-    const dfloat incl = warp_scan_df(run, lane);
-    dfloat excl = df_shfl_up(incl, 1);
-    if (lane == 0) excl = df_make(0.f);
-    const unsigned mask = __ballot_sync(0xffffffffu, df_above(df_add(base_acc, incl), th_hi, th_lo));
-    if (mask && lane == __ffs(mask) - 1) {
-      dfloat cum = df_add(base_acc, excl);
-      int cross_unit = -1, last_pos_unit = -1;
-      for (int unit = l0; unit < l1; ++unit) {
-        const float su = unit_sum(unit);
-        const dfloat next = df_add_f(cum, su);
-        if (su > 0.f) last_pos_unit = unit;
-        if (df_above(next, th_hi, th_lo)) { cross_unit = unit; break; }
-        cum = next;
-      }
-      // rounding can leave the crossing inside the run total only: take its last live unit
-      const int cu = cross_unit >= 0 ? cross_unit : last_pos_unit;
-      int tok = -1, lastpos = -1;
-      if (cu >= 0) {
-        float w[8];
-        fn.unit(trow, drow, cu, V, full, w);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          cum = df_add_f(cum, w[k]);
-          if (w[k] > 0.f) lastpos = cu * 8 + k;
-          if (tok < 0 && cross_unit >= 0 && df_above(cum, th_hi, th_lo)) tok = cu * 8 + k;
+      for (int j = 0; j < kUnits; ++j) {
+        const int unit = base + j * kWalkThreads + tid;
+        if (unit < full) {
+          rt[j].load(trow, unit);
+          if (fn.residual) rd[j].load(drow, unit);
         }
       }
-      sh.found = tok >= 0 ? tok : (lastpos >= 0 ? lastpos : sh.fallback);
+#pragma unroll
+      for (int j = 0; j < kUnits; ++j) {
+        const int unit = base + j * kWalkThreads + tid;
+        if (unit < nunits) {
+          float xt[8], xd[8], w[8];
+          rt[j].get(trow, unit, V, full, -INFINITY, xt);
+          if (fn.residual) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
+          fn(xt, xd, w);
+          usum[unit] = sum8(w);
+        }
+      }
     }
+    __syncthreads();
+  }
+  auto unit_sum = [&](int unit) -> float {
+    if (usum) return usum[unit];
+    float w[8];
+    fn.unit(trow, drow, unit, V, full, w);
+    return sum8(w);
+  };
+  // phase 2: this thread's run of units, scanned across the block
+  const int per = (nunits + kWalkThreads - 1) / kWalkThreads;
+  const int u0 = min(tid * per, nunits), u1 = min(u0 + per, nunits);
+  dfloat mine = df_make(0.f);
+  int lastp = -1;
+  for (int unit = u0; unit < u1; ++unit) {
+    const float su = unit_sum(unit);
+    mine = df_add_f(mine, su);
+    if (su > 0.f) lastp = unit;
+  }
+  const dfloat incl_w = warp_scan_df(mine, lane);
+  dfloat excl_w = df_shfl_up(incl_w, 1);
+  if (lane == 0) excl_w = df_make(0.f);
+  lastp = warp_max_i(lastp);
+  if (lane == 31) sh.wtot[warp] = incl_w;
+  if (lane == 0) sh.wlast[warp] = lastp;
+  __syncthreads();
+  // every warp scans the warp totals: its own base and the block total
+  const dfloat wsc = warp_scan_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f), lane);
+  dfloat wex = df_shfl_up(wsc, 1);
+  if (lane == 0) wex = df_make(0.f);
+  const dfloat wbase = {__shfl_sync(0xffffffffu, wex.hi, warp), __shfl_sync(0xffffffffu, wex.lo, warp)};
+  const dfloat total = {__shfl_sync(0xffffffffu, wsc.hi, 31), __shfl_sync(0xffffffffu, wsc.lo, 31)};
+  const int fb = warp_max_i(lane < kWalkWarps ? sh.wlast[lane] : -1);   // last unit with mass
+  const bool pos = total.hi > 0.f;
+  if (tid == 0) sh.total = df_to_d(total);
+  if (!search) {
+    __syncthreads();   // sh is reused by the next pass
+    return PassResult{-1, pos};
+  }
+  // theta = u * total as a double-float (exact product of u and total.hi, plus u * total.lo)
+  const float ph = u * total.hi;
+  const float pl = fmaf(u, total.hi, -ph) + u * total.lo;
+  const float th_hi = ph + pl, th_lo = pl - (th_hi - ph);
+  const dfloat prefix = df_add(wbase, excl_w);
+  const bool c = pos && df_above(df_add(wbase, incl_w), th_hi, th_lo);
+  const unsigned cm = __ballot_sync(0xffffffffu, c);
+  if (lane == 0) sh.wfirst[warp] = cm ? warp * 32 + __ffs(cm) - 1 : 0x7fffffff;
+  if (tid == 0) sh.found = -1;
+  __syncthreads();
+  int first = 0x7fffffff;
+#pragma unroll
+  for (int w = 0; w < kWalkWarps; ++w) first = min(first, sh.wfirst[w]);
+  if (tid == first) {
+    dfloat cum = prefix;
+    int cross_unit = -1, last_pos_unit = -1;
+    for (int unit = u0; unit < u1; ++unit) {
+      const float su = unit_sum(unit);
+      const dfloat nx = df_add_f(cum, su);
+      if (su > 0.f) last_pos_unit = unit;
+      if (df_above(nx, th_hi, th_lo)) { cross_unit = unit; break; }
+      cum = nx;
+    }
+    // rounding can leave the crossing inside the run total only: take its last live unit
+    const int cu = cross_unit >= 0 ? cross_unit : last_pos_unit;
+    int tok = -1, lastpos = -1;
+    if (cu >= 0) {
+      float w[8];
+      fn.unit(trow, drow, cu, V, full, w);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cum = df_add_f(cum, w[k]);
+        if (w[k] > 0.f) lastpos = cu * 8 + k;
+        if (tok < 0 && cross_unit >= 0 && df_above(cum, th_hi, th_lo)) tok = cu * 8 + k;
+      }
+    }
+    sh.found = tok >= 0 ? tok : lastpos;
   }
   __syncthreads();
-  res.tok = sh.found;
-  __syncthreads();
-  return res;
+  int tok = sh.found;
+  if (tok < 0 && pos) {
+    // no thread crossed (theta at the total by rounding): the last element with mass
+    if (tid == 0 && fb >= 0) {
+      float w[8];
+      fn.unit(trow, drow, fb, V, full, w);
+      int lp = -1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (w[k] > 0.f) lp = fb * 8 + k;
+      sh.found = lp;
+    }
+    __syncthreads();
+    tok = sh.found;
+  }
+  __syncthreads();   // sh is reused by the next pass
+  return PassResult{tok, pos};
 }
 
 // Thread 0: the ratio test of a later sibling under the sibling residual rule,
