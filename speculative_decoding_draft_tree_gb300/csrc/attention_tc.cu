@@ -885,13 +885,13 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
   uint64_t* p_full = s_free + 2;                  // [2]
   uint64_t* pv_done = p_full + 2;                 // [2]
   uint64_t* o_free = pv_done + 2;
-  uint64_t* drain = o_free + 1;
-  uint64_t* xa_bar = drain + 1;                   // [2] flag exchange
+  uint64_t* drain = o_free + 1;                   // [2]: the QK issuer's, the PV issuer's
+  uint64_t* xa_bar = drain + 2;                   // [2] flag exchange
   uint64_t* xb_bar = xa_bar + 2;                  // [2] maxima exchange
   uint64_t* xc_bar = xb_bar + 2;                  // [2] row-sum exchange
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xc_bar + 2);
   int* s_abort = reinterpret_cast<int*>(xc_bar + 3);
-  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 6 + 2 <= 64,
+  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 3 + 6 + 2 <= 64,
                 "barriers fit their 512-byte region");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -924,6 +924,7 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
     }
     tc::mbar_init(o_free, 4);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(drain + 1, 1);
     *s_abort = (tc::smem_u32(base) + kSmemEnd > tc::smem_u32(smem_raw) + kSmemBytes) ? 1 : 0;
     tc::fence_mbar_init();
   }
@@ -953,9 +954,12 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
     tma_producer(a, R, is_k, map, map8, is_k ? kKStages : kVStages, is_k ? sK : sV,
                  is_k ? k_full : v_full, is_k ? k_empty : v_empty, &mQs, sQ, kQAtom, kQBytes,
                  kRows / G, q_full, q_empty, abort_flag);
-  } else if (layout_ok && warp == 1) {
-    // ===================================================================== MMA issuer
+  } else if (layout_ok && (warp == 1 || warp == 3)) {
+    // ===================================================================== MMA issuers
+    // warp 1 issues S^T = K Q^T, warp 3 issues O^T += V^T P^T, each tile after tile; each thread
+    // commits its own operations, so a QK is never queued behind the wait for the previous P
     if (lane == 0) {
+      const bool is_qk = warp == 1;
       const uint32_t id_qk = tc::idesc_bf16_f32(128, kRows, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, kRows, true, false);
       const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV),
@@ -963,58 +967,53 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
       const uint32_t tO = tmem + kTmemO;
       int kv_it = 0, li = 0;
       bool ok = true;
-      auto issue_pv = [&](int prev, bool first_pv) -> bool {
-        const int pst = prev % kVStages, puse = prev / kVStages;
-        if (!tc::mbar_wait(p_full + (prev & 1), (prev >> 1) & 1, abort_flag, kWaitLimit)) return false;
-        if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) return false;
-        if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit))
-          return false;
-        tc::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // A = V^T (M = d, M-major), B = P^T (16 rows x 16 keys per step, K-major)
-          const uint64_t da = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
-          const uint64_t db = tc::smem_desc(aP + (prev & 1) * kPTile + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
-          tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
-        }
-        tc::mma_commit(v_empty + pst);
-        tc::mma_commit(pv_done + (prev & 1));
-        return true;
-      };
       ItemIter iter;
       iter.start(a, R);
       Item it;
       for (; ok && iter.next(a, R, it); ++li) {
-        if (!tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-        bool first_pv = true;
+        if (is_qk && !tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
         for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
           const int st = kv_it & 1, use = kv_it >> 1;
-          const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
-          if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-          if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-          tc::tc_fence_after();
-          const uint32_t tS = tmem + st * kRows;
+          if (is_qk) {
+            const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
+            if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint32_t tS = tmem + st * kRows;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // A = K (128 keys x 16 d per step, K-major), B = Q (16 rows x 16 d, K-major)
-            const uint64_t da = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = tc::smem_desc(aQ + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(s_full + st);
-          tc::mma_commit(k_empty + kst);
-          if (j == it.j1 - 1) tc::mma_commit(q_empty);
-          if (j > it.j0) {
-            if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
-            first_pv = false;
+            for (int kk = 0; kk < 8; ++kk) {
+              // A = K (128 keys x 16 d per step, K-major), B = Q (16 rows x 16 d, K-major)
+              const uint64_t da = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = tc::smem_desc(aQ + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
+              tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(s_full + st);
+            tc::mma_commit(k_empty + kst);
+            if (j == it.j1 - 1) tc::mma_commit(q_empty);
+          } else {
+            const int pst = kv_it % kVStages, puse = kv_it / kVStages;
+            const bool first_pv = j == it.j0;
+            if (!tc::mbar_wait(p_full + st, use & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            tc::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // A = V^T (M = d, M-major), B = P^T (16 rows x 16 keys per step, K-major)
+              const uint64_t da = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
+              const uint64_t db = tc::smem_desc(aP + st * kPTile + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
+              tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+            }
+            tc::mma_commit(v_empty + pst);
+            tc::mma_commit(pv_done + st);
           }
         }
-        if (!ok) break;
-        if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
       }
       if (!ok) *abort_flag = 1;
-      tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
+      // drain every tcgen05 operation issued by this thread before TMEM is released
+      uint64_t* my_drain = drain + (is_qk ? 0 : 1);
+      tc::mma_commit(my_drain);
+      tc::mbar_wait(my_drain, 0, abort_flag, kWaitLimit / 8);
     }
   } else if (layout_ok && warp >= 4) {
     // ===================================================================== softmax + epilogue
