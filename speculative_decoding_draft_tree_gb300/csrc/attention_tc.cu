@@ -20,15 +20,15 @@
 //   warp 0      Q and K producer, warp 2 V producer: 128-byte-swizzled TMA boxes (one per
 //               paged block and 64-column half, issued by 8 lanes); blocks past the request or
 //               with a bad block id are read from an out-of-range row (TMA fills zeros).  K has
-//               3 stages, released right after QK^T; V has 2, released after PV;
-//   warp 1      one thread issues tcgen05.mma: S = Q K^T (M=128, N=128, K=16 x 8) into one of two
-//               TMEM score buffers, O += P V (V as an MN-major operand) into the TMEM
-//               accumulator, and commits completions to mbarriers;
+//               4 stages, released right after QK^T; V has 2, released after PV;
+//   warp 1      one thread issues S = Q K^T (M=128, N=128, K=16 x 8) into one of two TMEM score
+//               buffers; warp 3, one thread, issues O += P V (P read from TMEM, V as an
+//               MN-major operand) into the TMEM accumulator; each commits its own completions;
 //   warps 4..11 softmax: the two warps of a TMEM lane quarter own the same 32 rows; each reads
 //               all 128 scores of its rows (the row max is computed redundantly, so no exchange
 //               is needed per tile) and exponentiates its own 64 keys with a lazily updated
 //               reference max (O rescaled only when the max grows by more than 2^8), writing P
-//               into the swizzled K-major P tile; the epilogue adds the two halves' row sums
+//               (bf16) into one of two TMEM P buffers; the epilogue adds the two halves' row sums
 //               (one bounded exchange per item) and writes O columns 64*half .. 64*half+63.
 // Every wait is bounded (clock64 limit); an expired wait flags SPEC_REQ_TIMEOUT and lets every
 // role drain and exit; TMEM is always freed.
@@ -474,11 +474,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   uint64_t* p_full = s_free + 2;                  // [2]: P buffer b written (8 softmax warps)
   uint64_t* pv_done = p_full + 2;                 // [2]: the PV that read P buffer b completed
   uint64_t* o_free = pv_done + 2;
-  uint64_t* drain = o_free + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  int* s_abort = reinterpret_cast<int*>(drain + 2);
-  uint64_t* ex_bar = drain + 3;                   // [4]: row-sum exchange of the softmax halves
-  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 2 + 1 + 4 <= 32,
+  uint64_t* drain = o_free + 1;                   // [2]: the QK issuer's, the PV issuer's
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  int* s_abort = reinterpret_cast<int*>(drain + 3);
+  uint64_t* ex_bar = drain + 4;                   // [4]: row-sum exchange of the softmax halves
+  static_assert(2 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2 + 2 + 1 + 2 + 2 + 4 <= 32,
                 "barriers fit their 256-byte region");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -511,6 +511,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     }
     tc::mbar_init(o_free, 8);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(drain + 1, 1);
     for (int q = 0; q < 4; ++q) tc::mbar_init(ex_bar + q, 2);
     // the 1024-byte aligned layout must fit in the dynamic allocation
     *s_abort = (tc::smem_u32(base) + kSmemEnd > tc::smem_u32(smem_raw) + kSmemBytes) ? 1 : 0;
@@ -544,67 +545,64 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
     tma_producer(a, R, is_k, map, map8, is_k ? kKStages : kVStages, is_k ? sK : sV,
                  is_k ? k_full : v_full, is_k ? k_empty : v_empty, &mQ, sQ, kAtom, kTile, tpt,
                  q_full, q_empty, abort_flag);
-  } else if (layout_ok && warp == 1) {
-    // ===================================================================== MMA issuer
+  } else if (layout_ok && (warp == 1 || warp == 3)) {
+    // ===================================================================== MMA issuers
+    // warp 1 issues S = Q K^T, warp 3 issues O += P V, each tile after tile; each thread commits
+    // its own operations, so a QK is never queued behind the wait for the previous P
     if (lane == 0) {
+      const bool is_qk = warp == 1;
       const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
       const uint32_t tO = tmem + 256;
       int kv_it = 0, li = 0;
       bool ok = true;
-      auto issue_pv = [&](int prev, bool first_pv) -> bool {
-        const int pst = prev % kVStages, puse = prev / kVStages;
-        if (!tc::mbar_wait(p_full + (prev & 1), (prev >> 1) & 1, abort_flag, kWaitLimit)) return false;
-        if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) return false;
-        if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit))
-          return false;
-        tc::tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // P buffer prev & 1 in TMEM columns 384 + 64 b: 16 keys = 8 columns per MMA
-          const uint32_t ta = tmem + kTmemP + 64 * (prev & 1) + 8 * kk;
-          const uint64_t db = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
-          tc::mma_bf16_ts(tO, ta, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
-        }
-        tc::mma_commit(v_empty + pst);
-        tc::mma_commit(pv_done + (prev & 1));
-        return true;
-      };
       ItemIter iter;
       iter.start(a, R);
       Item it;
       for (; ok && iter.next(a, R, it); ++li) {
-        if (!tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-        bool first_pv = true;
+        if (is_qk && !tc::mbar_wait(q_full, li & 1, abort_flag, kWaitLimit)) { ok = false; break; }
         for (int j = it.j0; j < it.j1; ++j, ++kv_it) {
           const int st = kv_it & 1, use = kv_it >> 1;
-          const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
-          if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-          if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
-          tc::tc_fence_after();
-          const uint32_t tS = tmem + st * 128;
+          if (is_qk) {
+            const int kst = kv_it % kKStages, kuse = kv_it / kKStages;
+            if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            tc::tc_fence_after();
+            const uint32_t tS = tmem + st * 128;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t da = tc::smem_desc(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            const uint64_t db = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(s_full + st);
-          tc::mma_commit(k_empty + kst);
-          if (j == it.j1 - 1) tc::mma_commit(q_empty);
-          if (j > it.j0) {
-            if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
-            first_pv = false;
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t da = tc::smem_desc(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+              const uint64_t db = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+              tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(s_full + st);
+            tc::mma_commit(k_empty + kst);
+            if (j == it.j1 - 1) tc::mma_commit(q_empty);
+          } else {
+            const int pst = kv_it % kVStages, puse = kv_it / kVStages;
+            const bool first_pv = j == it.j0;
+            if (!tc::mbar_wait(p_full + st, use & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
+            tc::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // P buffer st in TMEM columns 384 + 64 st: 16 keys = 8 columns per MMA
+              const uint32_t ta = tmem + kTmemP + 64 * st + 8 * kk;
+              const uint64_t db = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
+              tc::mma_bf16_ts(tO, ta, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+            }
+            tc::mma_commit(v_empty + pst);
+            tc::mma_commit(pv_done + st);
           }
         }
-        if (!ok) break;
-        if (!issue_pv(kv_it - 1, first_pv)) { ok = false; break; }
       }
       if (!ok) *abort_flag = 1;
       // drain every tcgen05 operation issued by this thread before TMEM is released
-      tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
+      uint64_t* my_drain = drain + (is_qk ? 0 : 1);
+      tc::mma_commit(my_drain);
+      tc::mbar_wait(my_drain, 0, abort_flag, kWaitLimit / 8);
     }
   } else if (layout_ok && warp >= 4) {
     // ===================================================================== softmax + epilogue
