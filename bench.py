@@ -325,23 +325,40 @@ def main():
     ms_per_step = 1e3 * t_total / args.steps
     value = world * tokens_per_step * args.steps / t_total
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers: every round's inputs are
+    # copied from pinned host memory and its accepted tokens copied back inside the timed region;
+    # two steps over separate input buffers (same KV cache) let round i + 1's upload on a copy
+    # stream overlap round i's kernels, as a serving loop would.  No L2 flush between rounds:
+    # each round streams 540 MB of K/V (4x L2) and the copy engine writes the round's inputs.
     e2e = None
     if not args.no_e2e:
         host_in = step.pinned_host_inputs()
-        host_out = step.host_output_buffers()
+        steps_ab = [step, step.twin()]
+        host_outs = [step.host_output_buffers(), step.host_output_buffers()]
+        copy_stream = torch.cuda.Stream()
+        ready = [torch.cuda.Event(), torch.cuda.Event()]
+        free = [torch.cuda.Event(), torch.cuda.Event()]
         for _ in range(2):
-            step.run_from_host(host_in, host_out)
+            for k in range(2):
+                steps_ab[k].run_from_host(host_in, host_outs[k], stream)
+        for k in range(2):
+            free[k].record(stream)
         torch.cuda.synchronize()
-        e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        copy_stream.wait_stream(stream)
         for i in range(args.steps):
-            l2_flush(i)
-            e_ev[i][0].record(stream)
-            step.run_from_host(host_in, host_out)
-            e_ev[i][1].record(stream)
+            k = i % 2
+            copy_stream.wait_event(free[k])
+            steps_ab[k].upload(host_in, copy_stream)
+            ready[k].record(copy_stream)
+            stream.wait_event(ready[k])
+            steps_ab[k].run(stream)
+            steps_ab[k].download(host_outs[k], stream)
+            free[k].record(stream)
+        e1.record(stream)
         torch.cuda.synchronize()
-        t_e2e = sum(a.elapsed_time(b) for a, b in e_ev) / 1e3
+        t_e2e = e0.elapsed_time(e1) / 1e3
         if world > 1:
             tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
             dist.all_reduce(tt, op=dist.ReduceOp.MAX)
@@ -349,7 +366,7 @@ def main():
         e2e = {"value": world * tokens_per_step * args.steps / t_e2e,
                "unit": "verified tree tokens/s",
                "h2d_bytes_per_step": VerifyStep.bytes_of(host_in),
-               "d2h_bytes_per_step": VerifyStep.bytes_of(host_out),
+               "d2h_bytes_per_step": VerifyStep.bytes_of(host_outs[0]),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
     if rank != 0:

@@ -4,8 +4,11 @@
 `VerifyStep` owns every output and workspace buffer for a fixed workload shape (allocated once
 with torch, never inside the timed calls) and runs the four library calls on the current stream.
 `run_from_host` is the end-to-end form: the step's inputs arrive in pinned host memory, are
-copied to the device, the round runs, and the accepted tokens come back to the host.
+copied to the device, the round runs, and the accepted tokens come back to the host.  For a
+stream of rounds, `twin()` gives a second step over its own copies of the per-round inputs (same
+KV cache), so that one step's `upload` on a copy stream overlaps the other's `run`.
 """
+import dataclasses
 from dataclasses import dataclass
 from typing import Dict, Optional
 
@@ -24,6 +27,7 @@ class VerifyStep:
     def __init__(self, w: Workload, sibling_rule: int = B.SPEC_SIBLING_RESIDUAL,
                  with_lse: bool = True):
         self.w = w
+        self.sibling_rule = sibling_rule
         dev = w.target.device
         if dev.type != "cuda":
             raise ValueError("VerifyStep needs the workload on a CUDA device")
@@ -103,18 +107,37 @@ class VerifyStep:
     def pinned_host_inputs(self) -> Dict[str, torch.Tensor]:
         return {k: v.detach().to("cpu").pin_memory() for k, v in self.step_input_tensors().items()}
 
+    def upload(self, host_inputs: Dict[str, torch.Tensor], stream=None):
+        """Copy a round's inputs from pinned host memory to this step's device tensors, on
+        `stream` (default: the current stream)."""
+        dev_in = self.step_input_tensors()
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            for k, h in host_inputs.items():
+                dev_in[k].copy_(h, non_blocking=True)
+
+    def download(self, host_out: Dict[str, torch.Tensor], stream=None):
+        """Copy the accepted tokens, lengths and new KV lengths to pinned host memory."""
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            host_out["out_tokens"].copy_(self.out_tokens, non_blocking=True)
+            host_out["out_len"].copy_(self.out_len, non_blocking=True)
+            host_out["new_kv_len"].copy_(self.new_kv_len, non_blocking=True)
+
     def run_from_host(self, host_inputs: Dict[str, torch.Tensor], host_out: Dict[str, torch.Tensor],
                       stream=None):
         """Copy the round's inputs from pinned host memory, run the round, copy the accepted
         tokens and lengths back.  Asynchronous on the stream; synchronise before reading
         host_out."""
-        dev_in = self.step_input_tensors()
-        for k, h in host_inputs.items():
-            dev_in[k].copy_(h, non_blocking=True)
+        self.upload(host_inputs, stream)
         self.run(stream)
-        host_out["out_tokens"].copy_(self.out_tokens, non_blocking=True)
-        host_out["out_len"].copy_(self.out_len, non_blocking=True)
-        host_out["new_kv_len"].copy_(self.new_kv_len, non_blocking=True)
+        self.download(host_out, stream)
+
+    def twin(self) -> "VerifyStep":
+        """A second step of the same shape over its own copies of the per-round input tensors
+        and the same KV cache: while one step runs a round, the next round's inputs can be
+        uploaded into the other (double buffering)."""
+        fresh = {k: v.clone() for k, v in self.step_input_tensors().items()}
+        return VerifyStep(dataclasses.replace(self.w, **fresh), self.sibling_rule,
+                          self.lse is not None)
 
     def host_output_buffers(self) -> Dict[str, torch.Tensor]:
         return dict(out_tokens=torch.empty_like(self.out_tokens, device="cpu").pin_memory(),

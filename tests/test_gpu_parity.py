@@ -191,3 +191,33 @@ def test_guard_bands_untouched():
     _sync()
     for name, buf in big.items():
         assert (buf[:pad] == sentinel).all() and (buf[-pad:] == sentinel).all(), name
+
+
+def test_twin_and_host_round_trip():
+    # a twin step (own input copies, shared KV cache) fed the same host inputs gives the same
+    # round as the original, whether run through run_from_host or upload / run / download
+    w = W.make_config(2, scale="small", device="cuda", num_layers=2)
+    step = VerifyStep(w)
+    host_in = step.pinned_host_inputs()
+    k0 = w.k_cache.clone()
+    v0 = w.v_cache.clone()
+    out_a = step.host_output_buffers()
+    step.run_from_host(host_in, out_a)
+    _sync()
+    res_a = {k: step.results()[k].cpu().clone() for k in ("out_tokens", "out_len", "path", "n_acc")}
+    w.k_cache.copy_(k0)
+    w.v_cache.copy_(v0)
+    twin = step.twin()
+    assert twin.w.k_cache.data_ptr() == w.k_cache.data_ptr()
+    assert twin.w.target.data_ptr() != w.target.data_ptr()
+    out_b = twin.host_output_buffers()
+    copy_stream = torch.cuda.Stream()
+    twin.upload(host_in, copy_stream)
+    torch.cuda.current_stream().wait_stream(copy_stream)
+    twin.run()
+    twin.download(out_b)
+    _sync()
+    for k, v in res_a.items():
+        assert torch.equal(twin.results()[k].cpu(), v), k
+    for k in out_a:
+        assert torch.equal(out_a[k], out_b[k]), k
