@@ -8,9 +8,11 @@ vocab 32000, 32 x d128 MHA heads, 2048 cached tokens per request, bf16, tau = 1)
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload CID] [--impl reference]
 
 Prints ONE JSON line (rank 0).  `value` is verified tree tokens per second over all ranks
-(device time of the K timed steps, max over ranks); `e2e` repeats the measurement through
-VerifyStep.run_from_host with the round's inputs in pinned host memory and the accepted tokens
-copied back inside the timed region.  `roofline` is for the tree-attention call (the dominant
+(device time of the K timed steps, max over ranks); `e2e` repeats the measurement through the
+public VerifyStep.upload / run / download with every round's inputs copied from pinned host
+memory and its accepted tokens copied back inside the timed region (two steps alternate so
+that the next round's upload overlaps the current round).  `roofline` is for the tree-attention
+call (the dominant
 kernel), with algorithmic bytes = the KV of every request read once + Q + O + LSE.
 `--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
 """
@@ -332,8 +334,8 @@ def main():
     # each round streams 540 MB of K/V (4x L2) and the copy engine writes the round's inputs.
     e2e = None
     if not args.no_e2e:
-        host_in = step.pinned_host_inputs()
-        steps_ab = [step, step.twin()]
+        steps_ab = [step.twin(), step.twin()]
+        host_in = steps_ab[0].pinned_host_inputs()
         host_outs = [step.host_output_buffers(), step.host_output_buffers()]
         copy_stream = torch.cuda.Stream()
         ready = [torch.cuda.Event(), torch.cuda.Event()]

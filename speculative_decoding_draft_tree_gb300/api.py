@@ -23,6 +23,22 @@ def _ws(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
+def _packed(tensors: Dict[str, torch.Tensor], device, pin: bool = False):
+    """One contiguous byte buffer holding tensors shaped like `tensors` at 256-byte aligned
+    offsets, and the views into it (one copy moves them all)."""
+    offs, off = {}, 0
+    for k, t in tensors.items():
+        off = (off + 255) // 256 * 256
+        offs[k] = off
+        off += t.numel() * t.element_size()
+    buf = torch.empty(max(off, 1), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for k, t in tensors.items()}
+    return buf, views
+
+
 class VerifyStep:
     def __init__(self, w: Workload, sibling_rule: int = B.SPEC_SIBLING_RESIDUAL,
                  with_lse: bool = True):
@@ -40,12 +56,16 @@ class VerifyStep:
         self.is_internal = torch.empty(N, dtype=torch.uint8, device=dev)
         self.o = torch.empty_like(w.q)
         self.lse = torch.empty((N, w.H_q), dtype=torch.float32, device=dev) if with_lse else None
-        self.out_tokens = torch.empty((Bn, w.max_path), **i32)
+        # the results a round sends back to the host share one buffer (one device-to-host copy)
+        self._out_pack, outs = _packed(dict(out_tokens=torch.empty((Bn, w.max_path), dtype=torch.int32),
+                                            out_len=torch.empty(Bn, dtype=torch.int32),
+                                            new_kv_len=torch.empty(Bn, dtype=torch.int32)), dev)
+        self.out_tokens, self.out_len = outs["out_tokens"], outs["out_len"]
         self.path = torch.empty((Bn, w.max_path), **i32)
-        self.out_len = torch.empty(Bn, **i32)
         self.n_acc = torch.empty(Bn, **i32)
         self.rejections = torch.empty(Bn, **i32)
-        self.new_kv_len = torch.empty(Bn, **i32)
+        self.new_kv_len = outs["new_kv_len"]
+        self._in_pack = None   # set by twin(): the per-round inputs in one device buffer
         self.blocks_in_use = torch.empty(Bn, **i32)
         self.slot_map = torch.empty((Bn, w.max_path, 2), **i32)
         self.k_layer0 = w.k_cache[0]
@@ -105,22 +125,31 @@ class VerifyStep:
                     draft=w.draft, q=w.q, block_table=w.block_table)
 
     def pinned_host_inputs(self) -> Dict[str, torch.Tensor]:
+        """The round's inputs in pinned host memory: one packed buffer ("_pack", same layout as
+        the step's device pack) for a step made by twin(), else one tensor per input."""
+        if self._in_pack is not None:
+            host = torch.empty(self._in_pack.numel(), dtype=torch.uint8).pin_memory()
+            host.copy_(self._in_pack)
+            return {"_pack": host}
         return {k: v.detach().to("cpu").pin_memory() for k, v in self.step_input_tensors().items()}
 
     def upload(self, host_inputs: Dict[str, torch.Tensor], stream=None):
         """Copy a round's inputs from pinned host memory to this step's device tensors, on
         `stream` (default: the current stream)."""
-        dev_in = self.step_input_tensors()
         with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
+            if "_pack" in host_inputs:
+                if self._in_pack is None or self._in_pack.numel() != host_inputs["_pack"].numel():
+                    raise ValueError("a packed upload needs a step made by twin() of the same shape")
+                self._in_pack.copy_(host_inputs["_pack"], non_blocking=True)
+                return
+            dev_in = self.step_input_tensors()
             for k, h in host_inputs.items():
                 dev_in[k].copy_(h, non_blocking=True)
 
     def download(self, host_out: Dict[str, torch.Tensor], stream=None):
         """Copy the accepted tokens, lengths and new KV lengths to pinned host memory."""
         with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream()):
-            host_out["out_tokens"].copy_(self.out_tokens, non_blocking=True)
-            host_out["out_len"].copy_(self.out_len, non_blocking=True)
-            host_out["new_kv_len"].copy_(self.new_kv_len, non_blocking=True)
+            host_out["_pack"].copy_(self._out_pack, non_blocking=True)
 
     def run_from_host(self, host_inputs: Dict[str, torch.Tensor], host_out: Dict[str, torch.Tensor],
                       stream=None):
@@ -135,15 +164,25 @@ class VerifyStep:
         """A second step of the same shape over its own copies of the per-round input tensors
         and the same KV cache: while one step runs a round, the next round's inputs can be
         uploaded into the other (double buffering)."""
-        fresh = {k: v.clone() for k, v in self.step_input_tensors().items()}
-        return VerifyStep(dataclasses.replace(self.w, **fresh), self.sibling_rule,
+        src = self.step_input_tensors()
+        pack, fresh = _packed(src, self.w.target.device)
+        for k, v in fresh.items():
+            v.copy_(src[k])
+        step = VerifyStep(dataclasses.replace(self.w, **fresh), self.sibling_rule,
                           self.lse is not None)
+        step._in_pack = pack
+        return step
 
     def host_output_buffers(self) -> Dict[str, torch.Tensor]:
-        return dict(out_tokens=torch.empty_like(self.out_tokens, device="cpu").pin_memory(),
-                    out_len=torch.empty_like(self.out_len, device="cpu").pin_memory(),
-                    new_kv_len=torch.empty_like(self.new_kv_len, device="cpu").pin_memory())
+        """Pinned host buffers for download(): "_pack" and the views out_tokens, out_len,
+        new_kv_len into it."""
+        pack, views = _packed(dict(out_tokens=self.out_tokens, out_len=self.out_len,
+                                   new_kv_len=self.new_kv_len), "cpu", pin=True)
+        return {"_pack": pack, **views}
 
     @staticmethod
     def bytes_of(tensors: Dict[str, torch.Tensor]) -> int:
+        """Bytes one copy of these buffers moves (a packed buffer counts once, padding included)."""
+        if "_pack" in tensors:
+            return tensors["_pack"].numel() * tensors["_pack"].element_size()
         return sum(t.numel() * t.element_size() for t in tensors.values())

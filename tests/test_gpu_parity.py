@@ -212,12 +212,14 @@ def test_twin_and_host_round_trip():
     assert twin.w.target.data_ptr() != w.target.data_ptr()
     out_b = twin.host_output_buffers()
     copy_stream = torch.cuda.Stream()
-    twin.upload(host_in, copy_stream)
+    packed_in = twin.pinned_host_inputs()
+    assert set(packed_in) == {"_pack"}
+    twin.upload(packed_in, copy_stream)
     torch.cuda.current_stream().wait_stream(copy_stream)
     twin.run()
     twin.download(out_b)
     _sync()
     for k, v in res_a.items():
         assert torch.equal(twin.results()[k].cpu(), v), k
-    for k in out_a:
+    for k in ("out_tokens", "out_len", "new_kv_len"):
         assert torch.equal(out_a[k], out_b[k]), k
