@@ -206,6 +206,28 @@ def run_oracle_sample(w, n_req):
     return time.perf_counter() - t0
 
 
+def rank_seeds(rank):
+    """Seeds of rank `rank`'s batch: every rank verifies its own requests of the same shape
+    (weak scaling), rank 0 the default workload."""
+    return dict(logits=1 + 1000 * rank, drafting=2 + 1000 * rank, qkv=3 + 1000 * rank)
+
+
+def max_over_ranks(seconds, world, device=None):
+    """The slowest rank's time, returned on every rank: the job is done when all ranks are."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank_step, steps, seconds, world):
+    """Units all ranks processed per second of the slowest rank."""
+    return world * units_per_rank_step * steps / seconds
+
+
 def cpu_baseline(w, n_req=None, budget_s=15.0):
     """Time the oracle on a bounded sample sized to about `budget_s` seconds."""
     sizes = w.tree_sizes()
@@ -264,9 +286,7 @@ def main():
     binding.load_library(build_if_missing=True)
     dev = torch.device("cuda", local_rank)
     # weak scaling: every rank verifies its own batch of the same shape
-    w = W.make_config(args.workload, scale="full", device=dev,
-                      seeds=dict(logits=1 + 1000 * rank, drafting=2 + 1000 * rank,
-                                 qkv=3 + 1000 * rank))
+    w = W.make_config(args.workload, scale="full", device=dev, seeds=rank_seeds(rank))
     tokens_per_step = int(sum(w.tree_sizes()))
     step = VerifyStep(w)
     stream = torch.cuda.current_stream()
@@ -320,12 +340,9 @@ def main():
     attn_ms = [e[0].elapsed_time(e[1]) for e in ev_attn]
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / len(attn_ms) / 1e3
-    if world > 1:
-        tt = torch.tensor([t_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_total = float(tt.item())
+    t_total = max_over_ranks(t_total, world, dev)
     ms_per_step = 1e3 * t_total / args.steps
-    value = world * tokens_per_step * args.steps / t_total
+    value = job_throughput(tokens_per_step, args.steps, t_total, world)
 
     # end to end through the public API with pinned host buffers: every round's inputs are
     # copied from pinned host memory and its accepted tokens copied back inside the timed region;
@@ -360,12 +377,8 @@ def main():
             free[k].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        t_e2e = e0.elapsed_time(e1) / 1e3
-        if world > 1:
-            tt = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e2e = float(tt.item())
-        e2e = {"value": world * tokens_per_step * args.steps / t_e2e,
+        t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+        e2e = {"value": job_throughput(tokens_per_step, args.steps, t_e2e, world),
                "unit": "verified tree tokens/s",
                "h2d_bytes_per_step": VerifyStep.bytes_of(host_in),
                "d2h_bytes_per_step": VerifyStep.bytes_of(host_outs[0]),
