@@ -13,14 +13,17 @@ Modules (each function cites the passage it follows):
   verify     -- temperature softmax, min(1, p/q) ratio test in tree order, residual resampling,
                 bonus token, greedy (tau = 0) argmax matching
   compact    -- KV commit/rollback of the accepted path
+  rope       -- rotary position embedding at the tree's position ids and the tree K/V written
+                into its paged cache slots (the step before attention)
 
 Pins (tests/test_oracle_*.py, run with -m "not gpu") tie each function to something other than
 itself: the page's 6-node mask table, the 123 / 45 node counts, E[L] = (1 - a^(g+1)) / (1 - a),
 exact losslessness by black-box bisection over the uniforms, chi-square against p, library
-scaled-dot-product attention for the T = 1 and chain special cases, and the sequential-decoding
-invariant for compaction.  No oracle function is "parity unpinned".
+scaled-dot-product attention for the T = 1 and chain special cases, the sequential-decoding
+invariant for compaction, and RoFormer's complex form, the frequencies as numbers, brute force
+over cache rows and chain = causal decoding for the RoPE step.  No oracle function is "parity unpinned".
 """
-from . import tree, attention, verify, compact  # noqa: F401
+from . import tree, attention, verify, compact, rope  # noqa: F401
 
 # request status bits (the oracle's own numbering of the data errors it detects)
 BAD_PARENT = 1
