@@ -59,7 +59,8 @@ def tree_rope_kv_write(q, k_new, v_new, pos_id, node_offset, prefix_len, block_t
     at pos_id[n]; its rotated k and its v go to logical slot prefix_len[r] + i, i.e. row
     (slot % bs) of physical block block_table[r][slot // bs].
 
-    Requests with a nonzero req_status (from the tree build) or a negative pos_id are skipped.
+    Requests with a nonzero req_status (from the tree build), a negative prefix length (no
+    cache slots) or a negative pos_id are skipped.
     A request whose slot maps outside [0, num_blocks) gets BAD_BLOCK and none of its nodes are
     written.  Returns dict(q fp64 [N, H_q, d] (NaN where skipped), k_cache, v_cache (fp64
     copies with the slots written), status [B])."""
@@ -78,6 +79,8 @@ def tree_rope_kv_write(q, k_new, v_new, pos_id, node_offset, prefix_len, block_t
         if status[r]:
             continue
         o, T, P = int(node_offset[r]), int(node_offset[r + 1] - node_offset[r]), int(prefix_len[r])
+        if P < 0:
+            continue
         dest = []
         for i in range(T):
             slot = P + i

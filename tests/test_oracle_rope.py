@@ -165,6 +165,11 @@ def test_bad_block_and_bad_request_are_skipped():
                                 c["kc"], c["vc"], req_status=[2, 0])
     assert list(out["status"]) == [2, OR.BAD_BLOCK]
     np.testing.assert_array_equal(out["k_cache"], c["kc"])
+    # a negative prefix length has no cache slots: nothing of that request is written
+    out = OR.tree_rope_kv_write(c["q"], c["k_new"], c["v_new"], pos, c["no"], [-1, 3], c["table"],
+                                c["kc"], c["vc"], req_status=[0, 0])
+    assert np.isnan(out["q"][:4]).all()
+    np.testing.assert_array_equal(out["k_cache"], c["kc"])
 
 
 def test_chain_equals_causal_decoding():
