@@ -12,8 +12,9 @@ Prints ONE JSON line (rank 0).  `value` is verified tree tokens per second over 
 public VerifyStep.upload / run / download with every round's inputs copied from pinned host
 memory and its accepted tokens copied back inside the timed region (two steps alternate so
 that the next round's upload overlaps the current round).  `roofline` is for the tree-attention
-call (the dominant
-kernel), with algorithmic bytes = the KV of every request read once + Q + O + LSE.
+call (the dominant kernel), with algorithmic bytes = the KV of every request read once + Q + O +
+LSE.  `next` measures the step before attention (rotary embedding at the tree's position ids
+plus the tree K/V slot write) alone and inside a step that includes it.
 `--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
 """
 import argparse
@@ -27,8 +28,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = 2
-# kernels of the library launched by one step: tree_build_kernel, attn_tc_kernel,
-# attn_merge_kernel, verify_rows_kernel, verify_walk_kernel, kv_compact_kernel
+# kernels of the library launched by one step: tree_build_kernel, attn_tc_small_kernel (or
+# attn_tc_kernel), attn_merge_kernel, verify_rows_kernel, verify_walk_kernel, kv_compact_kernel
 KERNELS_PER_STEP = 6
 FLUSH_BYTES = 256 << 20
 
@@ -97,6 +98,13 @@ def recorded_traffic():
         return rec["dram_bytes_read_per_launch"] + rec["dram_bytes_write_per_launch"]
     except Exception:
         return None
+
+
+def rope_bytes(w):
+    """Algorithmic bytes of the RoPE + tree K/V write step: every tree token's q, new k and new
+    v row read once and written once (q to the attention input, k and v to their cache slot)."""
+    es = 2 if w.dtype == "bf16" else 4
+    return 2 * w.N * (w.H_q + 2 * w.H_kv) * w.d * es
 
 
 def attention_bytes(w):
@@ -307,6 +315,19 @@ def main():
           for _ in range(args.steps)]
     ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+    # the step before attention (rotary embedding + tree K/V slot write), measured beside the
+    # step: alone, and as part of a step that includes it
+    step_r = VerifyStep(w)
+    k_new, v_new = W.new_tree_kv(w)
+    step_r.enable_rope(w.q.clone(), k_new, v_new)
+    def ev_pairs():
+        return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+
+    ev_rope, ev_fused, ev_tree, ev_step_r = ev_pairs(), ev_pairs(), ev_pairs(), ev_pairs()
+    for _ in range(3):
+        step_r.run()
+    torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -332,12 +353,41 @@ def main():
         a0.record(stream)
         step.attention()
         a1.record(stream)
+    for i in range(args.steps):   # the standalone rotary call, after a tree build
+        l2_flush(i)
+        step_r.tree_build()
+        r0, r1 = ev_rope[i]
+        r0.record(stream)
+        step_r.rope()
+        r1.record(stream)
+    for i in range(args.steps):   # the tree build alone, and fused with the rotary step
+        l2_flush(i)
+        r0, r1 = ev_tree[i]
+        r0.record(stream)
+        step_r.tree_build()
+        r1.record(stream)
+        l2_flush(i)
+        r0, r1 = ev_fused[i]
+        r0.record(stream)
+        step_r.tree_build_rope()
+        r1.record(stream)
+    for i in range(args.steps):   # a whole step with the fused launch
+        l2_flush(i)
+        r0, r1 = ev_step_r[i]
+        r0.record(stream)
+        step_r.run()
+        r1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop() if sampler else None
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     attn_ms = [e[0].elapsed_time(e[1]) for e in ev_attn]
+    def mean_s(evs):
+        return sum(e[0].elapsed_time(e[1]) for e in evs) / len(evs) / 1e3
+
+    t_rope, t_fused, t_tree, t_step_r = (mean_s(ev_rope), mean_s(ev_fused), mean_s(ev_tree),
+                                         mean_s(ev_step_r))
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / len(attn_ms) / 1e3
     t_total = max_over_ranks(t_total, world, dev)
@@ -397,6 +447,17 @@ def main():
                 "traffic": recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None,
                 "peak_kind": peak_kind, "algorithmic_bytes": abytes,
                 "us_per_launch": round(t_attn * 1e6, 2)}
+    rbytes = rope_bytes(w)
+    next_rows = {"rope_kv_write": {
+        "kernel": "spec_tree_build_rope_kv_write (tree build fused with the rotary step)",
+        "bound": "hbm", "algorithmic_bytes": rbytes,
+        "us_per_launch": round(t_fused * 1e6, 2),
+        "achieved": round(rbytes / t_fused / 1e9, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(rbytes / t_fused / 1e9 / peak, 4),
+        "us_tree_build_alone": round(t_tree * 1e6, 2),
+        "us_standalone_rope_call": round(t_rope * 1e6, 2),
+        "ms_per_step_with_it": round(1e3 * t_step_r, 4),
+        "value_with_it": round(tokens_per_step / t_step_r, 1)}}
     cb = None
     if not args.no_cpu_baseline:
         w_cpu = W.make_config(args.workload, scale="full", device="cpu")
@@ -409,7 +470,7 @@ def main():
         "data": "synthetic", "config": workload_description(w, args.workload),
         "requests_per_s": round(world * w.B * args.steps / t_total, 1),
         "accepted_tokens_per_request": round(float(out_len.float().mean()), 3),
-        "roofline": roofline, "cpu_baseline": cb, "e2e": e2e,
+        "roofline": roofline, "cpu_baseline": cb, "e2e": e2e, "next": next_rows,
         "clocks": clocks, "gpu_launches": KERNELS_PER_STEP * args.steps,
     }
     print(json.dumps(line))

@@ -95,6 +95,72 @@ spec_status_t spec_tree_build(const int32_t* parent, const int32_t* node_offset,
                               uint8_t* is_internal, int32_t* req_status, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * spec_tree_rope_kv_write  [TREE]
+ * The step before tree attention: rotary position embedding (RoFormer, Su et al. 2021, section
+ * 3.2 -- the pages say only that position ids must follow the tree) of every tree node's q and
+ * new k at its position id, and the node's K/V stored where spec_tree_attention reads it.
+ * For node n = node_offset[r] + i at position m = pos_id[n] (prefix_len[r] + depth, from
+ * spec_tree_build), pair j < rotary_dim/2 of each head row turns by m * base^(-2j/rotary_dim):
+ *   (a, b) -> (a cos - b sin, a sin + b cos),
+ * pair j being components (2j, 2j+1) when `interleaved` != 0 and (j, j + rotary_dim/2)
+ * otherwise (the half-split layout of LLaMA-family checkpoints); components past rotary_dim are
+ * copied unchanged.  Rotated q goes to q_out; rotated k and unchanged v go to logical slot
+ * prefix_len[r] + i of the paged cache (row slot % block_size of block
+ * block_table[r][slot / block_size]).  Arithmetic: angle formed and reduced modulo 2 pi in fp64,
+ * rotation in fp32, one rounding to `dtype`.
+ * Layouts (element type `dtype`, contiguous, 16-byte aligned): q_in, q_out [N][H_q][head_dim]
+ * (q_out == q_in rotates in place; partial overlap is not allowed); k_new, v_new
+ * [N][H_kv][head_dim]; k_cache, v_cache [num_blocks][H_kv][block_size][head_dim] (one layer);
+ * block_table [B][max_blocks_per_req], prefix_len [B], node_offset [B+1], pos_id [N] int32.
+ * Data errors: nodes of a request with req_status[r] != 0 (e.g. from spec_tree_build) are not
+ * touched; a request any of whose tree slots maps outside [0, num_blocks) gets
+ * SPEC_REQ_BAD_BLOCK and none of its nodes is written.
+ * Errors: SPEC_ERR_INVALID_ARG (null / misaligned pointers, bad sizes, rotary_dim odd or outside
+ * [2, head_dim], base not positive and finite); SPEC_ERR_UNSUPPORTED when a rotated pair would
+ * straddle 16-byte vectors (half-split: rotary_dim/2 must be a multiple of 8 bf16 / 4 fp32
+ * elements; interleaved: rotary_dim a multiple of 8 / 4) or rotary_dim > 256; SPEC_ERR_CUDA.
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  spec_dtype_t dtype;
+  int32_t B, N, H_q, H_kv, head_dim, rotary_dim;
+  int32_t interleaved;         /* 0: pairs (j, j + rotary_dim/2); 1: pairs (2j, 2j+1) */
+  int32_t block_size, num_blocks, max_blocks_per_req;
+  double base;                 /* e.g. 10000 (LLaMA-2), 500000 (LLaMA-3), 1e6 (Qwen2) */
+  const void* q_in;
+  void* q_out;
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int32_t* block_table;
+  const int32_t* prefix_len;
+  const int32_t* node_offset;
+  const int32_t* pos_id;
+  int32_t* req_status;
+} spec_rope_params;
+
+spec_status_t spec_tree_rope_kv_write(const spec_rope_params* p, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * spec_tree_build_rope_kv_write  [TREE]
+ * spec_tree_build and spec_tree_rope_kv_write in one launch: the tree outputs of
+ * spec_tree_build (same arguments, same results), then -- for every request the tree build
+ * accepts -- the rotary embedding and K/V slot write of spec_tree_rope_kv_write at
+ * pos = prefix_len + depth, described by `rope` (host pointer; its B and N must equal this
+ * call's, and its node_offset, prefix_len, pos_id and req_status must be NULL or this call's
+ * buffers).  req_status[r] ends as spec_tree_build's bits, or SPEC_REQ_BAD_BLOCK for a valid
+ * tree with a slot outside the pool (nothing of that request is then written to q_out or the
+ * cache); the results equal the two calls made in sequence.
+ * Errors: those of the two calls.
+ * ------------------------------------------------------------------------------------------ */
+spec_status_t spec_tree_build_rope_kv_write(const int32_t* parent, const int32_t* node_offset,
+                                            const int32_t* prefix_len, int32_t B, int32_t N,
+                                            int32_t T_max, int32_t* depth, int32_t* pos_id,
+                                            uint32_t* anc_mask, uint8_t* is_internal,
+                                            int32_t* req_status, const spec_rope_params* rope,
+                                            spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * spec_tree_attention  [TREE], [SURV 5.2, 12.4.3]
  * O[n][h] = sum_j softmax_j(scale * q[n][h] . k_j) v_j over the logical KV slots
  *   j in {0 .. P_r-1} U {P_r + a : a == i or a is an ancestor of i}

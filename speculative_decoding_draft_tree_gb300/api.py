@@ -83,12 +83,36 @@ class VerifyStep:
         self.comp = B.compact_params(w.k_cache, w.v_cache, w.block_table, w.prefix_len,
                                      self.path, self.n_acc, self.req_status, self.new_kv_len,
                                      self.slot_map, self.blocks_in_use, w.max_path)
+        self.rope_p = None
+
+    def enable_rope(self, q_raw, k_new, v_new, base=10000.0, rotary_dim=None, interleaved=False,
+                    fused=True):
+        """Add the step before attention to every round: q_raw, k_new, v_new ([N, H, d], the
+        tree tokens' projections before position encoding) are rotated at the tree's position
+        ids into the workload's q and into the tree slots of layer 0's cache.  fused: run it
+        inside the tree build's launch (spec_tree_build_rope_kv_write) instead of as a call of
+        its own after it."""
+        w = self.w
+        self.rope_fused = fused
+        self.rope_inputs = (q_raw, k_new, v_new)
+        self.rope_p = B.rope_params(q_raw, w.q, k_new, v_new, self.k_layer0, self.v_layer0,
+                                    w.block_table, w.prefix_len, w.node_offset, self.pos_id,
+                                    self.req_status, base, rotary_dim, interleaved)
 
     # individual stages ---------------------------------------------------------------------
+    def tree_build_rope(self, stream=None):
+        w = self.w
+        B.spec_tree_build_rope_kv_write(w.parent, w.node_offset, w.prefix_len, w.T_max,
+                                        self.depth, self.pos_id, self.anc_mask,
+                                        self.is_internal, self.req_status, self.rope_p, stream)
+
     def tree_build(self, stream=None):
         w = self.w
         B.spec_tree_build(w.parent, w.node_offset, w.prefix_len, w.T_max, self.depth, self.pos_id,
                           self.anc_mask, self.is_internal, self.req_status, stream)
+
+    def rope(self, stream=None):
+        B.spec_tree_rope_kv_write(self.rope_p, stream)
 
     def attention(self, stream=None):
         B.spec_tree_attention(self.attn, self.attn_ws, stream)
@@ -100,8 +124,15 @@ class VerifyStep:
         B.spec_kv_compact(self.comp, stream)
 
     def run(self, stream=None):
-        """One full round (4 library calls, 1 + 2 + 3 + 1 kernel launches on the stream)."""
-        self.tree_build(stream)
+        """One full round (4 library calls, 1 + 2 + 2 + 1 kernel launches on the stream; with
+        enable_rope, the tree build and the rotary step share one launch, or run as two calls
+        when fused=False)."""
+        if self.rope_p is not None and self.rope_fused:
+            self.tree_build_rope(stream)
+        else:
+            self.tree_build(stream)
+            if self.rope_p is not None:
+                self.rope(stream)
         self.attention(stream)
         self.verify(stream)
         self.compact(stream)

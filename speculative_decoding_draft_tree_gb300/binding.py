@@ -19,7 +19,7 @@ SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS = 0, 1
 SPEC_SIBLING_RESIDUAL, SPEC_SIBLING_INDEPENDENT = 0, 1
 REQ_BITS = dict(BAD_PARENT=1, BAD_SIZE=2, BAD_TOKEN=4, BAD_DRAFT_ROW=8, BAD_DEPTH=16,
                 BAD_BLOCK=32, TIMEOUT=64)
-EXPORTS = ["spec_tree_build", "spec_tree_attention", "spec_attention_workspace_size",
+EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_kv_write", "spec_tree_attention", "spec_attention_workspace_size",
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error"]
 
@@ -57,6 +57,15 @@ class SpecCompactParams(ctypes.Structure):
                 ("slot_map", _vp), ("blocks_in_use", _vp)]
 
 
+class SpecRopeParams(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("B", _i32), ("N", _i32), ("H_q", _i32), ("H_kv", _i32),
+                ("head_dim", _i32), ("rotary_dim", _i32), ("interleaved", _i32),
+                ("block_size", _i32), ("num_blocks", _i32), ("max_blocks_per_req", _i32),
+                ("base", ctypes.c_double), ("q_in", _vp), ("q_out", _vp), ("k_new", _vp),
+                ("v_new", _vp), ("k_cache", _vp), ("v_cache", _vp), ("block_table", _vp),
+                ("prefix_len", _vp), ("node_offset", _vp), ("pos_id", _vp), ("req_status", _vp)]
+
+
 _LIB = None
 
 
@@ -79,6 +88,11 @@ def load_library(build_if_missing=False):
     st = ctypes.c_int
     lib.spec_tree_build.restype = st
     lib.spec_tree_build.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+    lib.spec_tree_rope_kv_write.restype = st
+    lib.spec_tree_build_rope_kv_write.restype = st
+    lib.spec_tree_build_rope_kv_write.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
+                                                  _vp, _vp, ctypes.POINTER(SpecRopeParams), _vp]
+    lib.spec_tree_rope_kv_write.argtypes = [ctypes.POINTER(SpecRopeParams), _vp]
     lib.spec_tree_attention.restype = st
     lib.spec_tree_attention.argtypes = [ctypes.POINTER(SpecAttnParams), _vp, ctypes.c_size_t, _vp]
     lib.spec_attention_workspace_size.restype = ctypes.c_size_t
@@ -157,6 +171,56 @@ def spec_tree_build(parent, node_offset, prefix_len, T_max, depth, pos_id, anc_m
                                _ptr(depth), _ptr(pos_id), _ptr(anc_mask), _ptr(is_internal),
                                _ptr(req_status), _stream(stream))
     _check(code, "spec_tree_build")
+
+
+def rope_params(q_in, q_out, k_new, v_new, k_cache, v_cache, block_table, prefix_len,
+                node_offset, pos_id, req_status, base=10000.0, rotary_dim=None, interleaved=False):
+    """k_cache / v_cache: one layer, [num_blocks, H_kv, block_size, head_dim]."""
+    for t, n in ((q_in, "q_in"), (q_out, "q_out"), (k_new, "k_new"), (v_new, "v_new"),
+                 (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, q_in.dtype, n)
+    for t, n in ((block_table, "block_table"), (prefix_len, "prefix_len"),
+                 (node_offset, "node_offset"), (pos_id, "pos_id"), (req_status, "req_status")):
+        _need(t, torch.int32, n)
+    p = SpecRopeParams()
+    p.dtype = _dtype_code(q_in)
+    p.B = node_offset.numel() - 1
+    p.N, p.H_q, p.head_dim = q_in.shape
+    p.H_kv = k_new.shape[1]
+    if q_out.shape != q_in.shape or k_new.shape != (p.N, p.H_kv, p.head_dim) or v_new.shape != k_new.shape:
+        raise ValueError("q_out must match q_in and v_new must match k_new [N, H_kv, head_dim]")
+    p.rotary_dim = p.head_dim if rotary_dim is None else int(rotary_dim)
+    p.interleaved = 1 if interleaved else 0
+    p.num_blocks, _, p.block_size, _ = k_cache.shape
+    p.max_blocks_per_req = block_table.shape[1]
+    p.base = float(base)
+    p.q_in, p.q_out, p.k_new, p.v_new = q_in.data_ptr(), q_out.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+    p.k_cache, p.v_cache = k_cache.data_ptr(), v_cache.data_ptr()
+    p.block_table, p.prefix_len = block_table.data_ptr(), prefix_len.data_ptr()
+    p.node_offset, p.pos_id, p.req_status = node_offset.data_ptr(), pos_id.data_ptr(), req_status.data_ptr()
+    return p
+
+
+def spec_tree_build_rope_kv_write(parent, node_offset, prefix_len, T_max, depth, pos_id,
+                                  anc_mask, is_internal, req_status, rope, stream=None):
+    """spec_tree_build and spec_tree_rope_kv_write in one launch; `rope` from rope_params()
+    over the same node_offset / prefix_len / pos_id / req_status."""
+    lib = load_library()
+    for t, n in ((parent, "parent"), (node_offset, "node_offset"), (prefix_len, "prefix_len"),
+                 (depth, "depth"), (pos_id, "pos_id"), (req_status, "req_status"),
+                 (anc_mask, "anc_mask")):
+        _need(t, torch.int32, n)
+    _need(is_internal, torch.uint8, "is_internal")
+    code = lib.spec_tree_build_rope_kv_write(
+        _ptr(parent), _ptr(node_offset), _ptr(prefix_len), node_offset.numel() - 1,
+        parent.numel(), T_max, _ptr(depth), _ptr(pos_id), _ptr(anc_mask), _ptr(is_internal),
+        _ptr(req_status), ctypes.byref(rope), _stream(stream))
+    _check(code, "spec_tree_build_rope_kv_write")
+
+
+def spec_tree_rope_kv_write(params, stream=None):
+    code = load_library().spec_tree_rope_kv_write(ctypes.byref(params), _stream(stream))
+    _check(code, "spec_tree_rope_kv_write")
 
 
 def attention_params(q, k_cache, v_cache, block_table, prefix_len, node_offset, anc_mask, T_max,

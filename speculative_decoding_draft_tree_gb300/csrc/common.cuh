@@ -66,8 +66,10 @@ inline spec_status_t launch_result(cudaError_t e) {
 // device side
 // ------------------------------------------------------------------------------------------
 // Every kernel of the library calls pdl_wait() before its first global memory access (the
-// previous kernel on the stream may still be writing its inputs) and then pdl_trigger(), which
-// lets the next kernel be scheduled early.  Both are no-ops for a plain launch.
+// previous kernel on the stream may still be writing its inputs) and pdl_trigger(), which lets
+// the next kernel be scheduled early -- right after the wait in most kernels; after its stores
+// in a kernel whose run overlapped by the next kernel's waiting CTAs measured slower (the tree
+// build fused with the rotary step).  Both are no-ops for a plain launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

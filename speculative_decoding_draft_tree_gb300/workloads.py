@@ -258,6 +258,17 @@ def _finish(name, dtype, B, V, H_q, H_kv, d, bs, tau, parents_per_req, tokens, d
 SEEDS = dict(logits=1, drafting=2, qkv=3, kvlen=4, perm=5, uniform=0)
 
 
+def new_tree_kv(w: "Workload", seed: int = SEEDS["qkv"] + 29):
+    """The tree tokens' own K and V rows before they enter the cache: N(0, 1) in the workload's
+    dtype, [N, H_kv, d] each, on the workload's device (inputs of the RoPE + K/V write step)."""
+    g = _gen(seed, w.q.device)
+    shape = (w.N, w.H_kv, w.d)
+    td = _torch_dtype(w.dtype)
+    k = torch.randn(shape, generator=g, device=w.q.device, dtype=torch.float32).to(td)
+    v = torch.randn(shape, generator=g, device=w.q.device, dtype=torch.float32).to(td)
+    return k, v
+
+
 # ----------------------------------------------------------------------------------------------
 # Chains (configurations 1 and 2).
 # ----------------------------------------------------------------------------------------------

@@ -3,6 +3,7 @@ function include/spec_verify.h declares, and the Python structs match the C layo
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 
@@ -38,11 +39,30 @@ def test_status_strings(lib):
         assert lib.spec_status_string(code).decode() == name
 
 
-def test_struct_layouts_match_header():
-    # sizes follow from the C declarations (natural alignment on LP64)
-    assert ctypes.sizeof(B.SpecAttnParams) == 44 + 4 + 10 * 8
-    assert ctypes.sizeof(B.SpecVerifyParams) == 28 + 4 + 16 + 12 + 4 + 15 * 8
-    assert ctypes.sizeof(B.SpecCompactParams) == 36 + 4 + 8 + 10 * 8
+def test_struct_layouts_match_header(tmp_path):
+    """Every field offset and every struct size of the Python binding equals what a C compiler
+    makes of include/spec_verify.h."""
+    structs = {"spec_attn_params": B.SpecAttnParams, "spec_verify_params": B.SpecVerifyParams,
+               "spec_compact_params": B.SpecCompactParams, "spec_rope_params": B.SpecRopeParams}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec_verify.h"',
+             "int main(void) {"]
+    want = []
+    for cname, py in structs.items():
+        lines.append(f'  printf("%zu\\n", sizeof({cname}));')
+        want.append(ctypes.sizeof(py))
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("%zu\\n", offsetof({cname}, {fname}));')
+            want.append(getattr(py, fname).offset)
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    cc = subprocess.run(["gcc", "-I", build.INCLUDE, str(src), "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got == want
 
 
 def test_host_validation_without_gpu(lib):
@@ -50,6 +70,7 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_tree_attention(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_kv_compact(None, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_tree_rope_kv_write(None, None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_tree_build(None, None, None, 0, 0, 0, None, None, None, None, None,
                                None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_verify_workspace_size(None) == 0
