@@ -15,15 +15,17 @@ Modules (each function cites the passage it follows):
   compact    -- KV commit/rollback of the accepted path
   rope       -- rotary position embedding at the tree's position ids and the tree K/V written
                 into its paged cache slots (the step before attention)
+  lookahead  -- the lookahead-decoding mask (lookahead and verify branches in one forward)
 
 Pins (tests/test_oracle_*.py, run with -m "not gpu") tie each function to something other than
 itself: the page's 6-node mask table, the 123 / 45 node counts, E[L] = (1 - a^(g+1)) / (1 - a),
 exact losslessness by black-box bisection over the uniforms, chi-square against p, library
 scaled-dot-product attention for the T = 1 and chain special cases, the sequential-decoding
 invariant for compaction, and RoFormer's complex form, the frequencies as numbers, brute force
-over cache rows and chain = causal decoding for the RoPE step.  No oracle function is "parity unpinned".
+over cache rows and chain = causal decoding for the RoPE step; a hand-derived worked example,
+the page's token counts and its two mask rules for the lookahead mask.  No oracle function is "parity unpinned".
 """
-from . import tree, attention, verify, compact, rope  # noqa: F401
+from . import tree, attention, verify, compact, rope, lookahead  # noqa: F401
 
 # request status bits (the oracle's own numbering of the data errors it detects)
 BAD_PARENT = 1
