@@ -14,7 +14,8 @@ memory and its accepted tokens copied back inside the timed region (two steps al
 that the next round's upload overlaps the current round).  `roofline` is for the tree-attention
 call (the dominant kernel), with algorithmic bytes = the KV of every request read once + Q + O +
 LSE.  `next` measures the step before attention (rotary embedding at the tree's position ids
-plus the tree K/V slot write) alone and inside a step that includes it.
+plus the tree K/V slot write) alone and inside a step that includes it, and the lookahead-
+decoding forward (a second mask workload on the same kernels).
 `--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
 """
 import argparse
@@ -327,6 +328,13 @@ def main():
     ev_rope, ev_fused, ev_tree, ev_step_r = ev_pairs(), ev_pairs(), ev_pairs(), ev_pairs()
     for _ in range(3):
         step_r.run()
+    # the lookahead-decoding forward (2-D Jacobi window + candidate n-grams) as a second mask
+    # workload on the same kernels: its attention call alone and a whole greedy step
+    wl = W.lookahead_config(scale="full", device=dev, seeds=rank_seeds(rank))
+    step_l = VerifyStep(wl)
+    ev_look_attn, ev_look_step = ev_pairs(), ev_pairs()
+    for _ in range(3):
+        step_l.run()
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
@@ -377,6 +385,18 @@ def main():
         r0.record(stream)
         step_r.run()
         r1.record(stream)
+    for i in range(args.steps):   # the lookahead forward: attention alone, then a whole step
+        l2_flush(i)
+        step_l.tree_build()
+        r0, r1 = ev_look_attn[i]
+        r0.record(stream)
+        step_l.attention()
+        r1.record(stream)
+        l2_flush(i)
+        r0, r1 = ev_look_step[i]
+        r0.record(stream)
+        step_l.run()
+        r1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -388,6 +408,7 @@ def main():
 
     t_rope, t_fused, t_tree, t_step_r = (mean_s(ev_rope), mean_s(ev_fused), mean_s(ev_tree),
                                          mean_s(ev_step_r))
+    t_look_attn, t_look_step = mean_s(ev_look_attn), mean_s(ev_look_step)
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / len(attn_ms) / 1e3
     t_total = max_over_ranks(t_total, world, dev)
@@ -458,6 +479,16 @@ def main():
         "us_standalone_rope_call": round(t_rope * 1e6, 2),
         "ms_per_step_with_it": round(1e3 * t_step_r, 4),
         "value_with_it": round(tokens_per_step / t_step_r, 1)}}
+    lbytes = attention_bytes(wl)
+    look_tokens = int(sum(wl.tree_sizes()))
+    next_rows["lookahead"] = {
+        "workload": wl.name, "tree_tokens_per_step": look_tokens,
+        "kernel": "spec_tree_attention on the lookahead mask", "bound": "hbm",
+        "algorithmic_bytes": lbytes, "us_per_launch": round(t_look_attn * 1e6, 2),
+        "achieved": round(lbytes / t_look_attn / 1e9, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(lbytes / t_look_attn / 1e9 / peak, 4),
+        "ms_per_step": round(1e3 * t_look_step, 4),
+        "value": round(look_tokens / t_look_step, 1)}
     cb = None
     if not args.no_cpu_baseline:
         w_cpu = W.make_config(args.workload, scale="full", device="cpu")

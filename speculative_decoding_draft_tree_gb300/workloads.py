@@ -502,6 +502,78 @@ CONFIG_NAMES = {
 }
 
 
+# ----------------------------------------------------------------------------------------------
+# Lookahead decoding: one forward over a 2-D Jacobi window and G candidate n-grams.
+# ----------------------------------------------------------------------------------------------
+def lookahead_parents(W: int, N: int, G: int) -> List[int]:
+    """Shape of one lookahead-decoding forward as a parent array: the current token; the window
+    (step 0 at positions 1 .. W-1, step l at positions l .. l+W-1, each token after the token
+    one step and one position back); then G candidate n-gram chains of N - 1 tokens each."""
+    index = {(0, 0): 0}
+    parents = [-1]
+    for p in range(1, W):
+        index[(0, p)] = len(parents)
+        parents.append(index[(0, p - 1)])
+    for l in range(1, N - 1):
+        for p in range(l, l + W):
+            index[(l, p)] = len(parents)
+            parents.append(index[(l - 1, p - 1)])
+    for _ in range(G):
+        prev = 0
+        for _k in range(1, N):
+            parents.append(prev)
+            prev = len(parents) - 1
+    return parents
+
+
+def lookahead_workload(*, B: int, W: int, N: int, G: int, V: int, dtype: str, H_q: int, H_kv: int,
+                       d: int, prefix, device="cpu", bs: int = 16, num_layers: int = 1,
+                       target_std: float = 3.0, seeds: Optional[Dict] = None,
+                       name: str = "lookahead", T_max: Optional[int] = None) -> Workload:
+    """Greedy (tau = 0) lookahead decoding.  Window tokens are random guesses; candidate 0 of
+    request r follows the target's greedy choices for r mod N tokens (a pool hit of that
+    length), the other candidates are random.  Draft rows are the target rows (unused at
+    tau = 0)."""
+    seeds = dict(SEEDS, **(seeds or {}))
+    parents = lookahead_parents(W, N, G)
+    T = len(parents)
+    g = _gen(seeds["logits"], device)
+    tgt = torch.randn((B * T, V), generator=g, device=device) * target_std
+    greedy = tgt.to(_torch_dtype(dtype)).float().argmax(dim=-1).cpu().numpy()
+    gd = _gen(seeds["drafting"], device)
+    tokens = torch.randint(0, V, (B * T,), generator=gd, device=device).cpu().numpy()
+    tokens = tokens.astype(np.int32)
+    first_candidate = T - G * (N - 1)
+    for r in range(B):
+        hits = min(r % N, N - 1) if G > 0 else 0
+        prev = 0
+        for k in range(1, hits + 1):
+            node = first_candidate + k - 1
+            tokens[r * T + node] = greedy[r * T + prev]
+            prev = node
+    has_child = set(parents[1:])
+    draft_row = np.array([r * T + i if i in has_child else -1 for r in range(B) for i in range(T)],
+                         dtype=np.int32)
+    prefix = list(prefix) if hasattr(prefix, "__len__") else [int(prefix)] * B
+    return _finish(name, dtype, B, V, H_q, H_kv, d, bs, 0.0, [parents] * B, tokens, draft_row,
+                   prefix, tgt, tgt.clone(), device, num_layers, False, seeds, T_max=T_max,
+                   meta=dict(kind="lookahead", W=W, N=N, G=G))
+
+
+def lookahead_config(*, scale: str = "full", device="cpu", seeds: Optional[Dict] = None,
+                     num_layers: int = 1) -> Workload:
+    """Full: W = 15, N = 5, G = 15 (120 tokens per forward, the 7B setting's compute multiple),
+    8 requests, LLaMA-2-7B attention (32 x d128 MHA), 2048 cached tokens, vocab 32000.  Small:
+    the page's W = 5, N = 4, G = 5 example (30 tokens), 3 requests, odd sizes."""
+    if scale == "full":
+        return lookahead_workload(B=8, W=15, N=5, G=15, V=32000, dtype="bf16", H_q=32, H_kv=32,
+                                  d=128, prefix=2048, device=device, seeds=seeds,
+                                  num_layers=num_layers, name="lookahead_w15_n5_g15_b8_v32000")
+    return lookahead_workload(B=3, W=5, N=4, G=5, V=3001, dtype="bf16", H_q=4, H_kv=2, d=128,
+                              prefix=[301, 17, 160], device=device, seeds=seeds,
+                              num_layers=num_layers, name="lookahead_w5_n4_g5_b3_small")
+
+
 def make_config(cid: int, *, scale: str = "full", device="cpu", tau: Optional[float] = None,
                 sigma: float = 1.0, num_layers: int = 1, seeds: Optional[Dict] = None) -> Workload:
     full = scale == "full"

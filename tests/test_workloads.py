@@ -60,3 +60,10 @@ def test_generation_is_deterministic():
     b = W.make_config(4, scale="small")
     assert (a.tokens == b.tokens).all() and (a.target == b.target).all()
     assert (a.k_cache == b.k_cache).all() and (a.uniforms == b.uniforms).all()
+
+
+def test_lookahead_shape_matches_the_oracles_mask():
+    """The generator's lookahead trees are the oracle's (built from the page's mask rules)."""
+    from oracle import lookahead as OL
+    for W_, N_, G_ in [(5, 4, 5), (15, 5, 15), (10, 5, 10), (7, 5, 7), (3, 3, 2), (6, 2, 0)]:
+        assert W.lookahead_parents(W_, N_, G_) == OL.lookahead_parents(W_, N_, G_).tolist()
