@@ -23,6 +23,12 @@ Readings where the pages are silent (each one is listed in the design notes):
     a, b >= 0); child k is accepted iff u_acc < R_k(tok) / (N_k q(tok)), which for k = 0 is
     exactly p/q.  SIBLING_INDEPENDENT tests every sibling with p/q and resamples from
     max(0, p - q);
+  * SIBLING_MULTI_DRAFT (several draft models proposing siblings: "万字综述 10+ 种 LLM 投机采样推理
+    加速方案" 5.1, a group of small models predicting together; "投机推理算法的常见优化手段" 草稿树的生成,
+    merge-based trees built from k small models): draft_row[c] is the row child c itself was
+    drawn from, so siblings carry their own q_c.  The pages' rule is applied sibling after
+    sibling with no closed form: the running target starts as r = p, child c is accepted iff
+    u_acc < r(tok) / q_c(tok), and a rejection replaces r by norm(max(0, r - q_c));
   * a zero residual mass (N_k = 0, reachable only through rounding) stops the sibling loop and
     the final token is drawn from p;
   * tau applies to target and draft logits alike; draft probabilities are used as given;
@@ -37,6 +43,7 @@ from .tree import tree_build
 
 SIBLING_RESIDUAL = 0
 SIBLING_INDEPENDENT = 1
+SIBLING_MULTI_DRAFT = 2
 DRAFT_LOGITS = 0
 DRAFT_PROBS = 1
 
@@ -50,6 +57,13 @@ def softmax_at(x, tau):
     y = np.asarray(x, dtype=np.float64) / tau
     e = np.exp(y - y.max())
     return e / e.sum()
+
+
+def draft_q(draft, drow, V, tau, draft_kind):
+    """q of draft row drow: softmax(row / tau) for draft logits, the row itself for draft
+    probabilities."""
+    row = draft[drow, :V]
+    return softmax_at(row, tau) if draft_kind == DRAFT_LOGITS else np.asarray(row, np.float64)
 
 
 def inverse_cdf(w, u):
@@ -99,7 +113,11 @@ def verify(target, draft, draft_kind, draft_row, tokens, parent, node_offset, un
         kids_of = [[c for c in range(T) if par[c] == i] for i in range(T)]
         if any(not (0 <= tokens[o + c] < V) for c in range(1, T)):
             status[r] |= BAD_TOKEN
-        if tau > 0 and any(kids_of[i] and not (0 <= draft_row[o + i] < R) for i in range(T)):
+        if sibling_rule == SIBLING_MULTI_DRAFT:
+            # every drafted node names the row it was drawn from
+            if tau > 0 and any(not (0 <= draft_row[o + c] < R) for c in range(1, T)):
+                status[r] |= BAD_DRAFT_ROW
+        elif tau > 0 and any(kids_of[i] and not (0 <= draft_row[o + i] < R) for i in range(T)):
             status[r] |= BAD_DRAFT_ROW
         if int(tb["depth"][o:o + T].max()) + 1 > max_path:
             status[r] |= BAD_DEPTH
@@ -129,8 +147,37 @@ def verify(target, draft, draft_kind, draft_row, tokens, parent, node_offset, un
                 events.append(("sample", node, u_samp, gap))
                 kind = "bonus"
                 break
-            row = draft[draft_row[o + node], :V]
-            q = softmax_at(row, tau) if draft_kind == DRAFT_LOGITS else np.asarray(row, np.float64)
+            def q_of(drow):
+                return draft_q(draft, drow, V, tau, draft_kind)
+
+            if sibling_rule == SIBLING_MULTI_DRAFT:
+                target_now, accepted, w_final = p, None, None
+                for c in kids:
+                    tok = int(tokens[o + c])
+                    qc = q_of(draft_row[o + c])
+                    num, den = target_now[tok], qc[tok]
+                    a = num / den if den > 0 else (np.inf if num > 0 else 0.0)
+                    u = float(uniforms[o + c, 0])
+                    events.append(("test", node, c, a, u))
+                    if u < a:
+                        accepted = c
+                        break
+                    rejections += 1
+                    resid = np.maximum(0.0, target_now - qc)
+                    mass = resid.sum()
+                    if mass <= 0.0:
+                        w_final = p
+                        break
+                    target_now = resid / mass
+                if accepted is not None:
+                    path.append(accepted)
+                    node = accepted
+                    continue
+                final, gap = inverse_cdf(target_now if w_final is None else w_final, u_samp)
+                events.append(("sample", node, u_samp, gap))
+                kind = "correction"
+                break
+            q = q_of(draft_row[o + node])
             C, Nk = 0.0, 1.0
             accepted, w_final = None, None
             for c in kids:

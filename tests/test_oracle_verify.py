@@ -9,6 +9,9 @@
   outputs are observed), over the uniforms; the first emitted token must follow p_root and the
   next one p(. | first) to 1e-9.
 * The same losslessness by chi-square on vocab 16 with several iid siblings.
+* Multi-draft siblings (each child drawn from its own small model's q): the same exact
+  losslessness, and agreement with the closed-form residual rule when every sibling's q is the
+  same.
 * Greedy: with greedy drafts, tau -> 0+ sampling reproduces the tau = 0 argmax walk.
 """
 from collections import defaultdict
@@ -176,6 +179,91 @@ def test_exact_losslessness(shape, V, tau, kind):
         if cond.sum() > 1e-6:
             np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, (x,), tau), atol=1e-8)
     del probe
+
+
+def _multi_case(V, tau, kind, shape, rng):
+    """Like _tree_case, but child c is drawn from draft model k = its rank among its siblings,
+    with model k's own q in every context; draft row c holds the q child c was drawn from."""
+    T = len(shape)
+    tables_t, tables_q = {}, {}
+
+    def rows(ctx):
+        if ctx not in tables_t:
+            tables_t[ctx] = rng.normal(size=V) * 1.5
+        return tables_t[ctx], None
+
+    def qrow(ctx, k):
+        if (ctx, k) not in tables_q:
+            tables_q[(ctx, k)] = rng.normal(size=V) * 1.5
+        return tables_q[(ctx, k)]
+
+    rank = [0] * T
+    for c in range(1, T):
+        rank[c] = sum(1 for j in range(1, c) if shape[j] == shape[c])
+
+    def make(draft_tokens):
+        tokens = [0] + list(draft_tokens)
+        ctx = [()] * T
+        for i in range(1, T):
+            ctx[i] = ctx[shape[i]] + (tokens[i],)
+        tgt = np.stack([rows(ctx[i])[0] for i in range(T)])
+        drl = np.stack([np.zeros(V)] + [qrow(ctx[shape[c]], rank[c]) for c in range(1, T)])
+        if kind == OV.DRAFT_PROBS:
+            drl = np.stack([OV.softmax_at(x, 1.0) for x in drl])
+        return dict(target=tgt, draft=drl, kind=kind, draft_row=np.arange(T), tokens=tokens,
+                    parent=shape, tau=tau, V=V, ctx=ctx)
+
+    return make, rows
+
+
+@pytest.mark.parametrize("shape,V,tau,kind", [
+    ([-1, 0, 0, 0], 3, 1.0, OV.DRAFT_LOGITS),      # three siblings from three draft models
+    ([-1, 0, 0, 1], 3, 0.7, OV.DRAFT_PROBS),       # two models at the root, then one deeper
+])
+def test_exact_losslessness_multi_draft(shape, V, tau, kind):
+    rng = np.random.default_rng(12)
+    make, rows = _multi_case(V, tau, kind, shape, rng)
+    T = len(shape)
+    total = defaultdict(float)
+    for draft in product(range(V), repeat=T - 1):
+        case = make(draft)
+        w = 1.0
+        for c in range(1, T):   # node c was drawn from its own row's q
+            w *= _q_of(case, c)[draft[c - 1]]
+        for seq, pr in _exact_law(case, OV.SIBLING_MULTI_DRAFT).items():
+            total[seq] += w * pr
+    assert abs(sum(total.values()) - 1.0) < 1e-9
+    first = np.zeros(V)
+    for seq, pr in total.items():
+        first[seq[0]] += pr
+    np.testing.assert_allclose(first, _p_of(rows, (), tau), atol=1e-9)
+    for x in range(V):
+        cond = np.zeros(V)
+        for seq, pr in total.items():
+            if seq[0] == x and len(seq) >= 2:
+                cond[seq[1]] += pr
+        if cond.sum() > 1e-6:
+            np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, (x,), tau), atol=1e-8)
+
+
+def test_multi_draft_with_one_q_equals_the_closed_form():
+    """When every sibling was drawn from the same q, the sequential residual is the closed-form
+    k-fold residual: both rules take the same decisions on the same uniforms."""
+    rng = np.random.default_rng(13)
+    V, shape = 40, [-1, 0, 0, 0, 0, 1, 1, 2]
+    T = len(shape)
+    for trial in range(60):
+        tgt = rng.normal(size=(T, V)) * 2.0
+        q_parent = rng.normal(size=(T, V)) * 2.0
+        tokens = [0] + [int(x) for x in rng.integers(0, V, T - 1)]
+        uni = rng.random((T, 2))
+        # per-parent rows for the residual rule, the same rows named per child for multi-draft
+        per_child = np.array([0] + [shape[c] for c in range(1, T)])
+        a = OV.verify(tgt, q_parent, OV.DRAFT_LOGITS, np.arange(T), tokens, shape, [0, T], uni,
+                      1.0, V, T, sibling_rule=OV.SIBLING_RESIDUAL, T_max=T)
+        b = OV.verify(tgt, q_parent, OV.DRAFT_LOGITS, per_child, tokens, shape, [0, T], uni,
+                      1.0, V, T, sibling_rule=OV.SIBLING_MULTI_DRAFT, T_max=T)
+        assert a["out_tokens"] == b["out_tokens"] and a["rejections"].tolist() == b["rejections"].tolist()
 
 
 def test_independent_sibling_rule_is_biased():
