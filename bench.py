@@ -15,7 +15,7 @@ that the next round's upload overlaps the current round).  `roofline` is for the
 call (the dominant kernel), with algorithmic bytes = the KV of every request read once + Q + O +
 LSE.  `next` measures the step before attention (rotary embedding at the tree's position ids
 plus the tree K/V slot write) alone and inside a step that includes it, and the lookahead-
-decoding forward (a second mask workload on the same kernels).
+decoding forward (a second mask workload on the same kernels) and multi-draft verification.
 `--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
 """
 import argparse
@@ -335,6 +335,12 @@ def main():
     ev_look_attn, ev_look_step = ev_pairs(), ev_pairs()
     for _ in range(3):
         step_l.run()
+    # multi-draft verification (5 draft models' chains, every sibling with its own q)
+    wm = W.multidraft_config(scale="full", device=dev, seeds=rank_seeds(rank))
+    step_m = VerifyStep(wm, sibling_rule=binding.SPEC_SIBLING_MULTI_DRAFT)
+    ev_multi_ver, ev_multi_step = ev_pairs(), ev_pairs()
+    for _ in range(3):
+        step_m.run()
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
@@ -397,6 +403,19 @@ def main():
         r0.record(stream)
         step_l.run()
         r1.record(stream)
+    for i in range(args.steps):   # multi-draft: the verify call alone, then a whole step
+        l2_flush(i)
+        step_m.tree_build()
+        step_m.attention()
+        r0, r1 = ev_multi_ver[i]
+        r0.record(stream)
+        step_m.verify()
+        r1.record(stream)
+        l2_flush(i)
+        r0, r1 = ev_multi_step[i]
+        r0.record(stream)
+        step_m.run()
+        r1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -409,6 +428,7 @@ def main():
     t_rope, t_fused, t_tree, t_step_r = (mean_s(ev_rope), mean_s(ev_fused), mean_s(ev_tree),
                                          mean_s(ev_step_r))
     t_look_attn, t_look_step = mean_s(ev_look_attn), mean_s(ev_look_step)
+    t_multi_ver, t_multi_step = mean_s(ev_multi_ver), mean_s(ev_multi_step)
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / len(attn_ms) / 1e3
     t_total = max_over_ranks(t_total, world, dev)
@@ -489,6 +509,15 @@ def main():
         "frac": round(lbytes / t_look_attn / 1e9 / peak, 4),
         "ms_per_step": round(1e3 * t_look_step, 4),
         "value": round(look_tokens / t_look_step, 1)}
+    multi_tokens = int(sum(wm.tree_sizes()))
+    next_rows["multidraft"] = {
+        "workload": wm.name, "tree_tokens_per_step": multi_tokens,
+        "kernel": "spec_verify, multi-draft sibling rule (rows + walk kernels)",
+        "bound": "latency", "us_verify_call": round(t_multi_ver * 1e6, 2),
+        "rejections_per_request": round(float(step_m.rejections.float().mean()), 3),
+        "accepted_tokens_per_request": round(float(step_m.out_len.float().mean()), 3),
+        "ms_per_step": round(1e3 * t_multi_step, 4),
+        "value": round(multi_tokens / t_multi_step, 1)}
     cb = None
     if not args.no_cpu_baseline:
         w_cpu = W.make_config(args.workload, scale="full", device="cpu")

@@ -60,7 +60,9 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 typedef enum { SPEC_DRAFT_LOGITS = 0, SPEC_DRAFT_PROBS = 1 } spec_draft_kind_t;
 typedef enum {
   SPEC_SIBLING_RESIDUAL = 0,   /* default: child k is tested against the k-fold residual */
-  SPEC_SIBLING_INDEPENDENT = 1 /* every sibling tested against p; resample from max(0, p - q) */
+  SPEC_SIBLING_INDEPENDENT = 1, /* every sibling tested against p; resample from max(0, p - q) */
+  SPEC_SIBLING_MULTI_DRAFT = 2  /* siblings from different draft models, each with its own q:
+                                   draft_row[c] names the row CHILD c was drawn from */
 } spec_sibling_rule_t;
 
 /* Per-request data-error bits OR-ed into req_status[r]. */
@@ -214,6 +216,15 @@ spec_status_t spec_tree_attention(const spec_attn_params* p, void* workspace, si
  *     C_0 = 0, N_k = sum R_k, C_{k+1} = C_k + N_k; accept iff u_acc < R_k(tok)/(N_k q_i(tok))
  *     (k = 0: p/q, the pages' rule);
  *   SIBLING_INDEPENDENT: accept iff u_acc < p_i(tok)/q_i(tok) for every sibling;
+ *   SIBLING_MULTI_DRAFT ([SURV 5.1] a group of small models predicting together; [TREE]
+ *     merge-based trees from k small models): child c carries its own q_c = softmax(
+ *     draft[draft_row[c]] / tau) -- draft_row is indexed by the CHILD, and every non-root node
+ *     needs one (tau > 0).  The running target starts as R_0 = p_i, N_0 = 1; child j is
+ *     accepted iff u_acc < R_{j-1}(tok)/(N_{j-1} q_c(tok)), and a rejection gives
+ *     R_j = max(0, R_{j-1} - N_{j-1} q_c), N_j = sum R_j (the pages' norm(max(0, r - q))
+ *     applied sibling after sibling); all rejected: the final token is drawn from R_k.  Needs
+ *     two fp32 rows of ceil(V/64)*64 floats per request in the workspace (included in
+ *     spec_verify_workspace_size); spec_verify_noalloc refuses it (SPEC_ERR_UNSUPPORTED);
  *   tau == 0: accept iff tok == argmax p_i (lowest id on ties).
  * On acceptance descend to c.  The walk stops at a leaf (the final token is a bonus draw from
  * p_leaf with u_samp = uniforms[leaf][1]) or when every child is rejected (the final token is

@@ -23,6 +23,10 @@
 //      leaf max / argmax) is a block-wide pass: 16 warps own contiguous vocab ranges, per-warp
 //      double-float sums are scanned in token order, and the warp holding the crossing rescans
 //      its unit sums (kept in shared memory) to find the unit, then the unit's 8 elements.
+// Under the multi-draft sibling rule (siblings proposed by different draft models, each with its
+// own q) the running residual has no closed form: it is materialised per request in a
+// double-buffered fp32 scratch row, one vocab pass per rejected sibling (the last one is folded
+// into the final draw), and that case runs its own instantiation of the walk kernel.
 // Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
 #include <math.h>
 
@@ -47,7 +51,7 @@ struct VerifyDev {
   int64_t tld, dld;
   int32_t B, N, R, V, T_max, max_path;
   float tau, k2, inv_tau;  // k2 = log2(e) / tau
-  int32_t probs, residual_rule;
+  int32_t probs, residual_rule, multi;   // multi: the multi-draft sibling rule
   const int32_t* draft_row;
   const int32_t* tokens;
   const int32_t* parent;
@@ -63,6 +67,8 @@ struct VerifyDev {
   int32_t* rejections;
   RowStat* tstat;
   RowStat* dstat;
+  float* rbuf;          // multi-draft: per request, two residual rows of rld floats
+  int64_t rld;
   int32_t after_rows;   // the walk follows a rows kernel of the same call
 };
 
@@ -323,18 +329,20 @@ struct WalkSmem {
   int32_t path[SPEC_MAX_TREE];
   // per local node, gathered once in parallel before the walk
   int32_t tok[SPEC_MAX_TREE];
-  int32_t drow[SPEC_MAX_TREE];     // draft row of the node's children (internal nodes)
+  int32_t drow[SPEC_MAX_TREE];     // draft row of the node's children (internal nodes); under
+                                   // the multi-draft rule the row the node itself came from
   float xt[SPEC_MAX_TREE];         // target logit of the node's token in its parent's row
   float xd[SPEC_MAX_TREE];         // draft logit / probability of the node's token (parent's q)
   float uacc[SPEC_MAX_TREE], usamp[SPEC_MAX_TREE];
   float st_m[SPEC_MAX_TREE], sd_m[SPEC_MAX_TREE];     // row max of the node's target / draft row
-  float st_iz[SPEC_MAX_TREE], sd_iz[SPEC_MAX_TREE];   // float(1 / Z) of those rows
+  float st_iz[SPEC_MAX_TREE], sd_iz[SPEC_MAX_TREE];   // float(1 / Z) of those rows (draft
+                                                      // stats per child under multi-draft)
   double st_Z[SPEC_MAX_TREE], sd_Z[SPEC_MAX_TREE];
   int32_t st_arg[SPEC_MAX_TREE];
   uint8_t dec0[SPEC_MAX_TREE];     // outcome of the node's plain ratio test u < p / q
   PassSmem ps;
   double C, Nk;                    // sibling residual state (thread 0 only)
-  float Cf;
+  float Cf, Nf;
   int decision;
   int bad;                         // SPEC_REQ_* bits found by the validation
 };
@@ -416,6 +424,15 @@ struct WeightFn {
       w[k] = fmaxf(0.f, p - C * q);
     }
   }
+  // the functor interface of vocab_pass
+  __device__ __forceinline__ bool loads_t() const { return true; }
+  __device__ __forceinline__ bool loads_d() const { return residual; }
+  __device__ __forceinline__ bool stores() const { return false; }
+  __device__ __forceinline__ void apply(int, const float (&xt)[8], const float (&xd)[8],
+                                        float (&w)[8]) const {
+    (*this)(xt, xd, w);
+  }
+  __device__ __forceinline__ void store(int, const float (&)[8]) const {}
   template <typename TT, typename TD>
   __device__ __forceinline__ void unit(const TT* trow, const TD* drow, int u, int V, int full,
                                        float (&w)[8]) const {
@@ -423,6 +440,54 @@ struct WeightFn {
     load8(trow, u, V, full, -INFINITY, xt);
     if (residual) load8(drow, u, V, full, probs ? 0.f : -INFINITY, xd);
     (*this)(xt, xd, w);
+  }
+};
+
+// Weights of the multi-draft residual: w = max(0, S(x) - Nprev q_c(x)), where S is the running
+// residual R_{j-1} from the scratch row `src` (or p itself, src == nullptr, before the first
+// rejection) and q_c the rejected sibling's own draft distribution.  An update pass stores w to
+// `dst` (R_j); the final draw passes dst == nullptr.
+struct MultiFn {
+  bool probs;
+  float mt, md, k2, invZt, invZd, Nprev;
+  const float* src;
+  float* dst;
+  int V;
+  __device__ __forceinline__ bool loads_t() const { return src == nullptr; }
+  __device__ __forceinline__ bool loads_d() const { return true; }
+  __device__ __forceinline__ bool stores() const { return dst != nullptr; }
+  __device__ __forceinline__ void apply(int u, const float (&xt)[8], const float (&xd)[8],
+                                        float (&w)[8]) const {
+    float sv[8];
+    if (src) {
+      const float4 a = *reinterpret_cast<const float4*>(src + size_t(u) * 8);
+      const float4 b = *reinterpret_cast<const float4*>(src + size_t(u) * 8 + 4);
+      sv[0] = a.x; sv[1] = a.y; sv[2] = a.z; sv[3] = a.w;
+      sv[4] = b.x; sv[5] = b.y; sv[6] = b.z; sv[7] = b.w;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (u * 8 + k >= V) sv[k] = 0.f;   // the row's padding was never written
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sv[k] = ex2((xt[k] - mt) * k2) * invZt;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float q = probs ? xd[k] : ex2((xd[k] - md) * k2) * invZd;
+      w[k] = fmaxf(0.f, sv[k] - Nprev * q);
+    }
+  }
+  __device__ __forceinline__ void store(int u, const float (&w)[8]) const {
+    *reinterpret_cast<float4*>(dst + size_t(u) * 8) = make_float4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<float4*>(dst + size_t(u) * 8 + 4) = make_float4(w[4], w[5], w[6], w[7]);
+  }
+  template <typename TT, typename TD>
+  __device__ __forceinline__ void unit(const TT* trow, const TD* drow, int u, int Vv, int full,
+                                       float (&w)[8]) const {
+    float xt[8], xd[8];
+    if (!src) load8(trow, u, Vv, full, -INFINITY, xt);
+    load8(drow, u, Vv, full, probs ? 0.f : -INFINITY, xd);
+    apply(u, xt, xd, w);
   }
 };
 
@@ -443,13 +508,13 @@ __device__ __forceinline__ bool df_above(dfloat x, float th_hi, float th_lo) {
 // threads' double-float run sums gives every thread its prefix, the first thread whose inclusive
 // prefix passes theta walks its units, then the crossing unit's 8 elements.  No fp64: theta is a
 // double-float product.  Without `usum` (very large vocabularies) phase 2 recomputes unit sums.
-template <typename TT, typename TD>
-__device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const WeightFn& fn,
+template <typename TT, typename TD, typename Fn>
+__device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const Fn& fn,
                                  bool search, float u, float* usum, PassSmem& sh) {
   constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int full = V / 8, nunits = (V + 7) / 8;
-  if (usum) {
+  if (usum || fn.stores()) {
     for (int base = 0; base < nunits; base += kWalkThreads * kUnits) {
       RawUnit<TT> rt[kUnits];
       RawUnit<TD> rd[kUnits];
@@ -457,8 +522,8 @@ __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const We
       for (int j = 0; j < kUnits; ++j) {
         const int unit = base + j * kWalkThreads + tid;
         if (unit < full) {
-          rt[j].load(trow, unit);
-          if (fn.residual) rd[j].load(drow, unit);
+          if (fn.loads_t()) rt[j].load(trow, unit);
+          if (fn.loads_d()) rd[j].load(drow, unit);
         }
       }
 #pragma unroll
@@ -466,10 +531,11 @@ __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const We
         const int unit = base + j * kWalkThreads + tid;
         if (unit < nunits) {
           float xt[8], xd[8], w[8];
-          rt[j].get(trow, unit, V, full, -INFINITY, xt);
-          if (fn.residual) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
-          fn(xt, xd, w);
-          usum[unit] = sum8(w);
+          if (fn.loads_t()) rt[j].get(trow, unit, V, full, -INFINITY, xt);
+          if (fn.loads_d()) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
+          fn.apply(unit, xt, xd, w);
+          if (fn.stores()) fn.store(unit, w);
+          if (usum) usum[unit] = sum8(w);
         }
       }
     }
@@ -580,7 +646,17 @@ __device__ bool residual_ratio_test(const VerifyDev& a, const WalkSmem& sh, int 
   return double(sh.uacc[c]) * (sh.Nk * q) < num;
 }
 
-template <typename TT, typename TD>
+// Thread 0: the ratio test of a later sibling c under the multi-draft rule,
+// u < R_{j-1}(tok) / (N_{j-1} q_c(tok)) written as u * N_{j-1} * q_c(tok) < R_{j-1}(tok), with
+// R_{j-1} the scratch row the previous update pass stored.
+__device__ bool multi_ratio_test(const VerifyDev& a, const WalkSmem& sh, int c, const float* src) {
+  const double q = a.probs ? double(sh.xd[c])
+                           : double(expf((sh.xd[c] - sh.sd_m[c]) * a.inv_tau)) / sh.sd_Z[c];
+  const double num = double(src[sh.tok[c]]);
+  return double(sh.uacc[c]) * (sh.Nk * q) < num;
+}
+
+template <typename TT, typename TD, bool kMulti>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
   __shared__ WalkSmem sh;
   extern __shared__ float usum_dyn[];
@@ -610,7 +686,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
         if (tok < 0 || tok >= a.V) bad |= SPEC_REQ_BAD_TOKEN;
       }
       if (a.depth[n] + 1 > a.max_path) bad |= SPEC_REQ_BAD_DEPTH;
-      if (a.tau > 0.f && a.is_internal[n]) {
+      // the draft rows read: the children's row of every internal node, or under the
+      // multi-draft rule every drafted node's own row
+      if (a.tau > 0.f && (kMulti ? i > 0 : a.is_internal[n] != 0)) {
         const int dr = a.draft_row[n];
         if (dr < 0 || dr >= a.R) bad |= SPEC_REQ_BAD_DRAFT_ROW;
       }
@@ -647,10 +725,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     sh.next_sib[i] = -1;
     sh.uacc[i] = a.uniforms[2 * size_t(o + i)];
     sh.usamp[i] = a.uniforms[2 * size_t(o + i) + 1];
-    if (!greedy && a.is_internal[o + i]) sh.drow[i] = a.draft_row[o + i];
+    if (!greedy && (kMulti ? i > 0 : a.is_internal[o + i] != 0)) sh.drow[i] = a.draft_row[o + i];
     if (i > 0 && !greedy) {
       sh.xt[i] = elem<TT>::load1(target + size_t(o + p) * a.tld + t);
-      sh.xd[i] = elem<TD>::load1(draft + size_t(a.draft_row[o + p]) * a.dld + t);
+      const int dr = kMulti ? a.draft_row[o + i] : a.draft_row[o + p];
+      sh.xd[i] = elem<TD>::load1(draft + size_t(dr) * a.dld + t);
     }
   }
   __syncthreads();
@@ -676,6 +755,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       sh.st_Z[i] = ts.Z;
       sh.st_iz[i] = ts.inv_Z;
       sh.st_arg[i] = ts.arg;
+    }
+    // draft statistics: of the node's children's row, or (multi-draft) of its own row
+    if (kMulti ? i > 0 : a.is_internal[o + i] != 0) {
       if (!greedy) {
         if (!a.probs) {
           const RowStat ds = a.dstat[sh.drow[i]];
@@ -695,13 +777,14 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     for (int i = tid; i < T; i += kWalkThreads) {
       if (i > 0) {
         const int p = sh.par[i];
+        const int qi = kMulti ? i : p;   // whose draft statistics hold q for node i
         // plain ratio test u < p / q, as u * Zt < exp(((xt - mt) - (xd - md)) / tau) * Zd for
         // draft logits and u * q * Zt < exp((xt - mt) / tau) for draft probabilities
         const double u = double(sh.uacc[i]);
         bool acc;
         if (!a.probs) {
-          const float e = expf(((sh.xt[i] - sh.st_m[p]) - (sh.xd[i] - sh.sd_m[p])) * a.inv_tau);
-          acc = u * sh.st_Z[p] < double(e) * sh.sd_Z[p];
+          const float e = expf(((sh.xt[i] - sh.st_m[p]) - (sh.xd[i] - sh.sd_m[qi])) * a.inv_tau);
+          acc = u * sh.st_Z[p] < double(e) * sh.sd_Z[qi];
         } else {
           const float e = expf((sh.xt[i] - sh.st_m[p]) * a.inv_tau);
           acc = u * double(sh.xd[i]) * sh.st_Z[p] < double(e);
@@ -741,6 +824,75 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       fn.mt = block_row_max(trow, a.V, sh.ps);
       fn.k2 = a.k2;
       final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
+      break;
+    }
+    if (kMulti) {
+      // siblings from different draft models: R_0 = p, N_0 = 1; a rejected child c gives
+      // R_j = max(0, R_{j-1} - N_{j-1} q_c) (stored), N_j = sum R_j; the last sibling's residual
+      // is drawn from directly
+      float* const rows2 = a.rbuf + size_t(r) * 2 * a.rld;   // this request's two rows
+      const float* src = nullptr;
+      int flip = 0, accepted = -1, last = -1;
+      bool from_p = false;
+      if (tid == 0) { sh.Nk = 1.0; sh.Nf = 1.f; }
+      __syncthreads();
+      for (int c = fc; c >= 0; c = sh.next_sib[c]) {
+        bool acc;
+        if (c == fc) {
+          acc = sh.dec0[c] != 0;
+        } else {
+          if (tid == 0) sh.decision = multi_ratio_test(a, sh, c, src);
+          __syncthreads();
+          acc = sh.decision != 0;
+          __syncthreads();
+        }
+        if (acc) { accepted = c; break; }
+        ++rejections;
+        last = c;
+        if (sh.next_sib[c] < 0) break;
+        MultiFn upd{};
+        upd.probs = a.probs != 0;
+        upd.mt = sh.st_m[node]; upd.k2 = a.k2; upd.invZt = sh.st_iz[node];
+        upd.md = sh.sd_m[c]; upd.invZd = sh.sd_iz[c];
+        upd.Nprev = sh.Nf;
+        upd.src = src;
+        upd.dst = rows2 + flip * a.rld;
+        upd.V = a.V;
+        const TD* drow_c = draft + size_t(sh.drow[c]) * a.dld;
+        const PassResult pr = vocab_pass(trow, drow_c, a.V, upd, false, 0.f, usum, sh.ps);
+        if (tid == 0) { sh.Nk = sh.ps.total; sh.Nf = float(sh.ps.total); }
+        __syncthreads();
+        if (!pr.pos) { from_p = true; break; }
+        src = rows2 + flip * a.rld;
+        flip ^= 1;
+      }
+      if (accepted >= 0) {
+        if (tid == 0) sh.path[npath] = accepted;
+        ++npath;
+        node = accepted;
+        continue;
+      }
+      if (!from_p) {
+        MultiFn fin{};
+        fin.probs = a.probs != 0;
+        fin.mt = sh.st_m[node]; fin.k2 = a.k2; fin.invZt = sh.st_iz[node];
+        fin.md = sh.sd_m[last]; fin.invZd = sh.sd_iz[last];
+        fin.Nprev = sh.Nf;
+        fin.src = src;
+        fin.dst = nullptr;
+        fin.V = a.V;
+        const TD* drow_c = draft + size_t(sh.drow[last]) * a.dld;
+        const PassResult pr = vocab_pass(trow, drow_c, a.V, fin, true, u_samp, usum, sh.ps);
+        final_tok = pr.tok;
+        if (!pr.pos) from_p = true;
+      }
+      if (from_p) {
+        WeightFn fn{};
+        fn.residual = false;
+        fn.mt = sh.st_m[node];
+        fn.k2 = a.k2;
+        final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
+      }
       break;
     }
     const TD* drow = draft + size_t(sh.drow[node]) * a.dld;
@@ -818,14 +970,19 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
 }
 
 struct VerifyWs {
-  size_t tstat, dstat, total;
+  size_t tstat, dstat, rbuf, total;
+  int64_t rld;   // floats per residual row (multi-draft), a multiple of 64
 };
 
-static VerifyWs verify_ws_layout(int N, int R) {
+// multi_B > 0: the multi-draft rule's two residual rows per request (multi_B requests, vocab V)
+static VerifyWs verify_ws_layout(int N, int R, int multi_B = 0, int V = 0) {
   VerifyWs w;
   size_t off = 0;
   w.tstat = off; off = align_up(off + sizeof(RowStat) * size_t(N > 0 ? N : 1), 256);
   w.dstat = off; off = align_up(off + sizeof(RowStat) * size_t(R > 0 ? R : 1), 256);
+  w.rld = int64_t(align_up(size_t(V > 0 ? V : 1), 64));
+  w.rbuf = off;
+  if (multi_B > 0) off = align_up(off + sizeof(float) * 2 * size_t(multi_B) * size_t(w.rld), 256);
   w.total = off;
   return w;
 }
@@ -851,7 +1008,7 @@ static spec_status_t allow_unit_sums(K kernel, bool* raised) {
   return SPEC_OK;
 }
 
-template <typename TT, typename TD>
+template <typename TT, typename TD, bool kMulti>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   const int nunits = (d.V + 7) / 8;
   const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
@@ -867,10 +1024,11 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   }
   static bool raised_walk[64] = {false};
   if (dyn > 0) {
-    const spec_status_t st = allow_unit_sums(verify_walk_kernel<TT, TD>, raised_walk);
+    const spec_status_t st = allow_unit_sums(verify_walk_kernel<TT, TD, kMulti>, raised_walk);
     if (st != SPEC_OK) return st;
   }
-  return launch_result(launch_pdl(verify_walk_kernel<TT, TD>, dim3(d.B), dim3(kWalkThreads), dyn, s, dw));
+  return launch_result(launch_pdl(verify_walk_kernel<TT, TD, kMulti>, dim3(d.B),
+                                  dim3(kWalkThreads), dyn, s, dw));
 }
 
 }  // namespace spec
@@ -879,7 +1037,8 @@ extern "C" {
 
 size_t spec_verify_workspace_size(const spec_verify_params* p) {
   if (!p) return 0;
-  return spec::verify_ws_layout(p->N, p->R).total;
+  const bool multi = p->sibling_rule == SPEC_SIBLING_MULTI_DRAFT && p->tau > 0.f;
+  return spec::verify_ws_layout(p->N, p->R, multi ? p->B : 0, p->V).total;
 }
 
 spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
@@ -893,7 +1052,8 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   if (p->logits_dtype != SPEC_F32 && p->logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (p->draft_kind != SPEC_DRAFT_LOGITS && p->draft_kind != SPEC_DRAFT_PROBS)
     return SPEC_ERR_INVALID_ARG;
-  if (p->sibling_rule != SPEC_SIBLING_RESIDUAL && p->sibling_rule != SPEC_SIBLING_INDEPENDENT)
+  if (p->sibling_rule != SPEC_SIBLING_RESIDUAL && p->sibling_rule != SPEC_SIBLING_INDEPENDENT &&
+      p->sibling_rule != SPEC_SIBLING_MULTI_DRAFT)
     return SPEC_ERR_INVALID_ARG;
   if (!p->node_offset || !p->req_status || !p->out_tokens || !p->out_len || !p->path ||
       !p->n_acc)
@@ -909,7 +1069,8 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
     if (!p->draft || !aligned16(p->draft)) return SPEC_ERR_INVALID_ARG;
     if (p->draft_ld < p->V || (size_t(p->draft_ld) * des) % 16 != 0) return SPEC_ERR_INVALID_ARG;
   }
-  const VerifyWs lay = verify_ws_layout(p->N, p->R);
+  const bool multi = p->sibling_rule == SPEC_SIBLING_MULTI_DRAFT && p->tau > 0.f;
+  const VerifyWs lay = verify_ws_layout(p->N, p->R, multi ? p->B : 0, p->V);
   if (!workspace || ws_bytes < lay.total || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return SPEC_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
@@ -925,18 +1086,28 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   d.inv_tau = p->tau > 0.f ? 1.0f / p->tau : 0.f;
   d.probs = p->draft_kind == SPEC_DRAFT_PROBS;
   d.residual_rule = p->sibling_rule == SPEC_SIBLING_RESIDUAL;
+  d.multi = multi ? 1 : 0;
   d.draft_row = p->draft_row; d.tokens = p->tokens; d.parent = p->parent;
   d.node_offset = p->node_offset; d.depth = p->depth; d.is_internal = p->is_internal;
   d.uniforms = p->uniforms; d.req_status = p->req_status; d.out_tokens = p->out_tokens;
   d.out_len = p->out_len; d.path = p->path; d.n_acc = p->n_acc; d.rejections = p->rejections;
   d.tstat = reinterpret_cast<RowStat*>(ws + lay.tstat);
   d.dstat = reinterpret_cast<RowStat*>(ws + lay.dstat);
+  d.rbuf = multi ? reinterpret_cast<float*>(ws + lay.rbuf) : nullptr;
+  d.rld = lay.rld;
   cudaStream_t s = (cudaStream_t)stream;
-  if (p->logits_dtype == SPEC_BF16) {
-    if (d.probs) return launch_verify<__nv_bfloat16, float>(d, s);
-    return launch_verify<__nv_bfloat16, __nv_bfloat16>(d, s);
+  if (multi) {
+    if (p->logits_dtype == SPEC_BF16) {
+      if (d.probs) return launch_verify<__nv_bfloat16, float, true>(d, s);
+      return launch_verify<__nv_bfloat16, __nv_bfloat16, true>(d, s);
+    }
+    return launch_verify<float, float, true>(d, s);
   }
-  return launch_verify<float, float>(d, s);
+  if (p->logits_dtype == SPEC_BF16) {
+    if (d.probs) return launch_verify<__nv_bfloat16, float, false>(d, s);
+    return launch_verify<__nv_bfloat16, __nv_bfloat16, false>(d, s);
+  }
+  return launch_verify<float, float, false>(d, s);
 }
 
 }  // extern "C"

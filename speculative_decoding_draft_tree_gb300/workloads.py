@@ -503,6 +503,86 @@ CONFIG_NAMES = {
 
 
 # ----------------------------------------------------------------------------------------------
+# Several draft models (multi-draft verification: every sibling carries its own model's q).
+# ----------------------------------------------------------------------------------------------
+def multidraft_parents(k: int, gamma: int) -> List[int]:
+    """k chains of gamma drafts hanging off the root, chain m after chain m - 1 in node order:
+    the root's children come from k different draft models."""
+    parents = [-1]
+    for _ in range(k):
+        prev = 0
+        for _g in range(gamma):
+            parents.append(prev)
+            prev = len(parents) - 1
+    return parents
+
+
+def multidraft_workload(*, B: int, k: int, gamma: int, V: int, dtype: str, H_q: int, H_kv: int,
+                        d: int, prefix, tau: float, target_std: float = 3.0,
+                        noise_stds=None, device="cpu", bs: int = 16, num_layers: int = 1,
+                        draft_kind: int = DRAFT_LOGITS, seeds: Optional[Dict] = None,
+                        name: str = "multidraft", T_max: Optional[int] = None) -> Workload:
+    """k draft models each sample a chain of gamma tokens.  Model m's distribution at a node is
+    the target row there plus N(0, noise_stds[m]^2) (its own noise, so siblings at the root
+    carry different q); the token of each child is drawn from its model's softmax(row / tau)
+    (argmax at tau = 0), and draft row c holds the q child c was drawn from (the multi-draft
+    sibling rule's indexing; the root's entry is -1)."""
+    seeds = dict(SEEDS, **(seeds or {}))
+    noise_stds = list(noise_stds or [0.5 + 0.5 * m for m in range(k)])
+    parents = multidraft_parents(k, gamma)
+    T = len(parents)
+    g = _gen(seeds["logits"], device)
+    tgt = torch.randn((B * T, V), generator=g, device=device) * target_std
+    model_of = [-1] + [m for m in range(k) for _ in range(gamma)]
+    # one draft row per non-root node: its model's row at its parent's context
+    rows = []
+    for r in range(B):
+        for c in range(1, T):
+            rows.append(tgt[r * T + parents[c]]
+                        + torch.randn((V,), generator=g, device=device) * noise_stds[model_of[c]])
+    drf = torch.stack(rows)
+    td = _torch_dtype(dtype)
+    gd = _gen(seeds["drafting"], device)
+    if tau > 0:
+        probs = torch.softmax(drf.to(td).float() / tau, dim=-1)
+        picks = torch.multinomial(probs, 1, generator=gd).squeeze(1)
+    else:
+        picks = drf.to(td).float().argmax(dim=-1)
+    picks = picks.cpu().numpy()
+    roots = torch.randint(0, V, (B,), generator=gd, device=device).cpu().numpy()
+    tokens = np.zeros(B * T, dtype=np.int32)
+    draft_row = np.full(B * T, -1, dtype=np.int32)
+    for r in range(B):
+        tokens[r * T] = roots[r]
+        for c in range(1, T):
+            tokens[r * T + c] = picks[r * (T - 1) + c - 1]
+            draft_row[r * T + c] = r * (T - 1) + c - 1
+    if draft_kind == DRAFT_PROBS:
+        drf = torch.softmax(drf.to(td).float() / (tau if tau > 0 else 1.0), dim=-1)
+    prefix = list(prefix) if hasattr(prefix, "__len__") else [int(prefix)] * B
+    return _finish(name, dtype, B, V, H_q, H_kv, d, bs, tau, [parents] * B, tokens, draft_row,
+                   prefix, tgt, drf, device, num_layers, False, seeds, T_max=T_max,
+                   draft_kind=draft_kind, meta=dict(kind="multidraft", k=k, gamma=gamma))
+
+
+def multidraft_config(*, scale: str = "full", device="cpu", tau: float = 1.0,
+                      draft_kind: int = DRAFT_LOGITS, seeds: Optional[Dict] = None,
+                      num_layers: int = 1) -> Workload:
+    """Full: 5 draft models x 3 tokens (a 16-token tree, the SpecInfer multi-model setting),
+    16 requests, vocab 32000, LLaMA-7B attention (32 x d128 MHA), 2048 cached tokens.  Small:
+    3 models x 2 tokens, 3 requests, odd sizes."""
+    if scale == "full":
+        return multidraft_workload(B=16, k=5, gamma=3, V=32000, dtype="bf16", H_q=32, H_kv=32,
+                                   d=128, prefix=2048, tau=tau, device=device, seeds=seeds,
+                                   draft_kind=draft_kind, num_layers=num_layers,
+                                   name="multidraft_k5_g3_b16_v32000")
+    return multidraft_workload(B=3, k=3, gamma=2, V=2999, dtype="bf16", H_q=4, H_kv=2, d=128,
+                               prefix=[40, 301, 7], tau=tau, device=device, seeds=seeds,
+                               draft_kind=draft_kind, num_layers=num_layers,
+                               name="multidraft_k3_g2_b3_small")
+
+
+# ----------------------------------------------------------------------------------------------
 # Lookahead decoding: one forward over a 2-D Jacobi window and G candidate n-grams.
 # ----------------------------------------------------------------------------------------------
 def lookahead_parents(W: int, N: int, G: int) -> List[int]:
