@@ -16,6 +16,8 @@ Modules (each function cites the passage it follows):
   rope       -- rotary position embedding at the tree's position ids and the tree K/V written
                 into its paged cache slots (the step before attention)
   lookahead  -- the lookahead-decoding mask (lookahead and verify branches in one forward)
+  draft_tree -- building the draft tree: EAGLE-2 expansion of the most probable leaves, top-K
+                of each expanded row, ECHO's batch-wide budget, packing for verification
 
 Pins (tests/test_oracle_*.py, run with -m "not gpu") tie each function to something other than
 itself: the page's 6-node mask table, the 123 / 45 node counts, E[L] = (1 - a^(g+1)) / (1 - a),
@@ -23,9 +25,11 @@ exact losslessness by black-box bisection over the uniforms, chi-square against 
 scaled-dot-product attention for the T = 1 and chain special cases, the sequential-decoding
 invariant for compaction, and RoFormer's complex form, the frequencies as numbers, brute force
 over cache rows and chain = causal decoding for the RoPE step; a hand-derived worked example,
-the page's token counts and its two mask rules for the lookahead mask.  No oracle function is "parity unpinned".
+the page's token counts and its two mask rules for the lookahead mask; scipy's log_softmax, a
+brute-force top-K, path products recomputed by multiplying probabilities, the page's node counts
+and ECHO's optimality / ancestor closure for the draft-tree construction.  No oracle function is "parity unpinned".
 """
-from . import tree, attention, verify, compact, rope, lookahead  # noqa: F401
+from . import tree, attention, verify, compact, rope, lookahead, draft_tree  # noqa: F401
 
 # request status bits (the oracle's own numbering of the data errors it detects)
 BAD_PARENT = 1
