@@ -15,7 +15,8 @@ that the next round's upload overlaps the current round).  `roofline` is for the
 call (the dominant kernel), with algorithmic bytes = the KV of every request read once + Q + O +
 LSE.  `next` measures the step before attention (rotary embedding at the tree's position ids
 plus the tree K/V slot write) alone and inside a step that includes it, and the lookahead-
-decoding forward (a second mask workload on the same kernels) and multi-draft verification.
+decoding forward (a second mask workload on the same kernels), multi-draft verification and
+the device-side construction of the draft tree (EAGLE-2 expansion + ECHO budget).
 `--impl reference` times the CPU oracle on a bounded sample of the same workload instead.
 """
 import argparse
@@ -341,6 +342,26 @@ def main():
     ev_multi_ver, ev_multi_step = ev_pairs(), ev_pairs()
     for _ in range(3):
         step_m.run()
+    # building the draft tree on the device (EAGLE-2 top-5 expansion to depth 8, ECHO budget
+    # 2048) on the EAGLE-2 workload's shape; the draft model's rows of all levels resident
+    from speculative_decoding_draft_tree_gb300.api import DraftTreeBuilder
+    DT_B, DT_K, DT_D, DT_V, DT_KMAX = 64, 5, 8, 152064, 2048
+    dt_scales = [0.3 + 3.7 * ((17 * r) % 64) / 63.0 for r in range(DT_B)]
+    dt_rows = [W.draft_level_rows(B=DT_B, K=DT_K, V=DT_V, level=lv, device=dev,
+                                  seed=11 + rank, scales=dt_scales) for lv in range(1, DT_D + 1)]
+    dt_roots = torch.arange(DT_B, dtype=torch.int32, device=dev) * 37 % DT_V
+    builder = DraftTreeBuilder(DT_B, DT_K, DT_D, dev)
+
+    def build_tree():
+        builder.init(dt_roots)
+        for lv in range(1, DT_D + 1):
+            builder.expand(lv)
+            builder.append(lv, dt_rows[lv - 1], DT_V)
+        builder.echo(DT_KMAX)
+
+    ev_dt, ev_dt_append, ev_dt_echo = ev_pairs(), ev_pairs(), ev_pairs()
+    for _ in range(3):
+        build_tree()
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
@@ -403,6 +424,30 @@ def main():
         r0.record(stream)
         step_l.run()
         r1.record(stream)
+    for i in range(args.steps):   # draft tree: the whole construction; one full level's top-K
+        l2_flush(i)
+        r0, r1 = ev_dt[i]
+        r0.record(stream)
+        build_tree()
+        r1.record(stream)
+        builder.init(dt_roots)
+        for lv in (1, 2):
+            builder.expand(lv)
+            if lv == 1:
+                builder.append(lv, dt_rows[0], DT_V)
+        l2_flush(i)
+        r0, r1 = ev_dt_append[i]
+        r0.record(stream)
+        builder.append(2, dt_rows[1], DT_V)
+        r1.record(stream)
+        for lv in range(3, DT_D + 1):
+            builder.expand(lv)
+            builder.append(lv, dt_rows[lv - 1], DT_V)
+        l2_flush(i)
+        r0, r1 = ev_dt_echo[i]
+        r0.record(stream)
+        builder.echo(DT_KMAX)
+        r1.record(stream)
     for i in range(args.steps):   # multi-draft: the verify call alone, then a whole step
         l2_flush(i)
         step_m.tree_build()
@@ -429,6 +474,7 @@ def main():
                                          mean_s(ev_step_r))
     t_look_attn, t_look_step = mean_s(ev_look_attn), mean_s(ev_look_step)
     t_multi_ver, t_multi_step = mean_s(ev_multi_ver), mean_s(ev_multi_step)
+    t_dt, t_dt_append, t_dt_echo = mean_s(ev_dt), mean_s(ev_dt_append), mean_s(ev_dt_echo)
     t_total = sum(step_ms) / 1e3
     t_attn = sum(attn_ms) / len(attn_ms) / 1e3
     t_total = max_over_ranks(t_total, world, dev)
@@ -509,6 +555,18 @@ def main():
         "frac": round(lbytes / t_look_attn / 1e9 / peak, 4),
         "ms_per_step": round(1e3 * t_look_step, 4),
         "value": round(look_tokens / t_look_step, 1)}
+    # level 2 expands the 5 children of every root: 64 x 5 rows of 152064 bf16 logits
+    dt_bytes = DT_B * DT_K * DT_V * 2
+    next_rows["draft_tree"] = {
+        "workload": f"eagle2 top-{DT_K} expansion, depth {DT_D}, {DT_B} requests, vocab {DT_V},"
+                    f" ECHO K_max {DT_KMAX}",
+        "kernel": "spec_draft_topk_append (one expansion level, 320 rows)", "bound": "hbm",
+        "algorithmic_bytes": dt_bytes, "us_per_launch": round(t_dt_append * 1e6, 2),
+        "achieved": round(dt_bytes / t_dt_append / 1e9, 1), "peak": peak, "unit": "GB/s",
+        "frac": round(dt_bytes / t_dt_append / 1e9 / peak, 4),
+        "us_whole_construction": round(t_dt * 1e6, 2),
+        "us_echo_select_pack": round(t_dt_echo * 1e6, 2),
+        "tree_tokens": int(builder.node_offset[-1])}
     multi_tokens = int(sum(wm.tree_sizes()))
     next_rows["multidraft"] = {
         "workload": wm.name, "tree_tokens_per_step": multi_tokens,

@@ -320,6 +320,70 @@ typedef struct {
 
 spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Building the draft tree on the device  [TREE 草稿树的生成, 动态草稿长度]
+ * EAGLE-2 expands, level by level, only the K most probable leaves of the newest level (a
+ * leaf's score is the sum of the draft log-probabilities along its path, log q =
+ * log_softmax(draft_row / tau)[token]); each expansion adds the K most probable tokens of the
+ * expanded node's draft row.  ECHO then keeps a batch-wide budget of K_max tokens: every root
+ * and the K_max - B best non-root candidates of the batch.  The draft model's forward, which
+ * turns the chosen candidates into draft rows, is the caller's.
+ * Candidate pool (caller-owned device arrays, request r's candidates at [r * cap, r * cap +
+ * count[r])): parent (candidate index, -1 for the root), token, depth, score (fp32), row (the
+ * draft row its expansion produced, -1 if never), count.  cap <= 256.
+ * Ordering everywhere: by score (or log-probability) descending, ties to the lower candidate
+ * index / token id, then (ECHO) the lower request.  Selections compare the fp32 scores exactly.
+ * A drafting round: spec_draft_init; for level = 1 .. depth: spec_draft_expand_select, the
+ * caller's draft forward for the listed candidates, spec_draft_topk_append; then
+ * spec_echo_select_pack, whose outputs feed spec_tree_build / spec_verify (draft_row indexes
+ * the rows the caller produced, numbered row_base + r * K + j by the append calls).
+ * ------------------------------------------------------------------------------------------ */
+typedef struct {
+  int32_t B, cap;
+  int32_t* parent;   /* [B][cap] */
+  int32_t* token;    /* [B][cap] */
+  int32_t* depth;    /* [B][cap] */
+  float* score;      /* [B][cap] */
+  int32_t* row;      /* [B][cap] */
+  int32_t* count;    /* [B] */
+} spec_draft_pool;
+
+/* Pool entry 0 of request r = the root (root_tokens[r]), count = 1. */
+spec_status_t spec_draft_init(const spec_draft_pool* pool, const int32_t* root_tokens,
+                              spec_stream_t stream);
+
+/* The candidates to expand at `level` (1: the root; else the K best of depth level - 1), in
+ * increasing candidate index: expand[r][j], j < K, -1 past the chosen ones.  Grows count[r] by
+ * K per chosen candidate; if the pool cannot hold that many, fewer are chosen and req_status[r]
+ * (may be NULL) gets SPEC_REQ_BAD_SIZE.  1 <= K <= 16. */
+spec_status_t spec_draft_expand_select(const spec_draft_pool* pool, int32_t level, int32_t K,
+                                       int32_t* expand, int32_t* req_status,
+                                       spec_stream_t stream);
+
+/* For every expand[r][j] >= 0: the K most probable tokens of draft row r * K + j of `rows`
+ * ([B * K][ld], dtype F32 / BF16 logits, 16-byte aligned rows, V <= ld), log q =
+ * x / tau - logsumexp(row / tau) (one streaming read of the row), appended as the candidate's
+ * children in that order with score = its score + log q, depth = level; the candidate's row
+ * becomes row_base + r * K + j.  Call after spec_draft_expand_select of the same level.
+ * req_status (may be NULL) gets SPEC_REQ_TIMEOUT if a row's copy into shared memory never
+ * completed (a bounded wait); that expansion's children then carry token -1 and score -inf. */
+spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level, int32_t K,
+                                     const int32_t* expand, spec_dtype_t dtype, const void* rows,
+                                     int64_t ld, int32_t V, float tau, int32_t row_base,
+                                     int32_t* req_status, spec_stream_t stream);
+
+/* ECHO selection and packing: node_offset [B+1]; parent (local, -1 for roots), tokens, depth,
+ * draft_row (the node's row if one of its children was kept, else -1) and source (candidate
+ * index, may be NULL), each with room for min(K_max, B * cap) entries; N = node_offset[B].
+ * Kept candidates stay in candidate order (parents first), so the output is a valid tree in
+ * the layout spec_tree_build reads.  workspace: spec_echo_workspace_size(B, cap) bytes,
+ * 256-byte aligned. */
+size_t spec_echo_workspace_size(int32_t B, int32_t cap);
+spec_status_t spec_echo_select_pack(const spec_draft_pool* pool, int32_t K_max,
+                                    int32_t* node_offset, int32_t* parent, int32_t* tokens,
+                                    int32_t* depth, int32_t* draft_row, int32_t* source,
+                                    void* workspace, size_t ws_bytes, spec_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* spec_status_string(spec_status_t status);
 

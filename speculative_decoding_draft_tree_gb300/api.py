@@ -217,3 +217,69 @@ class VerifyStep:
         if "_pack" in tensors:
             return tensors["_pack"].numel() * tensors["_pack"].element_size()
         return sum(t.numel() * t.element_size() for t in tensors.values())
+
+
+class DraftTreeBuilder:
+    """The device side of building a draft tree for a batch: EAGLE-2 expansion of the K most
+    probable leaves per level, the K most probable tokens of each expanded row, and ECHO's
+    batch-wide budget of K_max tokens, packed for verification.  The draft model's forward
+    (candidates -> draft rows) is the caller's: between expand(level) and append(level, rows)
+    it writes row r * K + j of `rows` for the candidate expand_list[r, j].
+
+    Owns the candidate pool (capacity `cap` per request), the expand list, the ECHO workspace
+    and the packed outputs; every call is asynchronous on the current stream."""
+
+    def __init__(self, batch: int, K: int, depth: int, device, cap: Optional[int] = None):
+        cap = cap if cap is not None else 1 + K + (depth - 1) * K * K
+        if cap > 256:
+            raise ValueError("pool capacity above 256 candidates per request")
+        self.B, self.K, self.depth, self.cap = batch, K, depth, cap
+        nb = batch
+        i32 = dict(dtype=torch.int32, device=device)
+        self.parent = torch.full((nb, cap), -1, **i32)
+        self.token = torch.zeros((nb, cap), **i32)
+        self.depth_ = torch.zeros((nb, cap), **i32)
+        self.score = torch.zeros((nb, cap), dtype=torch.float32, device=device)
+        self.row = torch.full((nb, cap), -1, **i32)
+        self.count = torch.zeros(nb, **i32)
+        self.req_status = torch.zeros(nb, **i32)
+        self.expand_list = torch.full((nb, K), -1, **i32)
+        self.pool = _pool(self)
+        self.echo_ws = _ws(B.spec_echo_workspace_size(nb, cap), device)
+        n = nb * cap
+        self.node_offset = torch.zeros(nb + 1, **i32)
+        self.tree_parent = torch.zeros(n, **i32)
+        self.tree_tokens = torch.zeros(n, **i32)
+        self.tree_depth = torch.zeros(n, **i32)
+        self.tree_draft_row = torch.zeros(n, **i32)
+        self.tree_source = torch.zeros(n, **i32)
+
+    def init(self, root_tokens: torch.Tensor, stream=None):
+        self.req_status.zero_()
+        B.spec_draft_init(self.pool, root_tokens, stream)
+
+    def expand(self, level: int, stream=None):
+        B.spec_draft_expand_select(self.pool, level, self.K, self.expand_list, self.req_status,
+                                    stream)
+
+    def append(self, level: int, rows: torch.Tensor, V: int, tau: float = 1.0, stream=None):
+        """rows: [B * K, ld] draft logits of the listed candidates (level's rows numbered
+        (level - 1) * B * K + r * K + j in the packed draft_row)."""
+        B.spec_draft_topk_append(self.pool, level, self.K, self.expand_list, rows, V, tau,
+                                  (level - 1) * self.B * self.K, self.req_status, stream)
+
+    def echo(self, K_max: int, stream=None):
+        B.spec_echo_select_pack(self.pool, K_max, self.node_offset, self.tree_parent,
+                                 self.tree_tokens, self.tree_depth, self.tree_draft_row,
+                                 self.tree_source, self.echo_ws, stream)
+
+    def packed(self) -> Dict[str, torch.Tensor]:
+        """The packed trees (synchronises to read N)."""
+        N = int(self.node_offset[-1])
+        return dict(node_offset=self.node_offset, parent=self.tree_parent[:N],
+                    tokens=self.tree_tokens[:N], depth=self.tree_depth[:N],
+                    draft_row=self.tree_draft_row[:N], source=self.tree_source[:N])
+
+
+def _pool(b: "DraftTreeBuilder"):
+    return B.draft_pool(b.parent, b.token, b.depth_, b.score, b.row, b.count)

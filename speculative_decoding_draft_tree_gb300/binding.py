@@ -21,7 +21,9 @@ REQ_BITS = dict(BAD_PARENT=1, BAD_SIZE=2, BAD_TOKEN=4, BAD_DRAFT_ROW=8, BAD_DEPT
                 BAD_BLOCK=32, TIMEOUT=64)
 EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_kv_write", "spec_tree_attention", "spec_attention_workspace_size",
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
-           "spec_status_string", "spec_last_cuda_error"]
+           "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
+           "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
+           "spec_echo_select_pack"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -66,6 +68,11 @@ class SpecRopeParams(ctypes.Structure):
                 ("prefix_len", _vp), ("node_offset", _vp), ("pos_id", _vp), ("req_status", _vp)]
 
 
+class SpecDraftPool(ctypes.Structure):
+    _fields_ = [("B", _i32), ("cap", _i32), ("parent", _vp), ("token", _vp), ("depth", _vp),
+                ("score", _vp), ("row", _vp), ("count", _vp)]
+
+
 _LIB = None
 
 
@@ -105,6 +112,20 @@ def load_library(build_if_missing=False):
     lib.spec_verify_workspace_size.argtypes = [ctypes.POINTER(SpecVerifyParams)]
     lib.spec_kv_compact.restype = st
     lib.spec_kv_compact.argtypes = [ctypes.POINTER(SpecCompactParams), _vp]
+    lib.spec_draft_init.restype = st
+    lib.spec_draft_init.argtypes = [ctypes.POINTER(SpecDraftPool), _vp, _vp]
+    lib.spec_draft_expand_select.restype = st
+    lib.spec_draft_expand_select.argtypes = [ctypes.POINTER(SpecDraftPool), _i32, _i32, _vp, _vp,
+                                             _vp]
+    lib.spec_draft_topk_append.restype = st
+    lib.spec_draft_topk_append.argtypes = [ctypes.POINTER(SpecDraftPool), _i32, _i32, _vp,
+                                           ctypes.c_int, _vp, _i64, _i32, ctypes.c_float, _i32,
+                                           _vp, _vp]
+    lib.spec_echo_workspace_size.restype = ctypes.c_size_t
+    lib.spec_echo_workspace_size.argtypes = [_i32, _i32]
+    lib.spec_echo_select_pack.restype = st
+    lib.spec_echo_select_pack.argtypes = [ctypes.POINTER(SpecDraftPool), _i32, _vp, _vp, _vp,
+                                          _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
     lib.spec_last_cuda_error.restype = ctypes.c_int
@@ -340,3 +361,58 @@ def compact_params(k_cache, v_cache, block_table, prefix_len, path, n_acc, req_s
 def spec_kv_compact(params, stream=None):
     code = load_library().spec_kv_compact(ctypes.byref(params), _stream(stream))
     _check(code, "spec_kv_compact")
+
+
+# ----------------------------------------------------------------------------------------------
+def draft_pool(parent, token, depth, score, row, count):
+    """The candidate pool ([B, cap] int32 / fp32 arrays and count [B])."""
+    for t, n in ((parent, "parent"), (token, "token"), (depth, "depth"), (row, "row"),
+                 (count, "count")):
+        _need(t, torch.int32, n)
+    _need(score, torch.float32, "score")
+    p = SpecDraftPool()
+    p.B, p.cap = parent.shape
+    p.parent, p.token, p.depth = parent.data_ptr(), token.data_ptr(), depth.data_ptr()
+    p.score, p.row, p.count = score.data_ptr(), row.data_ptr(), count.data_ptr()
+    return p
+
+
+def spec_draft_init(pool, root_tokens, stream=None):
+    _need(root_tokens, torch.int32, "root_tokens")
+    _check(load_library().spec_draft_init(ctypes.byref(pool), _ptr(root_tokens), _stream(stream)),
+           "spec_draft_init")
+
+
+def spec_draft_expand_select(pool, level, K, expand, req_status=None, stream=None):
+    _need(expand, torch.int32, "expand")
+    code = load_library().spec_draft_expand_select(ctypes.byref(pool), level, K, _ptr(expand),
+                                                   _ptr(req_status), _stream(stream))
+    _check(code, "spec_draft_expand_select")
+
+
+def spec_draft_topk_append(pool, level, K, expand, rows, V, tau, row_base, req_status=None,
+                           stream=None):
+    _need(expand, torch.int32, "expand")
+    _need(rows, None, "rows")
+    code = load_library().spec_draft_topk_append(ctypes.byref(pool), level, K, _ptr(expand),
+                                                 _dtype_code(rows), _ptr(rows), rows.shape[1], V,
+                                                 float(tau), row_base, _ptr(req_status),
+                                                 _stream(stream))
+    _check(code, "spec_draft_topk_append")
+
+
+def spec_echo_workspace_size(B, cap):
+    return int(load_library().spec_echo_workspace_size(B, cap))
+
+
+def spec_echo_select_pack(pool, K_max, node_offset, parent, tokens, depth, draft_row, source,
+                          workspace, stream=None):
+    for t, n in ((node_offset, "node_offset"), (parent, "parent"), (tokens, "tokens"),
+                 (depth, "depth"), (draft_row, "draft_row")):
+        _need(t, torch.int32, n)
+    wsz = workspace.numel() * workspace.element_size()
+    code = load_library().spec_echo_select_pack(ctypes.byref(pool), K_max, _ptr(node_offset),
+                                                _ptr(parent), _ptr(tokens), _ptr(depth),
+                                                _ptr(draft_row), _ptr(source), _ptr(workspace),
+                                                wsz, _stream(stream))
+    _check(code, "spec_echo_select_pack")

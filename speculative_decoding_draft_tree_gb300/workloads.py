@@ -503,6 +503,21 @@ CONFIG_NAMES = {
 
 
 # ----------------------------------------------------------------------------------------------
+# Draft-model output for building trees on the device: one level's rows.
+# ----------------------------------------------------------------------------------------------
+def draft_level_rows(*, B: int, K: int, V: int, level: int, dtype: str = "bf16", device="cpu",
+                     seed: int = SEEDS["drafting"], scales=None) -> torch.Tensor:
+    """[B * K, ld] draft logits standing in for the draft model's output at one level: row
+    r * K + j ~ N(0, scales[r]^2) (a larger scale = a more confident request), seeded by
+    (seed, level); rows padded to a 16-byte multiple."""
+    g = _gen(seed * 1000 + level, device)
+    sc = torch.as_tensor(list(scales) if scales is not None else [1.0] * B, dtype=torch.float32,
+                         device=device)
+    x = torch.randn((B * K, V), generator=g, device=device) * sc.repeat_interleave(K)[:, None]
+    return _pad_rows(x.to(_torch_dtype(dtype)), _row_ld(V, dtype))
+
+
+# ----------------------------------------------------------------------------------------------
 # Several draft models (multi-draft verification: every sibling carries its own model's q).
 # ----------------------------------------------------------------------------------------------
 def multidraft_parents(k: int, gamma: int) -> List[int]:

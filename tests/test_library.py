@@ -43,7 +43,8 @@ def test_struct_layouts_match_header(tmp_path):
     """Every field offset and every struct size of the Python binding equals what a C compiler
     makes of include/spec_verify.h."""
     structs = {"spec_attn_params": B.SpecAttnParams, "spec_verify_params": B.SpecVerifyParams,
-               "spec_compact_params": B.SpecCompactParams, "spec_rope_params": B.SpecRopeParams}
+               "spec_compact_params": B.SpecCompactParams, "spec_rope_params": B.SpecRopeParams,
+               "spec_draft_pool": B.SpecDraftPool}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "spec_verify.h"',
              "int main(void) {"]
     want = []
@@ -71,6 +72,10 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_tree_attention(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_kv_compact(None, None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_tree_rope_kv_write(None, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_draft_init(None, None, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_echo_select_pack(None, 0, None, None, None, None, None, None, None, 0,
+                                     None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_echo_workspace_size(0, 0) == 0
     assert lib.spec_tree_build(None, None, None, 0, 0, 0, None, None, None, None, None,
                                None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_verify_workspace_size(None) == 0
