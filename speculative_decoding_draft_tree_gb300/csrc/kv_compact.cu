@@ -7,13 +7,20 @@
 // One CTA per (request, layer).  Slot P + d receives slot P + path[d] for d = 0..n_acc.  Because
 // path[d] >= d (the accepted path descends one level per step and nodes are numbered
 // breadth-first), copying in increasing d never overwrites a slot that a later step still has
-// to read: a later step d' > d reads P + path[d'] with path[d'] >= d' > d.  So the CTA walks d in
-// order with a barrier between steps and copies all heads and both caches of one step in
-// parallel with 16-byte vectors -- gather semantics without a staging buffer.  Identity steps
-// (path[d] == d, e.g. a fully accepted chain) copy nothing.
+// to read: a later step d' > d reads P + path[d'] with path[d'] >= d' > d.  The steps that move
+// a row (path[d] != d; identity steps such as a fully accepted chain copy nothing) are taken in
+// increasing d in groups of up to kCompactSteps: each thread takes one 16-byte position w of
+// the heads' rows (w < H_kv * head_dim * es / 16, in chunks of the block size), loads its K and
+// V vector of every step of the group, and after a barrier stores them -- gather semantics
+// with one memory round trip per group and chunk instead of one per step (within a group
+// every load precedes every store, positions of different chunks are disjoint, and groups
+// follow each other in increasing d).  Slot offsets come from shared memory.
 #include "common.cuh"
 
 namespace spec {
+
+constexpr int kCompactThreads = 512;
+constexpr int kCompactSteps = 8;   // moving steps staged per group (K and V: 2 vectors each)
 
 struct CompactDev {
   char* k;
@@ -30,7 +37,7 @@ struct CompactDev {
   int32_t H_kv, row_bytes, bs, num_blocks, max_blocks, max_path;
 };
 
-__global__ void __launch_bounds__(256) kv_compact_kernel(CompactDev a) {
+__global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(CompactDev a) {
   pdl_wait();
   pdl_trigger();
   const int r = blockIdx.x;
@@ -78,28 +85,59 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(CompactDev a) {
     return;
   }
   const int vec_per_row = a.row_bytes / 16;
-  const int per_step = a.H_kv * vec_per_row;
+  const int per_step = a.H_kv * vec_per_row;   // vectors of one cache for one step
   const size_t head_stride = size_t(a.bs) * a.row_bytes;
   const size_t block_stride = size_t(a.H_kv) * head_stride;
   char* kb = a.k + layer * a.layer_stride_bytes;
   char* vb = a.v + layer * a.layer_stride_bytes;
-  for (int d = 1; d <= na; ++d) {
-    const int pd = prow[d];
-    if (pd != d) {
-      const int src = P + pd, dst = P + d;
-      const size_t so = size_t(trow[src / a.bs]) * block_stride + size_t(src % a.bs) * a.row_bytes;
-      const size_t dof = size_t(trow[dst / a.bs]) * block_stride + size_t(dst % a.bs) * a.row_bytes;
-      for (int t = tid; t < 2 * per_step; t += blockDim.x) {
-        const int which = t / per_step;
-        const int rem = t - which * per_step;
-        const int h = rem / vec_per_row;
-        const int c = rem - h * vec_per_row;
-        char* base = which ? vb : kb;
-        const uint4 val = *reinterpret_cast<const uint4*>(base + so + h * head_stride + c * 16);
-        *reinterpret_cast<uint4*>(base + dof + h * head_stride + c * 16) = val;
-      }
+  // the moving steps, in increasing d, with their source and destination slot offsets
+  __shared__ int s_move[SPEC_MAX_TREE];
+  __shared__ size_t s_src[SPEC_MAX_TREE], s_dst[SPEC_MAX_TREE];
+  __shared__ int s_nmove;
+  if (tid == 0) {
+    int n = 0;
+    for (int d = 1; d <= na && d < SPEC_MAX_TREE; ++d)
+      if (prow[d] != d) s_move[n++] = d;
+    s_nmove = n;
+  }
+  __syncthreads();
+  const int nmove = s_nmove;
+  if (nmove > 0) {
+    for (int q = tid; q < nmove; q += kCompactThreads) {
+      const int d = s_move[q];
+      const int src = P + prow[d], dst = P + d;
+      s_src[q] = size_t(trow[src / a.bs]) * block_stride + size_t(src % a.bs) * a.row_bytes;
+      s_dst[q] = size_t(trow[dst / a.bs]) * block_stride + size_t(dst % a.bs) * a.row_bytes;
     }
     __syncthreads();
+    for (int w0 = 0; w0 < per_step; w0 += kCompactThreads) {
+      const int w = w0 + tid;
+      const bool mine = w < per_step;
+      const int h = mine ? w / vec_per_row : 0;
+      const size_t in_row = size_t(h) * head_stride + size_t(w - h * vec_per_row) * 16;
+      for (int g0 = 0; g0 < nmove; g0 += kCompactSteps) {
+        const int gsteps = min(kCompactSteps, nmove - g0);
+        uint4 kv[kCompactSteps][2];
+  #pragma unroll
+        for (int q = 0; q < kCompactSteps; ++q) {
+          if (mine && q < gsteps) {
+            const size_t o = s_src[g0 + q] + in_row;
+            kv[q][0] = *reinterpret_cast<const uint4*>(kb + o);
+            kv[q][1] = *reinterpret_cast<const uint4*>(vb + o);
+          }
+        }
+        __syncthreads();   // every source of the group is read before any destination is written
+  #pragma unroll
+        for (int q = 0; q < kCompactSteps; ++q) {
+          if (mine && q < gsteps) {
+            const size_t o = s_dst[g0 + q] + in_row;
+            *reinterpret_cast<uint4*>(kb + o) = kv[q][0];
+            *reinterpret_cast<uint4*>(vb + o) = kv[q][1];
+          }
+        }
+        __syncthreads();
+      }
+    }
   }
   if (layer == 0) {
     for (int k = tid; k < a.max_path; k += blockDim.x) {
@@ -152,5 +190,6 @@ extern "C" spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stre
   d.max_blocks = p->max_blocks_per_req;
   d.max_path = p->max_path;
   dim3 grid(p->B, p->num_layers);
-  return launch_result(launch_pdl(kv_compact_kernel, grid, dim3(256), 0, (cudaStream_t)stream, d));
+  return launch_result(
+      launch_pdl(kv_compact_kernel, grid, dim3(kCompactThreads), 0, (cudaStream_t)stream, d));
 }
