@@ -411,23 +411,35 @@ __device__ __forceinline__ uint64_t echo_key(float score, int r, int cap, int i)
 // One CTA: the M-th smallest key among all non-root candidates (M = K_max - B), found by eight
 // byte-wide passes from the top: each pass histograms the byte of the keys that share the
 // prefix found so far and descends into the bin holding the M-th.  kept[r][i] = key <= it.
+// The keys are read from the pool once into shared memory (non-candidates hold kNoKey); one warp
+// finds the bin (eight bins per lane and a shuffle scan); kept counts per request are summed
+// with shared atomics while marking.
+constexpr uint64_t kNoKey = ~0ull;
+constexpr int kEchoMaxKeys = 16384;   // keys held in shared memory (128 KB)
+constexpr int kEchoMaxB = 4096;       // requests whose kept counts are summed in shared memory
+
 __global__ void __launch_bounds__(kEchoThreads)
 echo_select_kernel(PoolDev p, int K_max, uint8_t* __restrict__ kept,
                    int32_t* __restrict__ kept_count) {
+  extern __shared__ uint64_t s_key[];   // [B * cap]
   __shared__ int hist[256];
+  __shared__ int s_cnt[kEchoMaxB];
   __shared__ uint64_t s_prefix;
   __shared__ int s_rank;
   __shared__ int s_total;
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.B * p.cap;
   if (tid == 0) s_total = 0;
+  for (int r = tid; r < p.B; r += kEchoThreads) s_cnt[r] = 0;
   __syncthreads();
   int mine = 0;
   for (int e = tid; e < n; e += kEchoThreads) {
     const int r = e / p.cap, i = e - r * p.cap;
-    if (i > 0 && i < min(p.count[r], p.cap)) ++mine;
+    const bool cand = i > 0 && i < min(p.count[r], p.cap);
+    s_key[e] = cand ? echo_key(p.score[e], r, p.cap, i) : kNoKey;
+    mine += cand ? 1 : 0;
   }
   atomicAdd(&s_total, mine);
   __syncthreads();
@@ -442,20 +454,32 @@ echo_select_kernel(PoolDev p, int K_max, uint8_t* __restrict__ kept,
       __syncthreads();
       const uint64_t hi_mask = pass == 7 ? 0ull : (~0ull << (shift + 8));
       for (int e = tid; e < n; e += kEchoThreads) {
-        const int r = e / p.cap, i = e - r * p.cap;
-        if (i == 0 || i >= min(p.count[r], p.cap)) continue;
-        const uint64_t key = echo_key(p.score[e], r, p.cap, i);
-        if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+        const uint64_t key = s_key[e];
+        if (key != kNoKey && (key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
       }
       __syncthreads();
-      if (tid == 0) {
-        int acc = 0, b = 0;
-        for (; b < 256; ++b) {
-          if (acc + hist[b] >= rank) break;
-          acc += hist[b];
+      if (warp == 0) {   // the bin where the running count reaches rank
+        int c8[8], sum = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) { c8[k] = hist[lane * 8 + k]; sum += c8[k]; }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
         }
-        s_prefix = prefix | (uint64_t(b) << shift);
-        s_rank = rank - acc;
+        const int excl = incl - sum;
+        const unsigned hit = __ballot_sync(0xffffffffu, excl < rank && incl >= rank);
+        if (lane == __ffs(hit) - 1) {
+          int acc = excl, b = lane * 8;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            if (acc + c8[k] >= rank) { b = lane * 8 + k; break; }
+            acc += c8[k];
+          }
+          s_prefix = prefix | (uint64_t(b) << shift);
+          s_rank = rank - acc;
+        }
       }
       __syncthreads();
       prefix = s_prefix;
@@ -466,22 +490,18 @@ echo_select_kernel(PoolDev p, int K_max, uint8_t* __restrict__ kept,
   // marks: roots always; non-roots by key (M == total: all; M == 0: none)
   for (int e = tid; e < n; e += kEchoThreads) {
     const int r = e / p.cap, i = e - r * p.cap;
-    const int cnt = min(p.count[r], p.cap);
+    const uint64_t key = s_key[e];
     uint8_t k = 0;
     if (i == 0) {
       k = 1;
-    } else if (i < cnt && M > 0) {
-      k = (M >= total) ? 1 : (echo_key(p.score[e], r, p.cap, i) <= prefix ? 1 : 0);
+    } else if (key != kNoKey && M > 0) {
+      k = (M >= total || key <= prefix) ? 1 : 0;
     }
     kept[e] = k;
+    if (k) atomicAdd(&s_cnt[r], 1);
   }
   __syncthreads();
-  for (int r = tid; r < p.B; r += kEchoThreads) {
-    int c = 0;
-    const int cnt = min(p.count[r], p.cap);
-    for (int i = 0; i < cnt; ++i) c += kept[size_t(r) * p.cap + i];
-    kept_count[r] = c;
-  }
+  for (int r = tid; r < p.B; r += kEchoThreads) kept_count[r] = s_cnt[r];
 }
 
 // One CTA per request: offsets by summing the earlier requests' counts, local indices by a
@@ -648,7 +668,13 @@ spec_status_t spec_echo_select_pack(const spec_draft_pool* pool, int32_t K_max,
   uint8_t* kept = static_cast<uint8_t*>(workspace);
   int32_t* kept_count = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) +
                                                    align_up(size_t(p.B) * size_t(p.cap), 256));
-  cudaError_t e = launch_pdl(echo_select_kernel, dim3(1), dim3(kEchoThreads), 0,
+  if (p.B * p.cap > kEchoMaxKeys || p.B > kEchoMaxB) return SPEC_ERR_UNSUPPORTED;
+  const size_t dyn = sizeof(uint64_t) * size_t(p.B) * size_t(p.cap);
+  static bool raised[64] = {false};
+  const spec_status_t st = allow_dynamic_smem(echo_select_kernel, sizeof(uint64_t) * kEchoMaxKeys,
+                                              raised);
+  if (st != SPEC_OK) return st;
+  cudaError_t e = launch_pdl(echo_select_kernel, dim3(1), dim3(kEchoThreads), dyn,
                              (cudaStream_t)stream, p, int(K_max), kept, kept_count);
   if (e == cudaSuccess)
     e = launch_pdl(echo_pack_kernel, dim3(p.B), dim3(kDraftThreads), 0, (cudaStream_t)stream, p,
