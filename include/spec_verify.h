@@ -372,6 +372,12 @@ spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level,
                                      int64_t ld, int32_t V, float tau, int32_t row_base,
                                      int32_t* req_status, spec_stream_t stream);
 
+/* Testing only: the following spec_draft_topk_append launches on the current device do not
+ * issue chunk `chunk` (16 KB units of a row) of any row, so the kernel's bounded wait for it
+ * runs out (about a second) and the call reports SPEC_REQ_TIMEOUT for those requests, as a lost
+ * copy would; -1 restores normal operation.  Synchronous (a host-to-device symbol copy). */
+spec_status_t spec_debug_draft_copy_stall(int32_t chunk);
+
 /* ECHO selection and packing: node_offset [B+1]; parent (local, -1 for roots), tokens, depth,
  * draft_row (the node's row if one of its children was kept, else -1) and source (candidate
  * index, may be NULL), each with room for min(K_max, B * cap) entries; N = node_offset[B].

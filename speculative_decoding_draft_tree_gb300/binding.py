@@ -23,7 +23,7 @@ EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_k
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
            "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
-           "spec_echo_select_pack"]
+           "spec_echo_select_pack", "spec_debug_draft_copy_stall"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -121,6 +121,8 @@ def load_library(build_if_missing=False):
     lib.spec_draft_topk_append.argtypes = [ctypes.POINTER(SpecDraftPool), _i32, _i32, _vp,
                                            ctypes.c_int, _vp, _i64, _i32, ctypes.c_float, _i32,
                                            _vp, _vp]
+    lib.spec_debug_draft_copy_stall.restype = st
+    lib.spec_debug_draft_copy_stall.argtypes = [_i32]
     lib.spec_echo_workspace_size.restype = ctypes.c_size_t
     lib.spec_echo_workspace_size.argtypes = [_i32, _i32]
     lib.spec_echo_select_pack.restype = st
@@ -416,3 +418,8 @@ def spec_echo_select_pack(pool, K_max, node_offset, parent, tokens, depth, draft
                                                 _ptr(draft_row), _ptr(source), _ptr(workspace),
                                                 wsz, _stream(stream))
     _check(code, "spec_echo_select_pack")
+
+
+def spec_debug_draft_copy_stall(chunk):
+    """Testing only: make the next top-K launches lose one chunk's copy (-1: off)."""
+    _check(load_library().spec_debug_draft_copy_stall(int(chunk)), "spec_debug_draft_copy_stall")

@@ -128,6 +128,10 @@ constexpr int kConsumerWarps = kConsumerThreads / 32;
 constexpr int kTopkThreads = kConsumerThreads + 32;   // + the producer warp
 constexpr long long kCopyWaitLimit = 2000000000LL;   // clock cycles (~1 s): a lost copy
 
+// Testing only (spec_debug_draft_copy_stall): a chunk index that the producer does not issue,
+// so that the consumers' bounded wait for it runs out; -1 (the default) disables it.
+__device__ int g_draft_copy_stall = -1;
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -159,7 +163,7 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
   extern __shared__ __align__(128) uint8_t ring_dyn[];   // kStages x kChunkBytes
   __shared__ __align__(8) uint64_t full[kStages];
   __shared__ __align__(8) uint64_t empty[kStages];
-  __shared__ int s_issued;
+  __shared__ int s_last_issued[kStages];   // the last chunk issued into each stage, -1 if none
   __shared__ float s_v[kConsumerWarps][kTopkMax];
   __shared__ int s_id[kConsumerWarps][kTopkMax];
   __shared__ float s_m[kConsumerWarps];
@@ -184,8 +188,8 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
   uint8_t* const ring = ring_dyn;
   if (tid == 0) {
     s_abort = 0;
-    s_issued = 0;
     for (int st = 0; st < kStages; ++st) {
+      s_last_issued[st] = -1;
       tc::mbar_init(&full[st], 1);
       tc::mbar_init(&empty[st], kConsumerWarps);
     }
@@ -198,6 +202,7 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
   int lid = 0x7fffffff;
   if (producer) {
     if (lane == 0) {
+      const int stall = g_draft_copy_stall;
       for (int c = 0; c < nchunks; ++c) {
         const int st = c % kStages;
         if (c >= kStages) {   // the stage's previous chunk must have been released
@@ -208,11 +213,12 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
           }
           tc::fence_proxy_async_smem();   // the consumers' reads before the copy's writes
         }
+        if (c == stall) continue;   // testing: this chunk never arrives
         const uint32_t bytes = uint32_t(min(kChunkBytes, row_bytes - c * kChunkBytes));
         tc::mbar_arrive_expect_tx(&full[st], bytes);
         bulk_load(ring + size_t(st) * kChunkBytes, src + size_t(c) * kChunkBytes, bytes,
                   &full[st]);
-        s_issued = c + 1;
+        s_last_issued[st] = c;
       }
     }
   } else {
@@ -331,10 +337,10 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
     // so none is still writing when the CTA exits, and mark the request
     if (tid == 0) {
       volatile int never = 0;
-      const int issued = s_issued;
-      for (int st = 0; st < kStages && st < issued; ++st) {
-        const int last = ((issued - 1 - st) / kStages) * kStages + st;
-        tc::mbar_wait(&full[st], uint32_t((last / kStages) & 1), &never, kCopyWaitLimit);
+      for (int st = 0; st < kStages; ++st) {
+        const int last = s_last_issued[st];
+        if (last >= 0)
+          tc::mbar_wait(&full[st], uint32_t((last / kStages) & 1), &never, kCopyWaitLimit);
       }
       if (req_status) atomicOr(&req_status[r], SPEC_REQ_TIMEOUT);
     }
@@ -646,6 +652,16 @@ spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level,
                    static_cast<const float*>(rows), ld, int(V), k2, inv_tau, int(row_base),
                    req_status);
   return launch_result(e);
+}
+
+spec_status_t spec_debug_draft_copy_stall(int32_t chunk) {
+  const int v = chunk < 0 ? -1 : chunk;
+  const cudaError_t e = cudaMemcpyToSymbol(spec::g_draft_copy_stall, &v, sizeof(v));
+  if (e != cudaSuccess) {
+    spec::set_last_cuda_error(e);
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
 }
 
 size_t spec_echo_workspace_size(int32_t B, int32_t cap) {
