@@ -312,6 +312,11 @@ def main():
     for _ in range(max(3, args.warmup)):
         step.run()
     torch.cuda.synchronize()
+    # the same step as one CUDA graph (the launches keep their programmatic dependencies)
+    step_graph = step.capture_graph()
+    for _ in range(3):
+        step_graph.replay()
+    torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -327,6 +332,7 @@ def main():
                 for _ in range(args.steps)]
 
     ev_rope, ev_fused, ev_tree, ev_step_r = ev_pairs(), ev_pairs(), ev_pairs(), ev_pairs()
+    ev_graph = ev_pairs()
     for _ in range(3):
         step_r.run()
     # the lookahead-decoding forward (2-D Jacobi window + candidate n-grams) as a second mask
@@ -380,6 +386,13 @@ def main():
         step.verify()
         step.compact()
         s1.record(stream)
+    # the same step replayed as one CUDA graph, same flush
+    for i in range(args.steps):
+        l2_flush(i)
+        g0, g1 = ev_graph[i]
+        g0.record(stream)
+        step_graph.replay()
+        g1.record(stream)
     # the attention call alone (roofline), same flush, on the same stream
     for i in range(args.steps):
         l2_flush(i)
@@ -473,6 +486,7 @@ def main():
     t_rope, t_fused, t_tree, t_step_r = (mean_s(ev_rope), mean_s(ev_fused), mean_s(ev_tree),
                                          mean_s(ev_step_r))
     t_look_attn, t_look_step = mean_s(ev_look_attn), mean_s(ev_look_step)
+    t_graph = max_over_ranks(mean_s(ev_graph), world, dev)
     t_multi_ver, t_multi_step = mean_s(ev_multi_ver), mean_s(ev_multi_step)
     t_dt, t_dt_append, t_dt_echo = mean_s(ev_dt), mean_s(ev_dt_append), mean_s(ev_dt_echo)
     t_total = sum(step_ms) / 1e3
@@ -587,6 +601,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic", "config": workload_description(w, args.workload),
         "requests_per_s": round(world * w.B * args.steps / t_total, 1),
+        "graph": {"ms_per_step": round(1e3 * t_graph, 4),
+                  "value": round(job_throughput(tokens_per_step, 1, t_graph, world), 1)},
         "accepted_tokens_per_request": round(float(out_len.float().mean()), 3),
         "roofline": roofline, "cpu_baseline": cb, "e2e": e2e, "next": next_rows,
         "clocks": clocks, "gpu_launches": KERNELS_PER_STEP * args.steps,

@@ -137,6 +137,20 @@ class VerifyStep:
         self.verify(stream)
         self.compact(stream)
 
+    def capture_graph(self) -> "torch.cuda.CUDAGraph":
+        """One round (run()) captured as a CUDA graph; replay() re-runs it on the same buffers.
+        The launches keep their programmatic dependencies inside the graph.  Call run() once
+        before capturing (first calls set per-device kernel attributes, which capture does not
+        allow)."""
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                self.run(side)
+        torch.cuda.current_stream().wait_stream(side)
+        return g
+
     def results(self) -> Dict[str, torch.Tensor]:
         return dict(req_status=self.req_status, depth=self.depth, pos_id=self.pos_id,
                     anc_mask=self.anc_mask, is_internal=self.is_internal, o=self.o, lse=self.lse,
