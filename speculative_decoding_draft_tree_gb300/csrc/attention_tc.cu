@@ -333,18 +333,16 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return r;
 }
 
-// In place: masked, log2-scaled scores of 32 columns starting at key `key0`; returns their max.
-// Columns inside the prefix need no mask (one multiply and one max per score).
-__device__ __forceinline__ float mask_max32(uint32_t (&x)[32], bool valid, int key0, int P,
-                                            const uint32_t (&anc)[8], int W, float sl2) {
+// Masked raw (unscaled) scores of 32 columns starting at key `key0`, in place: invisible keys
+// become -inf; returns the maximum of the visible ones.  Columns inside the prefix need no mask
+// (one max per score).  Scaling by a positive constant commutes with the maximum, so the caller
+// scales the maximum once and folds the scale into the exponentials' FMA.
+__device__ __forceinline__ float mask_max32_raw(uint32_t (&x)[32], bool valid, int key0, int P,
+                                                const uint32_t (&anc)[8], int W) {
   float mx = -INFINITY;
   if (key0 + 32 <= P) {
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const float v = __uint_as_float(x[c]) * sl2;
-      x[c] = __float_as_uint(v);
-      mx = fmaxf(mx, v);
-    }
+    for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
     return valid ? mx : -INFINITY;
   }
   const uint32_t wd = anc_window(anc, W, key0 - P);
@@ -352,7 +350,7 @@ __device__ __forceinline__ float mask_max32(uint32_t (&x)[32], bool valid, int k
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const bool vis = valid && ((c < npre) || ((wd >> c) & 1u));
-    const float v = vis ? __uint_as_float(x[c]) * sl2 : -INFINITY;
+    const float v = vis ? __uint_as_float(x[c]) : -INFINITY;
     x[c] = __float_as_uint(v);
     mx = fmaxf(mx, v);
   }
@@ -667,8 +665,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           tc::tmem_ld32(srow + 64 * (1 - hh), x0);
           tc::tmem_ld32(srow + 64 * (1 - hh) + 32, x1);
           tc::tmem_ld_wait();
-          tmax = fmaxf(mask_max32(x0, valid, kbase + 64 * (1 - hh), P, anc, a.W, sl2),
-                       mask_max32(x1, valid, kbase + 64 * (1 - hh) + 32, P, anc, a.W, sl2));
+          tmax = fmaxf(mask_max32_raw(x0, valid, kbase + 64 * (1 - hh), P, anc, a.W),
+                       mask_max32_raw(x1, valid, kbase + 64 * (1 - hh) + 32, P, anc, a.W));
         }
         // this half's 64 scores, kept for the exponentials; the S buffer is free afterwards
         uint32_t s0[32], s1[32];
@@ -678,8 +676,9 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(s_free + st);
-        tmax = fmaxf(tmax, mask_max32(s0, valid, kbase + 64 * hh, P, anc, a.W, sl2));
-        tmax = fmaxf(tmax, mask_max32(s1, valid, kbase + 64 * hh + 32, P, anc, a.W, sl2));
+        tmax = fmaxf(tmax, mask_max32_raw(s0, valid, kbase + 64 * hh, P, anc, a.W));
+        tmax = fmaxf(tmax, mask_max32_raw(s1, valid, kbase + 64 * hh + 32, P, anc, a.W));
+        tmax *= sl2;   // raw maximum -> log2 units (sl2 > 0; -inf stays -inf)
         const bool grow = tmax > m_ref + kLazyRescale;
         const float new_ref = grow ? tmax : m_ref;
         const float factor = (grow && m_ref != -INFINITY) ? ex2(m_ref - new_ref) : 1.f;
@@ -688,16 +687,16 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         uint32_t pk[32];
         float rowsum = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const float p0 = has_ref ? ex2(__uint_as_float(s0[c]) - new_ref) : 0.f;
-          const float p1 = has_ref ? ex2(__uint_as_float(s0[c + 1]) - new_ref) : 0.f;
+        for (int c = 0; c < 32; c += 2) {   // 2^(x sl2 - ref): one FMA per score
+          const float p0 = has_ref ? ex2(fmaf(__uint_as_float(s0[c]), sl2, -new_ref)) : 0.f;
+          const float p1 = has_ref ? ex2(fmaf(__uint_as_float(s0[c + 1]), sl2, -new_ref)) : 0.f;
           rowsum += p0 + p1;
           pk[c >> 1] = pack_bf16(p0, p1);
         }
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = has_ref ? ex2(__uint_as_float(s1[c]) - new_ref) : 0.f;
-          const float p1 = has_ref ? ex2(__uint_as_float(s1[c + 1]) - new_ref) : 0.f;
+          const float p0 = has_ref ? ex2(fmaf(__uint_as_float(s1[c]), sl2, -new_ref)) : 0.f;
+          const float p1 = has_ref ? ex2(fmaf(__uint_as_float(s1[c + 1]), sl2, -new_ref)) : 0.f;
           rowsum += p0 + p1;
           pk[16 + (c >> 1)] = pack_bf16(p0, p1);
         }
