@@ -79,3 +79,62 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_tree_build(None, None, None, 0, 0, 0, None, None, None, None, None,
                                None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_verify_workspace_size(None) == 0
+
+
+def _rope(**kw):
+    p = B.SpecRopeParams()
+    p.dtype, p.B, p.N, p.H_q, p.H_kv, p.head_dim = B.SPEC_BF16, 2, 4, 4, 2, 128
+    p.rotary_dim, p.interleaved, p.block_size, p.num_blocks, p.max_blocks_per_req = 128, 0, 16, 8, 4
+    p.base = 10000.0
+    fake = 0x100000   # 16-byte aligned, never dereferenced: validation fails first
+    for f in ("q_in", "q_out", "k_new", "v_new", "k_cache", "v_cache", "block_table", "prefix_len",
+              "node_offset", "pos_id", "req_status"):
+        setattr(p, f, fake)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(rotary_dim=127), B.SPEC_ERR_INVALID_ARG),          # odd
+    (dict(rotary_dim=256), B.SPEC_ERR_INVALID_ARG),          # above head_dim
+    (dict(rotary_dim=8), B.SPEC_ERR_UNSUPPORTED),            # half-split pair straddles vectors
+    (dict(rotary_dim=12, interleaved=1), B.SPEC_ERR_UNSUPPORTED),
+    (dict(base=0.0), B.SPEC_ERR_INVALID_ARG),
+    (dict(base=float("inf")), B.SPEC_ERR_INVALID_ARG),
+    (dict(head_dim=100), B.SPEC_ERR_INVALID_ARG),            # 200-byte rows: not 16-byte multiples
+    (dict(q_out=0x100004), B.SPEC_ERR_INVALID_ARG),          # misaligned
+    (dict(N=-1), B.SPEC_ERR_INVALID_ARG),
+])
+def test_rope_host_validation(lib, change, code):
+    p = _rope(**change)
+    assert lib.spec_tree_rope_kv_write(ctypes.byref(p), None) == code
+
+
+def test_fused_rope_build_checks_its_request_arrays(lib):
+    p = _rope()
+    fake = 0x100000
+    # the rope block's B / N must be the call's; a different node_offset buffer is refused
+    assert lib.spec_tree_build_rope_kv_write(fake, fake, fake, 3, 4, 8, fake, fake, fake, fake,
+                                             fake, ctypes.byref(p), None) == B.SPEC_ERR_INVALID_ARG
+    p.node_offset = 0x200000
+    assert lib.spec_tree_build_rope_kv_write(fake, fake, fake, 2, 4, 8, fake, fake, fake, fake,
+                                             fake, ctypes.byref(p), None) == B.SPEC_ERR_INVALID_ARG
+
+
+def test_draft_tree_host_validation(lib):
+    fake = 0x100000
+    pool = B.SpecDraftPool()
+    pool.B, pool.cap = 4, 300   # above 256 candidates per request
+    for f in ("parent", "token", "depth", "score", "row", "count"):
+        setattr(pool, f, fake)
+    assert lib.spec_draft_init(ctypes.byref(pool), fake, None) == B.SPEC_ERR_INVALID_ARG
+    pool.cap = 100
+    assert lib.spec_draft_expand_select(ctypes.byref(pool), 1, 17, fake, None,
+                                        None) == B.SPEC_ERR_INVALID_ARG   # K above 16
+    assert lib.spec_draft_topk_append(ctypes.byref(pool), 1, 5, fake, B.SPEC_BF16, fake, 1000,
+                                      1000, 0.0, 0, None, None) == B.SPEC_ERR_INVALID_ARG  # tau
+    assert lib.spec_draft_topk_append(ctypes.byref(pool), 1, 5, fake, B.SPEC_BF16, fake, 999,
+                                      1000, 1.0, 0, None, None) == B.SPEC_ERR_INVALID_ARG  # ld < V
+    assert lib.spec_echo_select_pack(ctypes.byref(pool), 64, fake, fake, fake, fake, fake, None,
+                                     fake, 16, None) == B.SPEC_ERR_INVALID_ARG   # small workspace
