@@ -495,55 +495,32 @@ def main():
     ms_per_step = 1e3 * t_total / args.steps
     value = job_throughput(tokens_per_step, args.steps, t_total, world)
 
-    # end to end through the public API with pinned host buffers: every round's inputs are
-    # copied from pinned host memory and its accepted tokens copied back inside the timed region;
-    # two steps over separate input buffers (same KV cache) let round i + 1's upload overlap
-    # round i's kernels, as a serving loop would.  No L2 flush between rounds:
+    # end to end through the public API (RoundPipeline) with pinned host buffers: every round's
+    # inputs are copied from pinned host memory and its accepted tokens copied back inside the
+    # timed region; two steps over separate buffers (same KV cache) let round i + 1's upload
+    # overlap round i's kernels, as a serving loop would.  No L2 flush between rounds:
     # each round streams 540 MB of K/V (4x L2) and the copy engine writes the round's inputs.
     e2e = None
     if not args.no_e2e:
-        steps_ab = [step.twin(), step.twin()]
-        host_in = steps_ab[0].pinned_host_inputs()
-        host_outs = [step.host_output_buffers(), step.host_output_buffers()]
-        # uploads and downloads each on a stream of their own, so that neither sits between two
-        # rounds' kernels: round i's inputs go to buffer i % 2 once round i - 2 (the last reader
-        # of that buffer) is done; round i runs once its inputs are in and round i - 2's results
-        # (the same output buffer) have been read back
-        up_stream, dl_stream = torch.cuda.Stream(), torch.cuda.Stream()
-        ready = [torch.cuda.Event(), torch.cuda.Event()]
-        done = [torch.cuda.Event(), torch.cuda.Event()]
-        dl_done = [torch.cuda.Event(), torch.cuda.Event()]
-        for _ in range(2):
-            for k in range(2):
-                steps_ab[k].run_from_host(host_in, host_outs[k], stream)
-        for k in range(2):
-            done[k].record(stream)
-            dl_done[k].record(stream)
+        from speculative_decoding_draft_tree_gb300.api import RoundPipeline
+        pipe = RoundPipeline(step, stream)
+        host_in = pipe.pinned_host_inputs()
+        for _ in range(4):
+            pipe.submit(host_in)
+        pipe.finish()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        up_stream.wait_stream(stream)
-        dl_stream.wait_stream(stream)
         for i in range(args.steps):
-            k = i % 2
-            up_stream.wait_event(done[k])
-            steps_ab[k].upload(host_in, up_stream)
-            ready[k].record(up_stream)
-            stream.wait_event(ready[k])
-            stream.wait_event(dl_done[k])
-            steps_ab[k].run(stream)
-            done[k].record(stream)
-            dl_stream.wait_event(done[k])
-            steps_ab[k].download(host_outs[k], dl_stream)
-            dl_done[k].record(dl_stream)
-        stream.wait_stream(dl_stream)   # the timed region ends with the last results on the host
+            pipe.submit(host_in)
+        pipe.finish()   # the timed region ends with the last results on the host
         e1.record(stream)
         torch.cuda.synchronize()
         t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
         e2e = {"value": job_throughput(tokens_per_step, args.steps, t_e2e, world),
                "unit": "verified tree tokens/s",
                "h2d_bytes_per_step": VerifyStep.bytes_of(host_in),
-               "d2h_bytes_per_step": VerifyStep.bytes_of(host_outs[0]),
+               "d2h_bytes_per_step": VerifyStep.bytes_of(pipe.host_outputs(0)),
                "ms_per_step": 1e3 * t_e2e / args.steps}
 
     if rank != 0:

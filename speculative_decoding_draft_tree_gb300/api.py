@@ -233,6 +233,61 @@ class VerifyStep:
         return sum(t.numel() * t.element_size() for t in tensors.values())
 
 
+class RoundPipeline:
+    """Rounds of one workload shape submitted from pinned host memory, double-buffered.
+
+    Two twins of a step (own input and output buffers, the same KV cache) alternate.  Each
+    submit() enqueues: the round's upload on an upload stream, its kernels on the compute stream,
+    and the read-back of its results on a download stream, ordered by events so that no copy sits
+    between two rounds' kernels: round i's upload waits for round i - 2 (the last reader of that
+    input buffer), round i's kernels wait for their inputs and for round i - 2's download (the
+    same output buffer).  Everything is asynchronous; results of round i are in
+    host_outputs(i) once finish() (or a later synchronisation) has returned."""
+
+    def __init__(self, step: VerifyStep, stream=None):
+        self.steps = [step.twin(), step.twin()]
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        self.up, self.dl = torch.cuda.Stream(), torch.cuda.Stream()
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]
+        self.done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.dl_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.host_outs = [step.host_output_buffers(), step.host_output_buffers()]
+        for k in range(2):
+            self.done[k].record(self.stream)
+            self.dl_done[k].record(self.stream)
+        self.up.wait_stream(self.stream)
+        self.dl.wait_stream(self.stream)
+        self.count = 0
+
+    def pinned_host_inputs(self) -> Dict[str, torch.Tensor]:
+        """A pinned host buffer in the layout submit() takes."""
+        return self.steps[0].pinned_host_inputs()
+
+    def host_outputs(self, i: int) -> Dict[str, torch.Tensor]:
+        """The pinned host results of round i (valid until round i + 2 is submitted)."""
+        return self.host_outs[i % 2]
+
+    def submit(self, host_inputs: Dict[str, torch.Tensor]) -> int:
+        k = self.count % 2
+        st = self.steps[k]
+        self.up.wait_event(self.done[k])
+        st.upload(host_inputs, self.up)
+        self.ready[k].record(self.up)
+        self.stream.wait_event(self.ready[k])
+        self.stream.wait_event(self.dl_done[k])
+        st.run(self.stream)
+        self.done[k].record(self.stream)
+        self.dl.wait_event(self.done[k])
+        st.download(self.host_outs[k], self.dl)
+        self.dl_done[k].record(self.dl)
+        self.count += 1
+        return self.count - 1
+
+    def finish(self):
+        """Make the compute stream wait for every submitted round's results on the host."""
+        self.stream.wait_stream(self.dl)
+
+
 class DraftTreeBuilder:
     """The device side of building a draft tree for a batch: EAGLE-2 expansion of the K most
     probable leaves per level, the K most probable tokens of each expanded row, and ECHO's

@@ -246,3 +246,33 @@ def test_graph_replay_matches_stream_launches():
         outs.append(out)
     for k in outs[0]:
         assert torch.equal(outs[0][k], outs[1][k]), k
+
+
+def test_round_pipeline_alternating_inputs():
+    # rounds of two different batches (same shape) submitted alternately through the
+    # double-buffered pipeline land in the right host buffers with the results that each batch
+    # gives when run alone
+    from speculative_decoding_draft_tree_gb300.api import RoundPipeline
+    wa = W.make_config(2, scale="small", device="cuda", num_layers=2)
+    wb = W.make_config(2, scale="small", device="cuda", num_layers=2,
+                       seeds=dict(logits=11, drafting=12, qkv=13))
+    keys = ("out_tokens", "out_len", "new_kv_len")
+    want = []
+    for w in (wa, wb):
+        s = VerifyStep(w)
+        s.run()
+        _sync()
+        want.append({k: getattr(s, k).cpu().clone() for k in keys})
+    assert not torch.equal(want[0]["out_tokens"], want[1]["out_tokens"])
+    pipe = RoundPipeline(VerifyStep(wa))
+    host = [pipe.pinned_host_inputs(), VerifyStep(wb).twin().pinned_host_inputs()]
+    for n_rounds in (2, 5):
+        first = pipe.count
+        for i in range(n_rounds):
+            pipe.submit(host[i % 2])
+        pipe.finish()
+        _sync()
+        for i in (n_rounds - 2, n_rounds - 1):
+            got = pipe.host_outputs(first + i)
+            for k in keys:
+                assert torch.equal(got[k], want[i % 2][k]), (n_rounds, i, k)
