@@ -288,6 +288,26 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
 spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * spec_verify_set_path -- no counterpart on the pages: which of the library's two forms of the
+ * same computation spec_verify and spec_verify_noalloc launch, for every later call in the
+ * process.
+ *   SPEC_VERIFY_PATH_AUTO (the default): calls with the residual or independent sibling rule
+ *     (or tau == 0), T_max <= 32 and T_max * S_t + (T_max - 1) * S_d <= 200 KiB run as one
+ *     cluster launch (8 CTAs per request, each holding its eighth of the request's rows in
+ *     shared memory), with S_t / S_d = ceil(ceil(V / 8) / 8) * 8 * the target / draft element
+ *     size (S_d = 0 at tau == 0); every other call runs the two-launch form;
+ *   SPEC_VERIFY_PATH_SPLIT: always the two-launch form (a row statistics kernel, then a walk
+ *     kernel with one CTA per request).
+ * Both forms give the same outputs except where fp32 rounding of the vocabulary sums decides:
+ * a ratio test or a draw whose uniform lies within about 1e-6 of its boundary.
+ * Not synchronised with calls in flight on other host threads.
+ * Errors: SPEC_ERR_INVALID_ARG for any other value.
+ * ------------------------------------------------------------------------------------------ */
+#define SPEC_VERIFY_PATH_AUTO  0
+#define SPEC_VERIFY_PATH_SPLIT 1
+spec_status_t spec_verify_set_path(int32_t path);
+
+/* ------------------------------------------------------------------------------------------
  * spec_kv_compact  [RATIO: KV Cache管理], [CSDN 4]
  * Commits the accepted path and rolls back the rest, in place, for every layer and KV head,
  * K and V: new[P_r + d] = old[P_r + path[r][d]] for d = 0 .. n_acc[r] (gather semantics: every

@@ -124,7 +124,8 @@ class VerifyStep:
         B.spec_kv_compact(self.comp, stream)
 
     def run(self, stream=None):
-        """One full round (4 library calls, 1 + 2 + 2 + 1 kernel launches on the stream; with
+        """One full round (4 library calls, 1 + 2 + 1 + 1 kernel launches on the stream -- the
+        verification takes 2 launches instead of 1 for trees of more than 32 nodes; with
         enable_rope, the tree build and the rotary step share one launch, or run as two calls
         when fused=False)."""
         if self.rope_p is not None and self.rope_fused:

@@ -17,13 +17,14 @@ SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS = 0, 1
 SPEC_SIBLING_RESIDUAL, SPEC_SIBLING_INDEPENDENT, SPEC_SIBLING_MULTI_DRAFT = 0, 1, 2
+SPEC_VERIFY_PATH_AUTO, SPEC_VERIFY_PATH_SPLIT = 0, 1
 REQ_BITS = dict(BAD_PARENT=1, BAD_SIZE=2, BAD_TOKEN=4, BAD_DRAFT_ROW=8, BAD_DEPTH=16,
                 BAD_BLOCK=32, TIMEOUT=64)
 EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_kv_write", "spec_tree_attention", "spec_attention_workspace_size",
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
            "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
-           "spec_echo_select_pack", "spec_debug_draft_copy_stall"]
+           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_set_path"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -123,6 +124,8 @@ def load_library(build_if_missing=False):
                                            _vp, _vp]
     lib.spec_debug_draft_copy_stall.restype = st
     lib.spec_debug_draft_copy_stall.argtypes = [_i32]
+    lib.spec_verify_set_path.restype = st
+    lib.spec_verify_set_path.argtypes = [_i32]
     lib.spec_echo_workspace_size.restype = ctypes.c_size_t
     lib.spec_echo_workspace_size.argtypes = [_i32, _i32]
     lib.spec_echo_select_pack.restype = st
@@ -334,6 +337,12 @@ def spec_verify_noalloc(params, stream=None):
     and race."""
     code = load_library().spec_verify_noalloc(ctypes.byref(params), _stream(stream))
     _check(code, "spec_verify_noalloc")
+
+
+def spec_verify_set_path(path):
+    """Which form later spec_verify calls launch: SPEC_VERIFY_PATH_AUTO (one cluster launch when
+    the call fits it) or SPEC_VERIFY_PATH_SPLIT (always the rows + walk kernels)."""
+    _check(load_library().spec_verify_set_path(int(path)), "spec_verify_set_path")
 
 
 def compact_params(k_cache, v_cache, block_table, prefix_len, path, n_acc, req_status,

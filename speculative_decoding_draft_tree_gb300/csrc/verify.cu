@@ -9,6 +9,10 @@
 //     P(. | ancestors(i)); verification walks every level of the tree;
 //   "万字综述 10+ 种 LLM 投机采样推理加速方案" (m.haoling.cc) 4.3 -- argmax sampling at temp = 0.
 //
+// Calls that fit it (residual or independent sibling rule, trees of at most 32 nodes, a
+// request's row slices within one CTA's shared memory) run as ONE cluster launch
+// (verify_cluster.cu: the rows of each request held on chip by a cluster of CTAs); the others,
+// and every call after spec_verify_set_path(SPEC_VERIFY_PATH_SPLIT), take the two-launch form.
 // Two launches on the caller's stream:
 //   1. rows  (one CTA per internal node's target row and, for tau > 0 with draft logits, per
 //      draft row; 512 threads): ONE streaming read of the row with 16-byte
@@ -30,9 +34,11 @@
 // Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
+#include "verify_cluster.cuh"
 
 namespace spec {
 
@@ -1008,6 +1014,9 @@ static spec_status_t allow_unit_sums(K kernel, bool* raised) {
   return SPEC_OK;
 }
 
+// which form spec_verify launches (spec_verify_set_path)
+static std::atomic<int> g_verify_path{SPEC_VERIFY_PATH_AUTO};
+
 template <typename TT, typename TD, bool kMulti>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   const int nunits = (d.V + 7) / 8;
@@ -1034,6 +1043,12 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
 }  // namespace spec
 
 extern "C" {
+
+spec_status_t spec_verify_set_path(int32_t path) {
+  if (path != SPEC_VERIFY_PATH_AUTO && path != SPEC_VERIFY_PATH_SPLIT) return SPEC_ERR_INVALID_ARG;
+  spec::g_verify_path.store(path, std::memory_order_relaxed);
+  return SPEC_OK;
+}
 
 size_t spec_verify_workspace_size(const spec_verify_params* p) {
   if (!p) return 0;
@@ -1096,6 +1111,21 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   d.rbuf = multi ? reinterpret_cast<float*>(ws + lay.rbuf) : nullptr;
   d.rld = lay.rld;
   cudaStream_t s = (cudaStream_t)stream;
+  if (!multi && g_verify_path.load(std::memory_order_relaxed) == SPEC_VERIFY_PATH_AUTO) {
+    ClusterVerifyArgs ca;
+    ca.target = p->target; ca.draft = p->draft; ca.tld = p->target_ld; ca.dld = p->draft_ld;
+    ca.B = p->B; ca.N = p->N; ca.R = p->R; ca.V = p->V; ca.T_max = p->T_max;
+    ca.max_path = p->max_path;
+    ca.tau = d.tau; ca.k2 = d.k2; ca.inv_tau = d.inv_tau;
+    ca.probs = d.probs; ca.residual_rule = d.residual_rule;
+    ca.draft_row = p->draft_row; ca.tokens = p->tokens; ca.parent = p->parent;
+    ca.node_offset = p->node_offset; ca.depth = p->depth; ca.is_internal = p->is_internal;
+    ca.uniforms = p->uniforms; ca.req_status = p->req_status; ca.out_tokens = p->out_tokens;
+    ca.out_len = p->out_len; ca.path = p->path; ca.n_acc = p->n_acc;
+    ca.rejections = p->rejections;
+    if (verify_cluster_fits(ca, int(tes), int(des)))
+      return launch_result(launch_verify_cluster(ca, int(tes), int(des), s));
+  }
   if (multi) {
     if (p->logits_dtype == SPEC_BF16) {
       if (d.probs) return launch_verify<__nv_bfloat16, float, true>(d, s);

@@ -1,0 +1,150 @@
+"""spec_verify's two forms against the oracle: the one-launch cluster form (trees of at most 32
+nodes whose row slices fit a CTA) and the two-launch form (row statistics kernel + walk kernel),
+chosen with spec_verify_set_path, on chains and small trees (sibling residual and independent
+rules), draft logits and probabilities, tau = 0, ragged vocabularies, data errors and more
+requests than one wave of clusters."""
+import numpy as np
+import pytest
+import torch
+
+import parity_util as PU
+from speculative_decoding_draft_tree_gb300 import binding as B
+from speculative_decoding_draft_tree_gb300 import workloads as W
+from speculative_decoding_draft_tree_gb300.api import VerifyStep
+
+pytestmark = pytest.mark.gpu
+
+PATHS = {"cluster": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT}
+
+
+@pytest.fixture(params=sorted(PATHS))
+def path(request):
+    B.spec_verify_set_path(PATHS[request.param])
+    yield request.param
+    B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+
+
+def _medusa(V=3001, dtype="bf16", tau=1.0, B_=4, ks=(2, 3, 2)):
+    return W.medusa_workload(B=B_, ks=ks, V=V, dtype=dtype, H_q=4, H_kv=4, d=128, prefix=40,
+                             tau=tau, device="cuda")
+
+
+def _specinfer(V=2001, dtype="f32", tau=0.7, B_=4, schedule=(3, 2, 1)):
+    return W.specinfer_workload(B=B_, schedule=schedule, V=V, dtype=dtype, H_q=4, H_kv=4, d=64,
+                                prefix=40, tau=tau, device="cuda")
+
+
+WORKLOADS = {
+    "chain_bf16": lambda: W.make_config(2, scale="small", device="cuda"),
+    "chain_greedy": lambda: W.make_config(2, scale="small", device="cuda", tau=0.0),
+    "chain_f32": lambda: W.make_config(1, scale="small", device="cuda"),
+    "medusa_232": lambda: _medusa(),
+    "medusa_232_greedy": lambda: _medusa(tau=0.0),
+    "medusa_f32_hot": lambda: _medusa(V=1999, dtype="f32", tau=1.6),
+    "specinfer_321": lambda: _specinfer(),
+    "specinfer_bf16_ragged": lambda: _specinfer(V=517, dtype="bf16", tau=1.0),
+    "probs_f32": lambda: W.chain_workload(B=5, gamma=4, V=2003, dtype="f32", H_q=4, H_kv=4, d=64,
+                                          prefix=40, tau=1.0, target_std=2.0, noise_std=1.0,
+                                          device="cuda", draft_kind=W.DRAFT_PROBS),
+    "probs_bf16": lambda: W.chain_workload(B=5, gamma=4, V=2003, dtype="bf16", H_q=4, H_kv=4,
+                                           d=128, prefix=40, tau=1.0, target_std=2.0,
+                                           noise_std=1.0, device="cuda",
+                                           draft_kind=W.DRAFT_PROBS),
+    "single_token_tiny_vocab": lambda: W.chain_workload(B=3, gamma=0, V=13, dtype="bf16", H_q=8,
+                                                        H_kv=2, d=128, prefix=17, tau=1.0,
+                                                        target_std=3.0, noise_std=1.0,
+                                                        device="cuda", T_max=4),
+    "many_requests": lambda: W.chain_workload(B=40, gamma=5, V=1001, dtype="bf16", H_q=4, H_kv=4,
+                                              d=128, prefix=20, tau=1.0, target_std=2.0,
+                                              noise_std=1.0, device="cuda"),
+}
+
+
+def _verify(w, rule):
+    snap = PU.snapshot(w)
+    step = VerifyStep(w, sibling_rule=rule)
+    step.tree_build()
+    step.verify()
+    torch.cuda.synchronize()
+    return step, snap
+
+
+@pytest.mark.parametrize("name", sorted(WORKLOADS))
+def test_verify_paths_against_oracle(name, path):
+    w = WORKLOADS[name]()
+    step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL)
+    PU.check_verify(w, step, PU.oracle_verify(w, snap))
+
+
+@pytest.mark.parametrize("name", ["medusa_232", "specinfer_321"])
+def test_independent_rule_paths(name, path):
+    w = WORKLOADS[name]()
+    step, snap = _verify(w, B.SPEC_SIBLING_INDEPENDENT)
+    PU.check_verify(w, step, PU.oracle_verify(w, snap, B.SPEC_SIBLING_INDEPENDENT))
+
+
+def test_both_forms_agree():
+    # the two forms on the same inputs: every request's outputs are equal unless the oracle
+    # itself puts one of its decisions within the fp32 band
+    for name in ("medusa_232", "specinfer_321", "chain_bf16", "many_requests"):
+        w = WORKLOADS[name]()
+        outs = {}
+        for p in ("cluster", "split"):
+            B.spec_verify_set_path(PATHS[p])
+            try:
+                step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL)
+            finally:
+                B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+            outs[p] = {k: PU.np_(getattr(step, k)).copy()
+                       for k in ("out_tokens", "out_len", "path", "n_acc", "rejections")}
+        orc = PU.oracle_verify(w, snap)
+        for r in range(w.B):
+            same = all(np.array_equal(outs["cluster"][k][r], outs["split"][k][r]) for k in outs["split"])
+            if not same:
+                events = orc["events"][r]
+                near = any((e[0] == "test" and abs(e[4] - e[3]) < PU.BAND) or
+                           (e[0] == "sample" and e[3] < PU.BAND) for e in events)
+                assert near, (name, r)
+
+
+def test_auto_takes_the_cluster_form_when_it_fits():
+    # the one-launch form never touches the statistics workspace; the two-launch form fills it
+    w = WORKLOADS["chain_bf16"]()
+    step = VerifyStep(w)
+    step.tree_build()
+    for p, touched in (("cluster", False), ("split", True)):
+        step.ver_ws.fill_(0xA5)
+        B.spec_verify_set_path(PATHS[p])
+        try:
+            step.verify()
+            torch.cuda.synchronize()
+        finally:
+            B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+        assert bool((step.ver_ws != 0xA5).any()) == touched, p
+    # a tree of more than 32 nodes always takes the two-launch form
+    w = W.make_config(3, scale="small", device="cuda")
+    step = VerifyStep(w)
+    step.tree_build()
+    step.ver_ws.fill_(0xA5)
+    step.verify()
+    torch.cuda.synchronize()
+    assert bool((step.ver_ws != 0xA5).any())
+
+
+def test_data_errors_both_forms(path):
+    # a bad draft row, a bad token and a bad parent: flagged per request, outputs cleared, the
+    # other requests verified as usual
+    w = _medusa(B_=5)
+    no = w.node_offset.cpu().numpy()
+    internal = [i for i in range(no[1] - no[0]) if int(w.draft_row[no[0] + i]) >= 0]
+    w.draft_row[no[0] + internal[1]] = w.R + 3
+    w.tokens[no[1] + 4] = -2
+    snap = PU.snapshot(w)
+    step = VerifyStep(w)
+    step.tree_build()
+    step.verify()
+    torch.cuda.synchronize()
+    st = PU.np_(step.req_status)
+    assert st[0] & B.REQ_BITS["BAD_DRAFT_ROW"]
+    assert st[1] & B.REQ_BITS["BAD_TOKEN"]
+    PU.check_verify(w, step, PU.oracle_verify(w, snap))

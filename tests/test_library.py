@@ -138,3 +138,10 @@ def test_draft_tree_host_validation(lib):
                                       1000, 1.0, 0, None, None) == B.SPEC_ERR_INVALID_ARG  # ld < V
     assert lib.spec_echo_select_pack(ctypes.byref(pool), 64, fake, fake, fake, fake, fake, None,
                                      fake, 16, None) == B.SPEC_ERR_INVALID_ARG   # small workspace
+
+
+def test_verify_path_switch(lib):
+    assert lib.spec_verify_set_path(B.SPEC_VERIFY_PATH_SPLIT) == B.SPEC_OK
+    assert lib.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO) == B.SPEC_OK
+    for bad in (-1, 2, 7):
+        assert lib.spec_verify_set_path(bad) == B.SPEC_ERR_INVALID_ARG
