@@ -57,6 +57,15 @@ WORKLOADS = {
     "many_requests": lambda: W.chain_workload(B=40, gamma=5, V=1001, dtype="bf16", H_q=4, H_kv=4,
                                               d=128, prefix=20, tau=1.0, target_std=2.0,
                                               noise_std=1.0, device="cuda"),
+    # more clusters than the GPU holds at once: several waves
+    "several_waves": lambda: W.chain_workload(B=200, gamma=3, V=517, dtype="bf16", H_q=4,
+                                              H_kv=4, d=128, prefix=20, tau=1.0, target_std=2.0,
+                                              noise_std=1.0, device="cuda"),
+    # a 13-token vocabulary leaves most CTAs of a cluster without a slice
+    "tiny_vocab_chain": lambda: W.chain_workload(B=4, gamma=4, V=13, dtype="bf16", H_q=4, H_kv=4,
+                                                 d=128, prefix=17, tau=1.0, target_std=1.0,
+                                                 noise_std=2.0, device="cuda"),
+    "tiny_vocab_tree": lambda: _medusa(V=11, tau=0.8),
 }
 
 
@@ -132,8 +141,8 @@ def test_auto_takes_the_cluster_form_when_it_fits():
 
 
 def test_data_errors_both_forms(path):
-    # a bad draft row, a bad token and a bad parent: flagged per request, outputs cleared, the
-    # other requests verified as usual
+    # a bad draft row and a bad token: flagged per request, outputs cleared, the other requests
+    # verified as usual
     w = _medusa(B_=5)
     no = w.node_offset.cpu().numpy()
     internal = [i for i in range(no[1] - no[0]) if int(w.draft_row[no[0] + i]) >= 0]
