@@ -121,6 +121,23 @@ def attention_bytes(w):
     return kv + q_o + w.N * w.H_q * 4
 
 
+def step_bytes(w, step):
+    """Algorithmic bytes of one whole step: the attention launch's, the verification's (every
+    internal node's target row and every draft row an internal node names read once, plus one
+    target and one draft row per request for the final draw) and the compaction's (K and V of
+    every moved slot read and written, per layer); the tree build's few bytes per node are left
+    out.  The moved slots are read from the step's own slot map after a round."""
+    es = 2 if w.dtype == "bf16" else 4
+    internal = step.is_internal.cpu().numpy().astype(bool)
+    rows = int(internal.sum())
+    drows = len(set(w.draft_row.cpu().numpy()[internal].tolist())) if w.tau > 0 else 0
+    ver = (rows + drows + w.B * (2 if w.tau > 0 else 1)) * w.V * es
+    sm = step.slot_map.cpu().numpy()
+    moved = int(((sm[..., 0] >= 0) & (sm[..., 0] != sm[..., 1])).sum())
+    comp = moved * 2 * 2 * w.H_kv * w.d * es * w.k_cache.shape[0]
+    return attention_bytes(w) + ver + comp
+
+
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -529,6 +546,7 @@ def main():
         return
     peak, peak_kind = measured_peaks()
     abytes = attention_bytes(w)
+    sbytes = step_bytes(w, step)
     achieved = abytes / t_attn / 1e9
     out_len = step.out_len.cpu()
     roofline = {"bound": "hbm", "kernel": "spec_tree_attention (tcgen05 main + merge)",
@@ -591,7 +609,11 @@ def main():
         "data": "synthetic", "config": workload_description(w, args.workload),
         "requests_per_s": round(world * w.B * args.steps / t_total, 1),
         "graph": {"ms_per_step": round(1e3 * t_graph, 4),
-                  "value": round(job_throughput(tokens_per_step, 1, t_graph, world), 1)},
+                  "value": round(job_throughput(tokens_per_step, 1, t_graph, world), 1),
+                  "step_roofline": {"bound": "hbm", "algorithmic_bytes": sbytes,
+                                    "achieved": round(sbytes / t_graph / 1e9, 1), "peak": peak,
+                                    "unit": "GB/s",
+                                    "frac": round(sbytes / t_graph / 1e9 / peak, 4)}},
         "accepted_tokens_per_request": round(float(out_len.float().mean()), 3),
         "roofline": roofline, "cpu_baseline": cb, "e2e": e2e, "next": next_rows,
         "clocks": clocks, "gpu_launches": KERNELS_PER_STEP * args.steps,
