@@ -32,8 +32,8 @@ sys.path.insert(0, ROOT)
 DEFAULT_WORKLOAD = 2
 # kernels of the library launched by one step of the default workload: tree_build_kernel,
 # attn_tc_small_kernel, attn_merge_kernel, verify_cluster_kernel (the one-launch verification
-# that trees of up to 32 nodes take), kv_compact_kernel
-KERNELS_PER_STEP = 5
+# that trees of up to 32 nodes take, with the KV compaction in the same launch)
+KERNELS_PER_STEP = 4
 FLUSH_BYTES = 256 << 20
 
 

@@ -341,6 +341,19 @@ typedef struct {
 spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * spec_verify_compact -- spec_verify followed by spec_kv_compact, in one call: same inputs,
+ * outputs and results as the two calls in that order.  When the verification takes its
+ * one-launch form (see spec_verify_set_path) the compaction runs inside that launch (one
+ * kernel for both); otherwise spec_kv_compact is launched after it.  The compaction reads the
+ * verification's own results, so c->path, c->n_acc, c->req_status must be v->path, v->n_acc,
+ * v->req_status, with c->B == v->B and c->max_path == v->max_path.
+ * Errors: as spec_verify and spec_kv_compact, plus SPEC_ERR_INVALID_ARG when c is NULL or does
+ * not match v as above.
+ * ------------------------------------------------------------------------------------------ */
+spec_status_t spec_verify_compact(const spec_verify_params* v, const spec_compact_params* c,
+                                  void* workspace, size_t ws_bytes, spec_stream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Building the draft tree on the device  [TREE 草稿树的生成, 动态草稿长度]
  * EAGLE-2 expands, level by level, only the K most probable leaves of the newest level (a
  * leaf's score is the sum of the draft log-probabilities along its path, log q =

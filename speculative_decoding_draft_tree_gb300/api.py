@@ -123,11 +123,16 @@ class VerifyStep:
     def compact(self, stream=None):
         B.spec_kv_compact(self.comp, stream)
 
+    def verify_compact(self, stream=None):
+        """verify() then compact() as one call (spec_verify_compact: one kernel for both when
+        the verification takes its one-launch form)."""
+        B.spec_verify_compact(self.ver, self.comp, self.ver_ws, stream)
+
     def run(self, stream=None):
-        """One full round (4 library calls, 1 + 2 + 1 + 1 kernel launches on the stream -- the
-        verification takes 2 launches instead of 1 for trees of more than 32 nodes; with
-        enable_rope, the tree build and the rotary step share one launch, or run as two calls
-        when fused=False)."""
+        """One full round: tree build, attention, then verification and compaction as one call
+        (1 + 2 + 1 kernel launches on the stream; the verification and compaction take 2 + 1
+        launches instead for trees of more than 32 nodes); with enable_rope, the tree build and
+        the rotary step share one launch, or run as two calls when fused=False."""
         if self.rope_p is not None and self.rope_fused:
             self.tree_build_rope(stream)
         else:
@@ -135,8 +140,7 @@ class VerifyStep:
             if self.rope_p is not None:
                 self.rope(stream)
         self.attention(stream)
-        self.verify(stream)
-        self.compact(stream)
+        self.verify_compact(stream)
 
     def capture_graph(self) -> "torch.cuda.CUDAGraph":
         """One round (run()) captured as a CUDA graph; replay() re-runs it on the same buffers.

@@ -24,7 +24,8 @@ EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_k
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
            "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
-           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_set_path"]
+           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_set_path",
+           "spec_verify_compact"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -126,6 +127,10 @@ def load_library(build_if_missing=False):
     lib.spec_debug_draft_copy_stall.argtypes = [_i32]
     lib.spec_verify_set_path.restype = st
     lib.spec_verify_set_path.argtypes = [_i32]
+    lib.spec_verify_compact.restype = st
+    lib.spec_verify_compact.argtypes = [ctypes.POINTER(SpecVerifyParams),
+                                        ctypes.POINTER(SpecCompactParams), _vp, ctypes.c_size_t,
+                                        _vp]
     lib.spec_echo_workspace_size.restype = ctypes.c_size_t
     lib.spec_echo_workspace_size.argtypes = [_i32, _i32]
     lib.spec_echo_select_pack.restype = st
@@ -337,6 +342,16 @@ def spec_verify_noalloc(params, stream=None):
     and race."""
     code = load_library().spec_verify_noalloc(ctypes.byref(params), _stream(stream))
     _check(code, "spec_verify_noalloc")
+
+
+def spec_verify_compact(vparams, cparams, workspace, stream=None):
+    """spec_verify then spec_kv_compact in one call (one kernel when the verification takes its
+    one-launch form); cparams must name vparams' path, n_acc and req_status."""
+    lib = load_library()
+    wsz = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    code = lib.spec_verify_compact(ctypes.byref(vparams), ctypes.byref(cparams), _ptr(workspace),
+                                   wsz, _stream(stream))
+    _check(code, "spec_verify_compact")
 
 
 def spec_verify_set_path(path):

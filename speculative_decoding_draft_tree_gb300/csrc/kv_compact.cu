@@ -16,26 +16,12 @@
 // every load precedes every store, positions of different chunks are disjoint, and groups
 // follow each other in increasing d).  Slot offsets come from shared memory.
 #include "common.cuh"
+#include "kv_compact.cuh"
 
 namespace spec {
 
 constexpr int kCompactThreads = 512;
 constexpr int kCompactSteps = 8;   // moving steps staged per group (K and V: 2 vectors each)
-
-struct CompactDev {
-  char* k;
-  char* v;
-  int64_t layer_stride_bytes;
-  const int32_t* block_table;
-  const int32_t* prefix_len;
-  const int32_t* path;
-  const int32_t* n_acc;
-  int32_t* req_status;
-  int32_t* new_kv_len;
-  int32_t* slot_map;
-  int32_t* blocks_in_use;
-  int32_t H_kv, row_bytes, bs, num_blocks, max_blocks, max_path;
-};
 
 __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(CompactDev a) {
   pdl_wait();
@@ -154,8 +140,7 @@ __global__ void __launch_bounds__(kCompactThreads) kv_compact_kernel(CompactDev 
 
 }  // namespace spec
 
-extern "C" spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream) {
-  using namespace spec;
+spec_status_t spec::make_compact_dev(const spec_compact_params* p, CompactDev* d) {
   if (!p) return SPEC_ERR_INVALID_ARG;
   if (p->dtype != SPEC_F32 && p->dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
   if (p->B < 1 || p->H_kv < 1 || p->head_dim < 1 || p->block_size < 1 || p->num_blocks < 1 ||
@@ -171,24 +156,32 @@ extern "C" spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stre
       !p->new_kv_len || !p->slot_map || !p->blocks_in_use)
     return SPEC_ERR_INVALID_ARG;
   if (p->num_layers > 65535) return SPEC_ERR_UNSUPPORTED;
+  d->k = static_cast<char*>(p->k_cache);
+  d->v = static_cast<char*>(p->v_cache);
+  d->layer_stride_bytes = p->layer_stride * es;
+  d->block_table = p->block_table;
+  d->prefix_len = p->prefix_len;
+  d->path = p->path;
+  d->n_acc = p->n_acc;
+  d->req_status = p->req_status;
+  d->new_kv_len = p->new_kv_len;
+  d->slot_map = p->slot_map;
+  d->blocks_in_use = p->blocks_in_use;
+  d->H_kv = p->H_kv;
+  d->row_bytes = row_bytes;
+  d->bs = p->block_size;
+  d->num_blocks = p->num_blocks;
+  d->max_blocks = p->max_blocks_per_req;
+  d->max_path = p->max_path;
+  d->num_layers = p->num_layers;
+  return SPEC_OK;
+}
+
+extern "C" spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream) {
+  using namespace spec;
   CompactDev d;
-  d.k = static_cast<char*>(p->k_cache);
-  d.v = static_cast<char*>(p->v_cache);
-  d.layer_stride_bytes = p->layer_stride * es;
-  d.block_table = p->block_table;
-  d.prefix_len = p->prefix_len;
-  d.path = p->path;
-  d.n_acc = p->n_acc;
-  d.req_status = p->req_status;
-  d.new_kv_len = p->new_kv_len;
-  d.slot_map = p->slot_map;
-  d.blocks_in_use = p->blocks_in_use;
-  d.H_kv = p->H_kv;
-  d.row_bytes = row_bytes;
-  d.bs = p->block_size;
-  d.num_blocks = p->num_blocks;
-  d.max_blocks = p->max_blocks_per_req;
-  d.max_path = p->max_path;
+  const spec_status_t st = make_compact_dev(p, &d);
+  if (st != SPEC_OK) return st;
   dim3 grid(p->B, p->num_layers);
   return launch_result(
       launch_pdl(kv_compact_kernel, grid, dim3(kCompactThreads), 0, (cudaStream_t)stream, d));

@@ -38,6 +38,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "kv_compact.cuh"
 #include "verify_cluster.cuh"
 
 namespace spec {
@@ -1056,8 +1057,12 @@ size_t spec_verify_workspace_size(const spec_verify_params* p) {
   return spec::verify_ws_layout(p->N, p->R, multi ? p->B : 0, p->V).total;
 }
 
-spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
-                          spec_stream_t stream) {
+}  // extern "C"
+
+// spec_verify, and with c != nullptr spec_verify_compact: the compaction runs inside the
+// one-launch verification when the call takes that form, else as spec_kv_compact after it.
+static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact_params* c,
+                                 void* workspace, size_t ws_bytes, spec_stream_t stream) {
   using namespace spec;
   if (!p) return SPEC_ERR_INVALID_ARG;
   if (p->B < 1 || p->N < 0 || p->R < 0 || p->V < 1 || p->T_max < 1 ||
@@ -1110,9 +1115,20 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
   d.dstat = reinterpret_cast<RowStat*>(ws + lay.dstat);
   d.rbuf = multi ? reinterpret_cast<float*>(ws + lay.rbuf) : nullptr;
   d.rld = lay.rld;
+  CompactDev cdev = {};
+  if (c) {
+    const spec_status_t cst = make_compact_dev(c, &cdev);
+    if (cst != SPEC_OK) return cst;
+    // the compaction reads the verification's own path, counts and status
+    if (c->B != p->B || c->path != p->path || c->n_acc != p->n_acc ||
+        c->req_status != p->req_status || c->max_path != p->max_path)
+      return SPEC_ERR_INVALID_ARG;
+  }
   cudaStream_t s = (cudaStream_t)stream;
   if (!multi && g_verify_path.load(std::memory_order_relaxed) == SPEC_VERIFY_PATH_AUTO) {
     ClusterVerifyArgs ca;
+    ca.compact = c ? 1 : 0;
+    ca.cd = cdev;
     ca.target = p->target; ca.draft = p->draft; ca.tld = p->target_ld; ca.dld = p->draft_ld;
     ca.B = p->B; ca.N = p->N; ca.R = p->R; ca.V = p->V; ca.T_max = p->T_max;
     ca.max_path = p->max_path;
@@ -1126,18 +1142,35 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
     if (verify_cluster_fits(ca, int(tes), int(des)))
       return launch_result(launch_verify_cluster(ca, int(tes), int(des), s));
   }
+  spec_status_t st;
   if (multi) {
-    if (p->logits_dtype == SPEC_BF16) {
-      if (d.probs) return launch_verify<__nv_bfloat16, float, true>(d, s);
-      return launch_verify<__nv_bfloat16, __nv_bfloat16, true>(d, s);
-    }
-    return launch_verify<float, float, true>(d, s);
+    if (p->logits_dtype == SPEC_BF16)
+      st = d.probs ? launch_verify<__nv_bfloat16, float, true>(d, s)
+                   : launch_verify<__nv_bfloat16, __nv_bfloat16, true>(d, s);
+    else
+      st = launch_verify<float, float, true>(d, s);
+  } else {
+    if (p->logits_dtype == SPEC_BF16)
+      st = d.probs ? launch_verify<__nv_bfloat16, float, false>(d, s)
+                   : launch_verify<__nv_bfloat16, __nv_bfloat16, false>(d, s);
+    else
+      st = launch_verify<float, float, false>(d, s);
   }
-  if (p->logits_dtype == SPEC_BF16) {
-    if (d.probs) return launch_verify<__nv_bfloat16, float, false>(d, s);
-    return launch_verify<__nv_bfloat16, __nv_bfloat16, false>(d, s);
-  }
-  return launch_verify<float, float, false>(d, s);
+  if (st != SPEC_OK || !c) return st;
+  return spec_kv_compact(c, stream);
+}
+
+extern "C" {
+
+spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
+                          spec_stream_t stream) {
+  return verify_impl(p, nullptr, workspace, ws_bytes, stream);
+}
+
+spec_status_t spec_verify_compact(const spec_verify_params* v, const spec_compact_params* c,
+                                  void* workspace, size_t ws_bytes, spec_stream_t stream) {
+  if (!c) return SPEC_ERR_INVALID_ARG;
+  return verify_impl(v, c, workspace, ws_bytes, stream);
 }
 
 }  // extern "C"

@@ -50,6 +50,7 @@ constexpr int kMaxT = 32;                      // nodes per request (one lane pe
 constexpr int kMaxRows = 2 * kMaxT;
 constexpr int kParts = 4;                      // warps per row slice in the statistics
 constexpr int kMaxDynSmem = 200 * 1024;        // row slices per CTA
+constexpr int kCompactGroup = 4;               // moving steps a thread loads before storing
 }  // namespace vcl
 
 struct ClSmem {
@@ -79,6 +80,10 @@ struct ClSmem {
   double C, Nk;                                 // sibling residual state (thread 0)
   float Cf;
   int32_t decision, bad, nint, found;
+  // KV compaction in the same launch: the moving steps and their slot offsets
+  int32_t cmove[vcl::kMaxT];
+  long long csrc[vcl::kMaxT], cdst[vcl::kMaxT];
+  int32_t cnmove, cbad;
 };
 
 __device__ __forceinline__ int cluster_rank() {
@@ -383,6 +388,114 @@ __device__ ClPass cl_pass(const TT* trow, const TD* drow, int nu, int u0, int pe
   return res;
 }
 
+// The KV compaction of spec_kv_compact for request r, run by every CTA of its cluster after
+// the walk (path = sh.path[0 .. npath - 1]): the same validation (BAD_PARENT / BAD_BLOCK, the
+// request rolled back), then slot P + d receives slot P + path[d] for every layer, KV head, K
+// and V.  The CTAs split the 16-byte positions of the rows (layer, head, offset); each thread
+// loads its position of every moving step of a group of kCompactGroup before storing any, so, with
+// path[d] >= d and groups taken in increasing d, every source is read before it is overwritten
+// (as in spec_kv_compact).  Rank 0 writes the slot map and the lengths.
+__device__ void cl_compact(const ClusterVerifyArgs& a, ClSmem& sh, int r, int rank, int ncl,
+                           int P, int npath) {
+  using namespace vcl;
+  const CompactDev& c = a.cd;
+  const int tid = threadIdx.x;
+  const int na = npath - 1;
+  int32_t* sm_row = c.slot_map + size_t(r) * c.max_path * 2;
+  const int32_t* trow = c.block_table + size_t(r) * c.max_blocks;
+  if (tid == 0) sh.cbad = 0;
+  __syncthreads();
+  const bool ok = na >= 0 && na < c.max_path && P >= 0;
+  if (ok) {
+    for (int d = tid; d <= na; d += kThreads) {
+      const int pd = sh.path[d];
+      bool good = (d == 0) ? (pd == 0) : (pd >= d);
+      const int lsb = (P + pd) / c.bs, ldb = (P + d) / c.bs;
+      good = good && lsb < c.max_blocks && ldb < c.max_blocks;
+      int flag = good ? 0 : SPEC_REQ_BAD_PARENT;
+      if (good) {
+        const int sb = trow[lsb], db = trow[ldb];
+        if (sb < 0 || sb >= c.num_blocks || db < 0 || db >= c.num_blocks) flag = SPEC_REQ_BAD_BLOCK;
+      }
+      if (flag) atomicOr(&sh.cbad, flag);
+    }
+  }
+  __syncthreads();
+  if (!ok || sh.cbad) {
+    if (rank == 0) {
+      if (tid == 0 && ok) atomicOr(&a.req_status[r], sh.cbad);
+      for (int k = tid; k < c.max_path; k += kThreads) { sm_row[2 * k] = -1; sm_row[2 * k + 1] = -1; }
+      if (tid == 0) {
+        c.new_kv_len[r] = P;
+        c.blocks_in_use[r] = (P + c.bs - 1) / c.bs;
+      }
+    }
+    return;
+  }
+  const size_t head_stride = size_t(c.bs) * c.row_bytes;
+  const size_t block_stride = size_t(c.H_kv) * head_stride;
+  if (tid == 0) {
+    int n = 0;
+    for (int d = 1; d <= na; ++d)
+      if (sh.path[d] != d) sh.cmove[n++] = d;
+    sh.cnmove = n;
+  }
+  __syncthreads();
+  const int nmove = sh.cnmove;
+  for (int q = tid; q < nmove; q += kThreads) {
+    const int d = sh.cmove[q];
+    const int src = P + sh.path[d], dst = P + d;
+    sh.csrc[q] = (long long)(size_t(trow[src / c.bs]) * block_stride + size_t(src % c.bs) * c.row_bytes);
+    sh.cdst[q] = (long long)(size_t(trow[dst / c.bs]) * block_stride + size_t(dst % c.bs) * c.row_bytes);
+  }
+  __syncthreads();
+  if (nmove > 0) {
+    const int vpr = c.row_bytes / 16;
+    const long long per_layer = (long long)c.H_kv * vpr;
+    const long long total = per_layer * c.num_layers;
+    const long long w0 = total * rank / ncl, w1 = total * (rank + 1) / ncl;
+    for (long long w = w0 + tid; w < w1; w += kThreads) {
+      const int layer = int(w / per_layer);
+      const int rem = int(w - layer * per_layer);
+      const int h = rem / vpr;
+      const size_t in_row = size_t(h) * head_stride + size_t(rem - h * vpr) * 16;
+      char* kb = c.k + layer * c.layer_stride_bytes;
+      char* vb = c.v + layer * c.layer_stride_bytes;
+      for (int g0 = 0; g0 < nmove; g0 += kCompactGroup) {
+        const int gs = min(kCompactGroup, nmove - g0);
+        uint4 kv[kCompactGroup][2];
+#pragma unroll
+        for (int q = 0; q < kCompactGroup; ++q) {
+          if (q < gs) {
+            const size_t o = size_t(sh.csrc[g0 + q]) + in_row;
+            kv[q][0] = *reinterpret_cast<const uint4*>(kb + o);
+            kv[q][1] = *reinterpret_cast<const uint4*>(vb + o);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kCompactGroup; ++q) {
+          if (q < gs) {
+            const size_t o = size_t(sh.cdst[g0 + q]) + in_row;
+            *reinterpret_cast<uint4*>(kb + o) = kv[q][0];
+            *reinterpret_cast<uint4*>(vb + o) = kv[q][1];
+          }
+        }
+      }
+    }
+  }
+  if (rank == 0) {
+    for (int k = tid; k < c.max_path; k += kThreads) {
+      const bool in = k <= na;
+      sm_row[2 * k] = in ? P + sh.path[k] : -1;
+      sm_row[2 * k + 1] = in ? P + k : -1;
+    }
+    if (tid == 0) {
+      c.new_kv_len[r] = P + na + 1;
+      c.blocks_in_use[r] = (P + na + 1 + c.bs - 1) / c.bs;
+    }
+  }
+}
+
 template <typename TT, typename TD>
 __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(ClusterVerifyArgs a) {
   using namespace vcl;
@@ -402,6 +515,7 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
   const TT* target = reinterpret_cast<const TT*>(a.target);
   const TD* draft = reinterpret_cast<const TD*>(a.draft);
   const int st0 = a.req_status[r];
+  const int P = a.compact ? a.cd.prefix_len[r] : 0;
   const int o = a.node_offset[r];
   const int T = a.node_offset[r + 1] - o;
   const bool range_ok = o >= 0 && T >= 1 && T <= a.T_max && o + T <= a.N;
@@ -414,6 +528,14 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
         a.out_len[r] = 0;
         a.n_acc[r] = -1;
         if (a.rejections) a.rejections[r] = 0;
+      }
+      if (a.compact) {   // the whole tree rolled back, as spec_kv_compact does for it
+        int32_t* sm_row = a.cd.slot_map + size_t(r) * a.cd.max_path * 2;
+        for (int k = tid; k < a.cd.max_path; k += kThreads) { sm_row[2 * k] = -1; sm_row[2 * k + 1] = -1; }
+        if (tid == 0) {
+          a.cd.new_kv_len[r] = P;
+          a.cd.blocks_in_use[r] = (P + a.cd.bs - 1) / a.cd.bs;
+        }
       }
     }
   };
@@ -765,6 +887,7 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
   } else if (owner == rank && tid == 0) {
     tok_row[npath - 1] = final_tok;
   }
+  if (a.compact) cl_compact(a, sh, r, rank, ncl, P, npath);
   // no CTA leaves while another may still read its shared memory
   if (!arrived) cluster_arrive();
   cluster_wait();

@@ -2,6 +2,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "kv_compact.cuh"
 
 namespace spec {
 
@@ -25,6 +26,10 @@ struct ClusterVerifyArgs {
   int32_t* path;
   int32_t* n_acc;
   int32_t* rejections;
+  // KV compaction in the same launch (spec_verify_compact): compact != 0; cd.path, cd.n_acc,
+  // cd.req_status and cd.max_path are the verification's own
+  int32_t compact;
+  CompactDev cd;
   // set at launch
   int32_t per_units;          // 8-element vocabulary units held by each CTA of a cluster
   int32_t t_slice, d_slice;   // shared-memory bytes of one target / draft row slice

@@ -157,3 +157,72 @@ def test_data_errors_both_forms(path):
     assert st[0] & B.REQ_BITS["BAD_DRAFT_ROW"]
     assert st[1] & B.REQ_BITS["BAD_TOKEN"]
     PU.check_verify(w, step, PU.oracle_verify(w, snap))
+
+
+def _run_pair(make, fused):
+    w = make()
+    step = VerifyStep(w)
+    step.tree_build()
+    if fused:
+        step.verify_compact()
+    else:
+        step.verify()
+        step.compact()
+    torch.cuda.synchronize()
+    out = {k: PU.np_(getattr(step, k)).copy()
+           for k in ("req_status", "out_tokens", "out_len", "path", "n_acc", "new_kv_len",
+                     "slot_map", "blocks_in_use")}
+    out["k"] = w.k_cache.float().cpu().numpy()
+    out["v"] = w.v_cache.float().cpu().numpy()
+    return out
+
+
+def _bad_tree():
+    w = _medusa(B_=5)
+    no = w.node_offset.cpu().numpy()
+    w.tokens[no[2] + 3] = w.V + 1
+    P3 = int(w.prefix_len[3])
+    w.block_table[3, P3 // w.bs] = w.k_cache.shape[1] + 9   # a tree slot's block out of range
+    return w
+
+
+FUSED = {
+    "chain_2_layers": lambda: W.make_config(2, scale="small", device="cuda", num_layers=2),
+    "medusa_2_layers": lambda: W.medusa_workload(B=4, ks=(2, 3, 2), V=3001, dtype="bf16", H_q=4,
+                                                 H_kv=2, d=128, prefix=40, tau=1.0, device="cuda",
+                                                 num_layers=2),
+    "specinfer_f32": lambda: _specinfer(),
+    "greedy_tree": lambda: _medusa(tau=0.0),
+    "several_waves": WORKLOADS["several_waves"],
+    "data_errors": _bad_tree,
+    "tree_over_32_nodes": lambda: W.make_config(3, scale="small", device="cuda", num_layers=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FUSED))
+def test_verify_compact_equals_the_two_calls(name):
+    # spec_verify_compact (compaction inside the one-launch verification, or launched after the
+    # two-launch form) gives the same outputs and the same cache, byte for byte, as spec_verify
+    # followed by spec_kv_compact
+    a = _run_pair(FUSED[name], fused=False)
+    b = _run_pair(FUSED[name], fused=True)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    if name == "data_errors":
+        assert a["req_status"][2] & B.REQ_BITS["BAD_TOKEN"]
+        assert a["req_status"][3] & B.REQ_BITS["BAD_BLOCK"]
+    if name.startswith("medusa"):
+        # accepted paths that are not the identity: slots were moved
+        sm = a["slot_map"]
+        assert ((sm[..., 0] >= 0) & (sm[..., 0] != sm[..., 1])).any()
+
+
+def test_verify_compact_host_checks():
+    w = WORKLOADS["chain_bf16"]()
+    step = VerifyStep(w)
+    other = torch.empty_like(step.path)
+    bad = B.compact_params(w.k_cache, w.v_cache, w.block_table, w.prefix_len, other, step.n_acc,
+                           step.req_status, step.new_kv_len, step.slot_map, step.blocks_in_use,
+                           w.max_path)
+    with pytest.raises(B.SpecError):
+        B.spec_verify_compact(step.ver, bad, step.ver_ws)
