@@ -145,3 +145,37 @@ def test_verify_path_switch(lib):
     assert lib.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO) == B.SPEC_OK
     for bad in (-1, 2, 7):
         assert lib.spec_verify_set_path(bad) == B.SPEC_ERR_INVALID_ARG
+
+
+def _fake_verify_and_compact():
+    fake = 0x100000   # 256-byte aligned, never dereferenced: validation fails first
+    v = B.SpecVerifyParams()
+    v.logits_dtype, v.draft_kind, v.sibling_rule = B.SPEC_BF16, B.SPEC_DRAFT_LOGITS, 0
+    v.B, v.N, v.R, v.V, v.target_ld, v.draft_ld, v.T_max, v.max_path, v.tau = (
+        2, 12, 10, 32000, 32000, 32000, 6, 6, 1.0)
+    for f in ("target", "draft", "draft_row", "tokens", "parent", "node_offset", "depth",
+              "is_internal", "uniforms", "req_status", "out_tokens", "out_len", "path", "n_acc",
+              "rejections"):
+        setattr(v, f, fake)
+    c = B.SpecCompactParams()
+    c.dtype, c.B, c.H_kv, c.head_dim, c.block_size = B.SPEC_BF16, 2, 4, 128, 16
+    c.num_blocks, c.max_blocks_per_req, c.num_layers, c.max_path, c.layer_stride = 64, 32, 1, 6, 0
+    for f in ("k_cache", "v_cache", "block_table", "prefix_len", "path", "n_acc", "req_status",
+              "new_kv_len", "slot_map", "blocks_in_use"):
+        setattr(c, f, fake)
+    return v, c
+
+
+@pytest.mark.parametrize("change", [dict(path=0x200000), dict(n_acc=0x200000),
+                                    dict(req_status=0x200000), dict(B=3), dict(max_path=7),
+                                    dict(head_dim=100)])
+def test_verify_compact_host_validation(lib, change):
+    # the compaction must read the verification's own results; mismatches are refused before
+    # any CUDA call
+    v, c = _fake_verify_and_compact()
+    for k, val in change.items():
+        setattr(c, k, val)
+    ws, wsz = 0x100000, 1 << 30
+    assert lib.spec_verify_compact(ctypes.byref(v), ctypes.byref(c), ws, wsz,
+                                   None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify_compact(ctypes.byref(v), None, ws, wsz, None) == B.SPEC_ERR_INVALID_ARG
