@@ -1139,8 +1139,10 @@ static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact
     ca.uniforms = p->uniforms; ca.req_status = p->req_status; ca.out_tokens = p->out_tokens;
     ca.out_len = p->out_len; ca.path = p->path; ca.n_acc = p->n_acc;
     ca.rejections = p->rejections;
-    if (verify_cluster_fits(ca, int(tes), int(des)))
-      return launch_result(launch_verify_cluster(ca, int(tes), int(des), s));
+    if (verify_cluster_fits(ca, int(tes), int(des))) {
+      const cudaError_t e = launch_verify_cluster(ca, int(tes), int(des), s);
+      if (e != cudaErrorNotSupported) return launch_result(e);
+    }
   }
   spec_status_t st;
   if (multi) {

@@ -975,7 +975,7 @@ static cudaError_t launch_cl(ClusterVerifyArgs a, int tes, int des, cudaStream_t
       best_cost = cost;
     }
   }
-  if (best_n == 0) return cudaErrorInvalidConfiguration;
+  if (best_n == 0) return cudaErrorNotSupported;   // the caller takes the two-launch form
   long long per = 0;
   const long long smem = cluster_smem(a, best_n, tes, des, &per);
   a.per_units = int(per);

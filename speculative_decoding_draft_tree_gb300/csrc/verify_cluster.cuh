@@ -43,6 +43,8 @@ bool verify_cluster_fits(const ClusterVerifyArgs& a, int tes, int des);
 
 // Launches the call on `s` (cluster launch, programmatic dependent launch allowed) with the
 // number of CTAs per request (1..8) that runs the batch in the fewest waves per unit of work.
+// Returns cudaErrorNotSupported, having launched nothing, when the device holds no such
+// cluster at once (the caller then takes the two-launch form).
 cudaError_t launch_verify_cluster(const ClusterVerifyArgs& a, int tes, int des, cudaStream_t s);
 
 }  // namespace spec
