@@ -66,6 +66,11 @@ WORKLOADS = {
                                                  d=128, prefix=17, tau=1.0, target_std=1.0,
                                                  noise_std=2.0, device="cuda"),
     "tiny_vocab_tree": lambda: _medusa(V=11, tau=0.8),
+    # the largest trees the one-launch form takes: 32 nodes (a full warp of nodes)
+    "chain_32_nodes": lambda: W.chain_workload(B=3, gamma=31, V=2003, dtype="bf16", H_q=4, H_kv=4,
+                                               d=128, prefix=30, tau=1.0, target_std=1.0,
+                                               noise_std=0.3, device="cuda"),
+    "medusa_31_nodes": lambda: _medusa(V=1999, ks=(2, 2, 2, 2), B_=3),
 }
 
 
