@@ -26,6 +26,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -49,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-requests", type=int, default=0)
+    ap.add_argument("--clocks-csv", default=None,
+                    help="keep the nvidia-smi samples taken during the timed region in this file")
     return ap.parse_args()
 
 
@@ -145,10 +148,11 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, path=None):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = path or os.path.join(tempfile.gettempdir(),
+                                         f"spec_bench_clocks_{os.getpid()}_{gpu_index}.csv")
 
     def start(self):
         try:
@@ -389,7 +393,7 @@ def main():
     for _ in range(3):
         build_tree()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local_rank) if rank == 0 else None
+    sampler = ClockSampler(local_rank, args.clocks_csv) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
