@@ -179,3 +179,41 @@ def test_verify_compact_host_validation(lib, change):
     assert lib.spec_verify_compact(ctypes.byref(v), ctypes.byref(c), ws, wsz,
                                    None) == B.SPEC_ERR_INVALID_ARG
     assert lib.spec_verify_compact(ctypes.byref(v), None, ws, wsz, None) == B.SPEC_ERR_INVALID_ARG
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "spec_verify.h"
+
+/* a plain C caller: status strings, and entry points that refuse their arguments before any
+   CUDA call (so this runs without a GPU) */
+int main(void) {
+  int fails = 0;
+  if (strcmp(spec_status_string(SPEC_OK), "SPEC_OK") != 0) ++fails;
+  if (spec_verify(NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
+  if (spec_verify_compact(NULL, NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
+  if (spec_verify_set_path(7) != SPEC_ERR_INVALID_ARG) ++fails;
+  if (spec_verify_set_path(SPEC_VERIFY_PATH_AUTO) != SPEC_OK) ++fails;
+  if (spec_kv_compact(NULL, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
+  if (spec_tree_attention(NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
+  if (spec_verify_workspace_size(NULL) != 0) ++fails;
+  printf("%d\n", fails);
+  return fails;
+}
+"""
+
+
+def test_plain_c_caller_links_and_runs(tmp_path, lib):
+    # the boundary is a C ABI: a C program compiled against the header links the shared library
+    # and calls it (validation paths only, no GPU needed)
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(build.LIB_PATH)
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", build.INCLUDE, str(src),
+                         "-L", libdir, "-lspecverify", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "0", (run.stdout, run.stderr)
