@@ -264,7 +264,24 @@ typedef struct {
   int32_t* path;
   int32_t* n_acc;
   int32_t* rejections;           /* may be NULL */
+  int32_t verify_path;           /* SPEC_VERIFY_PATH_AUTO (0, the default) or _SPLIT, below */
 } spec_verify_params;
+
+/* verify_path -- no counterpart on the pages: which of the library's two forms of the same
+ * computation this call launches.
+ *   SPEC_VERIFY_PATH_AUTO (0, what a zero-initialised struct asks for): calls with the residual
+ *     or independent sibling rule (or tau == 0), T_max <= 32 and
+ *     T_max * S_t + (T_max - 1) * S_d <= 200 KiB run as one cluster launch (up to 8 CTAs per
+ *     request, each holding its share of the request's rows in shared memory), with
+ *     S_t / S_d = ceil(ceil(V / 8) / 8) * 8 * the target / draft element size (S_d = 0 at
+ *     tau == 0); every other call runs the two-launch form;
+ *   SPEC_VERIFY_PATH_SPLIT: always the two-launch form (a row statistics kernel, then a walk
+ *     kernel with one CTA per request).
+ * Both forms give the same outputs except where fp32 rounding of the vocabulary sums decides:
+ * a ratio test or a draw whose uniform lies within about 1e-6 of its boundary.  The choice is
+ * per call: the library keeps no process-wide setting.  Any other value: SPEC_ERR_INVALID_ARG. */
+#define SPEC_VERIFY_PATH_AUTO  0
+#define SPEC_VERIFY_PATH_SPLIT 1
 
 size_t spec_verify_workspace_size(const spec_verify_params* p);
 spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,
@@ -280,32 +297,15 @@ spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t w
  * Limits: N <= 32768 tree nodes and R <= 32768 draft rows per call; larger batches return
  * SPEC_ERR_UNSUPPORTED (use spec_verify with a caller-owned workspace instead).
  * The first call on each device looks up the array's device address with that device current;
- * make that first call before any stream capture.  All calls share the one array: calls whose
- * kernels overlap on the GPU (other streams, other host threads on the same device) race.
+ * make that first call before any stream capture.  Later calls look it up again unless their
+ * stream is being captured, so a device reset between calls is safe.  All calls share the one
+ * array: calls whose kernels overlap on the GPU (other streams, other host threads on the same
+ * device) race.  The multi-draft sibling rule with tau > 0 is refused (SPEC_ERR_UNSUPPORTED).
  * Errors: as spec_verify, plus SPEC_ERR_UNSUPPORTED for sizes beyond the limits above and
  * SPEC_ERR_CUDA if the address lookup fails.
  * ------------------------------------------------------------------------------------------ */
 spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_stream_t stream);
 
-/* ------------------------------------------------------------------------------------------
- * spec_verify_set_path -- no counterpart on the pages: which of the library's two forms of the
- * same computation spec_verify and spec_verify_noalloc launch, for every later call in the
- * process.
- *   SPEC_VERIFY_PATH_AUTO (the default): calls with the residual or independent sibling rule
- *     (or tau == 0), T_max <= 32 and T_max * S_t + (T_max - 1) * S_d <= 200 KiB run as one
- *     cluster launch (8 CTAs per request, each holding its eighth of the request's rows in
- *     shared memory), with S_t / S_d = ceil(ceil(V / 8) / 8) * 8 * the target / draft element
- *     size (S_d = 0 at tau == 0); every other call runs the two-launch form;
- *   SPEC_VERIFY_PATH_SPLIT: always the two-launch form (a row statistics kernel, then a walk
- *     kernel with one CTA per request).
- * Both forms give the same outputs except where fp32 rounding of the vocabulary sums decides:
- * a ratio test or a draw whose uniform lies within about 1e-6 of its boundary.
- * Not synchronised with calls in flight on other host threads.
- * Errors: SPEC_ERR_INVALID_ARG for any other value.
- * ------------------------------------------------------------------------------------------ */
-#define SPEC_VERIFY_PATH_AUTO  0
-#define SPEC_VERIFY_PATH_SPLIT 1
-spec_status_t spec_verify_set_path(int32_t path);
 
 /* ------------------------------------------------------------------------------------------
  * spec_kv_compact  [RATIO: KV Cache管理], [CSDN 4]
@@ -343,7 +343,7 @@ spec_status_t spec_kv_compact(const spec_compact_params* p, spec_stream_t stream
 /* ------------------------------------------------------------------------------------------
  * spec_verify_compact -- spec_verify followed by spec_kv_compact, in one call: same inputs,
  * outputs and results as the two calls in that order.  When the verification takes its
- * one-launch form (see spec_verify_set_path) the compaction runs inside that launch (one
+ * one-launch form (see verify_path above) the compaction runs inside that launch (one
  * kernel for both); otherwise spec_kv_compact is launched after it.  The compaction reads the
  * verification's own results, so c->path, c->n_acc, c->req_status must be v->path, v->n_acc,
  * v->req_status, with c->B == v->B and c->max_path == v->max_path.

@@ -41,9 +41,10 @@ def _packed(tensors: Dict[str, torch.Tensor], device, pin: bool = False):
 
 class VerifyStep:
     def __init__(self, w: Workload, sibling_rule: int = B.SPEC_SIBLING_RESIDUAL,
-                 with_lse: bool = True):
+                 with_lse: bool = True, verify_path: int = B.SPEC_VERIFY_PATH_AUTO):
         self.w = w
         self.sibling_rule = sibling_rule
+        self.verify_path = verify_path
         dev = w.target.device
         if dev.type != "cuda":
             raise ValueError("VerifyStep needs the workload on a CUDA device")
@@ -78,7 +79,7 @@ class VerifyStep:
                                    w.parent, w.node_offset, self.depth, self.is_internal,
                                    w.uniforms, w.tau, w.V, w.T_max, w.max_path, self.req_status,
                                    self.out_tokens, self.out_len, self.path, self.n_acc,
-                                   self.rejections, sibling_rule)
+                                   self.rejections, sibling_rule, verify_path)
         self.ver_ws = _ws(B.spec_verify_workspace_size(self.ver), dev)
         self.comp = B.compact_params(w.k_cache, w.v_cache, w.block_table, w.prefix_len,
                                      self.path, self.n_acc, self.req_status, self.new_kv_len,
@@ -219,7 +220,7 @@ class VerifyStep:
         for k, v in fresh.items():
             v.copy_(src[k])
         step = VerifyStep(dataclasses.replace(self.w, **fresh), self.sibling_rule,
-                          self.lse is not None)
+                          self.lse is not None, self.verify_path)
         step._in_pack = pack
         return step
 

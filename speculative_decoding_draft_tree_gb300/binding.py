@@ -24,8 +24,7 @@ EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_k
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
            "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
-           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_set_path",
-           "spec_verify_compact"]
+           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_compact"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -49,7 +48,7 @@ class SpecVerifyParams(ctypes.Structure):
                 ("draft_row", _vp), ("tokens", _vp), ("parent", _vp), ("node_offset", _vp),
                 ("depth", _vp), ("is_internal", _vp), ("uniforms", _vp), ("req_status", _vp),
                 ("out_tokens", _vp), ("out_len", _vp), ("path", _vp), ("n_acc", _vp),
-                ("rejections", _vp)]
+                ("rejections", _vp), ("verify_path", _i32)]
 
 
 class SpecCompactParams(ctypes.Structure):
@@ -125,8 +124,6 @@ def load_library(build_if_missing=False):
                                            _vp, _vp]
     lib.spec_debug_draft_copy_stall.restype = st
     lib.spec_debug_draft_copy_stall.argtypes = [_i32]
-    lib.spec_verify_set_path.restype = st
-    lib.spec_verify_set_path.argtypes = [_i32]
     lib.spec_verify_compact.restype = st
     lib.spec_verify_compact.argtypes = [ctypes.POINTER(SpecVerifyParams),
                                         ctypes.POINTER(SpecCompactParams), _vp, ctypes.c_size_t,
@@ -294,7 +291,8 @@ def spec_tree_attention(params, workspace, stream=None):
 
 def verify_params(target, draft, draft_kind, draft_row, tokens, parent, node_offset, depth,
                   is_internal, uniforms, tau, V, T_max, max_path, req_status, out_tokens,
-                  out_len, path, n_acc, rejections=None, sibling_rule=SPEC_SIBLING_RESIDUAL):
+                  out_len, path, n_acc, rejections=None, sibling_rule=SPEC_SIBLING_RESIDUAL,
+                  verify_path=SPEC_VERIFY_PATH_AUTO):
     _need(target, None, "target")
     _need(draft, None, "draft")
     for t, n in ((draft_row, "draft_row"), (tokens, "tokens"), (parent, "parent"),
@@ -322,6 +320,7 @@ def verify_params(target, draft, draft_kind, draft_row, tokens, parent, node_off
     p.req_status, p.out_tokens, p.out_len = req_status.data_ptr(), out_tokens.data_ptr(), out_len.data_ptr()
     p.path, p.n_acc = path.data_ptr(), n_acc.data_ptr()
     p.rejections = None if rejections is None else _need(rejections, torch.int32, "rejections").data_ptr()
+    p.verify_path = int(verify_path)
     return p
 
 
@@ -352,12 +351,6 @@ def spec_verify_compact(vparams, cparams, workspace, stream=None):
     code = lib.spec_verify_compact(ctypes.byref(vparams), ctypes.byref(cparams), _ptr(workspace),
                                    wsz, _stream(stream))
     _check(code, "spec_verify_compact")
-
-
-def spec_verify_set_path(path):
-    """Which form later spec_verify calls launch: SPEC_VERIFY_PATH_AUTO (one cluster launch when
-    the call fits it) or SPEC_VERIFY_PATH_SPLIT (always the rows + walk kernels)."""
-    _check(load_library().spec_verify_set_path(int(path)), "spec_verify_set_path")
 
 
 def compact_params(k_cache, v_cache, block_table, prefix_len, path, n_acc, req_status,

@@ -1398,12 +1398,11 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   d.ctas = ctas;
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf(float(kD));
   d.scale_log2 = scale * 1.4426950408889634f;
-  static std::once_flag attr_once;
-  std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    cudaFuncSetAttribute(attn_tc_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         attn_s::kSmemBytes);
-  });
+  static DeviceOnce raised_main, raised_small;
+  spec_status_t st = raise_dyn_smem_once(attn_tc_kernel, kSmemBytes, raised_main);
+  if (st == SPEC_OK)
+    st = raise_dyn_smem_once(attn_tc_small_kernel, attn_s::kSmemBytes, raised_small);
+  if (st != SPEC_OK) return st;
   cudaError_t le;
   if ((long long)p->T_max * G <= attn_s::kRows) {
     // every unit has at most 16 query rows: the transposed kernel with a 16-row Q box

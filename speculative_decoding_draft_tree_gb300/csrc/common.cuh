@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "spec_verify.h"
@@ -31,6 +32,38 @@ inline spec_status_t launch_status() {
 }
 
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// One bit per device (ids 0..63) recording that a per-device host-side step (a kernel attribute)
+// was done.  Safe to share between host threads: the steps it guards are idempotent, so two
+// threads that both find the bit clear both do the step and both set the bit.
+struct DeviceOnce {
+  std::atomic<uint64_t> done{0};
+  bool test(int dev) const {
+    return ((done.load(std::memory_order_acquire) >> dev) & 1u) != 0;
+  }
+  void set(int dev) { done.fetch_or(uint64_t(1) << dev, std::memory_order_release); }
+};
+
+// Raises `kernel`'s dynamic shared memory limit to `bytes` on the current device, once per
+// device (`once` belongs to the kernel).
+template <typename K>
+spec_status_t raise_dyn_smem_once(K kernel, size_t bytes, DeviceOnce& once) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) set_last_cuda_error(e);
+    return SPEC_ERR_CUDA;
+  }
+  if (!once.test(dev)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
+    if (e != cudaSuccess) {
+      set_last_cuda_error(e);
+      return SPEC_ERR_CUDA;
+    }
+    once.set(dev);
+  }
+  return SPEC_OK;
+}
 
 // Launch with programmatic stream serialization allowed: the kernel may be scheduled while the
 // previous kernel on the stream is still running (once every CTA of that kernel has executed

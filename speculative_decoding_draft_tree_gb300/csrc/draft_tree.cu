@@ -575,26 +575,6 @@ echo_pack_kernel(PoolDev p, const uint8_t* __restrict__ kept,
   }
 }
 
-// raise a kernel's dynamic shared memory limit, once per device
-template <typename Kern>
-static spec_status_t allow_dynamic_smem(Kern kernel, size_t bytes, bool* raised) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
-    if (e != cudaSuccess) set_last_cuda_error(e);
-    return SPEC_ERR_CUDA;
-  }
-  if (!raised[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
-    if (e != cudaSuccess) {
-      set_last_cuda_error(e);
-      return SPEC_ERR_CUDA;
-    }
-    raised[dev] = true;
-  }
-  return SPEC_OK;
-}
-
 }  // namespace spec
 
 extern "C" {
@@ -635,10 +615,10 @@ spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level,
   const float inv_tau = 1.0f / tau;
   const dim3 grid(unsigned(p.B) * unsigned(K));
   const size_t dyn = size_t(kStages) * kChunkBytes;
-  static bool raised_bf16[64] = {false}, raised_f32[64] = {false};
+  static DeviceOnce raised_bf16, raised_f32;
   const spec_status_t st = dtype == SPEC_BF16
-      ? allow_dynamic_smem(draft_topk_append_kernel<__nv_bfloat16>, dyn, raised_bf16)
-      : allow_dynamic_smem(draft_topk_append_kernel<float>, dyn, raised_f32);
+      ? raise_dyn_smem_once(draft_topk_append_kernel<__nv_bfloat16>, dyn, raised_bf16)
+      : raise_dyn_smem_once(draft_topk_append_kernel<float>, dyn, raised_f32);
   if (st != SPEC_OK) return st;
   cudaError_t e;
   if (dtype == SPEC_BF16)
@@ -686,9 +666,9 @@ spec_status_t spec_echo_select_pack(const spec_draft_pool* pool, int32_t K_max,
                                                    align_up(size_t(p.B) * size_t(p.cap), 256));
   if (p.B * p.cap > kEchoMaxKeys || p.B > kEchoMaxB) return SPEC_ERR_UNSUPPORTED;
   const size_t dyn = sizeof(uint64_t) * size_t(p.B) * size_t(p.cap);
-  static bool raised[64] = {false};
-  const spec_status_t st = allow_dynamic_smem(echo_select_kernel, sizeof(uint64_t) * kEchoMaxKeys,
-                                              raised);
+  static DeviceOnce raised;
+  const spec_status_t st = raise_dyn_smem_once(echo_select_kernel, sizeof(uint64_t) * kEchoMaxKeys,
+                                               raised);
   if (st != SPEC_OK) return st;
   cudaError_t e = launch_pdl(echo_select_kernel, dim3(1), dim3(kEchoThreads), dyn,
                              (cudaStream_t)stream, p, int(K_max), kept, kept_count);

@@ -12,7 +12,7 @@
 // Calls that fit it (residual or independent sibling rule, trees of at most 32 nodes, a
 // request's row slices within one CTA's shared memory) run as ONE cluster launch
 // (verify_cluster.cu: the rows of each request held on chip by a cluster of CTAs); the others,
-// and every call after spec_verify_set_path(SPEC_VERIFY_PATH_SPLIT), take the two-launch form.
+// and every call whose verify_path field is SPEC_VERIFY_PATH_SPLIT, take the two-launch form.
 // Two launches on the caller's stream:
 //   1. rows  (one CTA per internal node's target row and, for tau > 0 with draft logits, per
 //      draft row; 512 threads): ONE streaming read of the row with 16-byte
@@ -994,29 +994,6 @@ static VerifyWs verify_ws_layout(int N, int R, int multi_B = 0, int V = 0) {
   return w;
 }
 
-// raise a kernel's dynamic shared memory limit to the unit-sum array's maximum, once per device
-template <typename K>
-static spec_status_t allow_unit_sums(K kernel, bool* raised) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= 64) {
-    if (e != cudaSuccess) set_last_cuda_error(e);
-    return SPEC_ERR_CUDA;
-  }
-  if (!raised[dev]) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(sizeof(float) * kWalkMaxSmemUnits));
-    if (e != cudaSuccess) {
-      set_last_cuda_error(e);
-      return SPEC_ERR_CUDA;
-    }
-    raised[dev] = true;
-  }
-  return SPEC_OK;
-}
-
-// which form spec_verify launches (spec_verify_set_path)
-static std::atomic<int> g_verify_path{SPEC_VERIFY_PATH_AUTO};
 
 template <typename TT, typename TD, bool kMulti>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
@@ -1032,9 +1009,10 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
       if (e != cudaSuccess) return launch_result(e);
     }
   }
-  static bool raised_walk[64] = {false};
+  static DeviceOnce raised_walk;   // the unit-sum array's maximum, once per device
   if (dyn > 0) {
-    const spec_status_t st = allow_unit_sums(verify_walk_kernel<TT, TD, kMulti>, raised_walk);
+    const spec_status_t st = raise_dyn_smem_once(verify_walk_kernel<TT, TD, kMulti>,
+                                                 sizeof(float) * kWalkMaxSmemUnits, raised_walk);
     if (st != SPEC_OK) return st;
   }
   return launch_result(launch_pdl(verify_walk_kernel<TT, TD, kMulti>, dim3(d.B),
@@ -1044,12 +1022,6 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
 }  // namespace spec
 
 extern "C" {
-
-spec_status_t spec_verify_set_path(int32_t path) {
-  if (path != SPEC_VERIFY_PATH_AUTO && path != SPEC_VERIFY_PATH_SPLIT) return SPEC_ERR_INVALID_ARG;
-  spec::g_verify_path.store(path, std::memory_order_relaxed);
-  return SPEC_OK;
-}
 
 size_t spec_verify_workspace_size(const spec_verify_params* p) {
   if (!p) return 0;
@@ -1074,6 +1046,8 @@ static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact
     return SPEC_ERR_INVALID_ARG;
   if (p->sibling_rule != SPEC_SIBLING_RESIDUAL && p->sibling_rule != SPEC_SIBLING_INDEPENDENT &&
       p->sibling_rule != SPEC_SIBLING_MULTI_DRAFT)
+    return SPEC_ERR_INVALID_ARG;
+  if (p->verify_path != SPEC_VERIFY_PATH_AUTO && p->verify_path != SPEC_VERIFY_PATH_SPLIT)
     return SPEC_ERR_INVALID_ARG;
   if (!p->node_offset || !p->req_status || !p->out_tokens || !p->out_len || !p->path ||
       !p->n_acc)
@@ -1125,7 +1099,7 @@ static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact
       return SPEC_ERR_INVALID_ARG;
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (!multi && g_verify_path.load(std::memory_order_relaxed) == SPEC_VERIFY_PATH_AUTO) {
+  if (!multi && p->verify_path == SPEC_VERIFY_PATH_AUTO) {
     ClusterVerifyArgs ca;
     ca.compact = c ? 1 : 0;
     ca.cd = cdev;
@@ -1186,10 +1160,13 @@ spec_status_t spec_verify_compact(const spec_verify_params* v, const spec_compac
 // process exits.  It covers up to kNoAllocMaxNodes tree nodes and kNoAllocMaxDraftRows draft
 // rows; larger batches are refused with SPEC_ERR_UNSUPPORTED.
 // The first call on each device looks the array's device address up (cudaGetSymbolAddress)
-// with that device current; make that first call before any stream capture.  All calls share
-// the array: calls whose kernels overlap on the GPU (different streams, or different host
-// threads on the same device) race on it.  Every call writes the statistics it reads before
-// reading them, so the contents left by an earlier call do not matter.
+// with that device current; make that first call before any stream capture.  Later calls look
+// it up again unless their stream is being captured (then the address found before is used), so
+// a device reset between calls does not leave a stale address behind.  All calls share the
+// array: calls whose kernels overlap on the GPU (different streams, or different host threads
+// on the same device) race on it.  Every call writes the statistics it reads before reading
+// them, so the contents left by an earlier call do not matter.  The multi-draft sibling rule
+// (tau > 0) needs residual rows on top of the statistics and is refused.
 // ------------------------------------------------------------------------------------------
 namespace spec {
 constexpr int kNoAllocMaxNodes = 32768;
@@ -1205,6 +1182,7 @@ extern "C" spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_s
   static std::mutex mu;
   static void* scratch_of[64] = {nullptr};
   if (!p) return SPEC_ERR_INVALID_ARG;
+  if (p->sibling_rule == SPEC_SIBLING_MULTI_DRAFT && p->tau > 0.f) return SPEC_ERR_UNSUPPORTED;
   if (p->N > kNoAllocMaxNodes || p->R > kNoAllocMaxDraftRows) return SPEC_ERR_UNSUPPORTED;
   const size_t need = spec_verify_workspace_size(p);
   if (need > kNoAllocScratchBytes) return SPEC_ERR_UNSUPPORTED;
@@ -1215,16 +1193,24 @@ extern "C" spec_status_t spec_verify_noalloc(const spec_verify_params* p, spec_s
     return SPEC_ERR_CUDA;
   }
   if (dev < 0 || dev >= 64) return SPEC_ERR_UNSUPPORTED;
+  // look the address up again unless the stream is being captured (a lookup may not be allowed
+  // then); a stream whose capture state cannot be read keeps the address found before
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusActive;
+  if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    cap = cudaStreamCaptureStatusActive;
+  }
   void* ptr = nullptr;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (!scratch_of[dev]) {
-      e = cudaGetSymbolAddress(&scratch_of[dev], g_verify_scratch);
+    if (!scratch_of[dev] || cap == cudaStreamCaptureStatusNone) {
+      void* found = nullptr;
+      e = cudaGetSymbolAddress(&found, g_verify_scratch);
       if (e != cudaSuccess) {
-        scratch_of[dev] = nullptr;
         set_last_cuda_error(e);
         return SPEC_ERR_CUDA;
       }
+      scratch_of[dev] = found;
     }
     ptr = scratch_of[dev];
   }

@@ -949,16 +949,16 @@ bool verify_cluster_fits(const ClusterVerifyArgs& a, int tes, int des) {
 template <typename TT, typename TD>
 static cudaError_t launch_cl(ClusterVerifyArgs a, int tes, int des, cudaStream_t s) {
   using namespace vcl;
-  static bool raised[64] = {false};
+  static DeviceOnce raised;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   auto kernel = verify_cluster_kernel<TT, TD>;
-  if (!raised[dev]) {
+  if (!raised.test(dev)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
-    raised[dev] = true;
+    raised.set(dev);
   }
   // CTAs per request: the fewest waves per unit of work, i.e. the least
   // ceil(B / resident clusters) / n; ties to the larger n

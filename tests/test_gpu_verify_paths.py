@@ -1,6 +1,6 @@
 """spec_verify's two forms against the oracle: the one-launch cluster form (trees of at most 32
 nodes whose row slices fit a CTA) and the two-launch form (row statistics kernel + walk kernel),
-chosen with spec_verify_set_path, on chains and small trees (sibling residual and independent
+chosen per call by the verify_path field, on chains and small trees (sibling residual and independent
 rules), draft logits and probabilities, tau = 0, ragged vocabularies, data errors and more
 requests than one wave of clusters."""
 import numpy as np
@@ -19,9 +19,7 @@ PATHS = {"cluster": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT}
 
 @pytest.fixture(params=sorted(PATHS))
 def path(request):
-    B.spec_verify_set_path(PATHS[request.param])
-    yield request.param
-    B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+    return request.param
 
 
 def _medusa(V=3001, dtype="bf16", tau=1.0, B_=4, ks=(2, 3, 2)):
@@ -74,9 +72,9 @@ WORKLOADS = {
 }
 
 
-def _verify(w, rule):
+def _verify(w, rule, path="cluster"):
     snap = PU.snapshot(w)
-    step = VerifyStep(w, sibling_rule=rule)
+    step = VerifyStep(w, sibling_rule=rule, verify_path=PATHS[path])
     step.tree_build()
     step.verify()
     torch.cuda.synchronize()
@@ -86,14 +84,14 @@ def _verify(w, rule):
 @pytest.mark.parametrize("name", sorted(WORKLOADS))
 def test_verify_paths_against_oracle(name, path):
     w = WORKLOADS[name]()
-    step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL)
+    step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL, path)
     PU.check_verify(w, step, PU.oracle_verify(w, snap))
 
 
 @pytest.mark.parametrize("name", ["medusa_232", "specinfer_321"])
 def test_independent_rule_paths(name, path):
     w = WORKLOADS[name]()
-    step, snap = _verify(w, B.SPEC_SIBLING_INDEPENDENT)
+    step, snap = _verify(w, B.SPEC_SIBLING_INDEPENDENT, path)
     PU.check_verify(w, step, PU.oracle_verify(w, snap, B.SPEC_SIBLING_INDEPENDENT))
 
 
@@ -104,11 +102,7 @@ def test_both_forms_agree():
         w = WORKLOADS[name]()
         outs = {}
         for p in ("cluster", "split"):
-            B.spec_verify_set_path(PATHS[p])
-            try:
-                step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL)
-            finally:
-                B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+            step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL, p)
             outs[p] = {k: PU.np_(getattr(step, k)).copy()
                        for k in ("out_tokens", "out_len", "path", "n_acc", "rejections")}
         orc = PU.oracle_verify(w, snap)
@@ -124,16 +118,12 @@ def test_both_forms_agree():
 def test_auto_takes_the_cluster_form_when_it_fits():
     # the one-launch form never touches the statistics workspace; the two-launch form fills it
     w = WORKLOADS["chain_bf16"]()
-    step = VerifyStep(w)
-    step.tree_build()
     for p, touched in (("cluster", False), ("split", True)):
+        step = VerifyStep(w, verify_path=PATHS[p])
+        step.tree_build()
         step.ver_ws.fill_(0xA5)
-        B.spec_verify_set_path(PATHS[p])
-        try:
-            step.verify()
-            torch.cuda.synchronize()
-        finally:
-            B.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO)
+        step.verify()
+        torch.cuda.synchronize()
         assert bool((step.ver_ws != 0xA5).any()) == touched, p
     # a tree of more than 32 nodes always takes the two-launch form
     w = W.make_config(3, scale="small", device="cuda")
@@ -154,7 +144,7 @@ def test_data_errors_both_forms(path):
     w.draft_row[no[0] + internal[1]] = w.R + 3
     w.tokens[no[1] + 4] = -2
     snap = PU.snapshot(w)
-    step = VerifyStep(w)
+    step = VerifyStep(w, verify_path=PATHS[path])
     step.tree_build()
     step.verify()
     torch.cuda.synchronize()

@@ -140,11 +140,13 @@ def test_draft_tree_host_validation(lib):
                                      fake, 16, None) == B.SPEC_ERR_INVALID_ARG   # small workspace
 
 
-def test_verify_path_switch(lib):
-    assert lib.spec_verify_set_path(B.SPEC_VERIFY_PATH_SPLIT) == B.SPEC_OK
-    assert lib.spec_verify_set_path(B.SPEC_VERIFY_PATH_AUTO) == B.SPEC_OK
+def test_verify_path_field_is_validated(lib):
+    # the form of the verification is chosen per call; values other than AUTO / SPLIT are
+    # refused before any CUDA call
+    v, _ = _fake_verify_and_compact()
     for bad in (-1, 2, 7):
-        assert lib.spec_verify_set_path(bad) == B.SPEC_ERR_INVALID_ARG
+        v.verify_path = bad
+        assert lib.spec_verify(ctypes.byref(v), 0x100000, 1 << 30, None) == B.SPEC_ERR_INVALID_ARG
 
 
 def _fake_verify_and_compact():
@@ -193,8 +195,13 @@ int main(void) {
   if (strcmp(spec_status_string(SPEC_OK), "SPEC_OK") != 0) ++fails;
   if (spec_verify(NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
   if (spec_verify_compact(NULL, NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
-  if (spec_verify_set_path(7) != SPEC_ERR_INVALID_ARG) ++fails;
-  if (spec_verify_set_path(SPEC_VERIFY_PATH_AUTO) != SPEC_OK) ++fails;
+  {
+    spec_verify_params v;
+    memset(&v, 0, sizeof(v));
+    if (v.verify_path != SPEC_VERIFY_PATH_AUTO) ++fails;   /* zero-initialised: the default */
+    v.verify_path = 7;
+    if (spec_verify(&v, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
+  }
   if (spec_kv_compact(NULL, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
   if (spec_tree_attention(NULL, NULL, 0, NULL) != SPEC_ERR_INVALID_ARG) ++fails;
   if (spec_verify_workspace_size(NULL) != 0) ++fails;
