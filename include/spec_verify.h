@@ -429,6 +429,11 @@ const char* spec_status_string(spec_status_t status);
 /* The cudaError_t (as int) behind the most recent SPEC_ERR_CUDA on this thread, 0 if none. */
 int spec_last_cuda_error(void);
 
+/* No counterpart on the pages: how many kernels this library has enqueued in this process, all
+ * threads and devices together (a launch made while a stream is captured counts once, when it
+ * is captured; replays of the graph are not launches of the library).  Diagnostics only. */
+uint64_t spec_kernel_launches(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_k
            "spec_verify", "spec_verify_workspace_size", "spec_verify_noalloc", "spec_kv_compact",
            "spec_status_string", "spec_last_cuda_error", "spec_draft_init",
            "spec_draft_expand_select", "spec_draft_topk_append", "spec_echo_workspace_size",
-           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_compact"]
+           "spec_echo_select_pack", "spec_debug_draft_copy_stall", "spec_verify_compact",
+           "spec_kernel_launches"]
 
 _vp = ctypes.c_void_p
 _i32 = ctypes.c_int32
@@ -133,6 +134,8 @@ def load_library(build_if_missing=False):
     lib.spec_echo_select_pack.restype = st
     lib.spec_echo_select_pack.argtypes = [ctypes.POINTER(SpecDraftPool), _i32, _vp, _vp, _vp,
                                           _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.spec_kernel_launches.restype = ctypes.c_uint64
+    lib.spec_kernel_launches.argtypes = []
     lib.spec_status_string.restype = ctypes.c_char_p
     lib.spec_status_string.argtypes = [ctypes.c_int]
     lib.spec_last_cuda_error.restype = ctypes.c_int
@@ -440,3 +443,9 @@ def spec_echo_select_pack(pool, K_max, node_offset, parent, tokens, depth, draft
 def spec_debug_draft_copy_stall(chunk):
     """Testing only: make the next top-K launches lose one chunk's copy (-1: off)."""
     _check(load_library().spec_debug_draft_copy_stall(int(chunk)), "spec_debug_draft_copy_stall")
+
+
+def spec_kernel_launches():
+    """Kernels the library has enqueued in this process so far (a launch captured into a CUDA
+    graph counts once, when captured; graph replays do not count)."""
+    return int(load_library().spec_kernel_launches())

@@ -19,6 +19,7 @@ namespace spec {
 // ------------------------------------------------------------------------------------------
 void set_last_cuda_error(cudaError_t e);
 int sm_count_current_device();
+void count_launch();   // one kernel enqueued by this library (spec_kernel_launches)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -83,7 +84,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 inline spec_status_t launch_result(cudaError_t e) {

@@ -10,6 +10,7 @@
 // thread waits on another.  Validation happens first, block-wide; req_status[r] is (re)written
 // here -- 0, or the SPEC_REQ_* bit of a bad request, whose outputs become -1 / 0.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "rope.cuh"
@@ -18,6 +19,9 @@ namespace spec {
 
 static thread_local int g_last_cuda_error = 0;
 void set_last_cuda_error(cudaError_t e) { g_last_cuda_error = int(e); }
+
+static std::atomic<unsigned long long> g_kernel_launches{0};
+void count_launch() { g_kernel_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int sm_count_current_device() {
   static std::mutex mu;
@@ -233,6 +237,10 @@ const char* spec_status_string(spec_status_t s) {
 }
 
 int spec_last_cuda_error(void) { return spec::g_last_cuda_error; }
+
+uint64_t spec_kernel_launches(void) {
+  return uint64_t(spec::g_kernel_launches.load(std::memory_order_relaxed));
+}
 
 spec_status_t spec_tree_build(const int32_t* parent, const int32_t* node_offset,
                               const int32_t* prefix_len, int32_t B, int32_t N, int32_t T_max,

@@ -996,7 +996,9 @@ static cudaError_t launch_cl(ClusterVerifyArgs a, int tes, int des, cudaStream_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a);
+  if (le == cudaSuccess) count_launch();
+  return le;
 }
 
 cudaError_t launch_verify_cluster(const ClusterVerifyArgs& a, int tes, int des, cudaStream_t s) {
