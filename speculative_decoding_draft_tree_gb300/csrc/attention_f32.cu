@@ -6,8 +6,12 @@
 //
 // fp32 inputs rule out the bf16 tensor-core path (a TF32 contraction would not meet an fp32
 // tolerance), and the fp32 workloads are small (a chain of a few tokens over a short prefix), so
-// this is a plain kernel: one warp per (node, query head); lanes split head_dim, every key's
-// score is a warp reduction, softmax is online in fp32.
+// this is a plain kernel, built for latency: one CTA of 128 threads per (node, query head).  Keys
+// go in chunks of 128, one key per thread: each thread looks its key's block up, forms the full
+// dot product with the query and copies its V row into shared memory (all its loads in flight
+// at once), so a chunk costs a few memory round trips instead of one per key; the chunk's
+// softmax is a block reduction (online across chunks, fp32), and thread c < head_dim then
+// accumulates output column c over the chunk's visible keys from shared memory.
 #include <math.h>
 
 #include "common.cuh"
@@ -29,13 +33,35 @@ struct AttnF32Dev {
   float scale;
 };
 
-__global__ void __launch_bounds__(128) attention_f32_kernel(AttnF32Dev a) {
+constexpr int kF32Threads = 128;   // keys per chunk and threads per CTA; head_dim <= 128
+
+__device__ __forceinline__ float block_reduce_f32(float v, float* red, bool is_max) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float x = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, x) : v + x;
+  }
+  __syncthreads();   // red is reused by consecutive reductions
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = red[0];
+#pragma unroll
+  for (int w = 1; w < kF32Threads / 32; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  return r;
+}
+
+__global__ void __launch_bounds__(kF32Threads) attention_f32_kernel(AttnF32Dev a) {
+  extern __shared__ float4 sv4[];   // [kF32Threads keys][head_dim / 4 + 1]: the chunk's V rows
+  __shared__ __align__(16) float sq[128];
+  __shared__ float sp[kF32Threads];
+  __shared__ int spb[kF32Threads];
+  __shared__ float red[kF32Threads / 32];
+  __shared__ int s_bad;
   pdl_wait();
   pdl_trigger();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long pair = long(blockIdx.x) * 4 + warp;
-  if (pair >= long(a.N) * a.H_q) return;
-  const int n = int(pair / a.H_q), h = int(pair % a.H_q);
+  const int tid = threadIdx.x;
+  const int n = int(blockIdx.x / unsigned(a.H_q)), h = int(blockIdx.x % unsigned(a.H_q));
   // request owning node n
   int lo = 0, hi = a.B - 1;
   while (lo < hi) {
@@ -43,7 +69,7 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttnF32Dev a) {
     if (a.node_offset[mid] <= n) lo = mid; else hi = mid - 1;
   }
   const int r = lo;
-  if (a.req_status[r] != 0) return;
+  if (a.req_status[r] != 0) return;   // uniform across the CTA
   const int o = a.node_offset[r];
   const int T = a.node_offset[r + 1] - o;
   const int P = a.prefix_len[r];
@@ -51,63 +77,78 @@ __global__ void __launch_bounds__(128) attention_f32_kernel(AttnF32Dev a) {
   const int kv_len = P + T;
   const int nblk = (kv_len + a.bs - 1) / a.bs;
   if (nblk > a.max_blocks) {
-    if (lane == 0) atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
+    if (tid == 0) atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
     return;
   }
   const int32_t* table = a.block_table + size_t(r) * a.max_blocks;
-  for (int b = lane; b < nblk; b += 32) {
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  for (int b = tid; b < nblk; b += kF32Threads) {
     const int pb = table[b];
-    if (pb < 0 || pb >= a.num_blocks) atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
+    if (pb < 0 || pb >= a.num_blocks) s_bad = 1;
   }
-  __syncwarp();
-  if (a.req_status[r] & SPEC_REQ_BAD_BLOCK) return;
-  constexpr int kMaxPerLane = 4;  // head_dim <= 128
-  float qv[kMaxPerLane], acc[kMaxPerLane];
   const float* qrow = a.q + (size_t(n) * a.H_q + h) * a.d;
-#pragma unroll
-  for (int e = 0; e < kMaxPerLane; ++e) {
-    const int c = lane + 32 * e;
-    qv[e] = c < a.d ? qrow[c] : 0.f;
-    acc[e] = 0.f;
+  if (tid < a.d) sq[tid] = qrow[tid];
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) atomicOr(&a.req_status[r], SPEC_REQ_BAD_BLOCK);
+    return;
   }
   const uint32_t* anc = a.anc + size_t(n) * a.W;
-  float m = -INFINITY, l = 0.f;
-  for (int j = 0; j < kv_len; ++j) {
-    if (j >= P) {
+  const int d4 = a.d >> 2;
+  const int vstride = d4 + 1;   // float4s per staged V row (padded against bank conflicts)
+  float m = -INFINITY, l = 0.f, acc = 0.f;
+  for (int c0 = 0; c0 < kv_len; c0 += kF32Threads) {
+    // scores: one key per thread
+    const int j = c0 + tid;
+    bool vis = j < kv_len;
+    if (vis && j >= P) {
       const int t = j - P;
-      if (!((anc[t >> 5] >> (t & 31)) & 1u)) continue;
+      vis = (anc[t >> 5] >> (t & 31)) & 1u;
     }
-    const int pb = table[j / a.bs];
-    const size_t off = ((size_t(pb) * a.H_kv + kvh) * a.bs + (j % a.bs)) * a.d;
-    float part = 0.f;
-#pragma unroll
-    for (int e = 0; e < kMaxPerLane; ++e) {
-      const int c = lane + 32 * e;
-      if (c < a.d) part = fmaf(qv[e], a.k[off + c], part);
+    float sc = -INFINITY;
+    int pb = -1;
+    if (vis) {
+      pb = table[j / a.bs];
+      const size_t row = ((size_t(pb) * a.H_kv + kvh) * a.bs + (j % a.bs)) * a.d;
+      const float4* krow = reinterpret_cast<const float4*>(a.k + row);
+      const float4* vrow = reinterpret_cast<const float4*>(a.v + row);
+      const float4* q4 = reinterpret_cast<const float4*>(sq);
+      float dot = 0.f;
+#pragma unroll 8
+      for (int e = 0; e < d4; ++e) {
+        const float4 kv = krow[e], qq = q4[e];
+        sv4[tid * vstride + e] = vrow[e];
+        dot = fmaf(qq.x, kv.x, dot);
+        dot = fmaf(qq.y, kv.y, dot);
+        dot = fmaf(qq.z, kv.z, dot);
+        dot = fmaf(qq.w, kv.w, dot);
+      }
+      sc = dot * a.scale;
     }
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) part += __shfl_xor_sync(0xffffffffu, part, s);
-    const float sc = part * a.scale;
-    const float mn = fmaxf(m, sc);
-    const float corr = expf(m - mn);
-    const float pj = expf(sc - mn);
-    l = l * corr + pj;
-#pragma unroll
-    for (int e = 0; e < kMaxPerLane; ++e) {
-      const int c = lane + 32 * e;
-      const float vv = c < a.d ? a.v[off + c] : 0.f;
-      acc[e] = acc[e] * corr + pj * vv;
-    }
+    const float cmax = block_reduce_f32(sc, red, true);
+    const float mn = fmaxf(m, cmax);
+    const float corr = m == -INFINITY ? 0.f : expf(m - mn);
+    const float pj = vis ? expf(sc - mn) : 0.f;
+    sp[tid] = pj;
+    spb[tid] = pb;
+    const float psum = block_reduce_f32(pj, red, false);   // its barriers publish sp, spb, sv4
+    l = l * corr + psum;
     m = mn;
+    // output column tid: the chunk's visible keys
+    if (tid < a.d) {
+      const float* sv = reinterpret_cast<const float*>(sv4);
+      float part = 0.f;
+      const int nk = min(kF32Threads, kv_len - c0);
+#pragma unroll 4
+      for (int k = 0; k < nk; ++k)
+        if (spb[k] >= 0) part = fmaf(sp[k], sv[k * 4 * vstride + tid], part);
+      acc = acc * corr + part;
+    }
+    __syncthreads();   // sp, spb and sv4 are rewritten by the next chunk
   }
-  float* orow = a.o + (size_t(n) * a.H_q + h) * a.d;
-  const float inv = 1.f / l;
-#pragma unroll
-  for (int e = 0; e < kMaxPerLane; ++e) {
-    const int c = lane + 32 * e;
-    if (c < a.d) orow[c] = acc[e] * inv;
-  }
-  if (a.lse && lane == 0) a.lse[size_t(n) * a.H_q + h] = m + logf(l);
+  if (tid < a.d) a.o[(size_t(n) * a.H_q + h) * a.d + tid] = acc / l;
+  if (a.lse && tid == 0) a.lse[size_t(n) * a.H_q + h] = m + logf(l);
 }
 
 spec_status_t launch_attention_f32(const spec_attn_params* p, cudaStream_t s) {
@@ -129,8 +170,14 @@ spec_status_t launch_attention_f32(const spec_attn_params* p, cudaStream_t s) {
   d.scale = p->scale > 0.f ? p->scale : 1.f / sqrtf(float(p->head_dim));
   const long pairs = long(p->N) * p->H_q;
   if (pairs == 0) return SPEC_OK;
-  const unsigned grid = unsigned((pairs + 3) / 4);
-  return launch_result(launch_pdl(attention_f32_kernel, dim3(grid), dim3(128), 0, s, d));
+  if (pairs > 0x7fffffffL) return SPEC_ERR_UNSUPPORTED;
+  const size_t dyn = sizeof(float4) * kF32Threads * size_t(p->head_dim / 4 + 1);   // <= 66 KB
+  static DeviceOnce raised;
+  const spec_status_t st = raise_dyn_smem_once(
+      attention_f32_kernel, sizeof(float4) * kF32Threads * size_t(128 / 4 + 1), raised);
+  if (st != SPEC_OK) return st;
+  return launch_result(launch_pdl(attention_f32_kernel, dim3(unsigned(pairs)),
+                                  dim3(kF32Threads), dyn, s, d));
 }
 
 }  // namespace spec
