@@ -6,30 +6,33 @@
 // instead of one KV copy per branch; 12.4.3 -- PagedAttention and FlashDecoding are the framework
 // features verification has to fit (paged KV blocks, KV split across CTAs + log-sum-exp merge).
 //
-// Work unit = (request r, KV head h, M-tile mt): the G query heads of h times up to 128/G tree
-// tokens, stacked token-major into 128 MMA rows (row m = t_local * G + g), against the
-// request's P_r + T_r logical KV slots in tiles of 128 keys (8 paged blocks of 16).  The units
-// are laid end to end (request, head, M-tile order) as one stream of KV tiles cut into equal
+// Rows: the G query heads of KV head h times up to 128/G tree tokens, stacked token-major into
+// 128 MMA rows per M-tile (row m = t_local * G + g).  Work unit = (request r, KV head h, pair of
+// M-tiles): each K/V tile of the request's P_r + T_r logical KV slots (tiles of 128 keys = 8
+// paged blocks of 16) is read from HBM once for both M-tiles of the pair, so a unit with 2 M-tiles
+// (up to 256 rows) costs one pass over its K/V, not two.  A unit with one M-tile splits its K/V
+// tiles between the two slots by parity and merges their softmax states at the end.  The units are
+// laid end to end (request, head, pair order) as one stream of K/V tiles cut into equal
 // contiguous ranges, one per persistent CTA (one CTA per SM); each CTA finds its own range with
 // two block-wide passes over the requests at start-up, so there is no separate partition launch.
 // A unit cut by a range boundary is computed in pieces that write fp32 partial outputs and
 // log-sum-exps; the CTA holding a cut unit's first piece leaves a merge record, and a small merge
 // kernel combines the pieces by log-sum-exp.  Every other unit writes its output directly.
 //
-// CTA (384 threads):
-//   warp 0      Q and K producer, warp 2 V producer: 128-byte-swizzled TMA boxes (one per
-//               paged block and 64-column half, issued by 8 lanes); blocks past the request or
-//               with a bad block id are read from an out-of-range row (TMA fills zeros).  K has
-//               4 stages, released right after QK^T; V has 2, released after PV;
-//   warp 1      one thread issues S = Q K^T (M=128, N=128, K=16 x 8) into one of two TMEM score
-//               buffers; warp 3, one thread, issues O += P V (P read from TMEM, V as an
-//               MN-major operand) into the TMEM accumulator; each commits its own completions;
-//   warps 4..11 softmax: the two warps of a TMEM lane quarter own the same 32 rows; each reads
-//               all 128 scores of its rows (the row max is computed redundantly, so no exchange
-//               is needed per tile) and exponentiates its own 64 keys with a lazily updated
-//               reference max (O rescaled only when the max grows by more than 2^8), writing P
-//               (bf16) into one of two TMEM P buffers; the epilogue adds the two halves' row sums
-//               (one bounded exchange per item) and writes O columns 64*half .. 64*half+63.
+// CTA (384 threads), two slots s = 0, 1 (an M-tile each, or half of the K/V tiles of one):
+//   warp 0      Q and K producer, warp 2 V producer: 128-byte-swizzled TMA boxes (one 4-D box per
+//               64-column half when a tile's 8 paged blocks are consecutive, else one per block,
+//               issued by 8 lanes); blocks past the request or with a bad block id are read from
+//               an out-of-range row (TMA fills zeros).  K has 3 stages, V 2; Q one tile per slot;
+//   warp 1      one thread issues every tcgen05.mma: S_s = Q_s K^T (M = N = 128, K = 16 x 8)
+//               into TMEM and O_s += P_s V (P_s read from TMEM, V as an MN-major operand) into
+//               the slot's TMEM accumulator, the slots interleaved so that one slot's products
+//               run while the other slot's softmax works;
+//   warps 4..7 (slot 0), 8..11 (slot 1): softmax, one query row per thread: the row maximum over
+//               the tile's visible keys (masked by the ancestor bits), exponentials against a
+//               lazily updated reference (O_s rescaled only when the maximum grows by more than
+//               2^8), P_s (bf16) written over S_s in TMEM; the epilogue normalises O_s and writes
+//               the output rows (a split unit: each slot writes 64 columns of the merged rows).
 // Every wait is bounded (clock64 limit); an expired wait flags SPEC_REQ_TIMEOUT and lets every
 // role drain and exit; TMEM is always freed.
 #include <cudaTypedefs.h>
@@ -47,31 +50,35 @@ constexpr int kD = 128;
 constexpr int kBS = 16;
 constexpr int kBM = 128;
 constexpr int kBN = 128;
-constexpr int kThreads = 384;                 // 4 control warps + 8 softmax warps
+constexpr int kThreads = 384;                 // 4 control warps + 2 slots x 4 softmax warps
 constexpr int kAtom = 16384;                  // 128 rows x 128 B
 constexpr int kTile = 2 * kAtom;              // 128 x 128 bf16
-constexpr int kKStages = 4;
+constexpr int kKStages = 3;
 constexpr int kVStages = 2;
-constexpr int kSmemQ = 0;
-constexpr int kSmemK = kSmemQ + kTile;
+constexpr int kSmemQ = 0;                     // one Q tile per slot
+constexpr int kSmemK = kSmemQ + 2 * kTile;
 constexpr int kSmemV = kSmemK + kKStages * kTile;
 constexpr int kSmemBar = kSmemV + kVStages * kTile;
-constexpr int kSmemRed = kSmemBar + 256;      // [2 buffers][2 halves][128 rows] fp32 exchange
-constexpr int kSmemEnd = kSmemRed + 2048;
+constexpr int kSmemX = kSmemBar + 256;        // [2 slots][reference, sum][128 rows] fp32
+constexpr int kSmemEnd = kSmemX + 2048;
 constexpr int kSmemBytes = 232448;            // the per-CTA maximum; the slack aligns the base
 constexpr long long kWaitLimit = 4000000000LL;     // clock cycles (~2 s)
 constexpr float kLazyRescale = 8.0f;          // log2 units
 constexpr int kMaxCtas = 1024;                // persistent CTAs at most
 constexpr int kMinTilesPerRange = 4;          // small problems use fewer, longer ranges
-// TMEM columns: S buffers 0-127 and 128-255, O accumulator 256-383, P buffers 384-447, 448-511
-constexpr uint32_t kTmemP = 384;
+constexpr int kPartRows = 2 * kBM;            // rows of one partial piece (up to two M-tiles)
+constexpr int kCtlRegs = 96;                  // registers per thread: control warpgroup
+constexpr int kSoftmaxRegs = 200;             // and each softmax warpgroup (setmaxnreg)
+static_assert(kCtlRegs * 128 + kSoftmaxRegs * 256 <= kThreads * 168, "register split fits");
+// TMEM columns: slot s's scores S_s (fp32) in 128 s .. 128 s + 127, overwritten in place by its
+// probabilities P_s (bf16 pairs) in 128 s .. 128 s + 63; slot s's output O_s in 256 + 128 s ..
 }  // namespace attn
 
 // A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1; the first piece's
 // partial slot is slot0 (2 ca, or 2 ca + 1 when the unit starts inside range ca), piece p > 0
-// starts range ca + p and uses slot 2 (ca + p).
+// starts range ca + p and uses slot 2 (ca + p).  The unit covers M-tiles mt .. mt + nmt - 1.
 struct MergeRec {
-  int np, h, mt, o, T, ca, slot0, pad;
+  int np, h, mt, nmt, o, T, ca, slot0;
 };
 
 struct TcDev {
@@ -83,8 +90,8 @@ struct TcDev {
   float* lse;
   int32_t* req_status;
   struct MergeRec* recs;   // [ctas]: the cut unit whose first piece CTA c holds (np = 0: none)
-  float* part_o;      // [2 ctas][128][128] partial outputs of the pieces of cut units
-  float* part_lse;    // [2 ctas][2][128] their log2-sum-exps, one copy per column half
+  float* part_o;      // [2 ctas][kPartRows][128] partial outputs of the pieces of cut units
+  float* part_lse;    // [2 ctas][kPartRows] their log2-sum-exps
   int B, N, H_q, H_kv, G, log2G, T_max, W, num_blocks, max_blocks, kv_rows, ctas;
   float scale_log2;
 };
@@ -99,15 +106,15 @@ static TcWs tc_ws_layout(int ctas) {
   const size_t slots = 2 * size_t(ctas);   // at most two partial pieces per range
   size_t off = 0;
   w.recs = off; off = align_up(off + sizeof(MergeRec) * size_t(ctas), 256);
-  w.part_o = off; off = align_up(off + sizeof(float) * slots * attn::kBM * attn::kD, 256);
-  w.part_lse = off; off = align_up(off + sizeof(float) * slots * 2 * attn::kBM, 256);
+  w.part_o = off; off = align_up(off + sizeof(float) * slots * attn::kPartRows * attn::kD, 256);
+  w.part_lse = off; off = align_up(off + sizeof(float) * slots * attn::kPartRows, 256);
   w.total = off;
   return w;
 }
 
 // ------------------------------------------------------------------------------ partition
 struct ReqGeom {
-  int o, T, P, mts, nts, units;
+  int o, T, P, mts, ups, nts, units;   // ups: units per KV head, one per pair of M-tiles
 };
 
 // Geometry of request r.  The status bits this kernel sets itself (BAD_BLOCK, TIMEOUT) are
@@ -123,8 +130,9 @@ __device__ __forceinline__ ReqGeom req_geom(const TcDev& a, int r) {
   const bool ok = st == 0 && g.T >= 1 && g.P >= 0 &&
                   (g.P + g.T + attn::kBS - 1) / attn::kBS <= a.max_blocks;
   g.mts = ok ? (g.T + tpt - 1) / tpt : 0;
+  g.ups = (g.mts + 1) >> 1;
   g.nts = ok ? (g.P + g.T + attn::kBN - 1) / attn::kBN : 0;
-  g.units = a.H_kv * g.mts;
+  g.units = a.H_kv * g.ups;
   return g;
 }
 
@@ -232,9 +240,12 @@ __device__ Range cta_range(const TcDev& a, long long* s64, int* s32) {
   return R;
 }
 
-// One piece of work: tiles [j0, j1) of unit (r, h, mt).
+// One piece of work: tiles [j0, j1) of unit (r, h, pair of M-tiles starting at mt).  pair: the
+// unit has M-tiles mt and mt + 1 (one per slot, both reading every K/V tile); otherwise it has
+// M-tile mt alone and the slots take alternate K/V tiles.
 struct Item {
   int r, h, mt, j0, j1;
+  bool pair;
   int slot;           // >= 0: a partial piece of a cut unit, written to part_o[slot]
   int o, T, P, nts;
   long long ubeg;     // stream index of the unit's first tile
@@ -266,8 +277,9 @@ struct ItemIter {
     const long long off = t - rbeg;
     const int u = int(off / g.nts);
     it.r = r;
-    it.h = u / g.mts;
-    it.mt = u - it.h * g.mts;
+    it.h = u / g.ups;
+    it.mt = 2 * (u - it.h * g.ups);
+    it.pair = it.mt + 1 < g.mts;
     it.j0 = int(off - (long long)u * g.nts);
     it.j1 = int(min((long long)g.nts, (long long)it.j0 + (R.t1 - t)));
     it.o = g.o;
@@ -287,7 +299,7 @@ struct ItemIter {
 __device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& R) {
   MergeRec rec;
   rec.np = 0;
-  rec.h = rec.mt = rec.o = rec.T = rec.ca = rec.slot0 = rec.pad = 0;
+  rec.h = rec.mt = rec.nmt = rec.o = rec.T = rec.ca = rec.slot0 = 0;
   if (R.t0 < R.t1) {
     const ReqGeom g = req_geom(a, R.r1);
     const long long u = (R.t1 - 1 - R.rbeg1) / g.nts;
@@ -295,8 +307,9 @@ __device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& 
     if (ubeg >= R.t0 && ubeg + g.nts > R.t1) {
       rec.ca = int(blockIdx.x);
       rec.np = range_of(ubeg + g.nts - 1, R.total, R.C) - rec.ca + 1;
-      rec.h = int(u) / g.mts;
-      rec.mt = int(u) - rec.h * g.mts;
+      rec.h = int(u) / g.ups;
+      rec.mt = 2 * (int(u) - rec.h * g.ups);
+      rec.nmt = rec.mt + 1 < g.mts ? 2 : 1;
       rec.o = g.o;
       rec.T = g.T;
       rec.slot0 = piece_slot(ubeg, R.total, R.C, rec.ca);
@@ -306,20 +319,6 @@ __device__ __forceinline__ void write_merge_record(const TcDev& a, const Range& 
 }
 
 // ------------------------------------------------------------------------------ main kernel
-__device__ __forceinline__ uint32_t anc_window(const uint32_t (&anc)[8], int W, int pos) {
-  // 32 mask bits starting at tree index `pos` (zero outside [0, 32 W))
-  if (pos <= -32 || pos >= 32 * W) return 0u;
-  const int wi = pos >= 0 ? (pos >> 5) : -1;
-  const int sh = pos - 32 * wi;
-  uint32_t lo = 0u, hi = 0u;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if (k == wi && k < W) lo = anc[k];
-    if (k == wi + 1 && k < W) hi = anc[k];
-  }
-  return sh == 0 ? lo : ((lo >> sh) | (hi << (32 - sh)));
-}
-
 // all 32 lanes wait; the outcome is made warp-uniform so warp-collective TMEM accesses that
 // follow are executed by the full warp or by none of it
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -327,34 +326,74 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
   return r;
 }
 
-// Masked raw (unscaled) scores of 32 columns starting at key `key0`, in place: invisible keys
-// become -inf; returns the maximum of the visible ones.  Columns inside the prefix need no mask
-// (one max per score).  Scaling by a positive constant commutes with the maximum, so the caller
-// scales the maximum once and folds the scale into the exponentials' FMA.
-__device__ __forceinline__ float mask_max32_raw(uint32_t (&x)[32], bool valid, int key0, int P,
-                                                const uint32_t (&anc)[8], int W) {
-  float mx = -INFINITY;
-  if (key0 + 32 <= P) {
+// 32 exponentials 2^(x sl + add) of one key chunk (masked keys hold -inf), summed into two
+// partial sums and stored as 16 columns of bf16 pairs at TMEM address `dst`
+__device__ __forceinline__ void exp_chunk(const uint32_t (&x)[32], float sl, float add, float& ra,
+                                          float& rb, uint32_t dst) {
+  uint32_t pk[16];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(x[c]));
-    return valid ? mx : -INFINITY;
+  for (int i = 0; i < 16; ++i) {
+    const float p0 = ex2(fmaf(__uint_as_float(x[2 * i]), sl, add));
+    const float p1 = ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl, add));
+    if (i & 1) rb += p0 + p1; else ra += p0 + p1;
+    pk[i] = pack_bf16(p0, p1);
   }
-  const uint32_t wd = anc_window(anc, W, key0 - P);
+  tc::tmem_st16(dst, pk);
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Maximum of 32 values as a tree of three-input maxima (17 operations, depth 4).
+__device__ __forceinline__ float max32_tree(const uint32_t (&x)[32]) {
+  float m[11];
+#pragma unroll
+  for (int c = 0; c < 10; ++c)
+    m[c] = fmax3(__uint_as_float(x[3 * c]), __uint_as_float(x[3 * c + 1]),
+                 __uint_as_float(x[3 * c + 2]));
+  m[10] = fmaxf(__uint_as_float(x[30]), __uint_as_float(x[31]));
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmaxf(m[9], m[10]);
+  return fmaxf(fmax3(a, b, c), d);
+}
+
+// 32 ancestor-mask bits of a query row starting at tree index `pos` (zero outside [0, 32 W)),
+// read from the row's words in global memory (only tiles that reach the tree need them)
+__device__ __forceinline__ uint32_t anc_window_g(const uint32_t* row, int W, int pos) {
+  if (row == nullptr || pos <= -32 || pos >= 32 * W) return 0u;
+  const int wi = pos >= 0 ? (pos >> 5) : -1;
+  const int sh = pos - 32 * wi;
+  const uint32_t lo = wi >= 0 ? __ldg(row + wi) : 0u;
+  const uint32_t hi = (sh != 0 && wi + 1 < W) ? __ldg(row + wi + 1) : 0u;
+  return sh == 0 ? lo : ((lo >> sh) | (hi << (32 - sh)));
+}
+
+// Masked raw (unscaled) scores of 32 columns starting at key `key0`, in place: invisible keys
+// become -inf; returns the maximum of the visible ones.  Columns inside the prefix need no mask.
+// Scaling by a positive constant commutes with the maximum, so the caller scales the maximum
+// once and folds the scale into the exponentials' FMA.  The row's ancestor bits are read from
+// global memory (`row` is null for a padding row).
+__device__ __forceinline__ float mask_max32_row(uint32_t (&x)[32], bool valid, int key0, int P,
+                                                const uint32_t* row, int W) {
+  if (key0 + 32 <= P) return valid ? max32_tree(x) : -INFINITY;
+  const uint32_t wd = anc_window_g(row, W, key0 - P);
   const int npre = P - key0;
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     const bool vis = valid && ((c < npre) || ((wd >> c) & 1u));
-    const float v = vis ? __uint_as_float(x[c]) : -INFINITY;
-    x[c] = __float_as_uint(v);
-    mx = fmaxf(mx, v);
+    x[c] = vis ? x[c] : __float_as_uint(-INFINITY);
   }
-  return mx;
+  return max32_tree(x);
 }
 
 // One lane waits (bounded), the warp gets the outcome.
@@ -369,8 +408,10 @@ __device__ __forceinline__ bool lane0_wait(uint64_t* bar, uint32_t parity, volat
 // consecutive physical blocks one 4-D box per 64-column half brings all eight (16 KB);
 // otherwise each lane issues the two boxes of its own page (2 KB each) -- small boxes cap the
 // copy rate well below HBM speed.  Pages past the request or with a bad block id are read from
-// an out-of-range row (TMA fills zeros).  The K warp also loads each item's Q: q_bytes from two
-// boxes of `qmap` at (0 | 64, head * G, first tree token + mt * q_tokens) into sQ, sQ + q_half.
+// an out-of-range row (TMA fills zeros).  The K warp also loads each item's Q: for each M-tile
+// b of the item (two for a pair item, else one), q_bytes from two boxes of `qmap` at
+// (0 | 64, head * G, first tree token + (mt + b) * q_tokens) into buffer b (sQ + b * q_bytes,
+// halves q_half apart), completing on q_full[b] once q_empty[b] released its previous contents.
 // Inlined into the kernel so that every tensor map address is the kernel parameter's own; a map
 // address in local or shared memory (which TMA cannot read) aborts without issuing a copy.
 // Returns false if a wait expired; every copy issued is waited for (bounded) before return.
@@ -381,13 +422,13 @@ __device__ __forceinline__ bool tma_producer(
     volatile int* abort_flag) {
   using namespace attn;
   const int lane = threadIdx.x & 31;
-  int kt = 0, li = 0;
+  int kt = 0, qn[2] = {0, 0};   // tiles and Q loads issued
   bool ok = !(__isLocal(map) || __isShared(map) || __isLocal(map8) || __isShared(map8) ||
               __isLocal(qmap) || __isShared(qmap));
   ItemIter iter;
   iter.start(a, R);
   Item it;
-  for (; ok && iter.next(a, R, it); ++li) {
+  while (ok && iter.next(a, R, it)) {
     const int nblk = (it.P + it.T + kBS - 1) / kBS;
     const int32_t* table = a.block_table + size_t(it.r) * a.max_blocks;
     // physical block of this lane's page of tile j: -1 past the request, -2 if invalid
@@ -404,13 +445,18 @@ __device__ __forceinline__ bool tma_producer(
       return pb;
     };
     if (is_k) {
-      if (li > 0 && !lane0_wait(q_empty, (li - 1) & 1, abort_flag)) { ok = false; break; }
-      if (lane == 0) {
-        tc::mbar_arrive_expect_tx(q_full, q_bytes);
-        const int row = it.o + it.mt * q_tokens;
-        tc::tma_load_3d(sQ, qmap, 0, it.h * a.G, row, q_full);
-        tc::tma_load_3d(sQ + q_half, qmap, 64, it.h * a.G, row, q_full);
+      for (int b = 0; b < (it.pair ? 2 : 1); ++b) {
+        if (qn[b] > 0 && !lane0_wait(q_empty + b, (qn[b] - 1) & 1, abort_flag)) { ok = false; break; }
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(q_full + b, q_bytes);
+          const int row = it.o + (it.mt + b) * q_tokens;
+          uint8_t* dst = sQ + b * q_bytes;
+          tc::tma_load_3d(dst, qmap, 0, it.h * a.G, row, q_full + b);
+          tc::tma_load_3d(dst + q_half, qmap, 64, it.h * a.G, row, q_full + b);
+        }
+        ++qn[b];
       }
+      if (!ok) break;
     }
     int pb_cur = tile_pb(it.j0);
     for (int j = it.j0; j < it.j1; ++j, ++kt) {
@@ -444,7 +490,8 @@ __device__ __forceinline__ bool tma_producer(
     // drain: wait for the copies issued last (bounded), so none is in flight at exit
     for (int k = max(0, kt - nstage); k < kt; ++k)
       tc::mbar_wait(full + k % nstage, (k / nstage) & 1, abort_flag, kWaitLimit / 8);
-    if (is_k && li > 0) tc::mbar_wait(q_full, (li - 1) & 1, abort_flag, kWaitLimit / 8);
+    for (int b = 0; is_k && b < 2; ++b)
+      if (qn[b] > 0) tc::mbar_wait(q_full + b, (qn[b] - 1) & 1, abort_flag, kWaitLimit / 8);
   }
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
@@ -454,6 +501,452 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mK8,
                const __grid_constant__ CUtensorMap mV8, TcDev a) {
   using namespace attn;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = base + kSmemQ;                    // slot s's Q tile at sQ + s * kTile
+  uint8_t* sK = base + kSmemK;
+  uint8_t* sV = base + kSmemV;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kSmemBar);
+  uint64_t* q_full = bars + 0;                    // [2] per Q buffer
+  uint64_t* q_empty = bars + 2;                   // [2]
+  uint64_t* k_full = bars + 4;                    // [kKStages]
+  uint64_t* k_empty = k_full + kKStages;          // [kKStages]
+  uint64_t* v_full = k_empty + kKStages;          // [kVStages]
+  uint64_t* v_empty = v_full + kVStages;          // [kVStages]
+  uint64_t* s_full = v_empty + kVStages;          // [2] per slot: S_s = Q K^T landed
+  uint64_t* p_full = s_full + 2;                  // [2]: P_s written (the slot's 4 warps)
+  uint64_t* pv_done = p_full + 2;                 // [2]: O_s += P_s V completed
+  uint64_t* o_free = pv_done + 2;                 // [2]: an item's epilogue has read O_s (8 warps)
+  uint64_t* drain = o_free + 2;                   // the MMA issuer's last operations
+  uint64_t* ex_bar = drain + 1;                   // [4] per lane quarter: the slots' exchange
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ex_bar + 4);
+  int* s_abort = reinterpret_cast<int*>(ex_bar + 5);
+  static_assert((4 + 2 * kKStages + 2 * kVStages + 8 + 1 + 4 + 2) * 8 <= 256,
+                "barriers fit their 256-byte region");
+  static_assert(kSmemK % 1024 == 0 && kSmemV % 1024 == 0, "swizzled tiles on 1024-byte bounds");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
+  // this CTA's range of the tile stream (the exchange area is free until the first epilogue)
+  const Range R = cta_range<kThreads>(a, reinterpret_cast<long long*>(base + kSmemX),
+                                      reinterpret_cast<int*>(base + kSmemX + 256));
+  if (tid == 0) write_merge_record(a, R);
+  if (R.t0 >= R.t1) return;   // uniform across the CTA: no work, nothing allocated yet
+  if (tid == 0) {
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(q_full + b, 1);
+      tc::mbar_init(q_empty + b, 1);
+      tc::mbar_init(s_full + b, 1);
+      tc::mbar_init(p_full + b, 4);
+      tc::mbar_init(pv_done + b, 1);
+      tc::mbar_init(o_free + b, 8);
+    }
+    for (int s = 0; s < kKStages; ++s) {
+      tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_empty + s, 1);
+    }
+    tc::mbar_init(drain, 1);
+    for (int q = 0; q < 4; ++q) tc::mbar_init(ex_bar + q, 2);
+    // the 1024-byte aligned layout must fit in the dynamic allocation
+    *s_abort = (tc::smem_u32(base) + kSmemEnd > tc::smem_u32(smem_raw) + kSmemBytes) ? 1 : 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(tmem_slot, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort_flag = s_abort;
+  const int G = a.G, log2G = a.log2G, tpt = kBM >> log2G;
+  const bool layout_ok = *abort_flag == 0;
+  // registers move from the control warpgroup (warps 0..3: TMA, MMA issue) to the two softmax
+  // warpgroups, which hold a row's 128 scores at once: 128 x 56 + 256 x 224 = the 384 x 168
+  // the block was launched with
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  if (layout_ok && (warp == 0 || warp == 2)) {
+    // ===================================================================== TMA producers
+    // warp 0 loads Q (one tile per M-tile of the item) and K, warp 2 loads V; on an expired wait
+    // the producer raises the abort flag itself
+    const bool is_k = warp == 0;
+    if (lane == 0) {
+      tc::prefetch_tensormap(is_k ? &mK : &mV);
+      tc::prefetch_tensormap(is_k ? &mK8 : &mV8);
+      if (is_k) tc::prefetch_tensormap(&mQ);
+    }
+    const CUtensorMap* map = is_k ? &mK : &mV;
+    const CUtensorMap* map8 = is_k ? &mK8 : &mV8;
+    tma_producer(a, R, is_k, map, map8, is_k ? kKStages : kVStages, is_k ? sK : sV,
+                 is_k ? k_full : v_full, is_k ? k_empty : v_empty, &mQ, sQ, kAtom, kTile, tpt,
+                 q_full, q_empty, abort_flag);
+  } else if (layout_ok && warp == 1) {
+    // ===================================================================== MMA issuer
+    // One thread issues both products of both slots, in the order
+    //   QK_0(0) QK_1(0) | PV_0(k) QK_0(k+1) PV_1(k) QK_1(k+1) | ...
+    // (slot s's k-th tile: tile k of a pair item; tile 2k + s otherwise); slot 1's products
+    // release the K/V stages of a pair item.  P_s lives in the columns of S_s: QK_s(k+1)
+    // overwrites what PV_s(k) reads, and both come from this thread, whose tcgen05.mma
+    // operations execute in issue order.  (Serving whichever slot's P is ready first, by
+    // polling both barriers, measured slower.)
+    if (lane == 0) {
+      const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_pv = tc::idesc_bf16_f32(128, 128, false, true);
+      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
+      int g0 = 0, li = 0;            // ring index of the item's first tile; items
+      int qn0 = 0, qn1 = 0;          // Q tiles consumed per buffer
+      int pvn0 = 0, pvn1 = 0;        // PV products issued per slot
+      bool ok = true;
+      ItemIter iter;
+      iter.start(a, R);
+      Item it;
+      for (; ok && iter.next(a, R, it); ++li) {
+        const int nt = it.j1 - it.j0;
+        const bool pair = it.pair;
+        const int n0 = pair ? nt : (nt + 1) >> 1, n1 = pair ? nt : nt >> 1;
+        const int nq = pair ? 2 : 1;
+        ok = tc::mbar_wait(q_full, qn0 & 1, abort_flag, kWaitLimit);
+        ++qn0;
+        if (ok && pair) {
+          ok = tc::mbar_wait(q_full + 1, qn1 & 1, abort_flag, kWaitLimit);
+          ++qn1;
+        }
+        if (!ok) break;
+        int qk_left = n0 + n1;
+        // release: this product is the stage's last reader (a split tile has one reader)
+        auto issue_qk = [&](int s, int k, bool release) -> bool {
+          const int g = g0 + (pair ? k : 2 * k + s);
+          const int kst = g % kKStages, kuse = g / kKStages;
+          if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) return false;
+          tc::tc_fence_after();
+          const uint32_t aQs = aQ + (pair ? s : 0) * kTile;
+          const uint32_t tS = tmem + 128 * s;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t da = tc::smem_desc(aQs + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            const uint64_t db =
+                tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
+            tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(s_full + s);
+          if (!pair || release) tc::mma_commit(k_empty + kst);
+          if (--qk_left == 0)
+            for (int b = 0; b < nq; ++b) tc::mma_commit(q_empty + b);
+          return true;
+        };
+        auto issue_pv = [&](int s, int k, bool release) -> bool {
+          const int g = g0 + (pair ? k : 2 * k + s);
+          const int vst = g % kVStages, vuse = g / kVStages;
+          int& pvn = s == 0 ? pvn0 : pvn1;
+          if (!tc::mbar_wait(p_full + s, pvn & 1, abort_flag, kWaitLimit)) return false;
+          if (!tc::mbar_wait(v_full + vst, vuse & 1, abort_flag, kWaitLimit)) return false;
+          // the first product of an item overwrites O_s: the previous epilogue must have read it
+          if (k == 0 && li > 0 && !tc::mbar_wait(o_free + s, (li - 1) & 1, abort_flag, kWaitLimit))
+            return false;
+          tc::tc_fence_after();
+          const uint32_t tO = tmem + 256 + 128 * s, tP = tmem + 128 * s;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // P_s: 16 keys = 8 columns per MMA
+            const uint64_t db = tc::smem_desc(aV + vst * kTile + kk * 2048, kAtom, 1024);
+            tc::mma_bf16_ts(tO, tP + 8 * kk, db, id_pv, (k > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::mma_commit(pv_done + s);
+          if (!pair || release) tc::mma_commit(v_empty + vst);
+          ++pvn;
+          return true;
+        };
+        if (n0 > 0) ok = issue_qk(0, 0, false);
+        if (ok && n1 > 0) ok = issue_qk(1, 0, true);
+        const int kmax = n0 > n1 ? n0 : n1;
+        for (int k = 0; ok && k < kmax; ++k) {
+          if (k < n0) {
+            ok = issue_pv(0, k, false);
+            if (ok && k + 1 < n0) ok = issue_qk(0, k + 1, false);
+          }
+          if (ok && k < n1) {
+            ok = issue_pv(1, k, true);
+            if (ok && k + 1 < n1) ok = issue_qk(1, k + 1, true);
+          }
+        }
+        g0 += nt;
+      }
+      if (!ok) *abort_flag = 1;
+      // drain every tcgen05 operation issued by this thread before TMEM is released
+      tc::mma_commit(drain);
+      tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+  if (layout_ok) {
+    // ===================================================================== softmax + epilogue
+    // warps 4..7 serve slot 0, warps 8..11 slot 1; warp w reads TMEM lanes 32 (w & 3) ..
+    // 32 (w & 3) + 31: one query row per thread, all 128 keys of a tile
+    const int s = (warp - 4) >> 2, q4 = warp & 3;
+    const int m = q4 * 32 + lane;
+    const uint32_t lane_addr = uint32_t(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + 128 * s;
+    const int t_loc = m >> log2G, g = m & (G - 1);
+    const float sl2 = a.scale_log2;
+    float* xch = reinterpret_cast<float*>(base + kSmemX);   // [2 slots][reference, sum][128]
+    int scnt = 0, ex_cnt = 0, g0 = 0, li = 0;
+    int pv_mine = 0, pv_other = 0;   // PV products of this slot / the other slot so far
+    bool ok = true;
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    for (; ok && iter.next(a, R, it); ++li) {
+      const int nt = it.j1 - it.j0;
+      const bool pair = it.pair;
+      const int n0 = pair ? nt : (nt + 1) >> 1, n1 = pair ? nt : nt >> 1;
+      const int ns = s == 0 ? n0 : n1;
+      const int o = it.o, T = it.T, P = it.P;
+      const int kv_len = P + T;
+      const int t = (it.mt + (pair ? s : 0)) * tpt + t_loc;
+      const bool valid = t < T;
+      const uint32_t* arow = valid ? a.anc + size_t(o + t) * a.W : nullptr;
+      float m_ref = -INFINITY, l = 0.f;
+      // a warp whose 32 rows are all padding keeps only the barrier handshakes and the V
+      // clearing: its P rows feed only its own O rows, which are never read
+      const bool live = __any_sync(0xffffffffu, valid);
+      for (int k = 0; k < ns; ++k) {
+        const int ti = pair ? k : 2 * k + s;
+        const int kbase = (it.j0 + ti) * kBN;
+        if (!warp_wait(s_full + s, scnt & 1, abort_flag)) { ok = false; break; }
+        ++scnt;
+        tc::tc_fence_after();
+        if (live) {
+          // the row's 128 scores at once (one TMEM wait), the maximum of the visible ones, then
+          // 128 independent exponentials 2^(x sl2 - ref), one FMA each, written as bf16 P over
+          // S in place (keys 32 c .. 32 c + 31 go to columns 16 c .. 16 c + 15).  The reference
+          // is lazy: it moves only when the tile's maximum passes it by more than 2^8, and then
+          // the row sum and O_s are rescaled.
+          uint32_t x0[32], x1[32], x2[32], x3[32];
+          tc::tmem_ld32(tS, x0);
+          tc::tmem_ld32(tS + 32, x1);
+          tc::tmem_ld32(tS + 64, x2);
+          tc::tmem_ld32(tS + 96, x3);
+          tc::tmem_ld_wait();
+          const float tmax =
+              fmaxf(fmaxf(mask_max32_row(x0, valid, kbase, P, arow, a.W),
+                          mask_max32_row(x1, valid, kbase + 32, P, arow, a.W)),
+                    fmaxf(mask_max32_row(x2, valid, kbase + 64, P, arow, a.W),
+                          mask_max32_row(x3, valid, kbase + 96, P, arow, a.W))) * sl2;
+          const bool up = tmax > m_ref + kLazyRescale;
+          const float ref = up ? tmax : m_ref;
+          const float factor = (up && m_ref != -INFINITY) ? ex2(m_ref - ref) : 1.f;
+          // O_s carries the factor (its previous product must have landed; an item's first
+          // tile finds nothing to rescale)
+          if (k > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+            if (!warp_wait(pv_done + s, (pv_mine - 1) & 1, abort_flag)) { ok = false; break; }
+            tc::tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+              uint32_t r32[32];
+              const uint32_t ta = tmem + lane_addr + 256 + 128 * s + c0;
+              tc::tmem_ld32(ta, r32);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                r32[c] = __float_as_uint(__uint_as_float(r32[c]) * factor);
+              tc::tmem_st32(ta, r32);
+            }
+          }
+          // a row with no visible key yet (ref = -inf) computes 2^(x - inf) = 0 for every key
+          // (masked keys hold -inf: -inf - inf = -inf, never -inf * 0)
+          const float sl = ref == -INFINITY ? 1.f : sl2;
+          const float add = ref == -INFINITY ? -INFINITY : -ref;
+          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+          exp_chunk(x0, sl, add, rs0, rs1, tS + 0);
+          exp_chunk(x1, sl, add, rs2, rs3, tS + 16);
+          exp_chunk(x2, sl, add, rs0, rs1, tS + 32);
+          exp_chunk(x3, sl, add, rs2, rs3, tS + 48);
+          tc::tmem_st_wait();
+          l = l * factor + ((rs0 + rs1) + (rs2 + rs3));
+          m_ref = ref;
+        }
+        // the request's last tile: zero the V rows past its KV length (stale cache rows times
+        // P = 0 must not turn into NaN) before the tile's first product reads them; TMA must
+        // have landed first.  Thread m clears key m in both 64-column atoms.
+        if (kbase + kBN > kv_len && (!pair || s == 0)) {
+          const int gv = g0 + ti;
+          const int vst = gv % kVStages, vuse = gv / kVStages;
+          if (!warp_wait(v_full + vst, vuse & 1, abort_flag)) { ok = false; break; }
+          if (m >= kv_len - kbase) {
+            uint8_t* vrow = sV + vst * kTile + (m >> 3) * 1024 + (m & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vrow + kAtom + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+          }
+          tc::fence_proxy_async_smem();
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(p_full + s);
+        ++pv_mine;
+      }
+      if (!ok) break;
+      pv_other += s == 0 ? n1 : n0;   // the other slot's products of this item
+      // epilogue: wait for the products whose O columns this warp reads (both slots' for a
+      // split unit)
+      if (ns > 0 && !warp_wait(pv_done + s, (pv_mine - 1) & 1, abort_flag)) { ok = false; break; }
+      if (!pair && (s == 0 ? n1 : n0) > 0 &&
+          !warp_wait(pv_done + (1 - s), (pv_other - 1) & 1, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::tc_fence_after();
+      float lt, M, w0 = 0.f, w1 = 0.f;
+      int c_lo, c_hi;     // output columns this warp writes
+      if (pair) {
+        lt = l;
+        M = m_ref;
+        c_lo = 0;
+        c_hi = 128;
+      } else {
+        // merge the two slots' halves of the K/V range: exchange (reference, sum) with the
+        // other slot's warp of this lane quarter; each slot then writes 64 output columns
+        xch[(s * 2 + 0) * 128 + m] = m_ref;
+        xch[(s * 2 + 1) * 128 + m] = l;
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(ex_bar + q4);
+        if (!warp_wait(ex_bar + q4, ex_cnt & 1, abort_flag)) { ok = false; break; }
+        ++ex_cnt;
+        const float m_o = xch[((1 - s) * 2 + 0) * 128 + m], l_o = xch[((1 - s) * 2 + 1) * 128 + m];
+        const float m0 = s == 0 ? m_ref : m_o, l0 = s == 0 ? l : l_o;
+        const float m1 = s == 0 ? m_o : m_ref, l1 = s == 0 ? l_o : l;
+        M = fmaxf(m0, m1);
+        w0 = (n0 > 0 && m0 != -INFINITY) ? ex2(m0 - M) : 0.f;
+        w1 = (n1 > 0 && m1 != -INFINITY) ? ex2(m1 - M) : 0.f;
+        lt = l0 * w0 + l1 * w1;
+        c_lo = 64 * s;
+        c_hi = c_lo + 64;
+      }
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse2 = lt > 0.f ? M + __log2f(lt) : -INFINITY;
+      if (live) {
+        const int row = (pair ? s * kBM : 0) + m;   // row of a partial piece
+        __nv_bfloat16* orow = a.o + (size_t(o + t) * a.H_q + it.h * G + g) * kD;
+        float* prow = it.slot >= 0 ? a.part_o + (size_t(it.slot) * kPartRows + row) * kD : nullptr;
+#pragma unroll 1
+        for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
+          uint32_t r32[32];
+          float v[32];
+          if (pair) {
+            tc::tmem_ld32(tmem + lane_addr + 256 + 128 * s + c0, r32);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(r32[c]) * inv;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = 0.f;
+            for (int u = 0; u < 2; ++u) {
+              if ((u == 0 ? n0 : n1) == 0) continue;   // warp-uniform: that slot had no tiles
+              tc::tmem_ld32(tmem + lane_addr + 256 + 128 * u + c0, r32);
+              tc::tmem_ld_wait();
+              const float wu = (u == 0 ? w0 : w1) * inv;
+#pragma unroll
+              for (int c = 0; c < 32; ++c) v[c] = fmaf(__uint_as_float(r32[c]), wu, v[c]);
+            }
+          }
+          if (valid) {
+            if (it.slot < 0) {
+#pragma unroll
+              for (int c = 0; c < 32; c += 8) {
+                uint4 w4;
+                w4.x = pack_bf16(v[c], v[c + 1]);
+                w4.y = pack_bf16(v[c + 2], v[c + 3]);
+                w4.z = pack_bf16(v[c + 4], v[c + 5]);
+                w4.w = pack_bf16(v[c + 6], v[c + 7]);
+                *reinterpret_cast<uint4*>(orow + c0 + c) = w4;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 32; c += 4)
+                *reinterpret_cast<float4*>(prow + c0 + c) = make_float4(v[c], v[c + 1], v[c + 2], v[c + 3]);
+            }
+          }
+        }
+        if (valid && (pair || s == 0)) {
+          if (it.slot < 0) {
+            if (a.lse) a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
+          } else {
+            a.part_lse[size_t(it.slot) * kPartRows + row] = lse2;
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        tc::mbar_arrive(o_free + 0);
+        tc::mbar_arrive(o_free + 1);
+      }
+      g0 += nt;
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (*abort_flag && tid == 0) {
+    // every request of this CTA's range is unreliable after an expired wait
+    ItemIter iter;
+    iter.start(a, R);
+    Item it;
+    while (iter.next(a, R, it)) atomicOr(&a.req_status[it.r], SPEC_REQ_TIMEOUT);
+  }
+  tc::tc_fence_after();
+  if (warp == 0) tc::tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------------------ one M-tile
+// For launches in which every unit has one M-tile (at most 128 query rows: G x T <= 128), a
+// kernel with one M-tile per CTA and its scores double-buffered, so that S = Q K^T of the next
+// tile runs while the softmax works on this one: S buffers in TMEM columns 0-127 and 128-255,
+// the O accumulator in 256-383, P (bf16) double-buffered in 384-447 and 448-511.  Warps: 0 Q/K
+// producer, 2 V producer, 1 issues QK, 3 issues PV; warps 4..11 softmax, two per TMEM lane
+// quarter, each exponentiating 64 of a tile's 128 keys against the full row's maximum (lazy
+// reference, O rescaled when it grows by more than 2^8); the epilogue adds the two halves' row
+// sums through a bounded exchange and each warp writes 64 output columns.
+namespace attn1 {
+using attn::kD;
+using attn::kBS;
+using attn::kBM;
+using attn::kBN;
+using attn::kAtom;
+using attn::kTile;
+using attn::kWaitLimit;
+using attn::kLazyRescale;
+using attn::kPartRows;
+constexpr int kThreads = 384;                 // 4 control warps + 8 softmax warps
+constexpr int kKStages = 4;
+constexpr int kVStages = 2;
+constexpr int kSmemQ = 0;
+constexpr int kSmemK = kSmemQ + kTile;
+constexpr int kSmemV = kSmemK + kKStages * kTile;
+constexpr int kSmemBar = kSmemV + kVStages * kTile;
+constexpr int kSmemRed = kSmemBar + 256;      // [2 buffers][2 halves][128 rows] fp32 exchange
+constexpr int kSmemEnd = kSmemRed + 2048;
+constexpr int kSmemBytes = 232448;            // the per-CTA maximum; the slack aligns the base
+constexpr uint32_t kTmemP = 384;
+}  // namespace attn1
+
+__global__ void __launch_bounds__(attn1::kThreads, 1)
+attn_tc_single_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+               const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mK8,
+               const __grid_constant__ CUtensorMap mV8, TcDev a) {
+  using namespace attn1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -632,9 +1125,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       const int kv_len = P + T;
       const int t = it.mt * tpt + t_loc;
       const bool valid = t < T;
-      uint32_t anc[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) anc[k] = (valid && k < a.W) ? a.anc[size_t(o + t) * a.W + k] : 0u;
+      const uint32_t* arow = valid ? a.anc + size_t(o + t) * a.W : nullptr;
       float m_ref = -INFINITY, l = 0.f;   // l: this half's share of the row sum
       // a warp whose 32 rows are all padding keeps only the barrier handshakes (and clears
       // its V rows on the last tile): no TMEM traffic, no math, no P writes -- its O rows
@@ -665,8 +1156,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           tc::tmem_ld32(srow + 64 * (1 - hh), x0);
           tc::tmem_ld32(srow + 64 * (1 - hh) + 32, x1);
           tc::tmem_ld_wait();
-          tmax = fmaxf(mask_max32_raw(x0, valid, kbase + 64 * (1 - hh), P, anc, a.W),
-                       mask_max32_raw(x1, valid, kbase + 64 * (1 - hh) + 32, P, anc, a.W));
+          tmax = fmaxf(mask_max32_row(x0, valid, kbase + 64 * (1 - hh), P, arow, a.W),
+                       mask_max32_row(x1, valid, kbase + 64 * (1 - hh) + 32, P, arow, a.W));
         }
         // this half's 64 scores, kept for the exponentials; the S buffer is free afterwards
         uint32_t s0[32], s1[32];
@@ -676,8 +1167,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(s_free + st);
-        tmax = fmaxf(tmax, mask_max32_raw(s0, valid, kbase + 64 * hh, P, anc, a.W));
-        tmax = fmaxf(tmax, mask_max32_raw(s1, valid, kbase + 64 * hh + 32, P, anc, a.W));
+        tmax = fmaxf(tmax, mask_max32_row(s0, valid, kbase + 64 * hh, P, arow, a.W));
+        tmax = fmaxf(tmax, mask_max32_row(s1, valid, kbase + 64 * hh + 32, P, arow, a.W));
         tmax *= sl2;   // raw maximum -> log2 units (sl2 > 0; -inf stays -inf)
         const bool grow = tmax > m_ref + kLazyRescale;
         const float new_ref = grow ? tmax : m_ref;
@@ -777,7 +1268,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         }
         if (valid && hh == 0 && a.lse) a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
       } else {
-        float* prow = a.part_o + (size_t(it.slot) * kBM + m) * kD + 64 * hh;
+        float* prow = a.part_o + (size_t(it.slot) * kPartRows + m) * kD + 64 * hh;
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t r32[32];
@@ -791,7 +1282,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
                               __uint_as_float(r32[c + 2]) * inv, __uint_as_float(r32[c + 3]) * inv);
           }
         }
-        if (valid) a.part_lse[(size_t(it.slot) * 2 + hh) * kBM + m] = lse2;
+        if (valid && hh == 0) a.part_lse[size_t(it.slot) * kPartRows + m] = lse2;
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -1184,8 +1675,8 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
             if (q == 0 && lane == 0 && a.lse)
               a.lse[size_t(o + t) * a.H_q + it.h * G + g] = lse2 * 0.6931471805599453f;
           } else {
-            a.part_o[(size_t(it.slot) * kBM + n) * kD + kl] = val;
-            if (q == 0 && lane < 2) a.part_lse[(size_t(it.slot) * 2 + lane) * kBM + n] = lse2;
+            a.part_o[(size_t(it.slot) * attn::kPartRows + n) * kD + kl] = val;
+            if (q == 0 && lane == 0) a.part_lse[size_t(it.slot) * attn::kPartRows + n] = lse2;
           }
         }
       }
@@ -1206,10 +1697,10 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
 }
 
 // ------------------------------------------------------------------------------ merge
-// CTA c merges the cut unit of record c by log-sum-exp of its pieces, in range order, into O and
-// lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2.  A unit has at most
-// kMergeFast pieces in the common case: their log-sum-exps and all 64 partial columns are loaded
-// in one batch; longer units take the general loop.
+// CTA (c, y) merges M-tile mt + y of the cut unit of record c by log-sum-exp of its pieces, in
+// range order, into O and lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2.  A
+// unit has at most kMergeFast pieces in the common case: their log-sum-exps and all 64 partial
+// columns are loaded in one batch; longer units take the general loop.
 constexpr int kMergeFast = 2;
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
@@ -1217,17 +1708,20 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   pdl_wait();
   pdl_trigger();
   const MergeRec rec = a.recs[blockIdx.x];
-  if (rec.np < 2) return;
+  const int y = blockIdx.y;
+  if (rec.np < 2 || y >= rec.nmt) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = (warp & 3) * 32 + lane, hh = warp >> 2;
   const int tpt = kBM >> a.log2G;
-  const int t = rec.mt * tpt + (m >> a.log2G), g = m & (a.G - 1);
+  const int t = (rec.mt + y) * tpt + (m >> a.log2G), g = m & (a.G - 1);
   if (t >= rec.T) return;
   const int np = rec.np;
+  const int row = y * kBM + m;   // row of the partial pieces
   auto slot_of = [&](int p) { return p == 0 ? rec.slot0 : 2 * (rec.ca + p); };
-  auto lse_of = [&](int p) { return a.part_lse[(size_t(slot_of(p)) * 2 + hh) * kBM + m]; };
+  auto lse_of = [&](int p) { return a.part_lse[size_t(slot_of(p)) * kPartRows + row]; };
   auto part_of = [&](int p) {
-    return reinterpret_cast<const float4*>(a.part_o + (size_t(slot_of(p)) * kBM + m) * kD + 64 * hh);
+    return reinterpret_cast<const float4*>(a.part_o + (size_t(slot_of(p)) * kPartRows + row) * kD +
+                                           64 * hh);
   };
   __nv_bfloat16* orow = a.o + (size_t(rec.o + t) * a.H_q + rec.h * a.G + g) * kD + 64 * hh;
   float M = -INFINITY, wsum = 0.f, out_lse;
@@ -1398,8 +1892,10 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   d.ctas = ctas;
   const float scale = p->scale > 0.f ? p->scale : 1.f / sqrtf(float(kD));
   d.scale_log2 = scale * 1.4426950408889634f;
-  static DeviceOnce raised_main, raised_small;
+  static DeviceOnce raised_main, raised_single, raised_small;
   spec_status_t st = raise_dyn_smem_once(attn_tc_kernel, kSmemBytes, raised_main);
+  if (st == SPEC_OK)
+    st = raise_dyn_smem_once(attn_tc_single_kernel, attn1::kSmemBytes, raised_single);
   if (st == SPEC_OK)
     st = raise_dyn_smem_once(attn_tc_small_kernel, attn_s::kSmemBytes, raised_small);
   if (st != SPEC_OK) return st;
@@ -1417,11 +1913,18 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
       return SPEC_ERR_INVALID_ARG;
     le = launch_pdl(attn_tc_small_kernel, dim3(ctas), dim3(attn_s::kThreads),
                     size_t(attn_s::kSmemBytes), s, mQs, mK, mV, mK8, mV8, d);
+  } else if ((long long)p->T_max * G <= kBM) {
+    // every unit has one M-tile: scores double-buffered, one M-tile per CTA
+    le = launch_pdl(attn_tc_single_kernel, dim3(ctas), dim3(attn1::kThreads),
+                    size_t(attn1::kSmemBytes), s, mQ, mK, mV, mK8, mV8, d);
   } else {
     le = launch_pdl(attn_tc_kernel, dim3(ctas), dim3(kThreads), size_t(kSmemBytes), s,
                     mQ, mK, mV, mK8, mV8, d);
   }
-  if (le == cudaSuccess) le = launch_pdl(attn_merge_kernel, dim3(ctas), dim3(256), 0, s, d);
+  // a record covers two M-tiles only when some unit has more than 128 query rows
+  const unsigned merge_y = (long long)p->T_max * G > kBM ? 2u : 1u;
+  if (le == cudaSuccess)
+    le = launch_pdl(attn_merge_kernel, dim3(ctas, merge_y), dim3(256), 0, s, d);
   return launch_result(le);
 }
 
