@@ -36,9 +36,15 @@ def log_softmax(row, tau=1.0):
 
 def topk(row, k, tau=1.0):
     """The k tokens with the largest log-probability (ties to the lower id), best first, and
-    their log-probabilities."""
+    their log-probabilities.  Every token at or above the k-th largest value is a candidate
+    (a library partition finds that value); the candidates are ordered by (value descending,
+    id) and the first k kept."""
     lq = log_softmax(row, tau)
-    order = sorted(range(len(lq)), key=lambda x: (-lq[x], x))[:k]
+    n = len(lq)
+    k = min(k, n)
+    kth = np.partition(lq, n - k)[n - k]
+    cand = np.nonzero(lq >= kth)[0]
+    order = sorted(cand.tolist(), key=lambda x: (-lq[x], x))[:k]
     return np.array(order, dtype=np.int64), lq[order]
 
 
