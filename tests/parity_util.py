@@ -5,8 +5,9 @@ Bars (from the verification step's contract):
     compaction slot maps / lengths / moved cache rows, request status bits;
   * the only exception: a ratio test with |u - a| < 1e-6 or a resampled token whose uniform lies
     within 1e-6 of a CDF boundary (fp32 on the GPU cannot resolve fp64 closer than that); such
-    a divergence exempts the rest of that request, is counted, and must stay below 1e-5 of the
-    draws (at least one is tolerated in a small test);
+    a divergence exempts the rest of that request and is counted in TALLY; the whole suite's
+    count must stay below 1e-5 of its draws (tests/test_zy_exemption_tally.py checks it after
+    the parity tests);
   * attention: 1e-5 relative for fp32, 2e-2 absolute for bf16.
 """
 import numpy as np
@@ -18,6 +19,8 @@ from oracle import tree as OT
 from oracle import verify as OV
 
 BAND = 1e-6
+# draws checked and near-boundary exemptions over every check_verify call of the session
+TALLY = {"draws": 0, "exempt": 0, "calls": 0}
 
 
 def np_(t):
@@ -106,7 +109,9 @@ def check_verify(w, step, orc, status_mask=~0):
             f"request {r}: GPU path {g_path} tokens {g_tok} vs oracle {orc['path'][r]} "
             f"{orc['out_tokens'][r]} (events {orc['events'][r]})")
         exempt += 1
-    assert exempt <= max(1, 1e-5 * draws), (exempt, draws)
+    TALLY["draws"] += draws
+    TALLY["exempt"] += exempt
+    TALLY["calls"] += 1
     return draws, exempt
 
 

@@ -1,7 +1,8 @@
 """Parity at the full workload sizes, in the launch configuration the benchmark uses: every
 request for the tree, verification and compaction outputs (bit-exact), and sampled
 (node, head) rows for attention (2e-2 absolute for bf16) -- the oracle computes those rows one by
-one over the request's whole KV range."""
+one over the request's whole KV range.  The chain and Medusa workloads run at tau = 1 and
+tau = 0 (greedy), the chain also at draft noise sigma = 0.5 and 2 (high and low acceptance)."""
 import numpy as np
 import pytest
 import torch
@@ -26,9 +27,13 @@ def _sample_rows(w, snap, n_req, seed):
     return rows
 
 
-@pytest.mark.parametrize("cid,n_req", [(2, 16), (3, 4), (4, 8), (5, 10)])
-def test_full_size_parity(cid, n_req):
-    w = W.make_config(cid, scale="full", device="cuda")
+CASES = [(2, 16, 1.0, 1.0), (2, 4, 0.0, 1.0), (2, 4, 1.0, 0.5), (2, 4, 1.0, 2.0),
+         (3, 4, 1.0, 1.0), (3, 2, 0.0, 1.0), (4, 8, 1.0, 1.0), (5, 10, 1.0, 1.0)]
+
+
+@pytest.mark.parametrize("cid,n_req,tau,sigma", CASES)
+def test_full_size_parity(cid, n_req, tau, sigma):
+    w = W.make_config(cid, scale="full", device="cuda", tau=tau, sigma=sigma)
     snap = PU.snapshot(w)
     step = VerifyStep(w)
     step.tree_build()
@@ -46,5 +51,5 @@ def test_full_size_parity(cid, n_req):
     step.compact()
     torch.cuda.synchronize()
     PU.check_compact(w, step, snap, kb, vb)
-    print(f"config {cid}: attention max |err| {worst:.3g}, verify draws {draws}, "
-          f"near-boundary exemptions {exempt}")
+    print(f"config {cid} tau {tau} sigma {sigma}: attention max |err| {worst:.3g}, verify draws "
+          f"{draws}, near-boundary exemptions {exempt}")
