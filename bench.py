@@ -56,6 +56,9 @@ def parse(argv=None):
                     help="the headline workload (1..5)")
     ap.add_argument("--configs", default=OTHER_CONFIGS,
                     help="workloads measured alongside the headline ('' for none)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests of the headline workload (same shape per request; default: "
+                         "the workload's own batch)")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -99,11 +102,10 @@ def median(xs):
 
 
 def workload_description(w, cid):
-    from speculative_decoding_draft_tree_gb300 import workloads as W
     sizes = w.tree_sizes()
     P = w.prefix_len.cpu().tolist()
     return {
-        "workload": W.CONFIG_NAMES[cid],
+        "workload": w.name,
         "batch_requests": w.B,
         "tree_tokens_per_step": int(sum(sizes)),
         "drafts_per_step": int(sum(sizes) - w.B),
@@ -537,7 +539,7 @@ def reference_arm(args, rank):
     if rank != 0:
         return
     from speculative_decoding_draft_tree_gb300 import workloads as W
-    w = W.make_config(args.workload, scale="full", device="cpu")
+    w = W.make_config(args.workload, scale="full", device="cpu", batch=args.batch)
     tokens_per_step = int(sum(w.tree_sizes()))
     vals = []
     budget = max(0.5, min(2.0, args.cpu_budget))
@@ -621,7 +623,8 @@ def main():
     # ---- set-up of every workload (weak scaling: every rank verifies its own batch)
     runs = {}
     for cid in cids:
-        w = W.make_config(cid, scale="full", device=dev, seeds=rank_seeds(rank))
+        w = W.make_config(cid, scale="full", device=dev, seeds=rank_seeds(rank),
+                          batch=args.batch if cid == args.workload else None)
         step = VerifyStep(w)
         for _ in range(max(3, args.warmup)):
             step.run()
@@ -736,7 +739,7 @@ def main():
     line["gpu_launches"] = head["gpu_launches_per_step"] * steps
     line["clocks"] = clocks
     line["timed_region_wall_s"] = round(timed_wall_s, 2)
-    line["configs"] = {W.CONFIG_NAMES[c]: results[c] for c in cids if c != args.workload}
+    line["configs"] = {runs[c]["w"].name: results[c] for c in cids if c != args.workload}
     line["alpha_sweep"] = sweep
     line["next"] = None if nxt is None else next_results(nxt, peaks)
     print(json.dumps(line))

@@ -670,8 +670,14 @@ def lookahead_config(*, scale: str = "full", device="cpu", seeds: Optional[Dict]
 
 
 def make_config(cid: int, *, scale: str = "full", device="cpu", tau: Optional[float] = None,
-                sigma: float = 1.0, num_layers: int = 1, seeds: Optional[Dict] = None) -> Workload:
+                sigma: float = 1.0, num_layers: int = 1, seeds: Optional[Dict] = None,
+                batch: Optional[int] = None) -> Workload:
+    """Workload `cid` (1..5) at full size or small.  `batch` (full size only) keeps the shape of
+    every request and takes fewer or more of them (the EAGLE-2 / ECHO budget scales with it)."""
     full = scale == "full"
+    if batch is not None and full and cid in (2, 3, 4, 5):
+        return _make_batch(cid, batch, device=device, tau=tau, sigma=sigma,
+                           num_layers=num_layers, seeds=seeds)
     name = CONFIG_NAMES[cid] + ("" if full else "_small")
     if cid == 1:
         return chain_workload(B=1, gamma=4, V=1000, dtype="f32", H_q=4, H_kv=4, d=64,
@@ -710,3 +716,23 @@ def make_config(cid: int, *, scale: str = "full", device="cpu", tau: Optional[fl
                                     K_max=150, device=device, num_layers=num_layers, name=name,
                                     seeds=seeds)
     raise ValueError(f"unknown configuration {cid}")
+
+
+def _make_batch(cid: int, B: int, *, device, tau, sigma, num_layers, seeds) -> Workload:
+    name = f"{CONFIG_NAMES[cid]}_batch{B}"
+    t = 1.0 if tau is None else tau
+    if cid == 2:
+        return chain_workload(B=B, gamma=5, V=32000, dtype="bf16", H_q=32, H_kv=32, d=128,
+                              prefix=2048, tau=t, target_std=3.0, noise_std=sigma, device=device,
+                              num_layers=num_layers, contiguous=True, name=name, seeds=seeds)
+    if cid == 3:
+        return medusa_workload(B=B, ks=(3, 5, 7), V=32000, dtype="bf16", H_q=40, H_kv=40, d=128,
+                               prefix=4096, tau=t, device=device, num_layers=num_layers,
+                               name=name, seeds=seeds)
+    if cid == 4:
+        return specinfer_workload(B=B, schedule=(3, 2, 2, 1, 1), V=128256, dtype="bf16", H_q=32,
+                                  H_kv=8, d=128, prefix=8192, tau=t, device=device,
+                                  num_layers=num_layers, name=name, seeds=seeds)
+    return eagle2_echo_workload(B=B, V=152064, dtype="bf16", H_q=64, H_kv=8, d=128,
+                                prefix_range=(1024, 32768), tau=t, K_max=2048 * B // 64,
+                                device=device, num_layers=num_layers, name=name, seeds=seeds)
