@@ -333,16 +333,40 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return r;
 }
 
-// 32 exponentials 2^(x sl + add) of one key chunk (masked keys hold -inf), summed into two
-// partial sums and stored as 16 columns of bf16 pairs at TMEM address `dst`
-__device__ __forceinline__ void exp_chunk(const uint32_t (&x)[32], float sl, float add, float& ra,
-                                          float& rb, uint32_t dst) {
+// Packed fp32 pairs (one 64-bit register pair): fma.rn.f32x2 / add.f32x2 do two lanes' worth of
+// FMA / add in one instruction.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// 32 exponentials 2^(x sl + add) of one key chunk (masked keys hold -inf), the arguments formed
+// two at a time by a packed FMA and summed two at a time into the packed partial sum `acc`, and
+// stored as 16 columns of bf16 pairs at TMEM address `dst`
+__device__ __forceinline__ void exp_chunk(const uint32_t (&x)[32], uint64_t sl2, uint64_t add2,
+                                          uint64_t& acc, uint32_t dst) {
   uint32_t pk[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float p0 = ex2(fmaf(__uint_as_float(x[2 * i]), sl, add));
-    const float p1 = ex2(fmaf(__uint_as_float(x[2 * i + 1]), sl, add));
-    if (i & 1) rb += p0 + p1; else ra += p0 + p1;
+    float y0, y1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1])), sl2, add2),
+              y0, y1);
+    const float p0 = ex2(y0), p1 = ex2(y1);
+    acc = f2_add(acc, f2_pack(p0, p1));
     pk[i] = pack_bf16(p0, p1);
   }
   tc::tmem_st16(dst, pk);
@@ -765,13 +789,17 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           // (masked keys hold -inf: -inf - inf = -inf, never -inf * 0)
           const float sl = ref == -INFINITY ? 1.f : sl2;
           const float add = ref == -INFINITY ? -INFINITY : -ref;
-          float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
-          exp_chunk(x0, sl, add, rs0, rs1, tS + 0);
-          exp_chunk(x1, sl, add, rs2, rs3, tS + 16);
-          exp_chunk(x2, sl, add, rs0, rs1, tS + 32);
-          exp_chunk(x3, sl, add, rs2, rs3, tS + 48);
+          const uint64_t sl2v = f2_pack(sl, sl), addv = f2_pack(add, add);
+          uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
+          exp_chunk(x0, sl2v, addv, acc0, tS + 0);
+          exp_chunk(x1, sl2v, addv, acc1, tS + 16);
+          exp_chunk(x2, sl2v, addv, acc0, tS + 32);
+          exp_chunk(x3, sl2v, addv, acc1, tS + 48);
           tc::tmem_st_wait();
-          l = l * factor + ((rs0 + rs1) + (rs2 + rs3));
+          float ra, rb, rc, rd;
+          f2_unpack(acc0, ra, rb);
+          f2_unpack(acc1, rc, rd);
+          l = l * factor + ((ra + rb) + (rc + rd));
           m_ref = ref;
         }
         // the request's last tile: zero the V rows past its KV length (stale cache rows times
