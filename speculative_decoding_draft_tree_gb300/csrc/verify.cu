@@ -19,24 +19,34 @@
 //      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over 32-element chunks
 //      (Kahan-compensated), then a block reduction (max, then a double-float sum) -> (m, Z);
 //      tau = 0 keeps (max, lowest argmax) instead;
-//   2. walk  (one CTA of 512 threads per request): validates the request's tokens, draft rows
+//   2. walk  (one cluster of 1..8 CTAs of 512 threads per request; CTA k of a cluster owns the
+//      k-th contiguous slice of the vocabulary): validates the request's tokens, draft rows
 //      and depths, then walks the tree.  A parallel prologue gathers
 //      every node's test operands and decides every plain ratio test u < p / q at once (thread
 //      per node, from (m, Z)); only later siblings under the residual rule are tested on the way,
 //      on thread 0.  Every vocab-wide step (sibling residual mass, residual / bonus inverse CDF,
-//      leaf max / argmax) is a block-wide pass: 16 warps own contiguous vocab ranges, per-warp
-//      double-float sums are scanned in token order, and the warp holding the crossing rescans
-//      its unit sums (kept in shared memory) to find the unit, then the unit's 8 elements.
+//      leaf max / argmax) is a pass over each CTA's slice: 16 warps own contiguous ranges of
+//      it, per-warp double-float sums are scanned in token order, the CTAs exchange their slice
+//      totals through distributed shared memory (one cluster barrier) and combine them in rank
+//      order, and the CTA whose range of the prefix holds the crossing rescans its unit sums
+//      (kept in shared memory) to find the unit, then the unit's 8 elements.  Every CTA of a
+//      cluster runs the same walk on the same values in the same order, so all take the same
+//      decisions and pass the same barriers.  A pass costs two exponentials per token, so one
+//      SM per request is bound by its special-function units; slicing the vocabulary over a
+//      cluster divides that time by the cluster size.
 // Under the multi-draft sibling rule (siblings proposed by different draft models, each with its
 // own q) the running residual has no closed form: it is materialised per request in a
 // double-buffered fp32 scratch row, one vocab pass per rejected sibling (the last one is folded
-// into the final draw), and that case runs its own instantiation of the walk kernel.
+// into the final draw), and that case runs its own instantiation of the walk kernel, with one
+// CTA per request: its ratio tests read single elements of the scratch row, which a slice
+// owned by another CTA would have written.
 // Randomness is never generated here: u_acc / u_samp come from the caller's uniforms.
 #include <math.h>
 
 #include <atomic>
 #include <mutex>
 
+#include "cluster.cuh"
 #include "common.cuh"
 #include "kv_compact.cuh"
 #include "verify_cluster.cuh"
@@ -77,6 +87,7 @@ struct VerifyDev {
   float* rbuf;          // multi-draft: per request, two residual rows of rld floats
   int64_t rld;
   int32_t after_rows;   // the walk follows a rows kernel of the same call
+  int32_t walk_per;     // 8-element vocabulary units of each CTA of a request's walk cluster
 };
 
 // ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
@@ -317,6 +328,10 @@ static_assert(kWalkWarps <= 32, "one warp scans the per-warp totals");
 // per-unit sums of a vocab pass stay in dynamic shared memory for vocabularies up to this many
 // 8-element units (V <= 262144); the search step then rescans them instead of the rows
 constexpr int kWalkMaxSmemUnits = 32768;
+// a request's walk runs on a cluster of up to kWalkMaxCl CTAs, each with a vocabulary slice of
+// at least kWalkMinUnits units (one per thread: below that a pass is bound by its barriers)
+constexpr int kWalkMaxCl = 8;
+constexpr int kWalkMinUnits = kWalkThreads;
 
 // scratch of the block-wide vocabulary passes
 struct PassSmem {
@@ -327,7 +342,43 @@ struct PassSmem {
   int ired[kWalkWarps];
   double total;              // the pass's total mass (read by thread 0)
   int found;
+  // read by the other CTAs of the cluster, per exchange (parity): this CTA's slice total (or
+  // slice max) and its last unit with mass (or slice argmax)
+  float px_hi[2], px_lo[2];
+  int px_last[2];
 };
+
+// This CTA's share of a request's walk: its rank in the request's cluster, the cluster's size,
+// the slice length and its own units [u0, u1); npass counts exchanges (the parity of the
+// exchange slot) and `arrived` records an early arrival on the kernel's last cluster barrier.
+struct Slice {
+  int rank, ncl, per, u0, u1;
+  int npass;
+  bool arrived;
+};
+
+// Publishes this CTA's (hi, lo, last) and returns, in lane k < ncl of every warp, rank k's
+// values (other lanes: fill_hi, 0, -1).  One cluster barrier; the slot written two exchanges
+// ago is free, since every CTA read it before arriving on the barrier of the exchange between.
+__device__ __forceinline__ void slice_exchange(PassSmem& sh, Slice& sl, float hi, float lo,
+                                               int last, float fill_hi, dfloat& rv, int& rl) {
+  const int slot = sl.npass & 1;
+  ++sl.npass;
+  if (threadIdx.x == 0) {
+    sh.px_hi[slot] = hi;
+    sh.px_lo[slot] = lo;
+    sh.px_last[slot] = last;
+  }
+  cluster_sync();
+  const int lane = threadIdx.x & 31;
+  rv = dfloat{fill_hi, 0.f};
+  rl = -1;
+  if (lane < sl.ncl) {
+    rv.hi = ld_cluster_f32(&sh.px_hi[slot], lane);
+    rv.lo = ld_cluster_f32(&sh.px_lo[slot], lane);
+    rl = ld_cluster_s32(&sh.px_last[slot], lane);
+  }
+}
 
 struct WalkSmem {
   int16_t par[SPEC_MAX_TREE];
@@ -360,38 +411,65 @@ __device__ __forceinline__ int warp_max_i(int v) {
   return v;
 }
 
+// Calls f(unit, x) for this thread's units of the slice (sl.u0 + tid + i * kWalkThreads, in
+// increasing i) with the unit's 8 values; kSlots units' loads stay in flight, each slot refilled
+// as soon as its unit is unpacked.
+template <int kSlots, typename T, typename F>
+__device__ __forceinline__ void slice_units(const T* row, int V, float fill, const Slice& sl,
+                                            F&& f) {
+  const int full = V / 8, vend = min(full, sl.u1);
+  const int first = sl.u0 + int(threadIdx.x);
+  RawUnit<T> rv[kSlots];
+#pragma unroll
+  for (int j = 0; j < kSlots; ++j)
+    if (first + j * kWalkThreads < vend) rv[j].load(row, first + j * kWalkThreads);
+  for (int base = first; base < sl.u1; base += kSlots * kWalkThreads) {
+#pragma unroll
+    for (int j = 0; j < kSlots; ++j) {
+      const int unit = base + j * kWalkThreads;
+      if (unit < sl.u1) {
+        float x[8];
+        rv[j].get(row, unit, V, full, fill, x);
+        const int nx = unit + kSlots * kWalkThreads;
+        if (nx < vend) rv[j].load(row, nx);
+        f(unit, x);
+      }
+    }
+  }
+}
+
+// The row max: each CTA over its slice, then over the cluster's slices.
 template <typename TT>
-__device__ float block_row_max(const TT* row, int V, PassSmem& sh) {
+__device__ float slice_row_max(const TT* row, int V, PassSmem& sh, Slice& sl) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int full = V / 8, nunits = (V + 7) / 8;
   float m = -INFINITY;
-  for (int unit = tid; unit < nunits; unit += kWalkThreads) {
-    float x[8];
-    load8(row, unit, V, full, -INFINITY, x);
+  slice_units<16 / int(sizeof(TT))>(row, V, -INFINITY, sl, [&](int, const float (&x)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) m = fmaxf(m, x[k]);
-  }
+  });
   m = warp_max(m);
   if (lane == 0) sh.fred[warp] = m;
   __syncthreads();
   const float M = warp_max(lane < kWalkWarps ? sh.fred[lane] : -INFINITY);  // every warp reduces
   __syncthreads();
-  return M;
+  dfloat rv;
+  int rl;
+  slice_exchange(sh, sl, M, 0.f, 0, -INFINITY, rv, rl);
+  return warp_max(rv.hi);
 }
 
+// The lowest index of the row max: each CTA over its slice, then over the cluster's slices.
 template <typename TT>
-__device__ int block_row_argmax(const TT* row, int V, PassSmem& sh) {
+__device__ int slice_row_argmax(const TT* row, int V, PassSmem& sh, Slice& sl) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int full = V / 8, nunits = (V + 7) / 8;
   float best = -INFINITY;
   int arg = 0x7fffffff;
-  for (int unit = tid; unit < nunits; unit += kWalkThreads) {
-    float x[8];
-    load8(row, unit, V, full, -INFINITY, x);
+  // a thread's units come in increasing order: a strict > keeps the lowest index
+  slice_units<16 / int(sizeof(TT))>(row, V, -INFINITY, sl, [&](int unit, const float (&x)[8]) {
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       if (x[k] > best) { best = x[k]; arg = unit * 8 + k; }
-  }
+  });
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     float ob = __shfl_xor_sync(0xffffffffu, best, off);
@@ -409,7 +487,18 @@ __device__ int block_row_argmax(const TT* row, int V, PassSmem& sh) {
     if (ob > bb || (ob == bb && oa < ba)) { bb = ob; ba = oa; }
   }
   __syncthreads();
-  return ba;
+  dfloat rv;
+  int rl;
+  slice_exchange(sh, sl, bb, 0.f, ba, -INFINITY, rv, rl);
+  float cb = rv.hi;
+  int ca = lane < sl.ncl ? rl : 0x7fffffff;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, cb, off);
+    const int oa = __shfl_xor_sync(0xffffffffu, ca, off);
+    if (ob > cb || (ob == cb && oa < ca)) { cb = ob; ca = oa; }
+  }
+  return ca;
 }
 
 // Element weights of the distribution being summed / sampled: p itself (bonus token, up to the
@@ -499,8 +588,9 @@ struct MultiFn {
 };
 
 struct PassResult {
-  int tok;    // sampled token (search passes), -1 otherwise
-  bool pos;   // the total mass is > 0
+  int tok;     // sampled token (search passes, in the owner CTA only), -1 otherwise
+  bool pos;    // the total mass is > 0
+  int owner;   // search passes with mass: the rank whose slice holds the token
 };
 
 // double-float value minus theta (th_hi + th_lo) is > 0
@@ -508,58 +598,94 @@ __device__ __forceinline__ bool df_above(dfloat x, float th_hi, float th_lo) {
   return ((x.hi - th_hi) + (x.lo - th_lo)) > 0.f;
 }
 
-// Block-wide pass over the vocabulary: total mass of the weights (sh.total, thread 0) and, when
-// `search`, the smallest token x with sum_{y<=x} w(y) > u * total.  Phase 1 stores every 8-element
-// unit's weight sum in shared memory (each thread issues the loads of kUnits units before it uses
-// any).  Phase 2 gives thread t the contiguous units [t * per, (t + 1) * per): a block scan of the
-// threads' double-float run sums gives every thread its prefix, the first thread whose inclusive
-// prefix passes theta walks its units, then the crossing unit's 8 elements.  No fp64: theta is a
-// double-float product.  Without `usum` (very large vocabularies) phase 2 recomputes unit sums.
+// Pass over the vocabulary, each CTA of the cluster over its slice: total mass of the weights
+// (sh.total, thread 0; the same value in every CTA) and, when `search`, the smallest token x with
+// sum_{y<=x} w(y) > u * total.  Phase 1 reads the slice (kUnits units' loads in flight per
+// thread); a mass pass ends with a block reduction of the threads' sums and the exchange of the
+// slice totals, a search pass stores every 8-element unit's weight sum in shared memory and
+// continues.  Phase 2 gives
+// thread t the contiguous units [t * run, (t + 1) * run) of the slice: a block scan of the
+// threads' double-float run sums gives every thread its prefix within the slice, the CTAs
+// exchange their slice totals and scan them in rank order, and in the CTA whose range holds
+// theta the first thread whose inclusive prefix passes it walks its units, then the crossing
+// unit's 8 elements.  No fp64: theta is a double-float product.  Without `usum` (very large
+// vocabularies) phase 2 recomputes unit sums.  A search pass with mass is the walk's final
+// draw: each CTA arrives on the kernel's last cluster barrier right after its remote reads.
 template <typename TT, typename TD, typename Fn>
 __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const Fn& fn,
-                                 bool search, float u, float* usum, PassSmem& sh) {
+                                 bool search, float u, float* usum, PassSmem& sh, Slice& sl) {
   constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int full = V / 8, nunits = (V + 7) / 8;
-  if (usum || fn.stores()) {
-    for (int base = 0; base < nunits; base += kWalkThreads * kUnits) {
-      RawUnit<TT> rt[kUnits];
-      RawUnit<TD> rd[kUnits];
+  const int full = V / 8;
+  const int s0 = sl.u0, s1 = sl.u1, nu = s1 - s0;
+  const int vend = min(full, s1);   // units of the slice read as whole vectors end here
+  // phase 1, thread t's units s0 + t + i * kWalkThreads: kUnits units' loads in flight, each
+  // slot refilled as soon as its unit is unpacked.  A search pass keeps the unit sums; a mass
+  // pass only the thread's total.
+  dfloat mine1 = df_make(0.f);
+  if (!search || usum || fn.stores()) {
+    const int first = s0 + tid;
+    RawUnit<TT> rt[kUnits];
+    RawUnit<TD> rd[kUnits];
 #pragma unroll
-      for (int j = 0; j < kUnits; ++j) {
-        const int unit = base + j * kWalkThreads + tid;
-        if (unit < full) {
-          if (fn.loads_t()) rt[j].load(trow, unit);
-          if (fn.loads_d()) rd[j].load(drow, unit);
-        }
+    for (int j = 0; j < kUnits; ++j) {
+      const int unit = first + j * kWalkThreads;
+      if (unit < vend) {
+        if (fn.loads_t()) rt[j].load(trow, unit);
+        if (fn.loads_d()) rd[j].load(drow, unit);
       }
+    }
+    for (int base = first; base < s1; base += kUnits * kWalkThreads) {
 #pragma unroll
       for (int j = 0; j < kUnits; ++j) {
-        const int unit = base + j * kWalkThreads + tid;
-        if (unit < nunits) {
+        const int unit = base + j * kWalkThreads;
+        if (unit < s1) {
           float xt[8], xd[8], w[8];
           if (fn.loads_t()) rt[j].get(trow, unit, V, full, -INFINITY, xt);
           if (fn.loads_d()) rd[j].get(drow, unit, V, full, fn.probs ? 0.f : -INFINITY, xd);
+          const int nx = unit + kUnits * kWalkThreads;
+          if (nx < vend) {
+            if (fn.loads_t()) rt[j].load(trow, nx);
+            if (fn.loads_d()) rd[j].load(drow, nx);
+          }
           fn.apply(unit, xt, xd, w);
           if (fn.stores()) fn.store(unit, w);
-          if (usum) usum[unit] = sum8(w);
+          const float su = sum8(w);
+          if (!search) mine1 = df_add_f(mine1, su);
+          else if (usum) usum[unit - s0] = su;
         }
       }
     }
-    __syncthreads();
   }
+  if (!search) {
+    // a mass pass: the slice total is a block reduction of the threads' totals
+    const dfloat wt = warp_sum_df(mine1);
+    if (lane == 0) sh.wtot[warp] = wt;
+    __syncthreads();
+    const dfloat ctot = warp_sum_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f));
+    dfloat rv;
+    int rl;
+    slice_exchange(sh, sl, ctot.hi, ctot.lo, -1, 0.f, rv, rl);
+    const dfloat rincl = warp_scan_df(rv, lane);
+    const dfloat total = {__shfl_sync(0xffffffffu, rincl.hi, sl.ncl - 1),
+                          __shfl_sync(0xffffffffu, rincl.lo, sl.ncl - 1)};
+    if (tid == 0) sh.total = df_to_d(total);
+    // no barrier: every read of sh.wtot came before the exchange's cluster barrier
+    return PassResult{-1, total.hi > 0.f, -1};
+  }
+  __syncthreads();
   auto unit_sum = [&](int unit) -> float {
-    if (usum) return usum[unit];
+    if (usum) return usum[unit - s0];
     float w[8];
     fn.unit(trow, drow, unit, V, full, w);
     return sum8(w);
   };
   // phase 2: this thread's run of units, scanned across the block
-  const int per = (nunits + kWalkThreads - 1) / kWalkThreads;
-  const int u0 = min(tid * per, nunits), u1 = min(u0 + per, nunits);
+  const int run = (nu + kWalkThreads - 1) / kWalkThreads;
+  const int a0 = s0 + min(tid * run, nu), a1 = min(a0 + run, s1);
   dfloat mine = df_make(0.f);
   int lastp = -1;
-  for (int unit = u0; unit < u1; ++unit) {
+  for (int unit = a0; unit < a1; ++unit) {
     const float su = unit_sum(unit);
     mine = df_add_f(mine, su);
     if (su > 0.f) lastp = unit;
@@ -571,61 +697,82 @@ __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const Fn
   if (lane == 31) sh.wtot[warp] = incl_w;
   if (lane == 0) sh.wlast[warp] = lastp;
   __syncthreads();
-  // every warp scans the warp totals: its own base and the block total
+  // every warp scans the warp totals: its own base and the slice total
   const dfloat wsc = warp_scan_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f), lane);
   dfloat wex = df_shfl_up(wsc, 1);
   if (lane == 0) wex = df_make(0.f);
   const dfloat wbase = {__shfl_sync(0xffffffffu, wex.hi, warp), __shfl_sync(0xffffffffu, wex.lo, warp)};
-  const dfloat total = {__shfl_sync(0xffffffffu, wsc.hi, 31), __shfl_sync(0xffffffffu, wsc.lo, 31)};
-  const int fb = warp_max_i(lane < kWalkWarps ? sh.wlast[lane] : -1);   // last unit with mass
+  const dfloat ctot = {__shfl_sync(0xffffffffu, wsc.hi, 31), __shfl_sync(0xffffffffu, wsc.lo, 31)};
+  const int fb = warp_max_i(lane < kWalkWarps ? sh.wlast[lane] : -1);   // slice's last unit with mass
+  // the cluster: slice totals in rank order
+  dfloat rv;
+  int rl;
+  slice_exchange(sh, sl, ctot.hi, ctot.lo, fb, 0.f, rv, rl);
+  const dfloat rincl = warp_scan_df(rv, lane);
+  const dfloat total = {__shfl_sync(0xffffffffu, rincl.hi, sl.ncl - 1),
+                        __shfl_sync(0xffffffffu, rincl.lo, sl.ncl - 1)};
+  const int lastall = warp_max_i(rl);
   const bool pos = total.hi > 0.f;
   if (tid == 0) sh.total = df_to_d(total);
-  if (!search) {
+  if (!pos) {
     __syncthreads();   // sh is reused by the next pass
-    return PassResult{-1, pos};
+    return PassResult{-1, pos, -1};
   }
+  cluster_arrive();   // no CTA reads another's shared memory after the final draw's exchange
+  sl.arrived = true;
   // theta = u * total as a double-float (exact product of u and total.hi, plus u * total.lo)
   const float ph = u * total.hi;
   const float pl = fmaf(u, total.hi, -ph) + u * total.lo;
   const float th_hi = ph + pl, th_lo = pl - (th_hi - ph);
-  const dfloat prefix = df_add(wbase, excl_w);
-  const bool c = pos && df_above(df_add(wbase, incl_w), th_hi, th_lo);
-  const unsigned cm = __ballot_sync(0xffffffffu, c);
-  if (lane == 0) sh.wfirst[warp] = cm ? warp * 32 + __ffs(cm) - 1 : 0x7fffffff;
+  const unsigned rm = __ballot_sync(0xffffffffu, lane < sl.ncl && df_above(rincl, th_hi, th_lo));
+  const int cstar = rm ? __ffs(rm) - 1 : -1;
+  // no rank crossed (theta at the total by rounding): the last unit with mass decides
+  const int owner = cstar >= 0 ? cstar : (lastall >= 0 ? lastall / sl.per : -1);
+  if (owner != sl.rank) return PassResult{-1, pos, owner};
+  dfloat rex = df_shfl_up(rincl, 1);
+  if (lane == 0) rex = df_make(0.f);
+  const dfloat rbase = {__shfl_sync(0xffffffffu, rex.hi, sl.rank),
+                        __shfl_sync(0xffffffffu, rex.lo, sl.rank)};
   if (tid == 0) sh.found = -1;
-  __syncthreads();
-  int first = 0x7fffffff;
+  if (cstar == sl.rank) {
+    const dfloat prefix = df_add(rbase, df_add(wbase, excl_w));
+    const bool c = a0 < a1 && df_above(df_add(rbase, df_add(wbase, incl_w)), th_hi, th_lo);
+    const unsigned cm = __ballot_sync(0xffffffffu, c);
+    if (lane == 0) sh.wfirst[warp] = cm ? warp * 32 + __ffs(cm) - 1 : 0x7fffffff;
+    __syncthreads();
+    int first = 0x7fffffff;
 #pragma unroll
-  for (int w = 0; w < kWalkWarps; ++w) first = min(first, sh.wfirst[w]);
-  if (tid == first) {
-    dfloat cum = prefix;
-    int cross_unit = -1, last_pos_unit = -1;
-    for (int unit = u0; unit < u1; ++unit) {
-      const float su = unit_sum(unit);
-      const dfloat nx = df_add_f(cum, su);
-      if (su > 0.f) last_pos_unit = unit;
-      if (df_above(nx, th_hi, th_lo)) { cross_unit = unit; break; }
-      cum = nx;
-    }
-    // rounding can leave the crossing inside the run total only: take its last live unit
-    const int cu = cross_unit >= 0 ? cross_unit : last_pos_unit;
-    int tok = -1, lastpos = -1;
-    if (cu >= 0) {
-      float w[8];
-      fn.unit(trow, drow, cu, V, full, w);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        cum = df_add_f(cum, w[k]);
-        if (w[k] > 0.f) lastpos = cu * 8 + k;
-        if (tok < 0 && cross_unit >= 0 && df_above(cum, th_hi, th_lo)) tok = cu * 8 + k;
+    for (int w = 0; w < kWalkWarps; ++w) first = min(first, sh.wfirst[w]);
+    if (tid == first) {
+      dfloat cum = prefix;
+      int cross_unit = -1, last_pos_unit = -1;
+      for (int unit = a0; unit < a1; ++unit) {
+        const float su = unit_sum(unit);
+        const dfloat nx = df_add_f(cum, su);
+        if (su > 0.f) last_pos_unit = unit;
+        if (df_above(nx, th_hi, th_lo)) { cross_unit = unit; break; }
+        cum = nx;
       }
+      // rounding can leave the crossing inside the run total only: take its last live unit
+      const int cu = cross_unit >= 0 ? cross_unit : last_pos_unit;
+      int tok = -1, lastpos = -1;
+      if (cu >= 0) {
+        float w[8];
+        fn.unit(trow, drow, cu, V, full, w);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          cum = df_add_f(cum, w[k]);
+          if (w[k] > 0.f) lastpos = cu * 8 + k;
+          if (tok < 0 && cross_unit >= 0 && df_above(cum, th_hi, th_lo)) tok = cu * 8 + k;
+        }
+      }
+      sh.found = tok >= 0 ? tok : lastpos;
     }
-    sh.found = tok >= 0 ? tok : lastpos;
   }
   __syncthreads();
   int tok = sh.found;
-  if (tok < 0 && pos) {
-    // no thread crossed (theta at the total by rounding): the last element with mass
+  if (tok < 0) {
+    // no thread crossed (theta at the slice's end by rounding): its last element with mass
     if (tid == 0 && fb >= 0) {
       float w[8];
       fn.unit(trow, drow, fb, V, full, w);
@@ -639,28 +786,35 @@ __device__ PassResult vocab_pass(const TT* trow, const TD* drow, int V, const Fn
     tok = sh.found;
   }
   __syncthreads();   // sh is reused by the next pass
-  return PassResult{tok, pos};
+  return PassResult{tok, pos, owner};
 }
 
 // Thread 0: the ratio test of a later sibling under the sibling residual rule,
-// u < max(0, p - C q) / (N q) written as u * N * q < max(0, p - C q) (q >= 0).
+// u < max(0, p - C q) / (N q) written as u * N * q < max(0, p - C q) (q >= 0), with both sides
+// multiplied by Zt (and Zd for draft logits), p = et / Zt, q = ed / Zd: no fp64 division (a
+// long dependent chain on GB300's fp64 unit, on the walk's critical path).
 template <typename TT, typename TD>
 __device__ bool residual_ratio_test(const VerifyDev& a, const WalkSmem& sh, int node, int c) {
-  const double p = double(expf((sh.xt[c] - sh.st_m[node]) * a.inv_tau)) / sh.st_Z[node];
-  const double q = a.probs ? double(sh.xd[c])
-                           : double(expf((sh.xd[c] - sh.sd_m[node]) * a.inv_tau)) / sh.sd_Z[node];
-  const double num = fmax(0.0, p - sh.C * q);
-  return double(sh.uacc[c]) * (sh.Nk * q) < num;
+  const double et = double(expf((sh.xt[c] - sh.st_m[node]) * a.inv_tau));
+  const double Zt = sh.st_Z[node];
+  const double u = double(sh.uacc[c]);
+  if (a.probs) {
+    const double qZ = double(sh.xd[c]) * Zt;   // q Zt
+    return u * (sh.Nk * qZ) < fmax(0.0, et - sh.C * qZ);
+  }
+  const double ed = double(expf((sh.xd[c] - sh.sd_m[node]) * a.inv_tau));
+  const double qZ = ed * Zt;                    // q Zt Zd
+  return u * (sh.Nk * qZ) < fmax(0.0, et * sh.sd_Z[node] - sh.C * qZ);
 }
 
 // Thread 0: the ratio test of a later sibling c under the multi-draft rule,
-// u < R_{j-1}(tok) / (N_{j-1} q_c(tok)) written as u * N_{j-1} * q_c(tok) < R_{j-1}(tok), with
-// R_{j-1} the scratch row the previous update pass stored.
+// u < R_{j-1}(tok) / (N_{j-1} q_c(tok)) written as u * N_{j-1} * q_c(tok) < R_{j-1}(tok) (times Zd
+// for draft logits), with R_{j-1} the scratch row the previous update pass stored.
 __device__ bool multi_ratio_test(const VerifyDev& a, const WalkSmem& sh, int c, const float* src) {
-  const double q = a.probs ? double(sh.xd[c])
-                           : double(expf((sh.xd[c] - sh.sd_m[c]) * a.inv_tau)) / sh.sd_Z[c];
   const double num = double(src[sh.tok[c]]);
-  return double(sh.uacc[c]) * (sh.Nk * q) < num;
+  if (a.probs) return double(sh.uacc[c]) * (sh.Nk * double(sh.xd[c])) < num;
+  const double ed = double(expf((sh.xd[c] - sh.sd_m[c]) * a.inv_tau));
+  return double(sh.uacc[c]) * (sh.Nk * ed) < num * sh.sd_Z[c];
 }
 
 template <typename TT, typename TD, bool kMulti>
@@ -673,7 +827,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   // before the statistics and before any store.  Without a rows kernel, wait first.
   if (!a.after_rows) pdl_wait();
   pdl_trigger();
-  const int r = blockIdx.x;
+  const int rank = cluster_rank(), ncl = cluster_size();
+  const int r = blockIdx.x / ncl;
   const int tid = threadIdx.x;
   int32_t* path_row = a.path + size_t(r) * a.max_path;
   int32_t* tok_row = a.out_tokens + size_t(r) * a.max_path;
@@ -705,17 +860,31 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   __syncthreads();
   const int st = st0 | sh.bad;
   if (st != 0) {
+    // the same exit in every CTA of the cluster (the same data), before any cluster barrier
     pdl_wait();
-    if (tid == 0 && sh.bad) atomicOr(&a.req_status[r], sh.bad);
-    for (int k = tid; k < a.max_path; k += kWalkThreads) { path_row[k] = -1; tok_row[k] = -1; }
-    if (tid == 0) {
-      a.out_len[r] = 0;
-      a.n_acc[r] = -1;
-      if (a.rejections) a.rejections[r] = 0;
+    if (rank == 0) {
+      if (tid == 0 && sh.bad) atomicOr(&a.req_status[r], sh.bad);
+      for (int k = tid; k < a.max_path; k += kWalkThreads) { path_row[k] = -1; tok_row[k] = -1; }
+      if (tid == 0) {
+        a.out_len[r] = 0;
+        a.n_acc[r] = -1;
+        if (a.rejections) a.rejections[r] = 0;
+      }
     }
     return;
   }
-  float* usum = (a.V + 7) / 8 <= kWalkMaxSmemUnits ? usum_dyn : nullptr;
+  Slice sl;
+  {
+    const int nunits = (a.V + 7) / 8;
+    sl.rank = rank;
+    sl.ncl = ncl;
+    sl.per = a.walk_per;
+    sl.u0 = min(rank * a.walk_per, nunits);
+    sl.u1 = min(sl.u0 + a.walk_per, nunits);
+    sl.npass = 0;
+    sl.arrived = false;
+  }
+  float* usum = a.walk_per <= kWalkMaxSmemUnits ? usum_dyn : nullptr;
   const TT* target = reinterpret_cast<const TT*>(a.target);
   const TD* draft = reinterpret_cast<const TD*>(a.draft);
   const bool greedy = a.tau == 0.f;
@@ -803,12 +972,12 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   if (tid == 0) sh.path[0] = 0;
   __syncthreads();
 
-  int node = 0, npath = 1, rejections = 0, final_tok = -1;
+  int node = 0, npath = 1, rejections = 0, final_tok = -1, owner = 0;
   while (true) {
     const TT* trow = target + size_t(o + node) * a.tld;
     const int fc = sh.first_child[node];
     if (greedy) {
-      const int best = fc >= 0 ? sh.st_arg[node] : block_row_argmax(trow, a.V, sh.ps);
+      const int best = fc >= 0 ? sh.st_arg[node] : slice_row_argmax(trow, a.V, sh.ps, sl);
       int acc = -1, rej = 0;
       for (int c = fc; c >= 0; c = sh.next_sib[c]) {
         if (sh.tok[c] == best) { acc = c; break; }
@@ -828,9 +997,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     if (fc < 0) {  // leaf: bonus token from p_leaf
       WeightFn fn{};
       fn.residual = false;
-      fn.mt = block_row_max(trow, a.V, sh.ps);
+      fn.mt = slice_row_max(trow, a.V, sh.ps, sl);
       fn.k2 = a.k2;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
+      const PassResult pr = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps, sl);
+      final_tok = pr.tok;
+      owner = pr.owner;
       break;
     }
     if (kMulti) {
@@ -866,7 +1037,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
         upd.dst = rows2 + flip * a.rld;
         upd.V = a.V;
         const TD* drow_c = draft + size_t(sh.drow[c]) * a.dld;
-        const PassResult pr = vocab_pass(trow, drow_c, a.V, upd, false, 0.f, usum, sh.ps);
+        const PassResult pr = vocab_pass(trow, drow_c, a.V, upd, false, 0.f, usum, sh.ps, sl);
         if (tid == 0) { sh.Nk = sh.ps.total; sh.Nf = float(sh.ps.total); }
         __syncthreads();
         if (!pr.pos) { from_p = true; break; }
@@ -889,8 +1060,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
         fin.dst = nullptr;
         fin.V = a.V;
         const TD* drow_c = draft + size_t(sh.drow[last]) * a.dld;
-        const PassResult pr = vocab_pass(trow, drow_c, a.V, fin, true, u_samp, usum, sh.ps);
+        const PassResult pr = vocab_pass(trow, drow_c, a.V, fin, true, u_samp, usum, sh.ps, sl);
         final_tok = pr.tok;
+        owner = pr.owner;
         if (!pr.pos) from_p = true;
       }
       if (from_p) {
@@ -898,7 +1070,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
         fn.residual = false;
         fn.mt = sh.st_m[node];
         fn.k2 = a.k2;
-        final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
+        const PassResult pr = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps, sl);
+        final_tok = pr.tok;
+        owner = pr.owner;
       }
       break;
     }
@@ -919,22 +1093,33 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       bool acc;
       if (c == fc || !a.residual_rule) {
         acc = sh.dec0[c] != 0;
+        // C_1 = C_0 + N_0 = 0 + 1
+        if (!acc && a.residual_rule) {
+          if (tid == 0) sh.C = 1.0;
+          res.C = 1.f;
+        }
       } else {
-        if (tid == 0) sh.decision = residual_ratio_test<TT, TD>(a, sh, node, c);
+        // thread 0 decides and, on a rejection, advances C_{k+1} = C_k + N_k; one barrier
+        // publishes both (they are rewritten only after the next pass's barriers)
+        if (tid == 0) {
+          const bool d = residual_ratio_test<TT, TD>(a, sh, node, c);
+          sh.decision = d;
+          if (!d) {
+            sh.C += sh.Nk;
+            sh.Cf = float(sh.C);
+          }
+        }
         __syncthreads();
         acc = sh.decision != 0;
-        __syncthreads();
+        if (!acc) res.C = sh.Cf;
       }
       if (acc) { accepted = c; break; }
       ++rejections;
       if (a.residual_rule) {
-        // C_{k+1} = C_k + N_k, N_{k+1} = sum_x max(0, p(x) - C_{k+1} q(x))
-        if (tid == 0) { sh.C += sh.Nk; sh.Cf = float(sh.C); }
-        __syncthreads();
-        res.C = sh.Cf;
+        // N_{k+1} = sum_x max(0, p(x) - C_{k+1} q(x))
         // after the last sibling the final draw below yields N_{k+1} itself
         if (sh.next_sib[c] < 0) break;
-        const PassResult pr = vocab_pass(trow, drow, a.V, res, false, 0.f, usum, sh.ps);
+        const PassResult pr = vocab_pass(trow, drow, a.V, res, false, 0.f, usum, sh.ps, sl);
         if (tid == 0) sh.Nk = sh.ps.total;
         if (!pr.pos) { from_p = true; break; }
       }
@@ -946,8 +1131,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       continue;
     }
     if (!from_p) {
-      const PassResult pr = vocab_pass(trow, drow, a.V, res, true, u_samp, usum, sh.ps);
+      const PassResult pr = vocab_pass(trow, drow, a.V, res, true, u_samp, usum, sh.ps, sl);
       final_tok = pr.tok;
+      owner = pr.owner;
       if (!pr.pos) from_p = true;
     }
     if (from_p) {
@@ -955,25 +1141,37 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       fn.residual = false;
       fn.mt = res.mt;
       fn.k2 = a.k2;
-      final_tok = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps).tok;
+      const PassResult pr = vocab_pass(trow, draft, a.V, fn, true, u_samp, usum, sh.ps, sl);
+      final_tok = pr.tok;
+      owner = pr.owner;
     }
     break;
   }
+  if (owner < 0) { owner = 0; final_tok = -1; }   // a row without mass: no token
   __syncthreads();
-  for (int k = tid; k < a.max_path; k += kWalkThreads) {
-    if (k < npath) {
-      path_row[k] = sh.path[k];
-      tok_row[k] = (k + 1 < npath) ? sh.tok[sh.path[k + 1]] : final_tok;
-    } else {
-      path_row[k] = -1;
-      tok_row[k] = -1;
+  // rank 0 writes the outputs, the owner of the final draw its token
+  if (rank == 0) {
+    for (int k = tid; k < a.max_path; k += kWalkThreads) {
+      if (k < npath) {
+        path_row[k] = sh.path[k];
+        if (k + 1 < npath) tok_row[k] = sh.tok[sh.path[k + 1]];
+        else if (owner == 0) tok_row[k] = final_tok;
+      } else {
+        path_row[k] = -1;
+        tok_row[k] = -1;
+      }
     }
+    if (tid == 0) {
+      a.out_len[r] = npath;
+      a.n_acc[r] = npath - 1;
+      if (a.rejections) a.rejections[r] = rejections;
+    }
+  } else if (owner == rank && tid == 0) {
+    tok_row[npath - 1] = final_tok;
   }
-  if (tid == 0) {
-    a.out_len[r] = npath;
-    a.n_acc[r] = npath - 1;
-    if (a.rejections) a.rejections[r] = rejections;
-  }
+  // no CTA leaves while another may still read its shared memory
+  if (!sl.arrived) cluster_arrive();
+  cluster_wait();
 }
 
 struct VerifyWs {
@@ -998,7 +1196,6 @@ static VerifyWs verify_ws_layout(int N, int R, int multi_B = 0, int V = 0) {
 template <typename TT, typename TD, bool kMulti>
 static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   const int nunits = (d.V + 7) / 8;
-  const size_t dyn = nunits <= kWalkMaxSmemUnits ? sizeof(float) * size_t(nunits) : 0;
   VerifyDev dw = d;
   {
     // draft-row statistics are needed only for tau > 0 with draft logits
@@ -1010,13 +1207,49 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
     }
   }
   static DeviceOnce raised_walk;   // the unit-sum array's maximum, once per device
-  if (dyn > 0) {
-    const spec_status_t st = raise_dyn_smem_once(verify_walk_kernel<TT, TD, kMulti>,
-                                                 sizeof(float) * kWalkMaxSmemUnits, raised_walk);
+  auto kernel = verify_walk_kernel<TT, TD, kMulti>;
+  {
+    const spec_status_t st = raise_dyn_smem_once(kernel, sizeof(float) * kWalkMaxSmemUnits,
+                                                 raised_walk);
     if (st != SPEC_OK) return st;
   }
-  return launch_result(launch_pdl(verify_walk_kernel<TT, TD, kMulti>, dim3(d.B),
-                                  dim3(kWalkThreads), dyn, s, dw));
+  // CTAs per request: the largest cluster (at most kWalkMaxCl) whose slices keep at least
+  // kWalkMinUnits units and whose clusters for the whole batch are resident at once; one CTA
+  // under the multi-draft rule
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return launch_result(e);
+  int ncl = 1;
+  if (!kMulti) {
+    for (int n = kWalkMaxCl; n >= 2; n >>= 1) {
+      const int per = (nunits + n - 1) / n;
+      if (per < kWalkMinUnits) continue;
+      const long long smem = per <= kWalkMaxSmemUnits ? 4LL * per : 0;
+      if (active_clusters(kernel, dev, n, kWalkThreads, smem) >= d.B) {
+        ncl = n;
+        break;
+      }
+    }
+  }
+  dw.walk_per = (nunits + ncl - 1) / ncl;
+  const size_t dyn = dw.walk_per <= kWalkMaxSmemUnits ? sizeof(float) * size_t(dw.walk_per) : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(d.B) * unsigned(ncl));
+  cfg.blockDim = dim3(kWalkThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(ncl);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kernel, dw);
+  if (e == cudaSuccess) count_launch();
+  return launch_result(e);
 }
 
 }  // namespace spec

@@ -32,11 +32,8 @@
 // cp.async.wait_all, the exchanges with hardware cluster barriers.
 #include <math.h>
 
-#include <map>
-#include <mutex>
-#include <tuple>
-
 #include "common.cuh"
+#include "cluster.cuh"
 #include "tc_ptx.cuh"
 #include "verify_cluster.cuh"
 
@@ -86,44 +83,6 @@ struct ClSmem {
   int32_t cnmove, cbad;
 };
 
-__device__ __forceinline__ int cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return int(r);
-}
-__device__ __forceinline__ int cluster_size() {
-  uint32_t n;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
-  return int(n);
-}
-// every thread of every CTA of the cluster; release / acquire order the shared-memory
-// accesses on either side
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_addr(const void* p, int rank) {
-  uint32_t ra;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(tc::smem_u32(p)), "r"(rank));
-  return ra;
-}
-__device__ __forceinline__ float ld_cluster_f32(const void* p, int rank) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr(p, rank)) : "memory");
-  return v;
-}
-__device__ __forceinline__ int ld_cluster_s32(const void* p, int rank) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr(p, rank)) : "memory");
-  return v;
-}
-// the two halves of cluster_sync, for a barrier whose wait comes later
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // 16-byte asynchronous global -> shared copy (L2 only), its commit and the wait for all of this
 // thread's copies
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -907,38 +866,6 @@ long long cluster_smem(const ClusterVerifyArgs& a, int n, int tes, int des, long
   return smem <= vcl::kMaxDynSmem ? smem : 0;
 }
 
-// clusters of n CTAs with `smem` bytes each that the device holds at once (cached)
-template <typename K>
-int active_clusters(K kernel, int dev, int n, long long smem) {
-  static std::mutex mu;
-  static std::map<std::tuple<const void*, int, int, long long>, int> cache;
-  const auto key = std::make_tuple(reinterpret_cast<const void*>(kernel), dev, n, smem);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(n));
-  cfg.blockDim = dim3(vcl::kThreads);
-  cfg.dynamicSmemBytes = size_t(smem);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(n);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int c = 0;
-  if (cudaOccupancyMaxActiveClusters(&c, kernel, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    c = 0;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  cache[key] = c;
-  return c;
-}
-
 }  // namespace
 
 bool verify_cluster_fits(const ClusterVerifyArgs& a, int tes, int des) {
@@ -967,7 +894,7 @@ static cudaError_t launch_cl(ClusterVerifyArgs a, int tes, int des, cudaStream_t
   for (int n = kMaxCl; n >= 1; --n) {
     const long long smem = cluster_smem(a, n, tes, des, nullptr);
     if (smem == 0) continue;
-    const int resident = active_clusters(kernel, dev, n, smem);
+    const int resident = active_clusters(kernel, dev, n, vcl::kThreads, smem);
     if (resident < 1) continue;
     const double cost = double((a.B + resident - 1) / resident) / n;
     if (best_n == 0 || cost < best_cost) {
