@@ -31,7 +31,8 @@
 //   warps 4..7 (slot 0), 8..11 (slot 1): softmax, one query row per thread: the row maximum over
 //               the tile's visible keys (masked by the ancestor bits), exponentials against a
 //               lazily updated reference (O_s rescaled only when the maximum grows by more than
-//               2^8), P_s (bf16) written over S_s in TMEM; the epilogue normalises O_s and writes
+//               2^8), P_s (bf16) written over the upper half of S_s in TMEM (a thread holds 64
+//               scores at a time: keys 0..63 are read twice); the epilogue normalises O_s and writes
 //               the output rows (a split unit: each slot writes 64 columns of the merged rows).
 // Every wait is bounded (clock64 limit); an expired wait flags SPEC_REQ_TIMEOUT and lets every
 // role drain and exit; TMEM is always freed.
@@ -70,8 +71,8 @@ constexpr int kPartRows = 2 * kBM;            // rows of one partial piece (up t
 constexpr int kCtlRegs = 96;                  // registers per thread: control warpgroup
 constexpr int kSoftmaxRegs = 200;             // and each softmax warpgroup (setmaxnreg)
 static_assert(kCtlRegs * 128 + kSoftmaxRegs * 256 <= kThreads * 168, "register split fits");
-// TMEM columns: slot s's scores S_s (fp32) in 128 s .. 128 s + 127, overwritten in place by its
-// probabilities P_s (bf16 pairs) in 128 s .. 128 s + 63; slot s's output O_s in 256 + 128 s ..
+// TMEM columns: slot s's scores S_s (fp32) in 128 s .. 128 s + 127, overwritten by its
+// probabilities P_s (bf16 pairs) in 128 s + 64 .. 128 s + 127; slot s's output O_s in 256 + 128 s ..
 }  // namespace attn
 
 // A unit cut by range boundaries: its pieces lie in ranges ca .. ca + np - 1; the first piece's
@@ -676,7 +677,7 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           if (k == 0 && li > 0 && !tc::mbar_wait(o_free + s, (li - 1) & 1, abort_flag, kWaitLimit))
             return false;
           tc::tc_fence_after();
-          const uint32_t tO = tmem + 256 + 128 * s, tP = tmem + 128 * s;
+          const uint32_t tO = tmem + 256 + 128 * s, tP = tmem + 128 * s + 64;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             // P_s: 16 keys = 8 columns per MMA
@@ -749,27 +750,48 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         ++scnt;
         tc::tc_fence_after();
         if (live) {
-          // the row's 128 scores at once (one TMEM wait), the maximum of the visible ones, then
-          // 128 independent exponentials 2^(x sl2 - ref), one FMA each, written as bf16 P over
-          // S in place (keys 32 c .. 32 c + 31 go to columns 16 c .. 16 c + 15).  The reference
-          // is lazy: it moves only when the tile's maximum passes it by more than 2^8, and then
-          // the row sum and O_s are rescaled.
-          uint32_t x0[32], x1[32], x2[32], x3[32];
+          // The maximum of the row's visible scores, then 128 independent exponentials
+          // 2^(x sl2 - ref), one FMA each, written as bf16 P into the upper half of S_s's columns
+          // (keys 32 c .. 32 c + 31 go to columns 64 + 16 c .. 64 + 16 c + 15).  At most 64
+          // scores are held at once: keys 0..63 are read for the maximum, then keys 64..127,
+          // whose exponentials go first (their P columns cover only their own scores), then keys
+          // 0..63 again.  The reference is lazy: it moves only when the tile's maximum passes it
+          // by more than 2^8, and then the row sum and O_s are rescaled.
+          uint32_t x0[32], x1[32];
           tc::tmem_ld32(tS, x0);
           tc::tmem_ld32(tS + 32, x1);
-          tc::tmem_ld32(tS + 64, x2);
-          tc::tmem_ld32(tS + 96, x3);
           tc::tmem_ld_wait();
-          const float tmax =
-              fmaxf(fmaxf(mask_max32_row(x0, valid, kbase, P, arow, a.W),
-                          mask_max32_row(x1, valid, kbase + 32, P, arow, a.W)),
-                    fmaxf(mask_max32_row(x2, valid, kbase + 64, P, arow, a.W),
-                          mask_max32_row(x3, valid, kbase + 96, P, arow, a.W))) * sl2;
+          const float max01 = fmaxf(mask_max32_row(x0, valid, kbase, P, arow, a.W),
+                                    mask_max32_row(x1, valid, kbase + 32, P, arow, a.W));
+          asm volatile("" ::"f"(max01));   // keys 0..63 are dead before 64..127 arrive
+          tc::tmem_ld32(tS + 64, x0);
+          tc::tmem_ld32(tS + 96, x1);
+          tc::tmem_ld_wait();
+          const float tmax = fmaxf(max01, fmaxf(mask_max32_row(x0, valid, kbase + 64, P, arow, a.W),
+                                                mask_max32_row(x1, valid, kbase + 96, P, arow, a.W))) *
+                             sl2;
           const bool up = tmax > m_ref + kLazyRescale;
           const float ref = up ? tmax : m_ref;
           const float factor = (up && m_ref != -INFINITY) ? ex2(m_ref - ref) : 1.f;
-          // O_s carries the factor (its previous product must have landed; an item's first
-          // tile finds nothing to rescale)
+          // a row with no visible key yet (ref = -inf) computes 2^(x - inf) = 0 for every key
+          // (masked keys hold -inf: -inf - inf = -inf, never -inf * 0)
+          const float sl = ref == -INFINITY ? 1.f : sl2;
+          const float add = ref == -INFINITY ? -INFINITY : -ref;
+          const uint64_t sl2v = f2_pack(sl, sl), addv = f2_pack(add, add);
+          uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
+          exp_chunk(x1, sl2v, addv, acc1, tS + 64 + 48);
+          exp_chunk(x0, sl2v, addv, acc0, tS + 64 + 32);
+          tc::tmem_ld32(tS, x0);
+          tc::tmem_ld32(tS + 32, x1);
+          tc::tmem_ld_wait();
+          mask_max32_row(x0, valid, kbase, P, arow, a.W);   // the masks again (max unused)
+          mask_max32_row(x1, valid, kbase + 32, P, arow, a.W);
+          exp_chunk(x1, sl2v, addv, acc1, tS + 64 + 16);
+          exp_chunk(x0, sl2v, addv, acc0, tS + 64);
+          // O_s carries the factor, after the exponentials (the scores are dead by then, which
+          // keeps the register peak down); its previous product must have landed -- it has,
+          // since S_s of this tile was computed after it -- and an item's first tile finds
+          // nothing to rescale
           if (k > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
             if (!warp_wait(pv_done + s, (pv_mine - 1) & 1, abort_flag)) { ok = false; break; }
             tc::tc_fence_after();
@@ -785,16 +807,6 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
               tc::tmem_st32(ta, r32);
             }
           }
-          // a row with no visible key yet (ref = -inf) computes 2^(x - inf) = 0 for every key
-          // (masked keys hold -inf: -inf - inf = -inf, never -inf * 0)
-          const float sl = ref == -INFINITY ? 1.f : sl2;
-          const float add = ref == -INFINITY ? -INFINITY : -ref;
-          const uint64_t sl2v = f2_pack(sl, sl), addv = f2_pack(add, add);
-          uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = f2_pack(0.f, 0.f);
-          exp_chunk(x0, sl2v, addv, acc0, tS + 0);
-          exp_chunk(x1, sl2v, addv, acc1, tS + 16);
-          exp_chunk(x2, sl2v, addv, acc0, tS + 32);
-          exp_chunk(x3, sl2v, addv, acc1, tS + 48);
           tc::tmem_st_wait();
           float ra, rb, rc, rd;
           f2_unpack(acc0, ra, rb);
