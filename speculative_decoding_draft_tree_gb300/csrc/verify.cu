@@ -284,7 +284,7 @@ __device__ RowStat row_stats(const T* row, const VerifyDev& a, RowScratch& sc, i
       dfloat tot = {sc.hi[0], sc.lo[0]};
       for (int w = 1; w < kRowWarps; ++w) tot = df_add(tot, dfloat{sc.hi[w], sc.lo[w]});
       const double Z = df_to_d(tot);
-      sc.out = RowStat{M, -1, Z, float(1.0 / Z), 0};
+      sc.out = RowStat{M, -1, Z, __frcp_rn(float(Z)), 0};   // fp32 reciprocal: no fp64 division
     }
   }
   row_sync(bar);

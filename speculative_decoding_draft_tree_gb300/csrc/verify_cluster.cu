@@ -167,7 +167,9 @@ struct ClWeight {
   }
 };
 
-// One warp, units [k0, k1) of a row slice: the max (and, greedy, the lowest argmax).
+// One warp, units [k0, k1) of a row slice: the max (and, greedy, the lowest argmax).  (This
+// kernel runs each phase once per launch, from a cold instruction cache: compact loops beat
+// unrolled ones here.)
 template <typename T>
 __device__ __forceinline__ void part_max(const T* row, int k0, int k1, int u0, bool greedy,
                                          int lane, float& best, int& arg) {
@@ -514,65 +516,67 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
   copy_slices(rows_s, a.t_slice, T, tbytes,
               [&](int j) { return target + size_t(o + j) * a.tld + size_t(u0) * 8; });
   cp_async_commit();
-  // the tree, tokens, depths, draft rows and uniforms; validation of tokens, parents, depths
-  {
-    int bad = 0;
-    for (int i = tid; i < T; i += kThreads) {
-      const int n = o + i;
-      const int p = a.parent[n];
-      const bool pok = i == 0 ? p == -1 : (p >= 0 && p < i);
+  // the tree, tokens, depths, draft rows and uniforms, one lane per node (T <= 32); validation
+  // of tokens, parents, depths; children and siblings from lanes sharing a parent; the draft
+  // slices (one per node with children, tau > 0); then the operands of the ratio tests -- each
+  // node's token in its parent's rows -- are requested, to be stored once the copies landed
+  float xt_r = 0.f, xd_r = 0.f;
+  bool has_t = false, has_d = false;
+  if (warp == 0) {
+    const int i = lane;
+    const bool in = i < T;
+    const int n = o + i;
+    int p = -1, t = -1, dr = -1, bad = 0;
+    bool pok = false;
+    if (in) {
+      p = a.parent[n];
+      pok = i == 0 ? p == -1 : (p >= 0 && p < i);
       if (!pok) bad |= SPEC_REQ_BAD_PARENT;
-      int t = -1;
       if (i > 0) {
         t = a.tokens[n];
         if (t < 0 || t >= V) bad |= SPEC_REQ_BAD_TOKEN;
       }
       if (a.depth[n] + 1 > a.max_path) bad |= SPEC_REQ_BAD_DEPTH;
+      dr = greedy ? -1 : a.draft_row[n];
       sh.par[i] = int16_t(pok ? p : -1);
       sh.tok[i] = t;
-      sh.drow[i] = greedy ? -1 : a.draft_row[n];
-      sh.first_child[i] = -1;
-      sh.next_sib[i] = -1;
+      sh.drow[i] = dr;
       sh.uacc[i] = a.uniforms[2 * size_t(n)];
       sh.usamp[i] = a.uniforms[2 * size_t(n) + 1];
     }
-    if (bad) atomicOr(&sh.bad, bad);
-  }
-  __syncthreads();
-  for (int i = tid; i < T; i += kThreads) {
-    const int p = sh.par[i];
-    if (i > 0 && p >= 0) {
-      int nxt = -1;
-      for (int k = i + 1; k < T; ++k)
-        if (sh.par[k] == p) { nxt = k; break; }
-      sh.next_sib[i] = int16_t(nxt);
-      bool first = true;
-      for (int k = p + 1; k < i; ++k)
-        if (sh.par[k] == p) { first = false; break; }
-      if (first) sh.first_child[p] = int16_t(i);
+    const bool child = in && i > 0 && pok;
+    // lanes with the same parent are siblings, in index order; a unique key otherwise
+    const unsigned peers = __match_any_sync(0xffffffffu, child ? p : -2 - i);
+    const unsigned has_child = __reduce_or_sync(0xffffffffu, child ? (1u << p) : 0u);
+    sh.first_child[i] = -1;
+    __syncwarp();
+    if (child) {
+      const unsigned later = peers & ~((2u << i) - 1u);
+      sh.next_sib[i] = int16_t(later ? __ffs(later) - 1 : -1);
+      if ((peers & ((1u << i) - 1u)) == 0) sh.first_child[p] = int16_t(i);
+    } else {
+      sh.next_sib[i] = -1;
     }
-  }
-  __syncthreads();
-  // draft slices: one per node with children (tau > 0), one lane per node
-  if (warp == 0) {
-    const bool need = !greedy && lane < T && sh.first_child[lane] >= 0;
-    const int dr = need ? sh.drow[lane] : 0;
+    const bool need = !greedy && in && ((has_child >> i) & 1u);
     const bool row_ok = need && dr >= 0 && dr < a.R;
     const unsigned m = __ballot_sync(0xffffffffu, row_ok);
-    const int slot = __popc(m & ((1u << lane) - 1u));
-    if (lane < T) sh.dslot[lane] = int8_t(row_ok ? slot : -1);
-    if (row_ok) sh.slot_node[slot] = int8_t(lane);
-    if (__any_sync(0xffffffffu, need && !row_ok) && lane == 0)
-      atomicOr(&sh.bad, SPEC_REQ_BAD_DRAFT_ROW);
-    if (lane == 0) sh.nint = __popc(m);
-  } else if (!greedy) {
-    // every valid non-root node's token in its parent's target and draft rows
-    for (int i = tid - 32; i < T; i += kThreads - 32) {
-      const int p = sh.par[i], t = sh.tok[i];
-      if (i > 0 && p >= 0 && t >= 0 && t < V) {
-        sh.xt[i] = elem<TT>::load1(target + size_t(o + p) * a.tld + t);
-        const int dr = sh.drow[p];
-        if (dr >= 0 && dr < a.R) sh.xd[i] = elem<TD>::load1(draft + size_t(dr) * a.dld + t);
+    const int slot = __popc(m & ((1u << i) - 1u));
+    if (in) sh.dslot[i] = int8_t(row_ok ? slot : -1);
+    if (row_ok) sh.slot_node[slot] = int8_t(i);
+    if (need && !row_ok) bad |= SPEC_REQ_BAD_DRAFT_ROW;
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (i == 0) {
+      sh.nint = __popc(m);
+      sh.bad = bad;
+    }
+    // the parent's draft row, from its lane
+    const int pdr = __shfl_sync(0xffffffffu, dr, child ? p : 0);
+    if (!greedy && child && t >= 0 && t < V) {
+      xt_r = elem<TT>::load1(target + size_t(o + p) * a.tld + t);
+      has_t = true;
+      if (pdr >= 0 && pdr < a.R) {
+        xd_r = elem<TD>::load1(draft + size_t(pdr) * a.dld + t);
+        has_d = true;
       }
     }
   }
@@ -597,6 +601,8 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
       }
     }
   }
+  if (has_t) sh.xt[lane] = xt_r;   // warp 0 only; the loads have had the copies' time to land
+  if (has_d) sh.xd[lane] = xd_r;
   cp_async_wait_all();
   __syncthreads();
   if (sh.bad) {
@@ -687,12 +693,12 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
       if (j < T) {
         sh.st_m[j] = M;
         sh.st_Z[j] = Z;
-        sh.st_iz[j] = float(1.0 / Z);
+        sh.st_iz[j] = __frcp_rn(float(Z));   // fp32: no fp64 division on the critical path
       } else {
         const int n = sh.slot_node[j - T];
         sh.sd_m[n] = M;
         sh.sd_Z[n] = Z;
-        sh.sd_iz[n] = float(1.0 / Z);
+        sh.sd_iz[n] = __frcp_rn(float(Z));
       }
     }
   }
@@ -778,12 +784,17 @@ __global__ void __launch_bounds__(vcl::kThreads, 1) verify_cluster_kernel(Cluste
         acc = sh.dec0[c] != 0;
       } else {
         if (tid == 0) {
-          // u < max(0, p - C q) / (N q) as u * N * q < max(0, p - C q)
-          const double p = double(expf((sh.xt[c] - sh.st_m[node]) * a.inv_tau)) / sh.st_Z[node];
-          const double q = a.probs ? double(sh.xd[c])
-                                   : double(expf((sh.xd[c] - sh.sd_m[node]) * a.inv_tau)) / sh.sd_Z[node];
-          const double num = fmax(0.0, p - sh.C * q);
-          sh.decision = double(sh.uacc[c]) * (sh.Nk * q) < num;
+          // u < max(0, p - C q) / (N q) as u * N * q < max(0, p - C q), both sides times Zt
+          // (and Zd for draft logits): no fp64 division
+          const double et = double(expf((sh.xt[c] - sh.st_m[node]) * a.inv_tau));
+          const double Zt = sh.st_Z[node], u = double(sh.uacc[c]);
+          if (a.probs) {
+            const double qZ = double(sh.xd[c]) * Zt;
+            sh.decision = u * (sh.Nk * qZ) < fmax(0.0, et - sh.C * qZ);
+          } else {
+            const double qZ = double(expf((sh.xd[c] - sh.sd_m[node]) * a.inv_tau)) * Zt;
+            sh.decision = u * (sh.Nk * qZ) < fmax(0.0, et * sh.sd_Z[node] - sh.C * qZ);
+          }
         }
         __syncthreads();
         acc = sh.decision != 0;
