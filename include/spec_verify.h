@@ -398,17 +398,18 @@ spec_status_t spec_draft_expand_select(const spec_draft_pool* pool, int32_t leve
  * x / tau - logsumexp(row / tau) (one streaming read of the row), appended as the candidate's
  * children in that order with score = its score + log q, depth = level; the candidate's row
  * becomes row_base + r * K + j.  Call after spec_draft_expand_select of the same level.
- * req_status (may be NULL) gets SPEC_REQ_TIMEOUT if a row's copy into shared memory never
- * completed (a bounded wait); that expansion's children then carry token -1 and score -inf. */
+ * req_status (may be NULL) gets SPEC_REQ_TIMEOUT if the launch's bounded wait ran out (only
+ * under the testing hook below); that expansion's children then carry token -1 and score -inf. */
 spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level, int32_t K,
                                      const int32_t* expand, spec_dtype_t dtype, const void* rows,
                                      int64_t ld, int32_t V, float tau, int32_t row_base,
                                      int32_t* req_status, spec_stream_t stream);
 
-/* Testing only: the following spec_draft_topk_append launches on the current device do not
- * issue chunk `chunk` (16 KB units of a row) of any row, so the kernel's bounded wait for it
- * runs out (about a second) and the call reports SPEC_REQ_TIMEOUT for those requests, as a lost
- * copy would; -1 restores normal operation.  Synchronous (a host-to-device symbol copy). */
+/* Testing only: with chunk >= 0, the following spec_draft_topk_append launches on the current
+ * device wait (bounded, about a second) for a device flag that nothing sets, so they run out
+ * their wait and report SPEC_REQ_TIMEOUT for those requests, as a lost read would, with
+ * children of token -1 and score -inf; -1 restores normal operation.  Synchronous (a
+ * host-to-device symbol copy). */
 spec_status_t spec_debug_draft_copy_stall(int32_t chunk);
 
 /* ECHO selection and packing: node_offset [B+1]; parent (local, -1 for roots), tokens, depth,

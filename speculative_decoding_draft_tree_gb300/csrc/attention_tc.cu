@@ -334,26 +334,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return r;
 }
 
-// Packed fp32 pairs (one 64-bit register pair): fma.rn.f32x2 / add.f32x2 do two lanes' worth of
-// FMA / add in one instruction.
-__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 
 // 32 exponentials 2^(x sl + add) of one key chunk (masked keys hold -inf), the arguments formed
 // two at a time by a packed FMA and summed two at a time into the packed partial sum `acc`, and
@@ -373,11 +353,6 @@ __device__ __forceinline__ void exp_chunk(const uint32_t (&x)[32], uint64_t sl2,
   tc::tmem_st16(dst, pk);
 }
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
 
 // Maximum of 32 values as a tree of three-input maxima (17 operations, depth 4).
 __device__ __forceinline__ float max32_tree(const uint32_t (&x)[32]) {

@@ -114,29 +114,31 @@ __device__ __forceinline__ bool better(float v, int id, float w, int jd) {
   return v > w || (v == w && id < jd);
 }
 
-// The row streams through a ring of kStages shared-memory chunks filled by bulk copies
-// (cp.async.bulk with mbarrier completion) that a producer warp issues; each consumer warp
-// releases a stage through its "empty" barrier when it is done with it, so the eight consumer
-// warps never wait for one another.  Each thread folds its 8-element units into an online max /
-// compensated sum (log-sum-exp), and each warp keeps its top-K list distributed over lanes
-// 0..K-1: a unit is offered only when its maximum reaches the warp's K-th value, and offers are
-// inserted one by one under a warp-uniform ballot, so the common path is one compare per unit.
+// The row streams straight into registers: thread t reads units u * kTopkThreads + t of each
+// kChunkBytes chunk (16-byte loads), the next chunk's loads in flight while it works on this one.
+// Each thread folds its units into an online max / compensated sum (log-sum-exp; the exponent
+// arguments and the sums two at a time with packed fp32 pairs), and each warp keeps its top-K list
+// distributed over lanes 0..K-1: a unit is offered only when its maximum reaches the warp's K-th
+// value, and offers are inserted one by one under a warp-uniform ballot, so the common path is
+// one compare per unit.
 constexpr int kChunkBytes = 16384;
-constexpr int kStages = 4;
-constexpr int kConsumerThreads = 256;
-constexpr int kConsumerWarps = kConsumerThreads / 32;
-constexpr int kTopkThreads = kConsumerThreads + 32;   // + the producer warp
-constexpr long long kCopyWaitLimit = 2000000000LL;   // clock cycles (~1 s): a lost copy
+constexpr int kTopkThreads = 256;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr long long kStallWaitLimit = 2000000000LL;   // clock cycles (~1 s)
 
-// Testing only (spec_debug_draft_copy_stall): a chunk index that the producer does not issue,
-// so that the consumers' bounded wait for it runs out; -1 (the default) disables it.
+// Testing only (spec_debug_draft_copy_stall): >= 0 makes every launch wait, bounded, for a device
+// flag that nothing sets, so that it takes its timeout path as a lost read would; -1 (the
+// default) disables it.
 __device__ int g_draft_copy_stall = -1;
+__device__ int g_draft_never_set = 0;
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-      ::"r"(tc::smem_u32(dst)), "l"(src), "r"(bytes), "r"(tc::smem_u32(bar)) : "memory");
+// fp32 value -> unsigned key in the same order (for an atomic maximum)
+__device__ __forceinline__ unsigned ordered_key(float v) {
+  const unsigned b = __float_as_uint(v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // insert (v, id) into the warp's distributed list (lane q < K holds the q-th best)
@@ -158,20 +160,22 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
                          int row_base, int32_t* __restrict__ req_status) {
   constexpr int kElems = kChunkBytes / int(sizeof(T));   // elements per chunk
   constexpr int kUnitsPerChunk = kElems / 8;
-  constexpr int kPerThread = kUnitsPerChunk / kConsumerThreads;
-  static_assert(kPerThread * kConsumerThreads == kUnitsPerChunk, "whole units per thread");
-  extern __shared__ __align__(128) uint8_t ring_dyn[];   // kStages x kChunkBytes
-  __shared__ __align__(8) uint64_t full[kStages];
-  __shared__ __align__(8) uint64_t empty[kStages];
-  __shared__ int s_last_issued[kStages];   // the last chunk issued into each stage, -1 if none
-  __shared__ float s_v[kConsumerWarps][kTopkMax];
-  __shared__ int s_id[kConsumerWarps][kTopkMax];
-  __shared__ float s_m[kConsumerWarps];
-  __shared__ double s_s[kConsumerWarps];
+  constexpr int kPerThread = kUnitsPerChunk / kTopkThreads;
+  constexpr int kVecs = int(sizeof(T)) / 2;              // 16-byte loads per 8-element unit
+  static_assert(kPerThread * kTopkThreads == kUnitsPerChunk, "whole units per thread");
+  __shared__ float s_v[kTopkWarps][kTopkMax];
+  __shared__ int s_id[kTopkWarps][kTopkMax];
+  __shared__ float s_m[kTopkWarps];
+  __shared__ double s_s[kTopkWarps];
   __shared__ float s_best_v[kTopkMax];
   __shared__ int s_best_id[kTopkMax];
   __shared__ float s_logz;
   __shared__ int s_abort;
+  // The CTA's admission floor: the largest of the warps' K-th values and first-chunk seeds.  An
+  // element of the row's top K is not below any warp's K-th value (that warp would hold K better
+  // elements), so a unit below the floor needs no offer; the floor only grows, and a stale read
+  // only admits more.
+  __shared__ unsigned s_floor;
   pdl_wait();
   const int row_i = blockIdx.x;
   const int r = row_i / K, j = row_i - r * K;
@@ -181,59 +185,42 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
     return;
   }
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool producer = warp == kConsumerWarps;
   const char* src = reinterpret_cast<const char*>(rows + size_t(row_i) * ld);
   const int row_bytes = (V * int(sizeof(T)) + 15) & ~15;   // within the padded row (ld)
   const int nchunks = (row_bytes + kChunkBytes - 1) / kChunkBytes;
-  uint8_t* const ring = ring_dyn;
   if (tid == 0) {
     s_abort = 0;
-    for (int st = 0; st < kStages; ++st) {
-      s_last_issued[st] = -1;
-      tc::mbar_init(&full[st], 1);
-      tc::mbar_init(&empty[st], kConsumerWarps);
+    s_floor = ordered_key(-INFINITY);
+    if (g_draft_copy_stall >= 0) {   // testing only: a wait that never completes, bounded
+      volatile int* flag = &g_draft_never_set;
+      const long long t0 = clock64();
+      while (*flag == 0 && clock64() - t0 < kStallWaitLimit) {
+      }
+      if (*flag == 0) s_abort = 1;
     }
-    tc::fence_mbar_init();
   }
   __syncthreads();
+  // this thread's units of chunk c (vectors past the row's padded end are not read)
+  uint4 nxt[kPerThread][kVecs];
+  auto fetch = [&](int c) {
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int off = c * kChunkBytes + (u * kTopkThreads + tid) * 16 * kVecs;
+#pragma unroll
+      for (int q = 0; q < kVecs; ++q)
+        nxt[u][q] = off + 16 * q < row_bytes ? ld_stream16(src + off + 16 * q) : make_uint4(0, 0, 0, 0);
+    }
+  };
 
   float m = -INFINITY, s = 0.f, comp = 0.f;
   float lv = -INFINITY;      // this lane's entry of the warp's top-K list (lanes < K)
   int lid = 0x7fffffff;
-  if (producer) {
-    if (lane == 0) {
-      const int stall = g_draft_copy_stall;
-      for (int c = 0; c < nchunks; ++c) {
-        const int st = c % kStages;
-        if (c >= kStages) {   // the stage's previous chunk must have been released
-          if (!tc::mbar_wait(&empty[st], uint32_t((c / kStages - 1) & 1), &s_abort,
-                             kCopyWaitLimit)) {
-            s_abort = 1;
-            break;
-          }
-          tc::fence_proxy_async_smem();   // the consumers' reads before the copy's writes
-        }
-        if (c == stall) continue;   // testing: this chunk never arrives
-        const uint32_t bytes = uint32_t(min(kChunkBytes, row_bytes - c * kChunkBytes));
-        tc::mbar_arrive_expect_tx(&full[st], bytes);
-        bulk_load(ring + size_t(st) * kChunkBytes, src + size_t(c) * kChunkBytes, bytes,
-                  &full[st]);
-        s_last_issued[st] = c;
-      }
-    }
-  } else {
+  if (s_abort == 0) {
     float thr = -INFINITY;   // the warp's K-th value
     float seed = -INFINITY;  // admission floor from the first chunk
     float mk2 = -INFINITY;   // m * k2
+    fetch(0);
     for (int c = 0; c < nchunks; ++c) {
-      const int st = c % kStages;
-      const bool got = tc::mbar_wait(&full[st], uint32_t((c / kStages) & 1), &s_abort,
-                                     kCopyWaitLimit);
-      if (!__all_sync(0xffffffffu, got)) {
-        s_abort = 1;
-        break;
-      }
-      const T* chunk = reinterpret_cast<const T*>(ring + size_t(st) * kChunkBytes);
       const int base_id = c * kElems;
       // this thread's units of the chunk, all in registers: one max, one rescale check, the
       // exponentials as independent work, one compensated step for the chunk
@@ -241,27 +228,26 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
       float x[kN];
 #pragma unroll
       for (int u = 0; u < kPerThread; ++u) {
-        const int unit = u * kConsumerThreads + tid;
         if constexpr (sizeof(T) == 2) {
-          elem<T>::unpack(*reinterpret_cast<const uint4*>(chunk + unit * 8), x + 8 * u);
+          elem<T>::unpack(nxt[u][0], x + 8 * u);
         } else {
-          elem<T>::unpack(*reinterpret_cast<const uint4*>(chunk + unit * 8), x + 8 * u);
-          elem<T>::unpack(*reinterpret_cast<const uint4*>(chunk + unit * 8 + 4), x + 8 * u + 4);
+          elem<T>::unpack(nxt[u][0], x + 8 * u);
+          elem<T>::unpack(nxt[u][kVecs - 1], x + 8 * u + 4);
         }
       }
+      if (c + 1 < nchunks) fetch(c + 1);   // the next chunk's loads fly while this one is folded
       if (base_id + kElems > V) {   // the row's last chunk: elements past V do not exist
 #pragma unroll
         for (int u = 0; u < kPerThread; ++u)
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            if (base_id + (u * kConsumerThreads + tid) * 8 + k >= V) x[8 * u + k] = -INFINITY;
+            if (base_id + (u * kTopkThreads + tid) * 8 + k >= V) x[8 * u + k] = -INFINITY;
       }
       float um[kPerThread];
 #pragma unroll
       for (int u = 0; u < kPerThread; ++u) {
         const float* xu = x + 8 * u;
-        um[u] = fmaxf(fmaxf(fmaxf(xu[0], xu[1]), fmaxf(xu[2], xu[3])),
-                      fmaxf(fmaxf(xu[4], xu[5]), fmaxf(xu[6], xu[7])));
+        um[u] = fmax3(fmax3(xu[0], xu[1], xu[2]), fmax3(xu[3], xu[4], xu[5]), fmaxf(xu[6], xu[7]));
       }
       float cm = um[0];
 #pragma unroll
@@ -273,14 +259,20 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
         m = cm;
         mk2 = m * k2;
       }
-      float e[kN];
+      // exponentials 2^(x k2 - m k2): arguments and sums two at a time
+      const uint64_t k2v = f2_pack(k2, k2), negv = f2_pack(-mk2, -mk2);
+      uint64_t acc[4] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f), f2_pack(0.f, 0.f),
+                         f2_pack(0.f, 0.f)};
 #pragma unroll
-      for (int k = 0; k < kN; ++k) e[k] = ex2(fmaf(x[k], k2, -mk2));
-#pragma unroll
-      for (int w = 1; w < kN; w <<= 1)
-#pragma unroll
-        for (int k = 0; k + w < kN; k += 2 * w) e[k] += e[k + w];
-      const float y = e[0] - comp;   // compensated sum, one step per chunk
+      for (int k = 0; k < kN; k += 2) {
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[k], x[k + 1]), k2v, negv), y0, y1);
+        acc[(k >> 1) & 3] = f2_add(acc[(k >> 1) & 3], f2_pack(ex2(y0), ex2(y1)));
+      }
+      float a0, a1, a2, a3;
+      f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+      f2_unpack(f2_add(acc[2], acc[3]), a2, a3);
+      const float y = ((a0 + a1) + (a2 + a3)) - comp;   // compensated sum, one step per chunk
       const float t = s + y;
       comp = (t - s) - y;
       s = t;
@@ -295,7 +287,9 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
         }
         const unsigned at = __ballot_sync(0xffffffffu, rank == K - 1);
         seed = at ? __shfl_sync(0xffffffffu, cm, __ffs(at) - 1) : -INFINITY;
+        if (lane == 0) atomicMax(&s_floor, ordered_key(seed));
       }
+      seed = fmaxf(seed, key_value(*reinterpret_cast<volatile unsigned*>(&s_floor)));
       // offers to the warp's list, one unit at a time; the offering lane names its elements
       // that reach the threshold and only those are inserted
 #pragma unroll
@@ -318,37 +312,24 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
 #pragma unroll
             for (int q = 1; q < 8; ++q) xk = (k == q) ? x[8 * u + q] : xk;
             const float v = __shfl_sync(0xffffffffu, xk, src_lane);
-            const int id = base_id + (u * kConsumerThreads + src_lane + warp * 32) * 8 + k;
+            const int id = base_id + (u * kTopkThreads + src_lane + warp * 32) * 8 + k;
             if (v >= fmaxf(thr, seed)) {   // the list may have moved since the mask was taken
               warp_list_insert(lv, lid, v, id, K, lane);
-              thr = __shfl_sync(0xffffffffu, lv, K - 1);
+              const float nt = __shfl_sync(0xffffffffu, lv, K - 1);
+              if (lane == 0 && nt > thr) atomicMax(&s_floor, ordered_key(nt));
+              thr = nt;
             }
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&empty[st]);
     }
   }
   __syncthreads();
   const bool ok = s_abort == 0;
-  if (!ok) {
-    // a copy or a release never came: wait (bounded) for the last copy issued into each stage,
-    // so none is still writing when the CTA exits, and mark the request
-    if (tid == 0) {
-      volatile int never = 0;
-      for (int st = 0; st < kStages; ++st) {
-        const int last = s_last_issued[st];
-        if (last >= 0)
-          tc::mbar_wait(&full[st], uint32_t((last / kStages) & 1), &never, kCopyWaitLimit);
-      }
-      if (req_status) atomicOr(&req_status[r], SPEC_REQ_TIMEOUT);
-    }
-    __syncthreads();
-  }
+  if (!ok && tid == 0 && req_status) atomicOr(&req_status[r], SPEC_REQ_TIMEOUT);
   pdl_trigger();
-  // log-sum-exp over the consumer warps: every thread's (m, s) rescaled to the block max
-  if (!producer) {
+  // log-sum-exp over the warps: every thread's (m, s) rescaled to the block max
+  {
     const float wm = warp_max(m);
     if (lane == 0) s_m[warp] = wm;
     if (lane < K) { s_v[warp][lane] = lv; s_id[warp][lane] = lid; }
@@ -356,20 +337,20 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
   __syncthreads();
   float M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, s_m[w]);
-  if (!producer) {
+  for (int w = 0; w < kTopkWarps; ++w) M = fmaxf(M, s_m[w]);
+  {
     dfloat ds = df_make(m == -INFINITY ? 0.f : (s - comp) * ex2((m - M) * k2));
     ds = warp_sum_df(ds);
     if (lane == 0) s_s[warp] = df_to_d(ds);
   }
   __syncthreads();
-  // the block's top-K from the warps' lists (warp 0, lane w < kConsumerWarps walks list w)
+  // the block's top-K from the warps' lists (warp 0, lane w < kTopkWarps walks list w)
   if (warp == 0) {
     int h = 0;
     for (int q = 0; q < K; ++q) {
       float bv = -INFINITY;
       int bid = 0x7fffffff;
-      if (lane < kConsumerWarps && h < K) { bv = s_v[lane][h]; bid = s_id[lane][h]; }
+      if (lane < kTopkWarps && h < K) { bv = s_v[lane][h]; bid = s_id[lane][h]; }
       float wv = bv;
       int wid = bid;
 #pragma unroll
@@ -378,12 +359,12 @@ draft_topk_append_kernel(PoolDev p, int level, int K, const int32_t* __restrict_
         const int oid = __shfl_xor_sync(0xffffffffu, wid, o);
         if (better(ov, oid, wv, wid)) { wv = ov; wid = oid; }
       }
-      if (lane < kConsumerWarps && h < K && bid == wid && bv == wv) ++h;
+      if (lane < kTopkWarps && h < K && bid == wid && bv == wv) ++h;
       if (lane == 0) { s_best_v[q] = wv; s_best_id[q] = wid; }
     }
     if (lane == 0) {
       double S = 0.0;
-      for (int w = 0; w < kConsumerWarps; ++w) S += s_s[w];
+      for (int w = 0; w < kTopkWarps; ++w) S += s_s[w];
       s_logz = float(log(S));
     }
   }
@@ -614,12 +595,7 @@ spec_status_t spec_draft_topk_append(const spec_draft_pool* pool, int32_t level,
   const float k2 = float(1.4426950408889634 / double(tau));
   const float inv_tau = 1.0f / tau;
   const dim3 grid(unsigned(p.B) * unsigned(K));
-  const size_t dyn = size_t(kStages) * kChunkBytes;
-  static DeviceOnce raised_bf16, raised_f32;
-  const spec_status_t st = dtype == SPEC_BF16
-      ? raise_dyn_smem_once(draft_topk_append_kernel<__nv_bfloat16>, dyn, raised_bf16)
-      : raise_dyn_smem_once(draft_topk_append_kernel<float>, dyn, raised_f32);
-  if (st != SPEC_OK) return st;
+  const size_t dyn = 0;
   cudaError_t e;
   if (dtype == SPEC_BF16)
     e = launch_pdl(draft_topk_append_kernel<__nv_bfloat16>, grid, dim3(kTopkThreads), dyn,

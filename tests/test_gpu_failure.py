@@ -1,7 +1,7 @@
-"""Failure detection on the GPU without a fault: a bounded device wait is made to run out (a copy
-that is never issued, through the library's testing hook) and the call must report it in the
-request status, keep its outputs well-formed, finish in bounded time, and leave the context
-usable for the next call."""
+"""Failure detection on the GPU without a fault: a bounded device wait is made to run out (a wait
+for a device flag that nothing sets, through the library's testing hook) and the call must report
+it in the request status, keep its outputs well-formed, finish in bounded time, and leave the
+context usable for the next call."""
 import time
 
 import numpy as np
@@ -16,7 +16,7 @@ from speculative_decoding_draft_tree_gb300.api import DraftTreeBuilder
 pytestmark = pytest.mark.gpu
 
 
-def test_lost_copy_times_out_and_the_context_stays_usable():
+def test_expired_wait_times_out_and_the_context_stays_usable():
     Bn, K, V = 4, 3, 3001
     roots = torch.arange(Bn, dtype=torch.int32, device="cuda") * 7
     rows = W.draft_level_rows(B=Bn, K=K, V=V, level=1, device="cuda", scales=[1.0, 2.0, 0.5, 3.0])
