@@ -601,6 +601,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
       const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, 128, false, true);
       const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
+      // base descriptors of the first Q buffer, K stage and V stage; buffer b's is kTile bytes
+      // (kTile / 16 in the address field) further
+      const uint64_t dQ0 = tc::smem_desc(aQ, 16, 1024), dK0 = tc::smem_desc(aK, 16, 1024);
+      const uint64_t dV0 = tc::smem_desc(aV, kAtom, 1024);
+      constexpr uint64_t kTileDesc = kTile >> 4;
       int g0 = 0, li = 0;            // ring index of the item's first tile; items
       int qn0 = 0, qn1 = 0;          // Q tiles consumed per buffer
       int pvn0 = 0, pvn1 = 0;        // PV products issued per slot
@@ -627,15 +632,20 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
           const int kst = g % kKStages, kuse = g / kKStages;
           if (!tc::mbar_wait(k_full + kst, kuse & 1, abort_flag, kWaitLimit)) return false;
           tc::tc_fence_after();
-          const uint32_t aQs = aQ + (pair ? s : 0) * kTile;
           const uint32_t tS = tmem + 128 * s;
+          // the tiles' base descriptors plus each K step's offset (in 16-byte units, inside the
+          // 14-bit address field), all formed before the first product: the eight products
+          // then go out back to back and the tensor pipe does not wait on this thread
+          const uint64_t dq = dQ0 + (pair ? s : 0) * kTileDesc, dk = dK0 + uint64_t(kst) * kTileDesc;
+          uint64_t da[8], db[8];
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t da = tc::smem_desc(aQs + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            const uint64_t db =
-                tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-            tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+            const uint64_t off = uint64_t(((kk >> 2) * kAtom + (kk & 3) * 32) >> 4);
+            da[kk] = dq + off;
+            db[kk] = dk + off;
           }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ss(tS, da[kk], db[kk], id_qk, kk > 0 ? 1u : 0u);
           tc::mma_commit(s_full + s);
           if (!pair || release) tc::mma_commit(k_empty + kst);
           if (--qk_left == 0)
@@ -653,11 +663,13 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
             return false;
           tc::tc_fence_after();
           const uint32_t tO = tmem + 256 + 128 * s, tP = tmem + 128 * s + 64;
+          const uint64_t dv = dV0 + uint64_t(vst) * kTileDesc;
+          const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            // P_s: 16 keys = 8 columns per MMA
-            const uint64_t db = tc::smem_desc(aV + vst * kTile + kk * 2048, kAtom, 1024);
-            tc::mma_bf16_ts(tO, tP + 8 * kk, db, id_pv, (k > 0 || kk > 0) ? 1u : 0u);
+            // P_s: 16 keys = 8 columns per MMA; V's rows of those keys 2048 bytes further per step
+            tc::mma_bf16_ts(tO, tP + 8 * kk, dv + uint64_t(kk * (2048 >> 4)), id_pv,
+                            kk > 0 ? 1u : acc0);
           }
           tc::mma_commit(pv_done + s);
           if (!pair || release) tc::mma_commit(v_empty + vst);
@@ -680,9 +692,11 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
         g0 += nt;
       }
       if (!ok) *abort_flag = 1;
-      // drain every tcgen05 operation issued by this thread before TMEM is released
+      // drain every tcgen05 operation issued by this thread before TMEM is released (bounded,
+      // and not cut short by the abort flag: TMEM must not be freed under a product)
       tc::mma_commit(drain);
-      tc::mbar_wait(drain, 0, abort_flag, kWaitLimit / 8);
+      volatile int never = 0;
+      tc::mbar_wait(drain, 0, &never, kWaitLimit / 8);
     }
   }
   } else {
@@ -1059,7 +1073,11 @@ attn_tc_single_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_const
       const bool is_qk = warp == 1;
       const uint32_t id_qk = tc::idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, 128, false, true);
-      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
+      // base descriptors (buffer b's is kTile bytes, kTile / 16 in the address field, further)
+      const uint64_t dQ0 = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = tc::smem_desc(tc::smem_u32(sV), kAtom, 1024);
+      constexpr uint64_t kTileDesc = kTile >> 4;
       const uint32_t tO = tmem + 256;
       int kv_it = 0, li = 0;
       bool ok = true;
@@ -1076,12 +1094,18 @@ attn_tc_single_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_const
             if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             tc::tc_fence_after();
             const uint32_t tS = tmem + st * 128;
+            // all eight products' descriptors first (base + the K step's offset): the products
+            // then go out back to back
+            const uint64_t dk = dK0 + uint64_t(kst) * kTileDesc;
+            uint64_t da[8], db[8];
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t da = tc::smem_desc(aQ + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              const uint64_t db = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+              const uint64_t off = uint64_t(((kk >> 2) * kAtom + (kk & 3) * 32) >> 4);
+              da[kk] = dQ0 + off;
+              db[kk] = dk + off;
             }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ss(tS, da[kk], db[kk], id_qk, kk > 0 ? 1u : 0u);
             tc::mma_commit(s_full + st);
             tc::mma_commit(k_empty + kst);
             if (j == it.j1 - 1) tc::mma_commit(q_empty);
@@ -1092,12 +1116,13 @@ attn_tc_single_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_const
             if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             tc::tc_fence_after();
+            const uint64_t dv = dV0 + uint64_t(pst) * kTileDesc;
+            const uint32_t acc0 = first_pv ? 0u : 1u;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               // P buffer st in TMEM columns 384 + 64 st: 16 keys = 8 columns per MMA
               const uint32_t ta = tmem + kTmemP + 64 * st + 8 * kk;
-              const uint64_t db = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
-              tc::mma_bf16_ts(tO, ta, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+              tc::mma_bf16_ts(tO, ta, dv + uint64_t(kk * (2048 >> 4)), id_pv, kk > 0 ? 1u : acc0);
             }
             tc::mma_commit(v_empty + pst);
             tc::mma_commit(pv_done + st);
@@ -1106,9 +1131,11 @@ attn_tc_single_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_const
       }
       if (!ok) *abort_flag = 1;
       // drain every tcgen05 operation issued by this thread before TMEM is released
+      // (bounded, and not cut short by the abort flag: TMEM must not be freed under a product)
       uint64_t* my_drain = drain + (is_qk ? 0 : 1);
       tc::mma_commit(my_drain);
-      tc::mbar_wait(my_drain, 0, abort_flag, kWaitLimit / 8);
+      volatile int never = 0;
+      tc::mbar_wait(my_drain, 0, &never, kWaitLimit / 8);
     }
   } else if (layout_ok && warp >= 4) {
     // ===================================================================== softmax + epilogue
@@ -1465,8 +1492,11 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
       const bool is_qk = warp == 1;
       const uint32_t id_qk = tc::idesc_bf16_f32(128, kRows, false, false);
       const uint32_t id_pv = tc::idesc_bf16_f32(128, kRows, true, false);
-      const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV),
-                     aP = tc::smem_u32(sPT);
+      // base descriptors (stage / buffer b's is its size / 16 further in the address field)
+      const uint64_t dQ0 = tc::smem_desc(tc::smem_u32(sQ), 16, 1024);
+      const uint64_t dK0 = tc::smem_desc(tc::smem_u32(sK), 16, 1024);
+      const uint64_t dV0 = tc::smem_desc(tc::smem_u32(sV), kAtom, 1024);
+      const uint64_t dP0 = tc::smem_desc(tc::smem_u32(sPT), 16, 1024);
       const uint32_t tO = tmem + kTmemO;
       int kv_it = 0, li = 0;
       bool ok = true;
@@ -1483,13 +1513,17 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
             if (use > 0 && !tc::mbar_wait(s_free + st, (use - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             tc::tc_fence_after();
             const uint32_t tS = tmem + st * kRows;
+            // A = K (128 keys x 16 d per step, K-major), B = Q (16 rows x 16 d, K-major); all
+            // descriptors first, then the eight products back to back
+            const uint64_t dk = dK0 + uint64_t(kst) * uint64_t(kTile >> 4);
+            uint64_t da[8], db[8];
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              // A = K (128 keys x 16 d per step, K-major), B = Q (16 rows x 16 d, K-major)
-              const uint64_t da = tc::smem_desc(aK + kst * kTile + (kk >> 2) * kAtom + (kk & 3) * 32, 16, 1024);
-              const uint64_t db = tc::smem_desc(aQ + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
-              tc::mma_bf16_ss(tS, da, db, id_qk, kk > 0 ? 1u : 0u);
+              da[kk] = dk + uint64_t(((kk >> 2) * kAtom + (kk & 3) * 32) >> 4);
+              db[kk] = dQ0 + uint64_t(((kk >> 2) * kQAtom + (kk & 3) * 32) >> 4);
             }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ss(tS, da[kk], db[kk], id_qk, kk > 0 ? 1u : 0u);
             tc::mma_commit(s_full + st);
             tc::mma_commit(k_empty + kst);
             if (j == it.j1 - 1) tc::mma_commit(q_empty);
@@ -1500,13 +1534,18 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
             if (!tc::mbar_wait(v_full + pst, puse & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             if (first_pv && li > 0 && !tc::mbar_wait(o_free, (li - 1) & 1, abort_flag, kWaitLimit)) { ok = false; break; }
             tc::tc_fence_after();
+            // A = V^T (M = d, M-major), B = P^T (16 rows x 16 keys per step, K-major)
+            const uint64_t dv = dV0 + uint64_t(pst) * uint64_t(kTile >> 4);
+            const uint64_t dp = dP0 + uint64_t(st) * uint64_t(kPTile >> 4);
+            const uint32_t acc0 = first_pv ? 0u : 1u;
+            uint64_t da[8], db[8];
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              // A = V^T (M = d, M-major), B = P^T (16 rows x 16 keys per step, K-major)
-              const uint64_t da = tc::smem_desc(aV + pst * kTile + kk * 2048, kAtom, 1024);
-              const uint64_t db = tc::smem_desc(aP + st * kPTile + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
-              tc::mma_bf16_ss(tO, da, db, id_pv, (first_pv && kk == 0) ? 0u : 1u);
+              da[kk] = dv + uint64_t(kk * (2048 >> 4));
+              db[kk] = dp + uint64_t(((kk >> 2) * kQAtom + (kk & 3) * 32) >> 4);
             }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) tc::mma_bf16_ss(tO, da[kk], db[kk], id_pv, kk > 0 ? 1u : acc0);
             tc::mma_commit(v_empty + pst);
             tc::mma_commit(pv_done + st);
           }
@@ -1514,9 +1553,11 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
       }
       if (!ok) *abort_flag = 1;
       // drain every tcgen05 operation issued by this thread before TMEM is released
+      // (bounded, and not cut short by the abort flag: TMEM must not be freed under a product)
       uint64_t* my_drain = drain + (is_qk ? 0 : 1);
       tc::mma_commit(my_drain);
-      tc::mbar_wait(my_drain, 0, abort_flag, kWaitLimit / 8);
+      volatile int never = 0;
+      tc::mbar_wait(my_drain, 0, &never, kWaitLimit / 8);
     }
   } else if (layout_ok && warp >= 4) {
     // ===================================================================== softmax + epilogue
