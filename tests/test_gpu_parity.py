@@ -248,6 +248,41 @@ def test_graph_replay_matches_stream_launches():
         assert torch.equal(outs[0][k], outs[1][k]), k
 
 
+@pytest.mark.parametrize("B_req,prefix,contiguous", [(3, 300, True), (1, 5000, False), (5, 40, False)])
+def test_attention_graph_replays_merge_cut_units(B_req, prefix, contiguous):
+    """Units cut across CTA ranges are merged by log-sum-exp from partial pieces kept in the
+    workspace, which is filled with stale bytes first (its contents need not be initialised).
+    Chains at these sizes cut units into 2 pieces (prefix 300), up to ~11 pieces (prefix 5000)
+    and cut none (prefix 40); every launch -- the stream launch and three replays of a captured
+    graph, the outputs cleared before each -- must give the oracle's result, bit-identical across
+    launches."""
+    w = W.chain_workload(B=B_req, gamma=5, V=1009, dtype="bf16", H_q=4, H_kv=4, d=128,
+                         prefix=prefix, tau=1.0, target_std=2.0, noise_std=1.0, device="cuda",
+                         contiguous=contiguous)
+    snap = PU.snapshot(w)
+    step = VerifyStep(w)
+    step.attn_ws.fill_(0xA5)   # counters and partials as stale bytes
+    step.tree_build()
+    step.attention()
+    _sync()
+    PU.check_attention(w, step, snap)
+    want_o, want_lse = step.o.clone(), step.lse.clone()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step.attention(side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        step.o.zero_()
+        step.lse.fill_(float("nan"))
+        g.replay()
+        _sync()
+        assert torch.equal(step.o, want_o)
+        assert torch.equal(step.lse, want_lse)
+
+
 def test_round_pipeline_alternating_inputs():
     # rounds of two different batches (same shape) submitted alternately through the
     # double-buffered pipeline land in the right host buffers with the results that each batch
