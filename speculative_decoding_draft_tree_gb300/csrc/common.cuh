@@ -178,6 +178,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) at global address p into L2: one
+// instruction, no registers held while the data moves.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, int bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

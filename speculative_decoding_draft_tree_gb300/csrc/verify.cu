@@ -972,10 +972,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
   if (tid == 0) sh.path[0] = 0;
   __syncthreads();
 
+  // this CTA's slice of a row (its whole 8-element units) moves into L2 ahead of the passes'
+  // loads: the passes keep only a few units per thread in flight, and a node's rejected
+  // siblings read the same two slices pass after pass
+  auto prefetch_slice = [&](const void* row, int es) {
+    constexpr int kPiece = 16384;
+    const int u1 = min(sl.u1, a.V / 8);
+    if (u1 <= sl.u0) return;
+    const char* p0 = static_cast<const char*>(row) + size_t(sl.u0) * 8 * es;
+    const int bytes = (u1 - sl.u0) * 8 * es;
+    for (int i = tid; i * kPiece < bytes; i += kWalkThreads)
+      prefetch_l2_bulk(p0 + size_t(i) * kPiece, min(kPiece, bytes - i * kPiece));
+  };
   int node = 0, npath = 1, rejections = 0, final_tok = -1, owner = 0;
   while (true) {
     const TT* trow = target + size_t(o + node) * a.tld;
     const int fc = sh.first_child[node];
+    if (!greedy) {
+      prefetch_slice(trow, int(sizeof(TT)));
+      if (fc >= 0 && !kMulti) prefetch_slice(draft + size_t(sh.drow[node]) * a.dld, int(sizeof(TD)));
+    }
     if (greedy) {
       const int best = fc >= 0 ? sh.st_arg[node] : slice_row_argmax(trow, a.V, sh.ps, sl);
       int acc = -1, rej = 0;
