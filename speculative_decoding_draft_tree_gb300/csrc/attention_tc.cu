@@ -1753,11 +1753,16 @@ attn_tc_small_kernel(const __grid_constant__ CUtensorMap mQs, const __grid_const
 }
 
 // ------------------------------------------------------------------------------ merge
-// CTA (c, y) merges M-tile mt + y of the cut unit of record c by log-sum-exp of its pieces, in
-// range order, into O and lse.  Warp w takes rows (w & 3) * 32 + lane and column half w >> 2.  A
-// unit has at most kMergeFast pieces in the common case: their log-sum-exps and all 64 partial
-// columns are loaded in one batch; longer units take the general loop.
+// CTA (c, y, z) merges rows 32 z .. 32 z + 31 of M-tile mt + y of the cut unit of record c by
+// log-sum-exp of its pieces, in range order, into O and lse.  Warp w takes rows w, w + 8, w + 16
+// and w + 24 of those and lane l columns 4l .. 4l + 3, so that every load of a partial row is
+// one 512-byte line and all of a thread's loads are in flight together (the merge is bound by
+// the latency of reading the pieces back).  A unit has at most kMergeFast pieces in the common
+// case: their log-sum-exps and values are loaded in one batch; longer units take the general
+// loop.
 constexpr int kMergeFast = 2;
+constexpr int kMergeBatch = 4;
+constexpr int kMergeSplit = attn::kBM / (8 * kMergeBatch);   // CTAs per M-tile
 
 __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   using namespace attn;
@@ -1767,92 +1772,95 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(TcDev a) {
   const int y = blockIdx.y;
   if (rec.np < 2 || y >= rec.nmt) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = (warp & 3) * 32 + lane, hh = warp >> 2;
   const int tpt = kBM >> a.log2G;
-  const int t = (rec.mt + y) * tpt + (m >> a.log2G), g = m & (a.G - 1);
-  if (t >= rec.T) return;
   const int np = rec.np;
-  const int row = y * kBM + m;   // row of the partial pieces
   auto slot_of = [&](int p) { return p == 0 ? rec.slot0 : 2 * (rec.ca + p); };
-  auto lse_of = [&](int p) { return a.part_lse[size_t(slot_of(p)) * kPartRows + row]; };
-  auto part_of = [&](int p) {
-    return reinterpret_cast<const float4*>(a.part_o + (size_t(slot_of(p)) * kPartRows + row) * kD +
-                                           64 * hh);
+  auto lse_of = [&](int p, int row) { return a.part_lse[size_t(slot_of(p)) * kPartRows + row]; };
+  auto part_of = [&](int p, int row) {
+    return reinterpret_cast<const float4*>(a.part_o + (size_t(slot_of(p)) * kPartRows + row) * kD)[lane];
   };
-  __nv_bfloat16* orow = a.o + (size_t(rec.o + t) * a.H_q + rec.h * a.G + g) * kD + 64 * hh;
-  float M = -INFINITY, wsum = 0.f, out_lse;
-  if (np <= kMergeFast) {
-    float ls[kMergeFast];
-    float4 v[kMergeFast][16];
-#pragma unroll
-    for (int p = 0; p < kMergeFast; ++p) {
-      ls[p] = p < np ? lse_of(p) : -INFINITY;
-      if (p < np) {
-        const float4* src = part_of(p);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) v[p][q] = src[q];
-      }
-    }
-#pragma unroll
-    for (int p = 0; p < kMergeFast; ++p) M = fmaxf(M, ls[p]);
-    float wt[kMergeFast];
-#pragma unroll
-    for (int p = 0; p < kMergeFast; ++p) {
-      wt[p] = ls[p] != -INFINITY ? ex2(ls[p] - M) : 0.f;
-      wsum += wt[p];
-    }
+  // row m of the M-tile: its output row (token t, head g) and its row in the pieces
+  auto out_row = [&](int m, int& t, int& g) {
+    t = (rec.mt + y) * tpt + (m >> a.log2G);
+    g = m & (a.G - 1);
+  };
+  auto store = [&](int t, int g, const float (&acc)[4], float wsum, float M) {
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const size_t orow = size_t(rec.o + t) * a.H_q + rec.h * a.G + g;
+    uint2 o2;
+    o2.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    o2.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(a.o + orow * kD + 4 * lane) = o2;
+    if (lane == 0 && a.lse) a.lse[orow] = (M + __log2f(wsum)) * 0.6931471805599453f;
+  };
+  for (int i0 = int(blockIdx.z) * kMergeBatch; i0 < int(blockIdx.z + 1) * kMergeBatch; i0 += kMergeBatch) {
+    if (np <= kMergeFast) {
+      float ls[kMergeBatch][kMergeFast];
+      float4 v[kMergeBatch][kMergeFast];
 #pragma unroll
-    for (int q = 0; q < 16; q += 2) {
-      float acc[8];
+      for (int b = 0; b < kMergeBatch; ++b) {
+        const int m = warp + 8 * (i0 + b);
+        int t, g;
+        out_row(m, t, g);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-#pragma unroll
-      for (int p = 0; p < kMergeFast; ++p) {
-        if (wt[p] != 0.f) {
-          acc[0] += wt[p] * v[p][q].x; acc[1] += wt[p] * v[p][q].y;
-          acc[2] += wt[p] * v[p][q].z; acc[3] += wt[p] * v[p][q].w;
-          acc[4] += wt[p] * v[p][q + 1].x; acc[5] += wt[p] * v[p][q + 1].y;
-          acc[6] += wt[p] * v[p][q + 1].z; acc[7] += wt[p] * v[p][q + 1].w;
+        for (int p = 0; p < kMergeFast; ++p) {
+          ls[b][p] = -INFINITY;
+          if (p < np && t < rec.T) {
+            ls[b][p] = lse_of(p, y * kBM + m);
+            v[b][p] = part_of(p, y * kBM + m);
+          }
         }
       }
-      uint4 o4;
-      o4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-      o4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-      o4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-      o4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(orow + 4 * q) = o4;
-    }
-  } else {
-    for (int p = 0; p < np; ++p) M = fmaxf(M, lse_of(p));
-    for (int p = 0; p < np; ++p) {
-      const float ls = lse_of(p);
-      if (ls != -INFINITY) wsum += ex2(ls - M);
-    }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll 1
-    for (int q = 0; q < 16; q += 2) {
-      float acc[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] = 0.f;
-      for (int p = 0; p < np; ++p) {
-        const float ls = lse_of(p);
-        if (ls == -INFINITY) continue;
-        const float wt = ex2(ls - M);
-        const float4 v0 = part_of(p)[q], v1 = part_of(p)[q + 1];
-        acc[0] += wt * v0.x; acc[1] += wt * v0.y; acc[2] += wt * v0.z; acc[3] += wt * v0.w;
-        acc[4] += wt * v1.x; acc[5] += wt * v1.y; acc[6] += wt * v1.z; acc[7] += wt * v1.w;
+      for (int b = 0; b < kMergeBatch; ++b) {
+        const int m = warp + 8 * (i0 + b);
+        int t, g;
+        out_row(m, t, g);
+        if (t >= rec.T) continue;
+        float M = -INFINITY, wsum = 0.f;
+#pragma unroll
+        for (int p = 0; p < kMergeFast; ++p) M = fmaxf(M, ls[b][p]);
+        float wt[kMergeFast];
+#pragma unroll
+        for (int p = 0; p < kMergeFast; ++p) {
+          wt[p] = ls[b][p] != -INFINITY ? ex2(ls[b][p] - M) : 0.f;
+          wsum += wt[p];
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < kMergeFast; ++p) {
+          if (wt[p] != 0.f) {
+            acc[0] += wt[p] * v[b][p].x; acc[1] += wt[p] * v[b][p].y;
+            acc[2] += wt[p] * v[b][p].z; acc[3] += wt[p] * v[b][p].w;
+          }
+        }
+        store(t, g, acc, wsum, M);
       }
-      uint4 o4;
-      o4.x = pack_bf16(acc[0] * inv, acc[1] * inv);
-      o4.y = pack_bf16(acc[2] * inv, acc[3] * inv);
-      o4.z = pack_bf16(acc[4] * inv, acc[5] * inv);
-      o4.w = pack_bf16(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(orow + 4 * q) = o4;
+    } else {
+      for (int b = 0; b < kMergeBatch; ++b) {
+        const int m = warp + 8 * (i0 + b);
+        int t, g;
+        out_row(m, t, g);
+        if (t >= rec.T) continue;
+        const int row = y * kBM + m;
+        float M = -INFINITY, wsum = 0.f;
+        for (int p = 0; p < np; ++p) M = fmaxf(M, lse_of(p, row));
+        for (int p = 0; p < np; ++p) {
+          const float ls = lse_of(p, row);
+          if (ls != -INFINITY) wsum += ex2(ls - M);
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int p = 0; p < np; ++p) {
+          const float ls = lse_of(p, row);
+          if (ls == -INFINITY) continue;
+          const float wt = ex2(ls - M);
+          const float4 v = part_of(p, row);
+          acc[0] += wt * v.x; acc[1] += wt * v.y; acc[2] += wt * v.z; acc[3] += wt * v.w;
+        }
+        store(t, g, acc, wsum, M);
+      }
     }
   }
-  out_lse = (M + __log2f(wsum)) * 0.6931471805599453f;
-  if (hh == 0 && a.lse) a.lse[size_t(rec.o + t) * a.H_q + rec.h * a.G + g] = out_lse;
 }
 
 // ------------------------------------------------------------------------------ host
@@ -1980,7 +1988,7 @@ spec_status_t launch_attention_tc(const spec_attn_params* p, void* ws, size_t ws
   // a record covers two M-tiles only when some unit has more than 128 query rows
   const unsigned merge_y = (long long)p->T_max * G > kBM ? 2u : 1u;
   if (le == cudaSuccess)
-    le = launch_pdl(attn_merge_kernel, dim3(ctas, merge_y), dim3(256), 0, s, d);
+    le = launch_pdl(attn_merge_kernel, dim3(ctas, merge_y, kMergeSplit), dim3(256), 0, s, d);
   return launch_result(le);
 }
 
