@@ -264,24 +264,30 @@ typedef struct {
   int32_t* path;
   int32_t* n_acc;
   int32_t* rejections;           /* may be NULL */
-  int32_t verify_path;           /* SPEC_VERIFY_PATH_AUTO (0, the default) or _SPLIT, below */
+  int32_t verify_path;           /* SPEC_VERIFY_PATH_AUTO (0, the default), _SPLIT or _WALK */
 } spec_verify_params;
 
-/* verify_path -- no counterpart on the pages: which of the library's two forms of the same
+/* verify_path -- no counterpart on the pages: which of the library's forms of the same
  * computation this call launches.
  *   SPEC_VERIFY_PATH_AUTO (0, what a zero-initialised struct asks for): calls with the residual
  *     or independent sibling rule (or tau == 0), T_max <= 32 and
  *     T_max * S_t + (T_max - 1) * S_d <= 200 KiB run as one cluster launch (up to 8 CTAs per
  *     request, each holding its share of the request's rows in shared memory), with
  *     S_t / S_d = ceil(ceil(V / 8) / 8) * 8 * the target / draft element size (S_d = 0 at
- *     tau == 0); every other call runs the two-launch form;
- *   SPEC_VERIFY_PATH_SPLIT: always the two-launch form (a row statistics kernel, then a walk
- *     kernel with one CTA per request).
- * Both forms give the same outputs except where fp32 rounding of the vocabulary sums decides:
+ *     tau == 0); the others with those rules and V >= 65536 run the walk form, every other call
+ *     the two-launch form;
+ *   SPEC_VERIFY_PATH_SPLIT: always the two-launch form (a row statistics kernel for every
+ *     internal node's rows, then a walk kernel with a cluster of CTAs per request);
+ *   SPEC_VERIFY_PATH_WALK: the walk kernel alone, which forms the statistics (max and sum, or
+ *     argmax at tau == 0) of the nodes it visits, one pass over their two rows each, instead of
+ *     reading every internal node's rows first (the multi-draft rule always runs the two-launch
+ *     form).
+ * All forms give the same outputs except where fp32 rounding of the vocabulary sums decides:
  * a ratio test or a draw whose uniform lies within about 1e-6 of its boundary.  The choice is
  * per call: the library keeps no process-wide setting.  Any other value: SPEC_ERR_INVALID_ARG. */
 #define SPEC_VERIFY_PATH_AUTO  0
 #define SPEC_VERIFY_PATH_SPLIT 1
+#define SPEC_VERIFY_PATH_WALK  2
 
 size_t spec_verify_workspace_size(const spec_verify_params* p);
 spec_status_t spec_verify(const spec_verify_params* p, void* workspace, size_t ws_bytes,

@@ -12,7 +12,12 @@
 // Calls that fit it (residual or independent sibling rule, trees of at most 32 nodes, a
 // request's row slices within one CTA's shared memory) run as ONE cluster launch
 // (verify_cluster.cu: the rows of each request held on chip by a cluster of CTAs); the others,
-// and every call whose verify_path field is SPEC_VERIFY_PATH_SPLIT, take the two-launch form.
+// and every call whose verify_path field is SPEC_VERIFY_PATH_SPLIT, take the two-launch form,
+// except that with those rules and a vocabulary of 65536 or more (or SPEC_VERIFY_PATH_WALK) the
+// walk runs alone and forms the statistics of the nodes it visits itself: one pass over each
+// visited internal node's target and draft rows (online max and compensated sum per thread,
+// combined over the block and the cluster in a fixed order), then that node's children's plain
+// ratio tests -- a few rows per request instead of every internal node's.
 // Two launches on the caller's stream:
 //   1. rows  (one CTA per internal node's target row and, for tau > 0 with draft logits, per
 //      draft row; 512 threads): ONE streaming read of the row with 16-byte
@@ -88,6 +93,8 @@ struct VerifyDev {
   int64_t rld;
   int32_t after_rows;   // the walk follows a rows kernel of the same call
   int32_t walk_per;     // 8-element vocabulary units of each CTA of a request's walk cluster
+  int32_t lazy;         // no rows kernel: the walk forms the statistics of the nodes it visits
+                        // (the kLazy walk)
 };
 
 // ---- 8-element units: one 16-byte load for bf16, two for fp32 ------------------------------
@@ -332,6 +339,8 @@ constexpr int kWalkMaxSmemUnits = 32768;
 // at least kWalkMinUnits units (one per thread: below that a pass is bound by its barriers)
 constexpr int kWalkMaxCl = 8;
 constexpr int kWalkMinUnits = kWalkThreads;
+// vocabularies from this size verify without the rows kernel by default (the kLazy walk)
+constexpr int kLazyMinVocab = 65536;
 
 // scratch of the block-wide vocabulary passes
 struct PassSmem {
@@ -346,6 +355,11 @@ struct PassSmem {
   // slice max) and its last unit with mass (or slice argmax)
   float px_hi[2], px_lo[2];
   int px_last[2];
+  // the statistics pass of two rows: per-warp maxima and sums of the second row, and per
+  // exchange (parity) this CTA's (max, sum hi, sum lo) of both rows
+  float fred2[kWalkWarps];
+  dfloat wtot2[kWalkWarps];
+  float sx[2][6];
 };
 
 // This CTA's share of a request's walk: its rank in the request's cluster, the cluster's size,
@@ -499,6 +513,116 @@ __device__ int slice_row_argmax(const TT* row, int V, PassSmem& sh, Slice& sl) {
     if (ob > cb || (ob == cb && oa < ca)) { cb = ob; ca = oa; }
   }
   return ca;
+}
+
+// The statistics of a node's target row and (drow non-null) of its draft row: each CTA reads its
+// slices of both rows once, each thread keeping an online maximum and a Kahan-compensated sum of
+// 2^((x - m) k2) per row (rescaled when the maximum grows), as the rows kernel forms them; the
+// block combines the threads' maxima, then their sums rescaled to the block maximum in
+// double-float; the CTAs exchange (max, sum) per row through distributed shared memory (one
+// cluster barrier) and every CTA combines them in rank order, so all hold the same (m, Z).
+template <typename TT, typename TD>
+__device__ __noinline__ void slice_row_stats(const TT* trow, const TD* drow, int V, float k2, PassSmem& sh,
+                                Slice& sl, float& mt, double& Zt, float& md, double& Zd) {
+  constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int full = V / 8, vend = min(full, sl.u1);
+  const bool two = drow != nullptr;
+  float m0 = -INFINITY, s0 = 0.f, c0 = 0.f, m1 = -INFINITY, s1 = 0.f, c1 = 0.f;
+  auto add = [&](const float (&x)[8], float& m, float& sum, float& comp) {
+    float cm = x[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) cm = fmaxf(cm, x[k]);
+    if (cm > m) {
+      const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
+      sum *= f;
+      comp *= f;
+      m = cm;
+    }
+    if (m != -INFINITY) {
+      float w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = ex2((x[k] - m) * k2);
+      const float y = sum8(w) - comp;
+      const float t = sum + y;
+      comp = (t - sum) - y;
+      sum = t;
+    }
+  };
+  const int first = sl.u0 + tid;
+  RawUnit<TT> rt[kUnits];
+  RawUnit<TD> rd[kUnits];
+#pragma unroll
+  for (int j = 0; j < kUnits; ++j) {
+    const int unit = first + j * kWalkThreads;
+    if (unit < vend) {
+      rt[j].load(trow, unit);
+      if (two) rd[j].load(drow, unit);
+    }
+  }
+  for (int base = first; base < sl.u1; base += kUnits * kWalkThreads) {
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+      const int unit = base + j * kWalkThreads;
+      if (unit < sl.u1) {
+        float xt[8], xd[8];
+        rt[j].get(trow, unit, V, full, -INFINITY, xt);
+        if (two) rd[j].get(drow, unit, V, full, -INFINITY, xd);
+        const int nx = unit + kUnits * kWalkThreads;
+        if (nx < vend) {
+          rt[j].load(trow, nx);
+          if (two) rd[j].load(drow, nx);
+        }
+        add(xt, m0, s0, c0);
+        if (two) add(xd, m1, s1, c1);
+      }
+    }
+  }
+  // the block: maxima, then the threads' sums rescaled to them
+  {
+    const float w0 = warp_max(m0), w1 = warp_max(m1);
+    if (lane == 0) { sh.fred[warp] = w0; sh.fred2[warp] = w1; }
+  }
+  __syncthreads();
+  const float B0 = warp_max(lane < kWalkWarps ? sh.fred[lane] : -INFINITY);
+  const float B1 = warp_max(lane < kWalkWarps ? sh.fred2[lane] : -INFINITY);
+  {
+    const dfloat t0 = warp_sum_df(df_make(m0 == -INFINITY ? 0.f : (s0 - c0) * ex2((m0 - B0) * k2)));
+    const dfloat t1 = warp_sum_df(df_make(m1 == -INFINITY ? 0.f : (s1 - c1) * ex2((m1 - B1) * k2)));
+    if (lane == 0) { sh.wtot[warp] = t0; sh.wtot2[warp] = t1; }
+  }
+  __syncthreads();
+  const dfloat S0 = warp_sum_df(lane < kWalkWarps ? sh.wtot[lane] : df_make(0.f));
+  const dfloat S1 = warp_sum_df(lane < kWalkWarps ? sh.wtot2[lane] : df_make(0.f));
+  // the cluster: every rank's (max, sum) of both rows, combined in rank order
+  const int slot = sl.npass & 1;
+  ++sl.npass;
+  if (tid == 0) {
+    sh.sx[slot][0] = B0; sh.sx[slot][1] = S0.hi; sh.sx[slot][2] = S0.lo;
+    sh.sx[slot][3] = B1; sh.sx[slot][4] = S1.hi; sh.sx[slot][5] = S1.lo;
+  }
+  cluster_sync();
+  float r0 = -INFINITY, r1 = -INFINITY;
+  dfloat q0 = df_make(0.f), q1 = df_make(0.f);
+  if (lane < sl.ncl) {
+    r0 = ld_cluster_f32(&sh.sx[slot][0], lane);
+    q0 = dfloat{ld_cluster_f32(&sh.sx[slot][1], lane), ld_cluster_f32(&sh.sx[slot][2], lane)};
+    r1 = ld_cluster_f32(&sh.sx[slot][3], lane);
+    q1 = dfloat{ld_cluster_f32(&sh.sx[slot][4], lane), ld_cluster_f32(&sh.sx[slot][5], lane)};
+  }
+  mt = warp_max(r0);
+  md = warp_max(r1);
+  // a rank's double-float sum times its rescale factor f = 2^((r - M) k2), exactly rounded parts
+  auto scaled = [&](dfloat q, float r, float M) -> dfloat {
+    if (r == -INFINITY) return df_make(0.f);
+    const float f = ex2((r - M) * k2);
+    const float hi = q.hi * f;
+    return dfloat{hi, fmaf(q.hi, f, -hi) + q.lo * f};
+  };
+  const dfloat i0 = warp_scan_df(scaled(q0, r0, mt), lane);
+  const dfloat i1 = warp_scan_df(scaled(q1, r1, md), lane);
+  Zt = df_to_d(dfloat{__shfl_sync(0xffffffffu, i0.hi, sl.ncl - 1), __shfl_sync(0xffffffffu, i0.lo, sl.ncl - 1)});
+  Zd = df_to_d(dfloat{__shfl_sync(0xffffffffu, i1.hi, sl.ncl - 1), __shfl_sync(0xffffffffu, i1.lo, sl.ncl - 1)});
 }
 
 // Element weights of the distribution being summed / sampled: p itself (bonus token, up to the
@@ -817,7 +941,9 @@ __device__ bool multi_ratio_test(const VerifyDev& a, const WalkSmem& sh, int c, 
   return double(sh.uacc[c]) * (sh.Nk * ed) < num * sh.sd_Z[c];
 }
 
-template <typename TT, typename TD, bool kMulti>
+// kLazy: no rows kernel before it; the walk forms the statistics of the nodes it visits (a
+// separate instance, so that the other keeps its register allocation)
+template <typename TT, typename TD, bool kMulti, bool kLazy>
 __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev a) {
   __shared__ WalkSmem sh;
   extern __shared__ float usum_dyn[];
@@ -924,7 +1050,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     }
   }
   pdl_wait();   // the rows kernel's statistics are complete
-  for (int i = tid; i < T; i += kWalkThreads) {
+  constexpr bool lazy = kLazy && !kMulti;   // else the statistics come from the rows kernel
+  for (int i = tid; i < T && !lazy; i += kWalkThreads) {
     if (a.is_internal[o + i]) {
       const RowStat ts = a.tstat[o + i];
       sh.st_m[i] = ts.m;
@@ -949,26 +1076,26 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
     }
   }
   __syncthreads();
-  if (!greedy) {
-    for (int i = tid; i < T; i += kWalkThreads) {
-      if (i > 0) {
-        const int p = sh.par[i];
-        const int qi = kMulti ? i : p;   // whose draft statistics hold q for node i
-        // plain ratio test u < p / q, as u * Zt < exp(((xt - mt) - (xd - md)) / tau) * Zd for
-        // draft logits and u * q * Zt < exp((xt - mt) / tau) for draft probabilities
-        const double u = double(sh.uacc[i]);
-        bool acc;
-        if (!a.probs) {
-          const float e = expf(((sh.xt[i] - sh.st_m[p]) - (sh.xd[i] - sh.sd_m[qi])) * a.inv_tau);
-          acc = u * sh.st_Z[p] < double(e) * sh.sd_Z[qi];
-        } else {
-          const float e = expf((sh.xt[i] - sh.st_m[p]) * a.inv_tau);
-          acc = u * double(sh.xd[i]) * sh.st_Z[p] < double(e);
-        }
-        sh.dec0[i] = acc ? 1 : 0;
-      }
+  // the plain ratio test u < p / q of node i from its parent's statistics, as
+  // u * Zt < exp(((xt - mt) - (xd - md)) / tau) * Zd for draft logits and
+  // u * q * Zt < exp((xt - mt) / tau) for draft probabilities
+  auto plain_test = [&](int i) {
+    const int p = sh.par[i];
+    const int qi = kMulti ? i : p;   // whose draft statistics hold q for node i
+    const double u = double(sh.uacc[i]);
+    bool acc;
+    if (!a.probs) {
+      const float e = expf(((sh.xt[i] - sh.st_m[p]) - (sh.xd[i] - sh.sd_m[qi])) * a.inv_tau);
+      acc = u * sh.st_Z[p] < double(e) * sh.sd_Z[qi];
+    } else {
+      const float e = expf((sh.xt[i] - sh.st_m[p]) * a.inv_tau);
+      acc = u * double(sh.xd[i]) * sh.st_Z[p] < double(e);
     }
-  }
+    sh.dec0[i] = acc ? 1 : 0;
+  };
+  if (!greedy && !lazy)
+    for (int i = tid; i < T; i += kWalkThreads)
+      if (i > 0) plain_test(i);
   if (tid == 0) sh.path[0] = 0;
   __syncthreads();
 
@@ -992,8 +1119,27 @@ __global__ void __launch_bounds__(kWalkThreads, 1) verify_walk_kernel(VerifyDev 
       prefetch_slice(trow, int(sizeof(TT)));
       if (fc >= 0 && !kMulti) prefetch_slice(draft + size_t(sh.drow[node]) * a.dld, int(sizeof(TD)));
     }
+    if constexpr (lazy) if (!greedy && fc >= 0) {
+      // this node's statistics, then its children's plain ratio tests
+      const TD* dr = a.probs ? nullptr : draft + size_t(sh.drow[node]) * a.dld;
+      float mt = 0.f, md = 0.f;
+      double Zt = 1.0, Zd = 1.0;
+      slice_row_stats<TT, TD>(trow, dr, a.V, a.k2, sh.ps, sl, mt, Zt, md, Zd);
+      if (tid == 0) {
+        sh.st_m[node] = mt;
+        sh.st_Z[node] = Zt;
+        sh.st_iz[node] = __frcp_rn(float(Zt));
+        sh.sd_m[node] = dr ? md : 0.f;
+        sh.sd_Z[node] = dr ? Zd : 1.0;
+        sh.sd_iz[node] = dr ? __frcp_rn(float(Zd)) : 1.f;
+      }
+      __syncthreads();
+      for (int i = tid; i < T; i += kWalkThreads)
+        if (i > 0 && sh.par[i] == node) plain_test(i);
+      __syncthreads();
+    }
     if (greedy) {
-      const int best = fc >= 0 ? sh.st_arg[node] : slice_row_argmax(trow, a.V, sh.ps, sl);
+      const int best = (fc >= 0 && !lazy) ? sh.st_arg[node] : slice_row_argmax(trow, a.V, sh.ps, sl);
       int acc = -1, rej = 0;
       for (int c = fc; c >= 0; c = sh.next_sib[c]) {
         if (sh.tok[c] == best) { acc = c; break; }
@@ -1214,19 +1360,20 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
   const int nunits = (d.V + 7) / 8;
   VerifyDev dw = d;
   {
-    // draft-row statistics are needed only for tau > 0 with draft logits
-    const int rows = d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
+    // draft-row statistics are needed only for tau > 0 with draft logits; with d.lazy the walk
+    // forms the statistics of the nodes it visits instead
+    const int rows = d.lazy ? 0 : d.N + ((d.tau > 0.f && !d.probs) ? d.R : 0);
     dw.after_rows = rows > 0 ? 1 : 0;
     if (rows > 0) {
       const cudaError_t e = launch_pdl(verify_rows_kernel<TT>, dim3(rows), dim3(kRowThreads), 0, s, d);
       if (e != cudaSuccess) return launch_result(e);
     }
   }
-  static DeviceOnce raised_walk;   // the unit-sum array's maximum, once per device
-  auto kernel = verify_walk_kernel<TT, TD, kMulti>;
+  static DeviceOnce raised_walk, raised_walk_lazy;   // the unit-sum array's maximum, per device
+  auto kernel = d.lazy ? verify_walk_kernel<TT, TD, kMulti, true> : verify_walk_kernel<TT, TD, kMulti, false>;
   {
     const spec_status_t st = raise_dyn_smem_once(kernel, sizeof(float) * kWalkMaxSmemUnits,
-                                                 raised_walk);
+                                                 d.lazy ? raised_walk_lazy : raised_walk);
     if (st != SPEC_OK) return st;
   }
   // CTAs per request: the largest cluster (at most kWalkMaxCl) whose slices keep at least
@@ -1296,7 +1443,8 @@ static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact
   if (p->sibling_rule != SPEC_SIBLING_RESIDUAL && p->sibling_rule != SPEC_SIBLING_INDEPENDENT &&
       p->sibling_rule != SPEC_SIBLING_MULTI_DRAFT)
     return SPEC_ERR_INVALID_ARG;
-  if (p->verify_path != SPEC_VERIFY_PATH_AUTO && p->verify_path != SPEC_VERIFY_PATH_SPLIT)
+  if (p->verify_path != SPEC_VERIFY_PATH_AUTO && p->verify_path != SPEC_VERIFY_PATH_SPLIT &&
+      p->verify_path != SPEC_VERIFY_PATH_WALK)
     return SPEC_ERR_INVALID_ARG;
   if (!p->node_offset || !p->req_status || !p->out_tokens || !p->out_len || !p->path ||
       !p->n_acc)
@@ -1348,6 +1496,13 @@ static spec_status_t verify_impl(const spec_verify_params* p, const spec_compact
       return SPEC_ERR_INVALID_ARG;
   }
   cudaStream_t s = (cudaStream_t)stream;
+  // the walk visits one path, usually a short one: with a large vocabulary the statistics of the
+  // few nodes it visits (a pass over their rows each) cost less than a rows kernel reading every
+  // internal node's rows first; below it the walk's own passes (and its prologue, which the rows
+  // kernel hides) cost more (measured: SpecInfer, vocab 128256, step 0.429 -> 0.386 ms; Medusa,
+  // vocab 32000, 0.140 -> 0.172 ms)
+  d.lazy = (!multi && (p->verify_path == SPEC_VERIFY_PATH_WALK ||
+                       (p->verify_path == SPEC_VERIFY_PATH_AUTO && p->V >= kLazyMinVocab))) ? 1 : 0;
   if (!multi && p->verify_path == SPEC_VERIFY_PATH_AUTO) {
     ClusterVerifyArgs ca;
     ca.compact = c ? 1 : 0;

@@ -1,6 +1,7 @@
-"""spec_verify's two forms against the oracle: the one-launch cluster form (trees of at most 32
-nodes whose row slices fit a CTA) and the two-launch form (row statistics kernel + walk kernel),
-chosen per call by the verify_path field, on chains and small trees (sibling residual and independent
+"""spec_verify's forms against the oracle: the one-launch cluster form (trees of at most 32
+nodes whose row slices fit a CTA), the two-launch form (row statistics kernel + walk kernel) and
+the walk alone forming the statistics of the nodes it visits, chosen per call by the verify_path
+field, on chains and small trees (sibling residual and independent
 rules), draft logits and probabilities, tau = 0, ragged vocabularies, data errors and more
 requests than one wave of clusters."""
 import numpy as np
@@ -14,7 +15,8 @@ from speculative_decoding_draft_tree_gb300.api import VerifyStep
 
 pytestmark = pytest.mark.gpu
 
-PATHS = {"cluster": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT}
+PATHS = {"cluster": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT,
+         "walk": B.SPEC_VERIFY_PATH_WALK}
 
 
 @pytest.fixture(params=sorted(PATHS))
@@ -118,21 +120,25 @@ def test_both_forms_agree():
 def test_auto_takes_the_cluster_form_when_it_fits():
     # the one-launch form never touches the statistics workspace; the two-launch form fills it
     w = WORKLOADS["chain_bf16"]()
-    for p, touched in (("cluster", False), ("split", True)):
+    for p, touched in (("cluster", False), ("split", True), ("walk", False)):
         step = VerifyStep(w, verify_path=PATHS[p])
         step.tree_build()
         step.ver_ws.fill_(0xA5)
         step.verify()
         torch.cuda.synchronize()
         assert bool((step.ver_ws != 0xA5).any()) == touched, p
-    # a tree of more than 32 nodes always takes the two-launch form
-    w = W.make_config(3, scale="small", device="cuda")
-    step = VerifyStep(w)
-    step.tree_build()
-    step.ver_ws.fill_(0xA5)
-    step.verify()
-    torch.cuda.synchronize()
-    assert bool((step.ver_ws != 0xA5).any())
+    # a tree of more than 32 nodes takes the two-launch form below a vocabulary of 65536 and the
+    # walk form from it (which never touches the statistics workspace)
+    for V, touched in ((3001, True), (65536, False)):
+        w = _medusa(V=V, ks=(3, 5, 7))   # 124 nodes
+        step = VerifyStep(w)
+        step.tree_build()
+        step.ver_ws.fill_(0xA5)
+        step.verify()
+        torch.cuda.synchronize()
+        assert bool((step.ver_ws != 0xA5).any()) == touched, V
+        orc = PU.oracle_verify(w, PU.snapshot(w), B.SPEC_SIBLING_RESIDUAL)
+        PU.check_verify(w, step, orc)
 
 
 def test_data_errors_both_forms(path):

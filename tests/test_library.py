@@ -141,10 +141,10 @@ def test_draft_tree_host_validation(lib):
 
 
 def test_verify_path_field_is_validated(lib):
-    # the form of the verification is chosen per call; values other than AUTO / SPLIT are
-    # refused before any CUDA call
+    # the form of the verification is chosen per call; values other than AUTO / SPLIT / WALK
+    # are refused before any CUDA call
     v, _ = _fake_verify_and_compact()
-    for bad in (-1, 2, 7):
+    for bad in (-1, 3, 7):
         v.verify_path = bad
         assert lib.spec_verify(ctypes.byref(v), 0x100000, 1 << 30, None) == B.SPEC_ERR_INVALID_ARG
 

@@ -23,8 +23,10 @@ def _snapshot(step):
     return {k: getattr(step, k).clone() for k in OUTPUTS}
 
 
-CASES = [(4, 1.0, "auto"), (5, 1.0, "auto"), (3, 0.0, "auto"), (2, 1.0, "split")]
-PATHS = {"auto": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT}
+CASES = [(4, 1.0, "auto"), (5, 1.0, "auto"), (3, 0.0, "auto"), (2, 1.0, "split"),
+         (4, 1.0, "walk"), (3, 0.0, "walk")]
+PATHS = {"auto": B.SPEC_VERIFY_PATH_AUTO, "split": B.SPEC_VERIFY_PATH_SPLIT,
+         "walk": B.SPEC_VERIFY_PATH_WALK}
 
 
 @pytest.mark.parametrize("cid,tau,path", CASES)
