@@ -569,8 +569,8 @@ attn_tc_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ C
   const int G = a.G, log2G = a.log2G, tpt = kBM >> log2G;
   const bool layout_ok = *abort_flag == 0;
   // registers move from the control warpgroup (warps 0..3: TMA, MMA issue) to the two softmax
-  // warpgroups, which hold a row's 128 scores at once: 128 x 56 + 256 x 224 = the 384 x 168
-  // the block was launched with
+  // warpgroups, which hold 64 of a row's scores at a time: 128 x 96 + 256 x 200 = 63488 of the
+  // 384 x 168 the block was launched with
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
   if (layout_ok && (warp == 0 || warp == 2)) {

@@ -1378,7 +1378,10 @@ static spec_status_t launch_verify(const VerifyDev& d, cudaStream_t s) {
     }
   }
   static DeviceOnce raised_walk, raised_walk_lazy;   // the unit-sum array's maximum, per device
-  auto kernel = d.lazy ? verify_walk_kernel<TT, TD, kMulti, true> : verify_walk_kernel<TT, TD, kMulti, false>;
+  // (the multi-draft rule always follows its rows kernel: no kLazy instance of it)
+  auto kernel = verify_walk_kernel<TT, TD, kMulti, false>;
+  if constexpr (!kMulti)
+    if (d.lazy) kernel = verify_walk_kernel<TT, TD, false, true>;
   {
     const spec_status_t st = raise_dyn_smem_once(kernel, sizeof(float) * kWalkMaxSmemUnits,
                                                  d.lazy ? raised_walk_lazy : raised_walk);
