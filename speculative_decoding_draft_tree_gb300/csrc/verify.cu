@@ -20,9 +20,10 @@
 // ratio tests -- a few rows per request instead of every internal node's.
 // Two launches on the caller's stream:
 //   1. rows  (one CTA per internal node's target row and, for tau > 0 with draft logits, per
-//      draft row; 512 threads): ONE streaming read of the row with 16-byte
-//      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over 32-element chunks
-//      (Kahan-compensated), then a block reduction (max, then a double-float sum) -> (m, Z);
+//      draft row; 256 threads, several CTAs per SM): ONE streaming read of the row with 16-byte
+//      loads; per-thread online max / sum of 2^((x - m) log2(e) / tau) over chunks of eight
+//      8-element units (Kahan-compensated), then a block reduction (max, then a double-float
+//      sum) -> (m, Z);
 //      tau = 0 keeps (max, lowest argmax) instead;
 //   2. walk  (one cluster of 1..8 CTAs of 512 threads per request; CTA k of a cluster owns the
 //      k-th contiguous slice of the vocabulary): validates the request's tokens, draft rows
