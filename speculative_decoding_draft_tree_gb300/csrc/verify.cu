@@ -516,61 +516,6 @@ __device__ int slice_row_argmax(const TT* row, int V, PassSmem& sh, Slice& sl) {
   return ca;
 }
 
-// One thread's units of a row slice (kG units' loads in flight): an online maximum and a
-// Kahan-compensated sum of 2^((x - m) k2), one maximum / rescale check and one compensated step
-// per group of kG units.
-template <typename T>
-__device__ __forceinline__ void stats_sweep(const T* row, int V, float k2, const Slice& sl,
-                                            float& m, float& sum, float& comp) {
-  constexpr int kG = 8 / int(sizeof(T));    // units in flight: 4 bf16, 2 fp32
-  const int full = V / 8, vend = min(full, sl.u1);
-  const int first = sl.u0 + int(threadIdx.x);
-  RawUnit<T> rv[kG];
-#pragma unroll
-  for (int j = 0; j < kG; ++j)
-    if (first + j * kWalkThreads < vend) rv[j].load(row, first + j * kWalkThreads);
-  for (int base = first; base < sl.u1; base += kG * kWalkThreads) {
-    float x[kG][8];
-#pragma unroll
-    for (int j = 0; j < kG; ++j) {
-      const int unit = base + j * kWalkThreads;
-      if (unit < sl.u1) {
-        rv[j].get(row, unit, V, full, -INFINITY, x[j]);
-        const int nx = unit + kG * kWalkThreads;
-        if (nx < vend) rv[j].load(row, nx);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[j][k] = -INFINITY;
-      }
-    }
-    float cm = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < kG; ++j)
-#pragma unroll
-      for (int k = 0; k < 8; ++k) cm = fmaxf(cm, x[j][k]);
-    if (cm > m) {
-      const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
-      sum *= f;
-      comp *= f;
-      m = cm;
-    }
-    if (m != -INFINITY) {
-      float tj[kG];
-#pragma unroll
-      for (int j = 0; j < kG; ++j) {
-        float w[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) w[k] = ex2((x[j][k] - m) * k2);
-        tj[j] = sum8(w);
-      }
-      const float y = tree_sum<kG>(tj) - comp;
-      const float t = sum + y;
-      comp = (t - sum) - y;
-      sum = t;
-    }
-  }
-}
-
 // The statistics of a node's target row and (drow non-null) of its draft row: each CTA reads its
 // slices of both rows once, each thread keeping an online maximum and a Kahan-compensated sum of
 // 2^((x - m) k2) per row (rescaled when the maximum grows), as the rows kernel forms them; the
@@ -583,10 +528,58 @@ __device__ __noinline__ void slice_row_stats(const TT* trow, const TD* drow, int
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool two = drow != nullptr;
   float m0 = -INFINITY, s0 = 0.f, c0 = 0.f, m1 = -INFINITY, s1 = 0.f, c1 = 0.f;
-  // the rows one after the other (their slices were prefetched into L2 when the walk reached
-  // the node), so that one row's units fill the registers
-  stats_sweep(trow, V, k2, sl, m0, s0, c0);
-  if (two) stats_sweep(drow, V, k2, sl, m1, s1, c1);
+  // both rows in one sweep, each unit's pair of vectors loaded together (kUnits in flight)
+  constexpr int kUnits = (sizeof(TT) == 2 && sizeof(TD) == 2) ? 4 : 2;
+  const int full = V / 8, vend = min(full, sl.u1);
+  auto add = [&](const float (&x)[8], float& m, float& sum, float& comp) {
+    float cm = x[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) cm = fmaxf(cm, x[k]);
+    if (cm > m) {
+      const float f = (m == -INFINITY) ? 0.f : ex2((m - cm) * k2);
+      sum *= f;
+      comp *= f;
+      m = cm;
+    }
+    if (m != -INFINITY) {
+      float w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = ex2((x[k] - m) * k2);
+      const float y = sum8(w) - comp;
+      const float t = sum + y;
+      comp = (t - sum) - y;
+      sum = t;
+    }
+  };
+  const int first = sl.u0 + tid;
+  RawUnit<TT> rt[kUnits];
+  RawUnit<TD> rd[kUnits];
+#pragma unroll
+  for (int j = 0; j < kUnits; ++j) {
+    const int unit = first + j * kWalkThreads;
+    if (unit < vend) {
+      rt[j].load(trow, unit);
+      if (two) rd[j].load(drow, unit);
+    }
+  }
+  for (int base = first; base < sl.u1; base += kUnits * kWalkThreads) {
+#pragma unroll
+    for (int j = 0; j < kUnits; ++j) {
+      const int unit = base + j * kWalkThreads;
+      if (unit < sl.u1) {
+        float xt[8], xd[8];
+        rt[j].get(trow, unit, V, full, -INFINITY, xt);
+        if (two) rd[j].get(drow, unit, V, full, -INFINITY, xd);
+        const int nx = unit + kUnits * kWalkThreads;
+        if (nx < vend) {
+          rt[j].load(trow, nx);
+          if (two) rd[j].load(drow, nx);
+        }
+        add(xt, m0, s0, c0);
+        if (two) add(xd, m1, s1, c1);
+      }
+    }
+  }
   // the block: maxima, then the threads' sums rescaled to them
   {
     const float w0 = warp_max(m0), w1 = warp_max(m1);
