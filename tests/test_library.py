@@ -66,6 +66,34 @@ def test_struct_layouts_match_header(tmp_path):
     assert got == want
 
 
+def test_constants_match_header(tmp_path):
+    """Every status code, dtype, draft kind, sibling rule, verification form and request status
+    bit the Python binding names has the value a C compiler gives it from the header."""
+    consts = {"SPEC_OK": B.SPEC_OK, "SPEC_ERR_INVALID_ARG": B.SPEC_ERR_INVALID_ARG,
+              "SPEC_ERR_UNSUPPORTED": B.SPEC_ERR_UNSUPPORTED, "SPEC_ERR_CUDA": B.SPEC_ERR_CUDA,
+              "SPEC_F32": B.SPEC_F32, "SPEC_BF16": B.SPEC_BF16,
+              "SPEC_DRAFT_LOGITS": B.SPEC_DRAFT_LOGITS, "SPEC_DRAFT_PROBS": B.SPEC_DRAFT_PROBS,
+              "SPEC_SIBLING_RESIDUAL": B.SPEC_SIBLING_RESIDUAL,
+              "SPEC_SIBLING_INDEPENDENT": B.SPEC_SIBLING_INDEPENDENT,
+              "SPEC_SIBLING_MULTI_DRAFT": B.SPEC_SIBLING_MULTI_DRAFT,
+              "SPEC_VERIFY_PATH_AUTO": B.SPEC_VERIFY_PATH_AUTO,
+              "SPEC_VERIFY_PATH_SPLIT": B.SPEC_VERIFY_PATH_SPLIT,
+              "SPEC_VERIFY_PATH_WALK": B.SPEC_VERIFY_PATH_WALK}
+    consts.update({f"SPEC_REQ_{k}": v for k, v in B.REQ_BITS.items()})
+    lines = ["#include <stdio.h>", '#include "spec_verify.h"', "int main(void) {"]
+    lines += [f'  printf("%d\\n", (int)({name}));' for name in consts]
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "consts.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "consts"
+    cc = subprocess.run(["gcc", "-I", build.INCLUDE, str(src), "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert dict(zip(consts, got)) == consts
+
+
 def test_host_validation_without_gpu(lib):
     # null parameter blocks are rejected before any CUDA call
     assert lib.spec_verify(None, None, 0, None) == B.SPEC_ERR_INVALID_ARG
