@@ -97,24 +97,26 @@ def test_independent_rule_paths(name, path):
     PU.check_verify(w, step, PU.oracle_verify(w, snap, B.SPEC_SIBLING_INDEPENDENT))
 
 
-def test_both_forms_agree():
-    # the two forms on the same inputs: every request's outputs are equal unless the oracle
+def test_the_forms_agree():
+    # the three forms on the same inputs: every request's outputs are equal unless the oracle
     # itself puts one of its decisions within the fp32 band
     for name in ("medusa_232", "specinfer_321", "chain_bf16", "many_requests"):
         w = WORKLOADS[name]()
         outs = {}
-        for p in ("cluster", "split"):
+        for p in ("cluster", "split", "walk"):
             step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL, p)
             outs[p] = {k: PU.np_(getattr(step, k)).copy()
                        for k in ("out_tokens", "out_len", "path", "n_acc", "rejections")}
         orc = PU.oracle_verify(w, snap)
-        for r in range(w.B):
-            same = all(np.array_equal(outs["cluster"][k][r], outs["split"][k][r]) for k in outs["split"])
-            if not same:
-                events = orc["events"][r]
-                near = any((e[0] == "test" and abs(e[4] - e[3]) < PU.BAND) or
-                           (e[0] == "sample" and e[3] < PU.BAND) for e in events)
-                assert near, (name, r)
+        for other in ("split", "walk"):
+            for r in range(w.B):
+                same = all(np.array_equal(outs["cluster"][k][r], outs[other][k][r])
+                           for k in outs[other])
+                if not same:
+                    events = orc["events"][r]
+                    near = any((e[0] == "test" and abs(e[4] - e[3]) < PU.BAND) or
+                               (e[0] == "sample" and e[3] < PU.BAND) for e in events)
+                    assert near, (name, other, r)
 
 
 def test_auto_takes_the_cluster_form_when_it_fits():
@@ -141,7 +143,7 @@ def test_auto_takes_the_cluster_form_when_it_fits():
         PU.check_verify(w, step, orc)
 
 
-def test_data_errors_both_forms(path):
+def test_data_errors_every_form(path):
     # a bad draft row and a bad token: flagged per request, outputs cleared, the other requests
     # verified as usual
     w = _medusa(B_=5)
