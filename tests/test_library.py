@@ -139,6 +139,40 @@ def test_rope_host_validation(lib, change, code):
     assert lib.spec_tree_rope_kv_write(ctypes.byref(p), None) == code
 
 
+def _attn(**kw):
+    p = B.SpecAttnParams()
+    p.dtype, p.B, p.N, p.T_max, p.H_q, p.H_kv, p.head_dim = B.SPEC_BF16, 2, 8, 6, 8, 2, 128
+    p.block_size, p.num_blocks, p.max_blocks_per_req, p.scale = 16, 8, 4, 128 ** -0.5
+    fake = 0x100000   # 16-byte aligned, never dereferenced: validation fails first
+    for f in ("q", "k_cache", "v_cache", "block_table", "prefix_len", "node_offset", "anc_mask",
+              "o", "req_status"):
+        setattr(p, f, fake)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("change", [
+    dict(dtype=7), dict(B=0), dict(N=-1), dict(T_max=0), dict(T_max=257),   # above SPEC_MAX_TREE
+    dict(H_q=6, H_kv=4),                      # query heads not a multiple of the KV heads
+    dict(head_dim=100),                       # 200-byte rows: not 16-byte multiples
+    dict(dtype=B.SPEC_F32, head_dim=2),       # 8-byte rows
+    dict(block_size=0), dict(num_blocks=0), dict(max_blocks_per_req=0),
+    dict(q=0x100008), dict(k_cache=0x100004), dict(v_cache=0x100002), dict(o=0x100001),
+    dict(q=None), dict(anc_mask=None), dict(block_table=None), dict(req_status=None),
+])
+def test_attention_host_validation(lib, change):
+    p = _attn(**change)
+    assert lib.spec_tree_attention(ctypes.byref(p), 0x100000, 1 << 30, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_attention_workspace_size(ctypes.byref(p)) == 0
+
+
+def test_attention_with_no_nodes_is_a_no_op(lib):
+    # N = 0: nothing to attend, the call succeeds before any CUDA call whatever the tensors
+    p = _attn(N=0, q=None, k_cache=None, v_cache=None, o=None, anc_mask=None)
+    assert lib.spec_tree_attention(ctypes.byref(p), None, 0, None) == B.SPEC_OK
+
+
 def test_fused_rope_build_checks_its_request_arrays(lib):
     p = _rope()
     fake = 0x100000
@@ -194,6 +228,53 @@ def _fake_verify_and_compact():
               "new_kv_len", "slot_map", "blocks_in_use"):
         setattr(c, f, fake)
     return v, c
+
+
+@pytest.mark.parametrize("change", [
+    dict(B=0), dict(N=-1), dict(R=-1), dict(V=0), dict(T_max=0), dict(T_max=257), dict(max_path=0),
+    dict(tau=-0.5), dict(tau=float("nan")), dict(tau=float("inf")),
+    dict(logits_dtype=5), dict(draft_kind=2), dict(sibling_rule=3),
+    dict(target_ld=31999),                              # a row shorter than the vocabulary
+    dict(target_ld=32001, draft_ld=32008),              # bf16 rows not 16-byte multiples
+    dict(draft_ld=31992),
+    dict(draft_kind=B.SPEC_DRAFT_PROBS, draft_ld=32002),   # fp32 rows of 128008 bytes
+    dict(target=0x100008), dict(draft=0x100004), dict(draft=None),
+    dict(tokens=None), dict(uniforms=None), dict(out_len=None), dict(n_acc=None),
+])
+def test_verify_host_validation(lib, change):
+    # every field is checked before any CUDA call
+    v, _ = _fake_verify_and_compact()
+    for k, val in change.items():
+        setattr(v, k, val)
+    assert lib.spec_verify(ctypes.byref(v), 0x100000, 1 << 30, None) == B.SPEC_ERR_INVALID_ARG
+
+
+def test_verify_workspace_checks(lib):
+    # too small, not 256-byte aligned or missing: refused before any CUDA call
+    v, _ = _fake_verify_and_compact()
+    need = lib.spec_verify_workspace_size(ctypes.byref(v))
+    assert need > 0
+    assert lib.spec_verify(ctypes.byref(v), 0x100000, need - 1, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify(ctypes.byref(v), 0x100080, need, None) == B.SPEC_ERR_INVALID_ARG
+    assert lib.spec_verify(ctypes.byref(v), None, need, None) == B.SPEC_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("change,code", [
+    (dict(dtype=9), B.SPEC_ERR_INVALID_ARG), (dict(B=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(H_kv=0), B.SPEC_ERR_INVALID_ARG), (dict(block_size=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(num_layers=0), B.SPEC_ERR_INVALID_ARG), (dict(max_path=0), B.SPEC_ERR_INVALID_ARG),
+    (dict(layer_stride=-8), B.SPEC_ERR_INVALID_ARG),
+    (dict(layer_stride=4), B.SPEC_ERR_INVALID_ARG),     # 8 bytes between layers (bf16)
+    (dict(head_dim=100), B.SPEC_ERR_INVALID_ARG),       # 200-byte rows
+    (dict(k_cache=0x100008), B.SPEC_ERR_INVALID_ARG), (dict(v_cache=None), B.SPEC_ERR_INVALID_ARG),
+    (dict(slot_map=None), B.SPEC_ERR_INVALID_ARG), (dict(blocks_in_use=None), B.SPEC_ERR_INVALID_ARG),
+    (dict(num_layers=65536), B.SPEC_ERR_UNSUPPORTED),   # one grid row per layer
+])
+def test_kv_compact_host_validation(lib, change, code):
+    _, c = _fake_verify_and_compact()
+    for k, val in change.items():
+        setattr(c, k, val)
+    assert lib.spec_kv_compact(ctypes.byref(c), None) == code
 
 
 @pytest.mark.parametrize("change", [dict(path=0x200000), dict(n_acc=0x200000),
