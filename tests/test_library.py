@@ -109,6 +109,22 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify_workspace_size(None) == 0
 
 
+@pytest.mark.parametrize("change", [
+    dict(B=0), dict(N=-1), dict(T_max=0), dict(T_max=257),   # outside [1, SPEC_MAX_TREE]
+    dict(node_offset=None), dict(prefix_len=None), dict(req_status=None),
+    dict(parent=None), dict(depth=None), dict(pos_id=None), dict(anc_mask=None),
+    dict(is_internal=None),
+])
+def test_tree_build_host_validation(lib, change):
+    fake = 0x100000   # never dereferenced: validation fails first
+    a = dict(parent=fake, node_offset=fake, prefix_len=fake, B=2, N=8, T_max=6, depth=fake,
+             pos_id=fake, anc_mask=fake, is_internal=fake, req_status=fake)
+    a.update(change)
+    assert lib.spec_tree_build(a["parent"], a["node_offset"], a["prefix_len"], a["B"], a["N"],
+                               a["T_max"], a["depth"], a["pos_id"], a["anc_mask"],
+                               a["is_internal"], a["req_status"], None) == B.SPEC_ERR_INVALID_ARG
+
+
 def _rope(**kw):
     p = B.SpecRopeParams()
     p.dtype, p.B, p.N, p.H_q, p.H_kv, p.head_dim = B.SPEC_BF16, 2, 4, 4, 2, 128
