@@ -6,8 +6,9 @@
 * Losslessness (the emitted tokens follow p; "推测解码 2026" and section 7.1 of the CSDN page),
   checked EXACTLY: the law of the oracle's output is integrated over every draft assignment and,
   by bisection on the oracle's own accept / reject and sampling decisions (black box: only its
-  outputs are observed), over the uniforms; the first emitted token must follow p_root and the
-  next one p(. | first) to 1e-9.
+  outputs are observed), over the uniforms; the first emitted token must follow p_root to 1e-9
+  and every later one, given the accepted tokens before it, p(. | those tokens) to 1e-8, down
+  to the bonus token after a fully accepted path.
 * The same losslessness by chi-square on vocab 16 with several iid siblings.
 * Multi-draft siblings (each child drawn from its own small model's q): the same exact
   losslessness, and agreement with the closed-form residual rule when every sibling's q is the
@@ -146,6 +147,24 @@ def _p_of(rows, ctx, tau):
     return torch.softmax(torch.tensor(rows(ctx)[0]) / tau, dim=0).numpy()
 
 
+def _assert_every_token_follows_p(total, rows, tau, V):
+    """The emitted tokens follow the target model: the first one p_root, and every later one,
+    given the tokens before it (accepted drafts, since a token follows them), p(. | those
+    tokens) -- down to the bonus token after a fully accepted path."""
+    first = np.zeros(V)
+    for seq, pr in total.items():
+        first[seq[0]] += pr
+    np.testing.assert_allclose(first, _p_of(rows, (), tau), atol=1e-9)
+    by_prefix = defaultdict(lambda: np.zeros(V))
+    for seq, pr in total.items():
+        for k in range(1, len(seq)):
+            by_prefix[seq[:k]][seq[k]] += pr
+    assert by_prefix
+    for prefix, cond in by_prefix.items():
+        if cond.sum() > 1e-4:
+            np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, prefix, tau), atol=1e-8)
+
+
 @pytest.mark.parametrize("shape,V,tau,kind", [
     ([-1, 0, 0, 0], 3, 1.0, OV.DRAFT_LOGITS),      # three iid siblings at the root
     ([-1, 0, 0, 1], 3, 0.7, OV.DRAFT_PROBS),       # two siblings, the first one has a child
@@ -165,19 +184,7 @@ def test_exact_losslessness(shape, V, tau, kind):
         for seq, pr in _exact_law(case, OV.SIBLING_RESIDUAL).items():
             total[seq] += w * pr
     assert abs(sum(total.values()) - 1.0) < 1e-9
-    p0 = _p_of(rows, (), tau)
-    first = np.zeros(V)
-    for seq, pr in total.items():
-        first[seq[0]] += pr
-    np.testing.assert_allclose(first, p0, atol=1e-9)
-    # second token, given the first one was an accepted draft x, follows p(. | x)
-    for x in range(V):
-        cond = np.zeros(V)
-        for seq, pr in total.items():
-            if seq[0] == x and len(seq) >= 2:
-                cond[seq[1]] += pr
-        if cond.sum() > 1e-6:
-            np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, (x,), tau), atol=1e-8)
+    _assert_every_token_follows_p(total, rows, tau, V)
     del probe
 
 
@@ -233,17 +240,7 @@ def test_exact_losslessness_multi_draft(shape, V, tau, kind):
         for seq, pr in _exact_law(case, OV.SIBLING_MULTI_DRAFT).items():
             total[seq] += w * pr
     assert abs(sum(total.values()) - 1.0) < 1e-9
-    first = np.zeros(V)
-    for seq, pr in total.items():
-        first[seq[0]] += pr
-    np.testing.assert_allclose(first, _p_of(rows, (), tau), atol=1e-9)
-    for x in range(V):
-        cond = np.zeros(V)
-        for seq, pr in total.items():
-            if seq[0] == x and len(seq) >= 2:
-                cond[seq[1]] += pr
-        if cond.sum() > 1e-6:
-            np.testing.assert_allclose(cond / cond.sum(), _p_of(rows, (x,), tau), atol=1e-8)
+    _assert_every_token_follows_p(total, rows, tau, V)
 
 
 def test_multi_draft_with_one_q_equals_the_closed_form():
