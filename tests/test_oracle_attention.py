@@ -125,3 +125,10 @@ def test_bad_block_flagged():
     out = OA.tree_attention(q, kc, vc, table, P, no, parent, bs=4)
     assert out["status"][0] == OA.BAD_BLOCK
     assert np.isnan(out["o"]).all()
+    # a partly filled last block (blocks of 4; prefix 4 puts the two nodes in slots 4, 5 of
+    # block 1, prefix 3 puts slot 4 alone there): a bad id there is still found
+    for P in (4, 3):
+        q, kc, vc, table, Pv, no, parent = _case([[-1, 0]], [P])
+        table[0, 1] = -1
+        out = OA.tree_attention(q, kc, vc, table, Pv, no, parent, bs=4)
+        assert out["status"][0] == OA.BAD_BLOCK, P

@@ -33,7 +33,7 @@ def test_log_softmax_and_topk():
     np.testing.assert_allclose(lps, sp_log_softmax(row)[[1, 2, 4, 3, 0]], atol=1e-12)
 
 
-def _random_build(B, V, K, D, K_max, seed, peaked=()):
+def _random_build(B, V, K, D, K_max, seed, peaked=(), tau=1.0):
     rng = np.random.default_rng(seed)
     store = {}
 
@@ -53,7 +53,7 @@ def _random_build(B, V, K, D, K_max, seed, peaked=()):
         return row_ids, rows
 
     roots = rng.integers(0, V, size=B)
-    pool, kept, packed = OD.build(roots, rows_of_level, K, D, K_max)
+    pool, kept, packed = OD.build(roots, rows_of_level, K, D, K_max, tau)
     return pool, kept, packed, store
 
 
@@ -111,6 +111,39 @@ def test_confident_requests_get_the_budget():
     sizes = [len(k) for k in kept]
     depths = [max(pool.cands[r][i]["depth"] for i in kept[r]) for r in range(2)]
     assert sizes[0] > sizes[1] and depths[0] > depths[1]
+
+
+@pytest.mark.parametrize("tau", [1.0, 0.5])
+def test_scores_are_path_log_probabilities(tau):
+    """Every score is the sum of scipy's log_softmax(row / tau)[token] along the path (the
+    root's is 0), and an expanded candidate's children are its row's K most probable tokens at
+    that temperature, best first."""
+    pool, kept, packed, store = _random_build(B=2, V=15, K=3, D=3, K_max=10 ** 6, seed=6, tau=tau)
+    for cs in pool.cands:
+        assert cs[0]["score"] == 0.0
+        for c in cs[1:]:
+            lp = sp_log_softmax(store[cs[c["parent"]]["row"]] / tau)
+            assert abs(c["score"] - (cs[c["parent"]]["score"] + lp[c["token"]])) < 1e-12
+        for i, c in enumerate(cs):
+            if c["row"] >= 0:
+                lp = sp_log_softmax(store[c["row"]] / tau)
+                kids = [x["token"] for x in cs if x["parent"] == i]
+                assert kids == np.argsort(-lp, kind="stable")[:3].tolist()
+
+
+def test_echo_ties_go_to_the_lower_request_then_the_lower_candidate():
+    # both requests draft from the same row, whose two best tokens tie: all four non-root
+    # candidates have the same score
+    row = np.array([2.0, 2.0, 1.0, 0.0, -1.0])
+
+    def rows_of_level(level, chosen):
+        return ([[0] * len(chosen[r]) for r in range(2)],
+                [[row] * len(chosen[r]) for r in range(2)])
+
+    for K_max, want in ((3, [[0, 1], [0]]), (4, [[0, 1, 2], [0]]), (5, [[0, 1, 2], [0, 1]])):
+        pool, kept, packed = OD.build([7, 7], rows_of_level, 2, 1, K_max)
+        assert [c["token"] for c in pool.cands[0][1:]] == [0, 1]
+        assert kept == want, K_max
 
 
 def test_packed_layout_is_a_tree():

@@ -87,6 +87,13 @@ DT_ECHO = ("ECHO budget", TD.test_echo_budget, (40,))
 DT_ECHO_SMALL = ("ECHO budget, small", TD.test_echo_budget, (8,))
 DT_CONFIDENT = ("confident requests", TD.test_confident_requests_get_the_budget, ())
 DT_PACKED = ("packed layout", TD.test_packed_layout_is_a_tree, ())
+DT_SCORES = ("scores at tau 0.5", TD.test_scores_are_path_log_probabilities, (0.5,))
+DT_TIES = ("ECHO ties", TD.test_echo_ties_go_to_the_lower_request_then_the_lower_candidate, ())
+INDEP_CHAIN = ("independent rule lossless on chains", TV.test_independent_rule_is_lossless_on_chains,
+               (OV.DRAFT_LOGITS,))
+ATTN_BAD_BLOCK = ("bad block flagged", TA.test_bad_block_flagged, ())
+ROPE_SKIPS = ("skipped nodes and requests", TR.test_bad_block_and_bad_request_are_skipped, ())
+TREE_INVALID = ("invalid trees flagged", TT.test_invalid_trees_flagged, ())
 
 MUTATIONS = [
     # --- verification (ratio test, residual, draws) ---
@@ -126,6 +133,9 @@ MUTATIONS = [
      [GREEDY_TIES]),
     ("token range check off by one", "verify",
      "not (0 <= tokens[o + c] < V)", "not (0 <= tokens[o + c] <= V)", [DATA_ERRORS]),
+    ("independent rule resamples from p", "verify",
+     "(C if sibling_rule == SIBLING_RESIDUAL else 1.0) * q",
+     "(C if sibling_rule == SIBLING_RESIDUAL else 0.0) * q", [INDEP_CHAIN]),
     ("multi-draft: later siblings tested against p", "verify",
      "num, den = target_now[tok], qc[tok]", "num, den = p[tok], qc[tok]", [LOSSLESS_MULTI]),
     ("multi-draft: residual not renormalised", "verify",
@@ -143,6 +153,8 @@ MUTATIONS = [
     ("children marked internal instead of parents", "tree",
      "is_internal[o + par[i]] = True", "is_internal[o + i] = True", [NODE_COUNTS]),
     ("mask transposed", "tree", "M[i, j] = True", "M[j, i] = True", [CHAIN_MASK]),
+    ("size bound one too loose", "tree",
+     "if T < 1 or T > T_max:", "if T < 1 or T > T_max + 1:", [TREE_INVALID]),
     # --- tree attention ---
     ("scale 1/d instead of 1/sqrt(d)", "attention",
      "scale = 1.0 / np.sqrt(d) if scale is None", "scale = 1.0 / d if scale is None", [DECODE]),
@@ -154,6 +166,8 @@ MUTATIONS = [
     ("a node does not see itself", "attention",
      "sorted(P + a for a in ancestors_or_self(par, i))",
      "sorted(P + a for a in ancestors_or_self(par, i)[1:])", [CHAIN_CAUSAL]),
+    ("bad-block range rounded down", "attention",
+     "nblk = -(-(P + T) // bs)", "nblk = (P + T) // bs", [ATTN_BAD_BLOCK]),
     ("K and V swapped", "attention",
      "o_out[n, h] = (w @ Vv) / z", "o_out[n, h] = (w @ K) / z", [DECODE]),
     # --- KV compaction ---
@@ -186,6 +200,8 @@ MUTATIONS = [
     ("rotary_dim ignored (whole head rotated)", "rope",
      "rotary_dim = d if rotary_dim is None else int(rotary_dim)", "rotary_dim = d", [ROPE_TAIL]),
     ("slot off by one", "rope", "slot = P + i", "slot = P + i + 1", [ROPE_SLOTS]),
+    ("negative position ids rotated", "rope",
+     "            if m < 0:\n                continue\n", "", [ROPE_SKIPS]),
     ("k written unrotated", "rope",
      "kc[blk, :, row, :] = rope(k_new[n], m, base, rotary_dim, interleaved)",
      "kc[blk, :, row, :] = k_new[n]", [ROPE_CHAIN]),
@@ -210,6 +226,14 @@ MUTATIONS = [
     ("ECHO keeps the least probable", "draft_tree",
      "nonroot.sort(key=lambda ri: (-sc(*ri), ri[0], ri[1]))",
      "nonroot.sort(key=lambda ri: (sc(*ri), ri[0], ri[1]))", [DT_CONFIDENT]),
+    ("top-K at tau 1 whatever the temperature", "draft_tree",
+     "tops = [[topk(rows[r][j], K, tau)", "tops = [[topk(rows[r][j], K)", [DT_SCORES]),
+    ("root score 1", "draft_tree",
+     'depth=0, score=0.0, row=-1', 'depth=0, score=1.0, row=-1', [DT_SCORES]),
+    ("ECHO ties to the higher request", "draft_tree",
+     "(-sc(*ri), ri[0], ri[1])", "(-sc(*ri), -ri[0], ri[1])", [DT_TIES]),
+    ("ECHO ties to the higher candidate", "draft_tree",
+     "(-sc(*ri), ri[0], ri[1])", "(-sc(*ri), ri[0], -ri[1])", [DT_TIES]),
     ("draft row kept on nodes with no kept child", "draft_tree",
      'draft_row.append(c["row"] if old in has_kept_child else -1)', 'draft_row.append(c["row"])',
      [DT_PACKED]),

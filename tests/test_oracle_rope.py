@@ -170,6 +170,15 @@ def test_bad_block_and_bad_request_are_skipped():
                                 c["kc"], c["vc"], req_status=[0, 0])
     assert np.isnan(out["q"][:4]).all()
     np.testing.assert_array_equal(out["k_cache"], c["kc"])
+    # a node with a negative position id is skipped: its q stays NaN and its slot unwritten
+    c = _paged_case([3], [5])
+    pos = np.array([5, -1, 6])
+    out = OR.tree_rope_kv_write(c["q"], c["k_new"], c["v_new"], pos, c["no"], c["P"], c["table"],
+                                c["kc"], c["vc"])
+    assert np.isnan(out["q"][1]).all() and not np.isnan(out["q"][[0, 2]]).any()
+    blk, row = c["table"][0, 6 // c["bs"]], 6 % c["bs"]   # node 1's slot: prefix 5 + 1
+    np.testing.assert_array_equal(out["k_cache"][blk, :, row], c["kc"][blk, :, row])
+    np.testing.assert_array_equal(out["v_cache"][blk, :, row], c["vc"][blk, :, row])
 
 
 def test_chain_equals_causal_decoding():

@@ -77,3 +77,6 @@ def test_invalid_trees_flagged():
     assert out["status"][0] == OT.BAD_PARENT
     out = OT.tree_build([], [0, 0], [0], T_max=8)
     assert out["status"][0] == OT.BAD_SIZE
+    # the size bound is inclusive: T = T_max is built, T = T_max + 1 is refused
+    out = OT.tree_build([-1, 0, 1] + [-1, 0], [0, 3, 5], [0, 0], T_max=2)
+    assert out["status"].tolist() == [OT.BAD_SIZE, 0]

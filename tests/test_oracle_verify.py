@@ -263,6 +263,23 @@ def test_multi_draft_with_one_q_equals_the_closed_form():
         assert a["out_tokens"] == b["out_tokens"] and a["rejections"].tolist() == b["rejections"].tolist()
 
 
+@pytest.mark.parametrize("kind", [OV.DRAFT_LOGITS, OV.DRAFT_PROBS])
+def test_independent_rule_is_lossless_on_chains(kind):
+    """With one child per node the per-sibling p/q test and its resampling from
+    norm(max(0, p - q)) are plain speculative sampling: the exact law follows p."""
+    rng = np.random.default_rng(14)
+    shape, V, tau = [-1, 0, 1], 4, 0.8
+    make, rows = _tree_case(V, tau, kind, shape, rng)
+    total = defaultdict(float)
+    for draft in product(range(V), repeat=2):
+        case = make(draft)
+        w = _q_of(case, 0)[draft[0]] * _q_of(case, 1)[draft[1]]
+        for seq, pr in _exact_law(case, OV.SIBLING_INDEPENDENT).items():
+            total[seq] += w * pr
+    assert abs(sum(total.values()) - 1.0) < 1e-9
+    _assert_every_token_follows_p(total, rows, tau, V)
+
+
 def test_independent_sibling_rule_is_biased():
     """The literal per-sibling p/q test (every sibling against the original p) is not lossless
     for several iid siblings: the exact law of the first token moves away from p."""
