@@ -56,6 +56,9 @@ def test_single_token_is_decode_attention():
             K, Vv = _dense(kc, vc, table[r], list(range(P[r] + 1)), h // 2, 4)
             ref = _sdpa_last_row(q[no[r], h], K, Vv, P[r] + 1)
             np.testing.assert_allclose(out["o"][no[r], h], ref, rtol=1e-12, atol=1e-12)
+            # lse: the natural log of the sum of exp(scaled scores), by the library's logsumexp
+            s = torch.tensor(K @ q[no[r], h] / np.sqrt(q.shape[2]))
+            assert abs(out["lse"][no[r], h] - float(torch.logsumexp(s, 0))) < 1e-12
 
 
 def test_kv_length_one():

@@ -80,3 +80,5 @@ def test_bad_block_flagged():
     out = OC.kv_compact(k, v, table, P, paths, [len(paths[0]) - 1], bs, 8)
     assert out["status"][0] == OC.BAD_BLOCK
     np.testing.assert_array_equal(out["k"], k)
+    # rolled back: the committed length and the blocks in use are the prefix's
+    assert out["new_kv_len"][0] == P[0] and out["blocks_in_use"][0] == -(-P[0] // bs)

@@ -87,6 +87,9 @@ DT_ECHO = ("ECHO budget", TD.test_echo_budget, (40,))
 DT_ECHO_SMALL = ("ECHO budget, small", TD.test_echo_budget, (8,))
 DT_CONFIDENT = ("confident requests", TD.test_confident_requests_get_the_budget, ())
 DT_PACKED = ("packed layout", TD.test_packed_layout_is_a_tree, ())
+GREEDY_TREE = ("greedy walk on a hand-made tree", TV.test_greedy_walk_on_a_hand_made_tree, ())
+ZERO_Q = ("zero draft probability", TV.test_a_draft_token_with_zero_draft_probability, ())
+COMPACT_BAD = ("bad block rolls back", TC.test_bad_block_flagged, ())
 DT_SCORES = ("scores at tau 0.5", TD.test_scores_are_path_log_probabilities, (0.5,))
 DT_TIES = ("ECHO ties", TD.test_echo_ties_go_to_the_lower_request_then_the_lower_candidate, ())
 INDEP_CHAIN = ("independent rule lossless on chains", TV.test_independent_rule_is_lossless_on_chains,
@@ -131,6 +134,12 @@ MUTATIONS = [
      "best = int(np.argmax(np.asarray(target[o + node, :V], dtype=np.float64)))",
      "best = int(V - 1 - np.argmax(np.asarray(target[o + node, :V], dtype=np.float64)[::-1]))",
      [GREEDY_TIES]),
+    ("greedy rejections counted twice", "verify",
+     "                    rejections += 1\n                if nxt is None:",
+     "                    rejections += 2\n                if nxt is None:", [GREEDY_TREE]),
+    ("q(x) = 0 read as a failed test", "verify",
+     "num, den = p[tok], q[tok]\n                a = num / den if den > 0 else (np.inf if num > 0 else 0.0)",
+     "num, den = p[tok], q[tok]\n                a = num / den if den > 0 else 0.0", [ZERO_Q]),
     ("token range check off by one", "verify",
      "not (0 <= tokens[o + c] < V)", "not (0 <= tokens[o + c] <= V)", [DATA_ERRORS]),
     ("independent rule resamples from p", "verify",
@@ -153,6 +162,9 @@ MUTATIONS = [
     ("children marked internal instead of parents", "tree",
      "is_internal[o + par[i]] = True", "is_internal[o + i] = True", [NODE_COUNTS]),
     ("mask transposed", "tree", "M[i, j] = True", "M[j, i] = True", [CHAIN_MASK]),
+    ("the root's first child does not make it internal", "tree",
+     "for i in range(1, T):\n            is_internal", "for i in range(2, T):\n            is_internal",
+     [CHAIN_MASK]),
     ("size bound one too loose", "tree",
      "if T < 1 or T > T_max:", "if T < 1 or T > T_max + 1:", [TREE_INVALID]),
     # --- tree attention ---
@@ -166,6 +178,8 @@ MUTATIONS = [
     ("a node does not see itself", "attention",
      "sorted(P + a for a in ancestors_or_self(par, i))",
      "sorted(P + a for a in ancestors_or_self(par, i)[1:])", [CHAIN_CAUSAL]),
+    ("lse in base 2", "attention",
+     "lse_out[n, h] = m + np.log(z)", "lse_out[n, h] = m + np.log2(z)", [DECODE]),
     ("bad-block range rounded down", "attention",
      "nblk = -(-(P + T) // bs)", "nblk = (P + T) // bs", [ATTN_BAD_BLOCK]),
     ("K and V swapped", "attention",
@@ -175,6 +189,9 @@ MUTATIONS = [
      "src, dst = P + pr[dd], P + dd", "src, dst = P + dd, P + pr[dd]", [SEQUENTIAL]),
     ("committed length without the last accepted slot", "compact",
      "new_len[r] = P + na + 1", "new_len[r] = P + na", [SEQUENTIAL]),
+    ("a bad block's request releases its prefix blocks", "compact",
+     "            status[r] |= BAD_BLOCK\n            blocks_in_use[r] = -(-P // bs)",
+     "            status[r] |= BAD_BLOCK\n            blocks_in_use[r] = 0", [COMPACT_BAD]),
     ("a request with a data error keeps its accepted path", "compact",
      "if status[r] or na < 0:", "if na < 0:", [ROLLBACK]),
     # --- lookahead mask ---
@@ -228,6 +245,8 @@ MUTATIONS = [
      "nonroot.sort(key=lambda ri: (sc(*ri), ri[0], ri[1]))", [DT_CONFIDENT]),
     ("top-K at tau 1 whatever the temperature", "draft_tree",
      "tops = [[topk(rows[r][j], K, tau)", "tops = [[topk(rows[r][j], K)", [DT_SCORES]),
+    ("an expanded candidate's children in reverse order", "draft_tree",
+     "for t, lp in zip(toks, lps):", "for t, lp in list(zip(toks, lps))[::-1]:", [DT_SCORES]),
     ("root score 1", "draft_tree",
      'depth=0, score=0.0, row=-1', 'depth=0, score=1.0, row=-1', [DT_SCORES]),
     ("ECHO ties to the higher request", "draft_tree",

@@ -65,6 +65,7 @@ def test_chain_mask_is_lower_triangular():
     out = OT.tree_build(W.chain_parents(T), [0, T], [0], T_max=8)
     np.testing.assert_array_equal(out["mask"][0], np.tril(np.ones((T, T), dtype=bool)))
     assert out["depth"].tolist() == list(range(T))
+    assert out["is_internal"].tolist() == [True] * (T - 1) + [False]   # all but the last
 
 
 def test_invalid_trees_flagged():

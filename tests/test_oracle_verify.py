@@ -403,6 +403,37 @@ def test_greedy_ties_go_to_lowest_token():
     assert res["out_tokens"][0] == [2, 1]
 
 
+def test_greedy_walk_on_a_hand_made_tree():
+    """tau = 0 on a tree whose argmaxes are set by hand: the root's children 1, 2, 3 carry
+    tokens 5, 6, 7 and the root's argmax is 6 (child 1 rejected, child 2 accepted); node 2's
+    children 4, 5 carry tokens 1, 2 and its argmax is 2 (child 4 rejected, child 5 accepted);
+    node 5 is a leaf, whose argmax 3 is the bonus token.  Two rejections in all."""
+    V = 8
+    parent = [-1, 0, 0, 0, 2, 2]
+    tokens = [0, 5, 6, 7, 1, 2]
+    tgt = np.zeros((6, V))
+    tgt[0, 6] = tgt[2, 2] = tgt[5, 3] = 1.0
+    res = OV.verify(tgt, np.zeros((6, V)), OV.DRAFT_LOGITS, np.arange(6), tokens, parent, [0, 6],
+                    np.zeros((6, 2)), 0.0, V, 4, T_max=6)
+    assert res["path"][0] == [0, 2, 5]
+    assert res["out_tokens"][0] == [6, 2, 3]
+    assert res["rejections"][0] == 2 and res["n_acc"][0] == 2 and res["out_len"][0] == 3
+
+
+def test_a_draft_token_with_zero_draft_probability():
+    """min(1, p / q) with q(x) = 0: p / q is +inf when p(x) > 0 (accepted whatever u is) and the
+    test fails when p(x) = 0 as well (rejected whatever u is)."""
+    V = 4
+    q = np.array([[0.5, 0.5, 0.0, 0.0]])
+    tgt = np.zeros((2, V))
+    tgt[0, 3] = -1e4                     # p(3) = 0 in fp64
+    for tok, accepted in ((2, True), (3, False)):
+        for u in (0.0, 0.999999):
+            res = OV.verify(tgt, q, OV.DRAFT_PROBS, [0, 0], [0, tok], [-1, 0], [0, 2],
+                            np.array([[0.5, 0.5], [u, 0.5]]), 1.0, V, 2, T_max=2)
+            assert (res["n_acc"][0] == 1) == accepted, (tok, u)
+
+
 def test_data_errors_flagged():
     V = 10
     tgt = np.zeros((3, V))
