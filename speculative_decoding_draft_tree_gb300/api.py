@@ -40,6 +40,11 @@ def _packed(tensors: Dict[str, torch.Tensor], device, pin: bool = False):
 
 
 class VerifyStep:
+    """One verification round's outputs, workspaces and C-ABI parameter blocks over a workload's
+    device tensors.  verify_path is SPEC_VERIFY_PATH_AUTO (the form is chosen per call from the
+    tree sizes and the vocabulary), _SPLIT (row statistics kernel, then the walk) or _WALK (the
+    walk forms the statistics of the nodes it visits)."""
+
     def __init__(self, w: Workload, sibling_rule: int = B.SPEC_SIBLING_RESIDUAL,
                  with_lse: bool = True, verify_path: int = B.SPEC_VERIFY_PATH_AUTO):
         self.w = w
@@ -131,8 +136,9 @@ class VerifyStep:
 
     def run(self, stream=None):
         """One full round: tree build, attention, then verification and compaction as one call
-        (1 + 2 + 1 kernel launches on the stream; the verification and compaction take 2 + 1
-        launches instead for trees of more than 32 nodes); with enable_rope, the tree build and
+        (1 + 2 + 1 kernel launches on the stream; for trees of more than 32 nodes the
+        verification and compaction take 1 + 1 launches in the walk form, the default from a
+        vocabulary of 65536, and 2 + 1 in the two-launch form); with enable_rope, the tree build and
         the rotary step share one launch, or run as two calls when fused=False."""
         if self.rope_p is not None and self.rope_fused:
             self.tree_build_rope(stream)
