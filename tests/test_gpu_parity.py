@@ -93,6 +93,15 @@ def test_chain_block_boundaries_f32():
     run_and_check(w, attention=True)
 
 
+def test_maximum_tree_size():
+    # trees of exactly SPEC_MAX_TREE = 256 nodes (Medusa ks = (15, 16): 1 + 15 + 240), eight
+    # query heads per KV head: 2048 query rows per request, 16 M-tiles
+    w = W.medusa_workload(B=2, ks=(15, 16), V=3001, dtype="bf16", H_q=8, H_kv=1, d=128,
+                          prefix=[40, 77], tau=1.0, device="cuda")
+    assert w.tree_sizes() == [256, 256]
+    run_and_check(w, attention=True)
+
+
 def _corrupt_workload():
     w = W.make_config(5, scale="small", device="cuda", num_layers=2)
     no = w.node_offset.cpu().numpy()
