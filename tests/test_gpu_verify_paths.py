@@ -143,6 +143,44 @@ def test_auto_takes_the_cluster_form_when_it_fits():
         PU.check_verify(w, step, orc)
 
 
+def _zero_q_workload(device="cuda"):
+    """A Medusa (2, 3, 2) workload with draft probabilities in which some drafted tokens have
+    draft probability exactly 0: in every request the root's second child (tested, after a
+    rejection of the first, by the residual rule) and the first child of the root's first
+    child (a plain ratio test)."""
+    w = W.medusa_workload(B=6, ks=(2, 3, 2), V=3001, dtype="bf16", H_q=4, H_kv=4, d=128,
+                          prefix=40, tau=1.0, device=device)
+    V = w.V
+    probs = torch.zeros(w.draft.shape, dtype=torch.float32, device=w.draft.device)
+    probs[:, :V] = torch.softmax(w.draft[:, :V].float(), dim=-1)
+    no, par = w.node_offset.cpu().numpy(), w.parent.cpu().numpy()
+    tok, drow = w.tokens.cpu().numpy(), w.draft_row.cpu().numpy()
+    for r in range(w.B):
+        o, T = int(no[r]), int(no[r + 1] - no[r])
+        kids = [[c for c in range(1, T) if par[o + c] == i] for i in range(T)]
+        probs[int(drow[o]), int(tok[o + kids[0][1]])] = 0.0
+        a = kids[0][0]
+        probs[int(drow[o + a]), int(tok[o + kids[a][0]])] = 0.0
+    w.draft = probs
+    w.draft_kind = W.DRAFT_PROBS
+    return w
+
+
+def test_zero_draft_probability(path):
+    # q(x) = 0 makes p / q = +inf: such a child is accepted whenever it is tested (its p is
+    # positive), by the plain test and by the residual test alike
+    w = _zero_q_workload()
+    step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL, path)
+    orc = PU.oracle_verify(w, snap)
+    tested = [(r, e[2]) for r in range(w.B) for e in orc["events"][r]
+              if e[0] == "test" and e[3] == np.inf]
+    assert tested
+    PU.check_verify(w, step, orc)
+    path_of = PU.np_(step.path)
+    for r, c in tested:
+        assert c in path_of[r].tolist(), (r, c)
+
+
 def test_data_errors_every_form(path):
     # a bad draft row and a bad token: flagged per request, outputs cleared, the other requests
     # verified as usual
