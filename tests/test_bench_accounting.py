@@ -74,8 +74,9 @@ def test_rope_bytes_are_the_rows_read_and_written(cid):
     v_new = torch.randn((w.N, w.H_kv, w.d), generator=torch.Generator().manual_seed(2)).numpy()
     kc = w.k_cache[0].float().numpy()
     vc = w.v_cache[0].float().numpy()
-    out = OR.tree_rope_kv_write(w.q.float().numpy(), k_new, v_new, tb["pos_id"], w.node_offset.numpy(),
-                                w.prefix_len.numpy(), w.block_table.numpy(), kc, vc)
+    out = OR.tree_rope_kv_write(w.q.float().numpy(), k_new, v_new, tb["pos_id"],
+                                w.node_offset.numpy(), w.prefix_len.numpy(), w.block_table.numpy(),
+                                kc, vc)
     assert not out["status"].any()
     q_rows = int((~np.isnan(out["q"]).any(axis=-1)).sum())          # (node, head) rows written
     k_rows = int((out["k_cache"] != kc).any(axis=-1).sum())         # cache rows written
