@@ -14,7 +14,8 @@ HEADER = os.path.join(build.INCLUDE, "spec_verify.h")
 
 
 def declared_functions():
-    text = open(HEADER, encoding="utf-8").read()
+    with open(HEADER, encoding="utf-8") as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
 

@@ -31,6 +31,8 @@ def test_log_softmax_and_topk():
     toks, lps = OD.topk(row, 5)
     assert toks.tolist() == [1, 2, 4, 3, 0]
     np.testing.assert_allclose(lps, sp_log_softmax(row)[[1, 2, 4, 3, 0]], atol=1e-12)
+    toks, lps = OD.topk(row, 10)             # K above the vocabulary: every token, best first
+    assert toks.tolist() == [1, 2, 4, 3, 0, 5]
 
 
 def _random_build(B, V, K, D, K_max, seed, peaked=(), tau=1.0):

@@ -25,7 +25,9 @@ GOLD = os.path.join(os.path.dirname(__file__), "golden", "lookahead_w3_n3_g2.txt
 def _golden():
     par = pos = None
     rows = []
-    for line in open(GOLD, encoding="utf-8"):
+    with open(GOLD, encoding="utf-8") as f:
+        lines = f.read().splitlines()
+    for line in lines:
         if line.startswith("#") or not line.strip():
             continue
         f = line.split()

@@ -15,6 +15,7 @@ in-place sequential copy in the compaction (equal to the gather because path[d] 
 import importlib.util
 import types
 
+import numpy as np
 import pytest
 
 import test_oracle_attention as TA
@@ -30,7 +31,8 @@ from oracle import verify as OV
 def _load(modname, old=None, new=None):
     """A fresh copy of oracle.<modname>, with the one occurrence of `old` replaced by `new`."""
     spec = importlib.util.find_spec(f"oracle.{modname}")
-    src = open(spec.origin, encoding="utf-8").read()
+    with open(spec.origin, encoding="utf-8") as f:
+        src = f.read()
     if old is not None:
         assert src.count(old) == 1, f"{modname}: {old!r} occurs {src.count(old)} times"
         src = src.replace(old, new)
@@ -89,6 +91,10 @@ DT_CONFIDENT = ("confident requests", TD.test_confident_requests_get_the_budget,
 DT_PACKED = ("packed layout", TD.test_packed_layout_is_a_tree, ())
 GREEDY_TREE = ("greedy walk on a hand-made tree", TV.test_greedy_walk_on_a_hand_made_tree, ())
 ZERO_Q = ("zero draft probability", TV.test_a_draft_token_with_zero_draft_probability, ())
+ZERO_MASS = ("zero residual mass draws from p", TV.test_zero_residual_mass_draws_from_p,
+             (OV.SIBLING_RESIDUAL,))
+ZERO_MASS_MULTI = ("zero residual mass draws from p, multi-draft",
+                   TV.test_zero_residual_mass_draws_from_p, (OV.SIBLING_MULTI_DRAFT,))
 COMPACT_BAD = ("bad block rolls back", TC.test_bad_block_flagged, ())
 DT_SCORES = ("scores at tau 0.5", TD.test_scores_are_path_log_probabilities, (0.5,))
 DT_TIES = ("ECHO ties", TD.test_echo_ties_go_to_the_lower_request_then_the_lower_candidate, ())
@@ -140,6 +146,19 @@ MUTATIONS = [
     ("q(x) = 0 read as a failed test", "verify",
      "num, den = p[tok], q[tok]\n                a = num / den if den > 0 else (np.inf if num > 0 else 0.0)",
      "num, den = p[tok], q[tok]\n                a = num / den if den > 0 else 0.0", [ZERO_Q]),
+    ("greedy checks draft rows it never reads", "verify",
+     "elif tau > 0 and any(kids_of[i] and", "elif any(kids_of[i] and", [DATA_ERRORS]),
+    ("multi-draft checks the parents' rows", "verify",
+     "if tau > 0 and any(not (0 <= draft_row[o + c] < R) for c in range(1, T)):",
+     "if tau > 0 and any(kids_of[i] and not (0 <= draft_row[o + i] < R) for i in range(T)):",
+     [DATA_ERRORS]),
+    ("zero residual mass: final draw from the (empty) residual", "verify",
+     "                    if Nk <= 0.0:\n                        w_final = p\n",
+     "                    if Nk <= 0.0:\n                        w_final = np.maximum(0.0, p - C * q)\n",
+     [ZERO_MASS]),
+    ("multi-draft zero residual mass: final draw from the residual", "verify",
+     "                    if mass <= 0.0:\n                        w_final = p\n",
+     "                    if mass <= 0.0:\n                        w_final = resid\n", [ZERO_MASS_MULTI]),
     ("token range check off by one", "verify",
      "not (0 <= tokens[o + c] < V)", "not (0 <= tokens[o + c] <= V)", [DATA_ERRORS]),
     ("independent rule resamples from p", "verify",
@@ -228,6 +247,8 @@ MUTATIONS = [
      [DT_TOPK]),
     ("top-K ties to the higher id", "draft_tree",
      "key=lambda x: (-lq[x], x)", "key=lambda x: (-lq[x], -x)", [DT_TOPK]),
+    ("top-K one short when K reaches the vocabulary", "draft_tree",
+     "k = min(k, n)", "k = min(k, n - 1)", [DT_TOPK]),
     ("path score without the parent's score", "draft_tree",
      'score=cs[i]["score"] + float(lp)', "score=float(lp)", [DT_PATHS]),
     ("the K worst leaves expanded", "draft_tree",
@@ -264,7 +285,8 @@ def _run_pins(modname, module, pins, monkeypatch):
     holder, attr = HOLDER[modname]
     failed = []
     for name, fn, args in pins:
-        with monkeypatch.context() as mp:
+        # a planted mistake may divide by a zero mass: its warnings are expected
+        with monkeypatch.context() as mp, np.errstate(all="ignore"):
             mp.setattr(holder, attr, module)
             try:
                 fn(*args)

@@ -9,7 +9,9 @@ from conftest import golden_path
 
 def _read_mask_fixture():
     parent, rows = None, []
-    for line in open(golden_path("tree6_mask.txt"), encoding="utf-8"):
+    with open(golden_path("tree6_mask.txt"), encoding="utf-8") as f:
+        lines = f.read().splitlines()
+    for line in lines:
         line = line.strip()
         if not line or line.startswith("#"):
             continue
@@ -39,7 +41,9 @@ def test_position_ids_are_prefix_plus_depth():
 
 def _read_counts():
     rows = {}
-    for line in open(golden_path("node_counts.txt"), encoding="utf-8"):
+    with open(golden_path("node_counts.txt"), encoding="utf-8") as f:
+        lines = f.read().splitlines()
+    for line in lines:
         if line.startswith("#") or not line.strip():
             continue
         name, ks, per_depth, total, leaves = [x.strip() for x in line.split("|")]

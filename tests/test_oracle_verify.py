@@ -447,3 +447,33 @@ def test_data_errors_flagged():
     assert r["status"][0] == OV.BAD_DEPTH
     r = OV.verify(draft_row=[0, 1, -1], tokens=[0, 3, 4], max_path=3, **base)
     assert r["status"][0] == 0 and r["out_len"][0] >= 1
+    # greedy reads no draft row: an out-of-range one is not an error at tau = 0
+    r = OV.verify(draft_row=[-1, 9, -1], tokens=[0, 3, 4], max_path=3,
+                  **dict(base, tau=0.0))
+    assert r["status"][0] == 0 and r["out_len"][0] >= 1
+    # multi-draft: each drafted node names the row it was drawn from; the rows its parent
+    # would name are not read
+    multi = dict(base, sibling_rule=OV.SIBLING_MULTI_DRAFT)
+    r = OV.verify(draft_row=[-1, 0, 1], tokens=[0, 3, 4], max_path=3, **multi)
+    assert r["status"][0] == 0
+    r = OV.verify(draft_row=[0, 1, 2], tokens=[0, 3, 4], max_path=3, **multi)
+    assert r["status"][0] == OV.BAD_DRAFT_ROW
+
+
+@pytest.mark.parametrize("rule", [OV.SIBLING_RESIDUAL, OV.SIBLING_MULTI_DRAFT])
+def test_zero_residual_mass_draws_from_p(rule):
+    """Draft probabilities q = 2p (not normalised, as a caller may pass them): the test
+    accepts with p / q = 1/2, and after a rejection max(0, p - q) is 0 everywhere, so the final
+    token is drawn from p itself, by the inverse CDF over ascending token id."""
+    V = 5
+    logits = np.array([0.3, -1.0, 1.2, 0.0, 0.7])
+    p = np.exp(logits - logits.max())
+    p /= p.sum()
+    q = 2.0 * p
+    for u_samp in (0.05, 0.4, 0.75, 0.97):
+        uni = np.array([[0.5, u_samp], [0.6, 0.5]])   # u_acc = 0.6 >= 1/2: rejected
+        res = OV.verify(np.stack([logits, logits]), q[None, :], OV.DRAFT_PROBS, [0, 0], [0, 2],
+                        [-1, 0], [0, 2], uni, 1.0, V, 2, sibling_rule=rule, T_max=2)
+        want = int(np.nonzero(np.cumsum(p) > u_samp)[0][0])
+        assert res["path"][0] == [0] and res["rejections"][0] == 1
+        assert res["out_tokens"][0] == [want], (u_samp, res["out_tokens"][0], want)
