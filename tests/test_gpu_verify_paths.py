@@ -181,6 +181,37 @@ def test_zero_draft_probability(path):
         assert c in path_of[r].tolist(), (r, c)
 
 
+def _zero_mass_workload(device="cuda"):
+    """A Medusa (2, 3, 2) workload with draft probabilities in which the root's draft row is
+    q = 2 p_root (not normalised): the root's first child passes the ratio test iff
+    u < p / q = 1/2, and after its rejection max(0, p - q) is 0 everywhere, so the final token
+    is drawn from p.  The root's first child gets u = 0.75 (rejected) in even requests and 0.25
+    (accepted) in odd ones."""
+    w = W.medusa_workload(B=8, ks=(2, 3, 2), V=3001, dtype="bf16", H_q=4, H_kv=4, d=128,
+                          prefix=40, tau=0.8, device=device)
+    V = w.V
+    probs = torch.zeros(w.draft.shape, dtype=torch.float32, device=w.draft.device)
+    probs[:, :V] = torch.softmax(w.draft[:, :V].float(), dim=-1)
+    no, par, drow = w.node_offset.cpu().numpy(), w.parent.cpu().numpy(), w.draft_row.cpu().numpy()
+    for r in range(w.B):
+        o = int(no[r])
+        probs[int(drow[o]), :V] = 2.0 * torch.softmax(w.target[o, :V].float() / w.tau, dim=-1)
+        first = next(c for c in range(1, int(no[r + 1]) - o) if par[o + c] == 0)
+        w.uniforms[o + first, 0] = 0.75 if r % 2 == 0 else 0.25
+    w.draft = probs
+    w.draft_kind = W.DRAFT_PROBS
+    return w
+
+
+def test_zero_residual_mass_draws_from_p(path):
+    w = _zero_mass_workload()
+    step, snap = _verify(w, B.SPEC_SIBLING_RESIDUAL, path)
+    orc = PU.oracle_verify(w, snap)
+    for r in range(0, w.B, 2):   # the oracle stopped at the root after one rejection
+        assert orc["path"][r] == [0] and orc["rejections"][r] == 1, r
+    PU.check_verify(w, step, orc)
+
+
 def test_data_errors_every_form(path):
     # a bad draft row and a bad token: flagged per request, outputs cleared, the other requests
     # verified as usual
