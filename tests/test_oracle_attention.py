@@ -61,6 +61,18 @@ def test_single_token_is_decode_attention():
             assert abs(out["lse"][no[r], h] - float(torch.logsumexp(s, 0))) < 1e-12
 
 
+def test_explicit_scale():
+    # a caller's own softmax scale replaces 1/sqrt(d): library attention with the same scale
+    q, kc, vc, table, P, no, parent = _case([[-1]], [9])
+    out = OA.tree_attention(q, kc, vc, table, P, no, parent, bs=4, scale=0.3)
+    for h in range(4):
+        K, Vv = _dense(kc, vc, table[0], list(range(P[0] + 1)), h // 2, 4)
+        ref = F.scaled_dot_product_attention(
+            torch.tensor(q[0, h]).view(1, 1, 1, -1), torch.tensor(K).view(1, 1, P[0] + 1, -1),
+            torch.tensor(Vv).view(1, 1, P[0] + 1, -1), scale=0.3).view(-1).numpy()
+        np.testing.assert_allclose(out["o"][0, h], ref, rtol=1e-12, atol=1e-12)
+
+
 def test_kv_length_one():
     q, kc, vc, table, P, no, parent = _case([[-1]], [0])
     out = OA.tree_attention(q, kc, vc, table, P, no, parent, bs=4)

@@ -68,6 +68,7 @@ CHAIN_MASK = ("chain mask", TT.test_chain_mask_is_lower_triangular, ())
 NODE_COUNTS = ("printed node counts", TT.test_printed_node_counts, ("medusa",))
 DECODE = ("decode attention", TA.test_single_token_is_decode_attention, ())
 KV_ONE = ("KV length one", TA.test_kv_length_one, ())
+EXPLICIT_SCALE = ("explicit scale", TA.test_explicit_scale, ())
 TREE_PATH = ("tree node = sequence over its path", TA.test_tree_node_equals_sequence_over_its_path, ())
 CHAIN_CAUSAL = ("chain = causal attention", TA.test_chain_is_causal_attention, ())
 SEQUENTIAL = ("compaction = sequential decoding", TC.test_compaction_equals_sequential_decoding, ())
@@ -197,6 +198,9 @@ MUTATIONS = [
     ("a node does not see itself", "attention",
      "sorted(P + a for a in ancestors_or_self(par, i))",
      "sorted(P + a for a in ancestors_or_self(par, i)[1:])", [CHAIN_CAUSAL]),
+    ("a caller's scale ignored", "attention",
+     "scale = 1.0 / np.sqrt(d) if scale is None else scale", "scale = 1.0 / np.sqrt(d)",
+     [EXPLICIT_SCALE]),
     ("lse in base 2", "attention",
      "lse_out[n, h] = m + np.log(z)", "lse_out[n, h] = m + np.log2(z)", [DECODE]),
     ("bad-block range rounded down", "attention",
