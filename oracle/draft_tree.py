@@ -21,8 +21,7 @@ Readings (the page names the quantities, not the procedure's details):
   * the packed tree keeps each request's kept candidates in candidate-index order (parents
     first); a node's draft row is the row its expansion produced if one of its children was
     kept, else -1.
-Everything is fp64 except where a score is given as fp32 input: selections on given scores
-compare those values exactly.
+Everything is fp64.
 """
 import numpy as np
 
@@ -60,18 +59,17 @@ class Pool:
         return len(self.cands)
 
 
-def expand_select(pool, level, K, score_of=None):
+def expand_select(pool, level, K):
     """Which candidates to expand at `level`: the root at level 1, else the K best (score, then
     lower index) of depth level - 1.  Returns per request the chosen candidate indices in
-    increasing order.  score_of(r, i) overrides the score used for ranking (given fp32)."""
+    increasing order."""
     out = []
     for r, cs in enumerate(pool.cands):
         if level == 1:
             out.append([0])
             continue
         front = [i for i, c in enumerate(cs) if c["depth"] == level - 1]
-        sc = (lambda i: score_of(r, i)) if score_of else (lambda i: cs[i]["score"])
-        best = sorted(front, key=lambda i: (-sc(i), i))[:K]
+        best = sorted(front, key=lambda i: (-cs[i]["score"], i))[:K]
         out.append(sorted(best))
     return out
 
@@ -88,12 +86,11 @@ def append_children(pool, chosen, row_ids, tops, level):
                                row=-1))
 
 
-def echo_select(pool, K_max, score_of=None):
+def echo_select(pool, K_max):
     """Kept candidate indices per request: every root plus the K_max - B best non-root
     candidates of the batch (score, then request, then index)."""
     nonroot = [(r, i) for r, cs in enumerate(pool.cands) for i in range(1, len(cs))]
-    sc = score_of if score_of else (lambda r, i: pool.cands[r][i]["score"])
-    nonroot.sort(key=lambda ri: (-sc(*ri), ri[0], ri[1]))
+    nonroot.sort(key=lambda ri: (-pool.cands[ri[0]][ri[1]]["score"], ri[0], ri[1]))
     keep = set((r, 0) for r in range(pool.B)) | set(nonroot[:max(0, K_max - pool.B)])
     return [sorted(i for i in range(len(cs)) if (r, i) in keep) for r, cs in enumerate(pool.cands)]
 

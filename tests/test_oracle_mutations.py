@@ -256,18 +256,19 @@ MUTATIONS = [
     ("path score without the parent's score", "draft_tree",
      'score=cs[i]["score"] + float(lp)', "score=float(lp)", [DT_PATHS]),
     ("the K worst leaves expanded", "draft_tree",
-     "best = sorted(front, key=lambda i: (-sc(i), i))[:K]",
-     "best = sorted(front, key=lambda i: (sc(i), i))[:K]", [DT_PATHS]),
+     'best = sorted(front, key=lambda i: (-cs[i]["score"], i))[:K]',
+     'best = sorted(front, key=lambda i: (cs[i]["score"], i))[:K]', [DT_PATHS]),
     ("one leaf too many expanded", "draft_tree",
-     "best = sorted(front, key=lambda i: (-sc(i), i))[:K]",
-     "best = sorted(front, key=lambda i: (-sc(i), i))[:K + 1]", [DT_COUNTS]),
+     'best = sorted(front, key=lambda i: (-cs[i]["score"], i))[:K]',
+     'best = sorted(front, key=lambda i: (-cs[i]["score"], i))[:K + 1]', [DT_COUNTS]),
     ("ECHO budget not net of the roots", "draft_tree",
      "nonroot[:max(0, K_max - pool.B)]", "nonroot[:max(0, K_max)]", [DT_ECHO]),
     ("ECHO drops the roots", "draft_tree",
      "keep = set((r, 0) for r in range(pool.B)) | set(", "keep = set() | set(", [DT_ECHO_SMALL]),
     ("ECHO keeps the least probable", "draft_tree",
-     "nonroot.sort(key=lambda ri: (-sc(*ri), ri[0], ri[1]))",
-     "nonroot.sort(key=lambda ri: (sc(*ri), ri[0], ri[1]))", [DT_CONFIDENT]),
+     'nonroot.sort(key=lambda ri: (-pool.cands[ri[0]][ri[1]]["score"], ri[0], ri[1]))',
+     'nonroot.sort(key=lambda ri: (pool.cands[ri[0]][ri[1]]["score"], ri[0], ri[1]))',
+     [DT_CONFIDENT]),
     ("top-K at tau 1 whatever the temperature", "draft_tree",
      "tops = [[topk(rows[r][j], K, tau)", "tops = [[topk(rows[r][j], K)", [DT_SCORES]),
     ("an expanded candidate's children in reverse order", "draft_tree",
@@ -275,9 +276,9 @@ MUTATIONS = [
     ("root score 1", "draft_tree",
      'depth=0, score=0.0, row=-1', 'depth=0, score=1.0, row=-1', [DT_SCORES]),
     ("ECHO ties to the higher request", "draft_tree",
-     "(-sc(*ri), ri[0], ri[1])", "(-sc(*ri), -ri[0], ri[1])", [DT_TIES]),
+     '["score"], ri[0], ri[1]))', '["score"], -ri[0], ri[1]))', [DT_TIES]),
     ("ECHO ties to the higher candidate", "draft_tree",
-     "(-sc(*ri), ri[0], ri[1])", "(-sc(*ri), ri[0], -ri[1])", [DT_TIES]),
+     '["score"], ri[0], ri[1]))', '["score"], ri[0], -ri[1]))', [DT_TIES]),
     ("draft row kept on nodes with no kept child", "draft_tree",
      'draft_row.append(c["row"] if old in has_kept_child else -1)', 'draft_row.append(c["row"])',
      [DT_PACKED]),
