@@ -56,3 +56,15 @@ def test_reference_arm_under_torchrun():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the contract's keys, on the GPU arm's metric and workload
+    for k in ("metric", "unit", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    assert line["metric"] == "verified tree tokens/s" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "chain_g4_v1000_f32"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["unit"] == line["unit"]
+    assert cb["cores"] >= 1 and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
