@@ -28,7 +28,7 @@ over cache rows and chain = causal decoding for the RoPE step; a hand-derived wo
 the page's token counts and its two mask rules for the lookahead mask; scipy's log_softmax, a
 brute-force top-K, path products recomputed by multiplying probabilities, the page's node counts
 and ECHO's optimality / ancestor closure for the draft-tree construction.
-tests/test_oracle_mutations.py plants 70 plausible mistakes, one at a time, in fresh copies of
+tests/test_oracle_mutations.py plants 73 plausible mistakes, one at a time, in fresh copies of
 these modules, and each makes a named pin fail.  No oracle function is "parity unpinned".
 """
 from . import tree, attention, verify, compact, rope, lookahead, draft_tree  # noqa: F401

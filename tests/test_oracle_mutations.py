@@ -92,6 +92,9 @@ DT_CONFIDENT = ("confident requests", TD.test_confident_requests_get_the_budget,
 DT_PACKED = ("packed layout", TD.test_packed_layout_is_a_tree, ())
 GREEDY_TREE = ("greedy walk on a hand-made tree", TV.test_greedy_walk_on_a_hand_made_tree, ())
 ZERO_Q = ("zero draft probability", TV.test_a_draft_token_with_zero_draft_probability, ())
+CDF_GAP = ("inverse CDF and its edge distance", TV.test_inverse_cdf_and_its_distance_to_the_edges,
+           ())
+RATIOS = ("recorded ratios", TV.test_recorded_ratios_are_p_over_q, ())
 ZERO_MASS = ("zero residual mass draws from p", TV.test_zero_residual_mass_draws_from_p,
              (OV.SIBLING_RESIDUAL,))
 ZERO_MASS_MULTI = ("zero residual mass draws from p, multi-draft",
@@ -160,6 +163,14 @@ MUTATIONS = [
     ("multi-draft zero residual mass: final draw from the residual", "verify",
      "                    if mass <= 0.0:\n                        w_final = p\n",
      "                    if mass <= 0.0:\n                        w_final = resid\n", [ZERO_MASS_MULTI]),
+    ("a draw's edge distance not normalised", "verify",
+     "lo = c[x - 1] / total if x > 0 else 0.0", "lo = c[x - 1] if x > 0 else 0.0", [CDF_GAP]),
+    ("every draw recorded far from an edge", "verify",
+     "return x, min(u - lo, hi - u)", "return x, 1.0", [CDF_GAP]),
+    ("recorded ratio clipped at 1", "verify",
+     '                u = float(uniforms[o + c, 0])\n                events.append(("test", node, c, a, u))',
+     '                u = float(uniforms[o + c, 0])\n                events.append(("test", node, c, min(a, 1.0), u))',
+     [RATIOS]),
     ("token range check off by one", "verify",
      "not (0 <= tokens[o + c] < V)", "not (0 <= tokens[o + c] <= V)", [DATA_ERRORS]),
     ("independent rule resamples from p", "verify",

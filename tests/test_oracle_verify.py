@@ -403,6 +403,36 @@ def test_greedy_ties_go_to_lowest_token():
     assert res["out_tokens"][0] == [2, 1]
 
 
+def test_inverse_cdf_and_its_distance_to_the_edges():
+    """The smallest x with sum_{y <= x} w(y) > u * sum(w), and the distance from u to the nearer
+    edge of x's CDF interval (what the parity tests read to exempt draws near an edge)."""
+    w = [1.0, 2.0, 3.0, 4.0]                  # CDF edges 0, 0.1, 0.3, 0.6, 1
+    for u, x, gap in ((0.0, 0, 0.0), (0.05, 0, 0.05), (0.25, 1, 0.05), (0.3, 2, 0.0),
+                      (0.5, 2, 0.1), (0.61, 3, 0.01), (0.99, 3, 0.01)):
+        got_x, got_gap = OV.inverse_cdf(w, u)
+        assert got_x == x, u
+        assert abs(got_gap - gap) < 1e-15, u
+
+
+def test_recorded_ratios_are_p_over_q():
+    """Every ("test", node, child, a, u) event carries a = p(tok) / q(tok) of the child's token
+    (the first sibling's plain ratio), with p and q the library's softmax at tau."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(21)
+    V, T, tau = 30, 5, 0.8
+    tgt = rng.normal(size=(T, V)) * 2
+    drf = rng.normal(size=(T, V)) * 2
+    tokens = [0] + [int(x) for x in rng.integers(0, V, T - 1)]
+    uni = np.full((T, 2), 1e-9)                  # every test passes: the walk goes to the leaf
+    res = OV.verify(tgt, drf, OV.DRAFT_LOGITS, np.arange(T), tokens, list(range(-1, T - 1)),
+                    [0, T], uni, tau, V, T, T_max=T)
+    tests = [e for e in res["events"][0] if e[0] == "test"]
+    assert [e[2] for e in tests] == [1, 2, 3, 4]
+    for _, node, c, a, u in tests:
+        want = softmax(tgt[node] / tau)[tokens[c]] / softmax(drf[node] / tau)[tokens[c]]
+        assert abs(a - want) < 1e-12 * want and u == 1e-9
+
+
 def test_greedy_walk_on_a_hand_made_tree():
     """tau = 0 on a tree whose argmaxes are set by hand: the root's children 1, 2, 3 carry
     tokens 5, 6, 7 and the root's argmax is 6 (child 1 rejected, child 2 accepted); node 2's
