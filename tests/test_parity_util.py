@@ -1,0 +1,89 @@
+"""The parity harness's own verification bar, on the CPU: check_verify passes the oracle's own
+results, fails a divergence whose decisions all lie clear of the fp32 band, and exempts one (and
+counts it) only when the oracle's decision at the divergence lies within the band.  A stand-in
+for the GPU's outputs is built from the oracle's results."""
+import copy
+import types
+
+import numpy as np
+import pytest
+import torch
+
+import parity_util as PU
+from speculative_decoding_draft_tree_gb300 import workloads as W
+
+
+@pytest.fixture(autouse=True)
+def keep_tally():
+    # the suite-wide exemption tally belongs to the GPU parity tests
+    saved = dict(PU.TALLY)
+    yield
+    PU.TALLY.clear()
+    PU.TALLY.update(saved)
+
+
+def _case():
+    w = W.make_config(3, scale="small", device="cpu")   # Medusa (3, 5, 7), two requests
+    orc = PU.oracle_verify(w, PU.snapshot(w))
+    assert not orc["status"].any()
+    return w, orc
+
+
+def _as_step(w, orc):
+    path = np.full((w.B, w.max_path), -1, dtype=np.int32)
+    toks = np.full((w.B, w.max_path), -1, dtype=np.int32)
+    for r in range(w.B):
+        path[r, :len(orc["path"][r])] = orc["path"][r]
+        toks[r, :len(orc["out_tokens"][r])] = orc["out_tokens"][r]
+    t = torch.from_numpy
+    return types.SimpleNamespace(
+        req_status=t(orc["status"].astype(np.int32)), out_len=t(orc["out_len"].astype(np.int32)),
+        n_acc=t(orc["n_acc"].astype(np.int32)), path=t(path), out_tokens=t(toks),
+        rejections=t(orc["rejections"].astype(np.int32)))
+
+
+def test_the_oracles_own_results_pass():
+    w, orc = _case()
+    draws, exempt = PU.check_verify(w, _as_step(w, orc), orc)
+    assert draws >= w.B and exempt == 0
+
+
+def test_a_divergence_clear_of_the_band_fails():
+    w, orc = _case()
+    assert not any(PU._near(orc["events"][0], n) for n in orc["path"][0])
+    step = _as_step(w, orc)
+    L = int(orc["out_len"][0])
+    step.out_tokens[0, L - 1] = (int(step.out_tokens[0, L - 1]) + 1) % w.V   # another final token
+    with pytest.raises(AssertionError):
+        PU.check_verify(w, step, orc)
+    step = _as_step(w, orc)                       # a path one node shorter
+    if L >= 2:
+        step.path[0, L - 1] = -1
+        step.n_acc[0] -= 1
+        step.out_len[0] -= 1
+        with pytest.raises(AssertionError):
+            PU.check_verify(w, step, orc)
+    step = _as_step(w, orc)                       # a status bit the oracle did not set
+    step.req_status[1] = 4
+    with pytest.raises(AssertionError):
+        PU.check_verify(w, step, orc)
+
+
+def test_a_divergence_within_the_band_is_exempted_and_counted():
+    w, orc = _case()
+    stop = orc["path"][0][-1]
+    near = copy.deepcopy(orc)
+    # the oracle's final draw at the stop node put within the band of a CDF edge
+    near["events"][0] = [e if not (e[0] == "sample" and e[1] == stop)
+                         else (e[0], e[1], e[2], 0.5 * PU.BAND) for e in orc["events"][0]]
+    assert PU._near(near["events"][0], stop)
+    step = _as_step(w, orc)
+    L = int(orc["out_len"][0])
+    step.out_tokens[0, L - 1] = (int(step.out_tokens[0, L - 1]) + 1) % w.V
+    before = PU.TALLY["exempt"]
+    draws, exempt = PU.check_verify(w, step, near)
+    assert exempt == 1 and PU.TALLY["exempt"] == before + 1
+    # the same divergence in the other request, whose decisions are clear of the band, fails
+    step.out_tokens[1, int(orc["out_len"][1]) - 1] += 1
+    with pytest.raises(AssertionError):
+        PU.check_verify(w, step, near)
