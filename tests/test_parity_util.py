@@ -1,7 +1,8 @@
-"""The parity harness's own verification bar, on the CPU: check_verify passes the oracle's own
-results, fails a divergence whose decisions all lie clear of the fp32 band, and exempts one (and
-counts it) only when the oracle's decision at the divergence lies within the band.  A stand-in
-for the GPU's outputs is built from the oracle's results."""
+"""The parity harness's own bars, on the CPU, with stand-ins for the GPU's outputs built from the
+oracle's results: check_verify passes the oracle's own results, fails a divergence whose
+decisions all lie clear of the fp32 band, and exempts one (and counts it) only when the oracle's
+decision at the divergence lies within the band; check_attention passes the oracle's output in
+the kernel's dtype and fails an output or LSE element beyond its bar."""
 import copy
 import types
 
@@ -87,3 +88,29 @@ def test_a_divergence_within_the_band_is_exempted_and_counted():
     step.out_tokens[1, int(orc["out_len"][1]) - 1] += 1
     with pytest.raises(AssertionError):
         PU.check_verify(w, step, near)
+
+
+@pytest.mark.parametrize("cid", [1, 3])     # fp32 chain, bf16 Medusa tree
+def test_the_attention_bar(cid):
+    from oracle import attention as OA
+    w = W.make_config(cid, scale="small", device="cpu")
+    snap = PU.snapshot(w)
+    orc = OA.tree_attention(PU.f32(w.q).astype(np.float64), w.k_cache[0].float().numpy(),
+                            w.v_cache[0].float().numpy(), snap["block_table"], snap["prefix_len"],
+                            snap["node_offset"], snap["parent"], w.bs)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    step = types.SimpleNamespace(req_status=torch.zeros(w.B, dtype=torch.int32),
+                                 o=torch.from_numpy(orc["o"]).to(td),
+                                 lse=torch.from_numpy(orc["lse"]).float())
+    assert PU.check_attention(w, step, snap) < (2e-2 if w.dtype == "bf16" else 1e-5)
+    # one output element off by more than the bar (bf16: 2e-2 absolute; fp32: 1e-5 relative)
+    bad = step.o.clone()
+    bad[1, 0, 3] += 0.05 if w.dtype == "bf16" else 1e-3 * (1 + abs(float(bad[1, 0, 3])))
+    with pytest.raises(AssertionError):
+        PU.check_attention(w, types.SimpleNamespace(req_status=step.req_status, o=bad,
+                                                    lse=step.lse), snap)
+    bad_lse = step.lse.clone()
+    bad_lse[2, 1] += 1e-3
+    with pytest.raises(AssertionError):
+        PU.check_attention(w, types.SimpleNamespace(req_status=step.req_status, o=step.o,
+                                                    lse=bad_lse), snap)
