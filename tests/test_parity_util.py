@@ -2,7 +2,8 @@
 oracle's results: check_verify passes the oracle's own results, fails a divergence whose
 decisions all lie clear of the fp32 band, and exempts one (and counts it) only when the oracle's
 decision at the divergence lies within the band; check_attention passes the oracle's output in
-the kernel's dtype and fails an output or LSE element beyond its bar."""
+the kernel's dtype and fails an output or LSE element beyond its bar; check_tree fails a single
+flipped mask bit; check_compact fails one wrong element of a moved row and a wrong block count."""
 import copy
 import types
 
@@ -114,3 +115,64 @@ def test_the_attention_bar(cid):
     with pytest.raises(AssertionError):
         PU.check_attention(w, types.SimpleNamespace(req_status=step.req_status, o=step.o,
                                                     lse=bad_lse), snap)
+
+
+def test_the_tree_bar():
+    from oracle import tree as OT
+    w = W.make_config(4, scale="small", device="cpu")   # SpecInfer trees
+    snap = PU.snapshot(w)
+    orc = OT.tree_build(snap["parent"], snap["node_offset"], snap["prefix_len"], w.T_max)
+    words = np.zeros((w.N, (w.T_max + 31) // 32), dtype=np.uint32)
+    no = snap["node_offset"]
+    for r in range(w.B):
+        o, T = int(no[r]), int(no[r + 1] - no[r])
+        for i, j in zip(*np.nonzero(orc["mask"][r])):
+            words[o + i, j >> 5] |= np.uint32(1) << np.uint32(j & 31)
+    t = torch.from_numpy
+
+    def step(anc):
+        return types.SimpleNamespace(
+            req_status=torch.zeros(w.B, dtype=torch.int32), depth=t(orc["depth"].astype(np.int32)),
+            pos_id=t(orc["pos_id"].astype(np.int32)),
+            is_internal=t(orc["is_internal"].astype(np.uint8)), anc_mask=t(anc.view(np.int32)))
+
+    PU.check_tree(w, step(words), snap)
+    bad = words.copy()
+    bad[int(no[1]) + 2, 0] ^= np.uint32(1)    # node 2 of request 1 loses its root bit
+    with pytest.raises(AssertionError):
+        PU.check_tree(w, step(bad), snap)
+
+
+def test_the_compaction_bar():
+    from oracle import compact as OC
+    w = W.make_config(3, scale="small", device="cpu", num_layers=2)
+    snap = PU.snapshot(w)
+    orc = PU.oracle_verify(w, snap)
+    kb = PU.cache_region(w.k_cache, w, snap, range(w.B))
+    vb = PU.cache_region(w.v_cache, w, snap, range(w.B))
+    comp = OC.kv_compact(w.k_cache.float().numpy(), w.v_cache.float().numpy(), snap["block_table"],
+                         snap["prefix_len"], orc["path"], orc["n_acc"], w.bs, w.max_path,
+                         status=orc["status"])
+    assert (comp["slot_map"][..., 0] != comp["slot_map"][..., 1]).any()   # rows do move
+    w.k_cache.copy_(torch.from_numpy(comp["k"]).to(w.k_cache.dtype))      # exact: bf16 values
+    w.v_cache.copy_(torch.from_numpy(comp["v"]).to(w.v_cache.dtype))
+    step = _as_step(w, orc)
+    t = torch.from_numpy
+    step.new_kv_len = t(comp["new_kv_len"].astype(np.int32))
+    step.slot_map = t(comp["slot_map"].astype(np.int32))
+    step.blocks_in_use = t(comp["blocks_in_use"].astype(np.int32))
+    PU.check_compact(w, step, snap, kb, vb)
+    # one element of a moved row written wrong
+    r, d = next((r, d) for r in range(w.B) for d in range(w.max_path)
+                if comp["slot_map"][r, d, 0] != comp["slot_map"][r, d, 1])
+    dst = int(comp["slot_map"][r, d, 1])
+    blk = int(snap["block_table"][r, dst // w.bs])
+    keep = w.v_cache[1, blk, 0, dst % w.bs, 5].clone()
+    w.v_cache[1, blk, 0, dst % w.bs, 5] += 1.0
+    with pytest.raises(AssertionError):
+        PU.check_compact(w, step, snap, kb, vb)
+    w.v_cache[1, blk, 0, dst % w.bs, 5] = keep
+    PU.check_compact(w, step, snap, kb, vb)
+    step.blocks_in_use[r] += 1
+    with pytest.raises(AssertionError):
+        PU.check_compact(w, step, snap, kb, vb)
