@@ -3,7 +3,9 @@ oracle's results: check_verify passes the oracle's own results, fails a divergen
 decisions all lie clear of the fp32 band, and exempts one (and counts it) only when the oracle's
 decision at the divergence lies within the band; check_attention passes the oracle's output in
 the kernel's dtype and fails an output or LSE element beyond its bar; check_tree fails a single
-flipped mask bit; check_compact fails one wrong element of a moved row and a wrong block count."""
+flipped mask bit; check_compact fails one wrong element of a moved row and a wrong block count;
+the draft-tree comparison's near-tie detector flags a near tie at a top-K boundary and neither
+an exact tie nor a clear row."""
 import copy
 import types
 
@@ -176,3 +178,23 @@ def test_the_compaction_bar():
     step.blocks_in_use[r] += 1
     with pytest.raises(AssertionError):
         PU.check_compact(w, step, snap, kb, vb)
+
+
+def test_the_draft_tree_near_tie_detector():
+    # the draft-tree comparison exempts only requests that pass a decision fp32 cannot settle
+    import test_gpu_draft_tree as TG
+    from oracle import draft_tree as OD
+    K, V = 2, 6
+    clear = np.array([3.0, 1.0, 0.0, -1.0, -2.0, -3.0])      # top-2 and the 3rd well apart
+    near = np.array([3.0, 1.0, 1.0 - 1e-6, -1.0, -2.0, -3.0])  # 2nd and 3rd within fp32's reach
+    exact = np.array([3.0, 1.0, 1.0, -1.0, -2.0, -3.0])       # an exact tie: lower id both sides
+    rows_np = [np.stack([clear, clear, near, near, exact, exact])]   # level 1: rows r * K + j
+    log = {}
+
+    def rows_of_level(level, chosen):
+        log[level] = [list(c) for c in chosen]
+        return ([[r * K + j for j in range(len(chosen[r]))] for r in range(3)],
+                [[rows_np[0][r * K + j] for j in range(len(chosen[r]))] for r in range(3)])
+
+    pool, kept, packed = OD.build([0, 0, 0], rows_of_level, K, 1, 10 ** 6)
+    assert TG._near_ties(pool, log, rows_np, K, 1.0, 10 ** 6) == {1}
