@@ -69,7 +69,9 @@ typedef enum {
 #define SPEC_REQ_BAD_PARENT    1   /* parent[0] != -1 or parent[i] not in [0, i) */
 #define SPEC_REQ_BAD_SIZE      2   /* T_r < 1, T_r > T_max, or node_offset not monotone / > N */
 #define SPEC_REQ_BAD_TOKEN     4   /* a draft token id outside [0, V) */
-#define SPEC_REQ_BAD_DRAFT_ROW 8   /* tau > 0 and a node with children has draft_row outside [0, R) */
+#define SPEC_REQ_BAD_DRAFT_ROW 8   /* tau > 0 and a draft row read is outside [0, R): a node
+                                      with children's, or under the multi-draft rule a drafted
+                                      node's own */
 #define SPEC_REQ_BAD_DEPTH     16  /* a root-to-node path longer than max_path */
 #define SPEC_REQ_BAD_BLOCK     32  /* a needed block_table entry outside [0, num_blocks) */
 #define SPEC_REQ_TIMEOUT       64  /* a bounded device-side wait gave up (the result is invalid) */

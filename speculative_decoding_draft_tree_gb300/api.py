@@ -312,8 +312,8 @@ class DraftTreeBuilder:
 
     def __init__(self, batch: int, K: int, depth: int, device, cap: Optional[int] = None):
         cap = cap if cap is not None else 1 + K + (depth - 1) * K * K
-        if cap > 256:
-            raise ValueError("pool capacity above 256 candidates per request")
+        if cap > B.SPEC_MAX_TREE:
+            raise ValueError(f"pool capacity above {B.SPEC_MAX_TREE} candidates per request")
         self.B, self.K, self.depth, self.cap = batch, K, depth, cap
         nb = batch
         i32 = dict(dtype=torch.int32, device=device)

@@ -18,6 +18,7 @@ SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_DRAFT_LOGITS, SPEC_DRAFT_PROBS = 0, 1
 SPEC_SIBLING_RESIDUAL, SPEC_SIBLING_INDEPENDENT, SPEC_SIBLING_MULTI_DRAFT = 0, 1, 2
 SPEC_VERIFY_PATH_AUTO, SPEC_VERIFY_PATH_SPLIT, SPEC_VERIFY_PATH_WALK = 0, 1, 2
+SPEC_MAX_TREE = 256
 REQ_BITS = dict(BAD_PARENT=1, BAD_SIZE=2, BAD_TOKEN=4, BAD_DRAFT_ROW=8, BAD_DEPTH=16,
                 BAD_BLOCK=32, TIMEOUT=64)
 EXPORTS = ["spec_tree_build", "spec_tree_rope_kv_write", "spec_tree_build_rope_kv_write", "spec_tree_attention", "spec_attention_workspace_size",

@@ -79,7 +79,7 @@ def test_constants_match_header(tmp_path):
               "SPEC_SIBLING_MULTI_DRAFT": B.SPEC_SIBLING_MULTI_DRAFT,
               "SPEC_VERIFY_PATH_AUTO": B.SPEC_VERIFY_PATH_AUTO,
               "SPEC_VERIFY_PATH_SPLIT": B.SPEC_VERIFY_PATH_SPLIT,
-              "SPEC_VERIFY_PATH_WALK": B.SPEC_VERIFY_PATH_WALK}
+              "SPEC_VERIFY_PATH_WALK": B.SPEC_VERIFY_PATH_WALK, "SPEC_MAX_TREE": B.SPEC_MAX_TREE}
     consts.update({f"SPEC_REQ_{k}": v for k, v in B.REQ_BITS.items()})
     lines = ["#include <stdio.h>", '#include "spec_verify.h"', "int main(void) {"]
     lines += [f'  printf("%d\\n", (int)({name}));' for name in consts]
