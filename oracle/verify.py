@@ -29,8 +29,9 @@ Readings where the pages are silent (each one is listed in the design notes):
     drawn from, so siblings carry their own q_c.  The pages' rule is applied sibling after
     sibling with no closed form: the running target starts as r = p, child c is accepted iff
     u_acc < r(tok) / q_c(tok), and a rejection replaces r by norm(max(0, r - q_c));
-  * a zero residual mass (N_k = 0, reachable only through rounding) stops the sibling loop and
-    the final token is drawn from p;
+  * a zero residual mass (N_k = 0: through rounding for normalised rows, exactly for draft
+    probabilities that sum to more than 1, e.g. q = 2p) stops the sibling loop and the final
+    token is drawn from p;
   * tau applies to target and draft logits alike; draft probabilities are used as given;
     tau = 0 accepts a child iff its token is argmax p_i (lowest id on ties) and the final token
     is argmax p at the stop node;
