@@ -5,7 +5,8 @@ decision at the divergence lies within the band; check_attention passes the orac
 the kernel's dtype and fails an output or LSE element beyond its bar; check_tree fails a single
 flipped mask bit; check_compact fails one wrong element of a moved row and a wrong block count;
 the draft-tree comparison's near-tie detector flags a near tie at a top-K boundary and neither
-an exact tie nor a clear row."""
+an exact tie nor a clear row; the RoPE bar passes the oracle rounded once to fp32 or bf16 and
+fails the opposite rotation and a changed pass-through component."""
 import copy
 import types
 
@@ -198,3 +199,26 @@ def test_the_draft_tree_near_tie_detector():
 
     pool, kept, packed = OD.build([0, 0, 0], rows_of_level, K, 1, 10 ** 6)
     assert TG._near_ties(pool, log, rows_np, K, 1.0, 10 ** 6) == {1}
+
+
+def test_the_rope_bar():
+    import test_gpu_rope as TGR
+    from oracle import rope as OR
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn((6, 4, 128), generator=g).bfloat16().double().numpy()   # exact in bf16
+    for inter in (False, True):
+        ref = OR.rope(x, 1000, 10000.0, 64, inter)
+        # the oracle's value rounded once to the output type passes
+        TGR._assert_rotated(ref.astype(np.float32).astype(np.float64), ref, x, "f32", 64, inter)
+        TGR._assert_rotated(torch.from_numpy(ref).bfloat16().double().numpy(), ref, x, "bf16",
+                            64, inter)
+        # the rotation the other way fails, in either output type
+        wrong = OR.rope(x, -1000, 10000.0, 64, inter)
+        for dt in ("f32", "bf16"):
+            with pytest.raises(AssertionError):
+                TGR._assert_rotated(wrong, ref, x, dt, 64, inter)
+        # a component past rotary_dim must be copied exactly
+        tail = ref.copy()
+        tail[0, 0, 100] += 1e-3
+        with pytest.raises(AssertionError):
+            TGR._assert_rotated(tail, ref, x, "f32", 64, inter)
